@@ -1,0 +1,468 @@
+/*
+ * qr_oracle.c -- slow, scalar CPU oracle for the block-quantized two-shot
+ * all-reduce codec.  TEST INFRASTRUCTURE ONLY (see qr_oracle.h): the product
+ * path never includes, links or calls this file.
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared.
+ * -ffp-contract=off matters: every float operation below must round on its
+ * own (x*r is rounded before the clip, the rank sum is rounded after each
+ * add), exactly as written.
+ *
+ * Citations name the source page and section:
+ *   [QR]  "QuickReduce INT3 quantization and benchmarking on MI355" (AMD blog)
+ *   [FC]  "Flash Communication" review record, arXiv 2412.04964
+ */
+#include "qr_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define TILE 2048   /* values per tile: 1152 B = 2048/2 + 64*2 for INT4 [QR Design Highlights] */
+#define BLOCK 32    /* values per fp16 scale [QR Design Highlights] */
+#define NBLOCK (TILE / BLOCK)
+#define NSLOT (TILE / 8)  /* one q2w uint16 / q1w uint8 per 8-value slot [QR Design Highlights] */
+
+/* ------------------------------------------------------------------------ */
+/* Number formats, written from the IEEE-754 definitions.  Every float is a  */
+/* dyadic rational that a double holds exactly, so each conversion is done  */
+/* on exact values: find the quantum (the spacing of representable values   */
+/* at the input's magnitude), round |x|/quantum to the nearest integer with  */
+/* ties to even, and assemble the bit pattern.                               */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest multiple of `quantum` (a power of two) to a >= 0, ties to the even
+ * multiple.  a/quantum is exact in double, so is its fractional part. */
+static double round_to_quantum(double a, double quantum)
+{
+    double v = a / quantum;
+    double fl = floor(v);
+    double frac = v - fl;
+    if (frac > 0.5) return (fl + 1.0) * quantum;
+    if (frac < 0.5) return fl * quantum;
+    return (fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0) * quantum;
+}
+
+/* floor(log2(a)) for a > 0, exactly (frexp is exact). */
+static int ilog2(double a)
+{
+    int e;
+    frexp(a, &e);
+    return e - 1;
+}
+
+/* binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits.
+ * Normal quantum 2^(E-10) for E >= -14, subnormal quantum 2^-24,
+ * largest finite 65504; anything that rounds above it is infinity. */
+uint16_t orc_f32_to_f16(float f)
+{
+    uint32_t fb;
+    memcpy(&fb, &f, sizeof fb);
+    uint16_t sign = (uint16_t)((fb >> 16) & 0x8000u);
+    if (isnan(f)) return (uint16_t)(sign | 0x7E00u);
+    if (isinf(f)) return (uint16_t)(sign | 0x7C00u);
+    double a = fabs((double)f);
+    if (a == 0.0) return sign;
+    int E = ilog2(a);
+    double quantum = (E < -14) ? ldexp(1.0, -24) : ldexp(1.0, E - 10);
+    double r = round_to_quantum(a, quantum);
+    if (r > 65504.0) return (uint16_t)(sign | 0x7C00u);
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -14)) /* subnormal: r = m * 2^-24, m < 1024 */
+        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -24)));
+    E = ilog2(r);
+    double frac = r / ldexp(1.0, E) - 1.0; /* a multiple of 2^-10 in [0,1) */
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(frac * 1024.0));
+}
+
+float orc_f16_to_f32(uint16_t h)
+{
+    int sign = h >> 15;
+    int ex = (h >> 10) & 0x1F;
+    int man = h & 0x3FF;
+    double v;
+    if (ex == 0x1F) v = man ? NAN : INFINITY;
+    else if (ex == 0) v = ldexp((double)man, -24);
+    else v = ldexp((double)(1024 + man), ex - 25);
+    return (float)(sign ? -v : v);
+}
+
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits.
+ * Normal quantum 2^(E-7) for E >= -126, subnormal quantum 2^-133,
+ * largest finite (2 - 2^-7) * 2^127. */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t fb;
+    memcpy(&fb, &f, sizeof fb);
+    uint16_t sign = (uint16_t)((fb >> 16) & 0x8000u);
+    if (isnan(f)) return (uint16_t)(sign | 0x7FC0u);
+    if (isinf(f)) return (uint16_t)(sign | 0x7F80u);
+    double a = fabs((double)f);
+    if (a == 0.0) return sign;
+    int E = ilog2(a);
+    double quantum = (E < -126) ? ldexp(1.0, -133) : ldexp(1.0, E - 7);
+    double r = round_to_quantum(a, quantum);
+    if (r > ldexp(255.0, 120)) return (uint16_t)(sign | 0x7F80u); /* (2-2^-7)*2^127 */
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -126))
+        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -133)));
+    E = ilog2(r);
+    double frac = r / ldexp(1.0, E) - 1.0; /* a multiple of 2^-7 in [0,1) */
+    return (uint16_t)(sign | (uint16_t)((E + 127) << 7) | (uint16_t)(frac * 128.0));
+}
+
+float orc_bf16_to_f32(uint16_t h)
+{
+    int sign = h >> 15;
+    int ex = (h >> 7) & 0xFF;
+    int man = h & 0x7F;
+    double v;
+    if (ex == 0xFF) v = man ? NAN : INFINITY;
+    else if (ex == 0) v = ldexp((double)man, -133);
+    else v = ldexp((double)(128 + man), ex - 134);
+    return (float)(sign ? -v : v);
+}
+
+void orc_f32_to_f16_n(const float *f, size_t n, uint16_t *h)
+{
+    for (size_t i = 0; i < n; ++i) h[i] = orc_f32_to_f16(f[i]);
+}
+
+void orc_f16_to_f32_n(const uint16_t *h, size_t n, float *f)
+{
+    for (size_t i = 0; i < n; ++i) f[i] = orc_f16_to_f32(h[i]);
+}
+
+void orc_f32_to_bf16_n(const float *f, size_t n, uint16_t *h)
+{
+    for (size_t i = 0; i < n; ++i) h[i] = orc_f32_to_bf16(f[i]);
+}
+
+void orc_bf16_to_f32_n(const uint16_t *h, size_t n, float *f)
+{
+    for (size_t i = 0; i < n; ++i) f[i] = orc_bf16_to_f32(h[i]);
+}
+
+static float widen(int dtype, uint16_t h)
+{
+    return dtype == ORC_FP16 ? orc_f16_to_f32(h) : orc_bf16_to_f32(h);
+}
+
+static uint16_t narrow(int dtype, float f)
+{
+    return dtype == ORC_FP16 ? orc_f32_to_f16(f) : orc_f32_to_bf16(f);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sizes and the tile layout                                                 */
+/* ------------------------------------------------------------------------ */
+
+static int bits_ok(int bits) { return bits == 3 || bits == 4 || bits == 6 || bits == 8; }
+
+size_t orc_tile_values(void) { return TILE; }
+
+/* Codes take bits*2048/8 = 256*bits bytes, then 64 fp16 scales (128 B):
+ * INT4 1152 B and INT3 896 B as printed in [QR Design Highlights]. */
+size_t orc_tile_bytes(int bits)
+{
+    return bits_ok(bits) ? (size_t)256 * (size_t)bits + 128 : 0;
+}
+
+size_t orc_wire_bytes(int bits, size_t n)
+{
+    return ((n + TILE - 1) / TILE) * orc_tile_bytes(bits);
+}
+
+static size_t scale_offset(int bits) { return (size_t)256 * (size_t)bits; }
+
+static void put_u16(uint8_t *p, uint32_t v)
+{
+    p[0] = (uint8_t)(v & 0xFF);
+    p[1] = (uint8_t)((v >> 8) & 0xFF);
+}
+
+static void put_u32(uint8_t *p, uint32_t v)
+{
+    p[0] = (uint8_t)(v & 0xFF);
+    p[1] = (uint8_t)((v >> 8) & 0xFF);
+    p[2] = (uint8_t)((v >> 16) & 0xFF);
+    p[3] = (uint8_t)((v >> 24) & 0xFF);
+}
+
+static uint32_t get_u16(const uint8_t *p) { return (uint32_t)p[0] | ((uint32_t)p[1] << 8); }
+
+static uint32_t get_u32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+/* Slot k of a tile holds the codes u[0..7] of values 8k..8k+7. */
+static void pack_slot(int bits, const uint8_t *u, uint8_t *tile, int k)
+{
+    uint32_t lo = 0, hi = 0;
+    int j;
+    switch (bits) {
+    case 8: /* one byte per code */
+        for (j = 0; j < 8; ++j) tile[8 * k + j] = u[j];
+        break;
+    case 4: /* eight 4-bit codes in one 32-bit word [QR Design Highlights] */
+        for (j = 0; j < 8; ++j) lo |= (uint32_t)(u[j] & 0xF) << (4 * j);
+        put_u32(tile + 4 * k, lo);
+        break;
+    case 3: /* low 2 bits -> uint16 q2w, high bit -> uint8 q1w [QR Design Highlights] */
+        for (j = 0; j < 8; ++j) {
+            lo |= (uint32_t)(u[j] & 0x3) << (2 * j);
+            hi |= (uint32_t)((u[j] >> 2) & 0x1) << j;
+        }
+        put_u16(tile + 2 * k, lo);
+        tile[512 + k] = (uint8_t)hi;
+        break;
+    case 6: /* INT3-style split: low 4 bits as INT4, high 2 bits as a q2w word */
+        for (j = 0; j < 8; ++j) {
+            lo |= (uint32_t)(u[j] & 0xF) << (4 * j);
+            hi |= (uint32_t)((u[j] >> 4) & 0x3) << (2 * j);
+        }
+        put_u32(tile + 4 * k, lo);
+        put_u16(tile + 1024 + 2 * k, hi);
+        break;
+    }
+}
+
+static void unpack_slot(int bits, const uint8_t *tile, int k, uint8_t *u)
+{
+    uint32_t lo, hi;
+    int j;
+    switch (bits) {
+    case 8:
+        for (j = 0; j < 8; ++j) u[j] = tile[8 * k + j];
+        break;
+    case 4:
+        lo = get_u32(tile + 4 * k);
+        for (j = 0; j < 8; ++j) u[j] = (uint8_t)((lo >> (4 * j)) & 0xF);
+        break;
+    case 3:
+        lo = get_u16(tile + 2 * k);
+        hi = tile[512 + k];
+        for (j = 0; j < 8; ++j)
+            u[j] = (uint8_t)(((lo >> (2 * j)) & 0x3) | (((hi >> j) & 0x1) << 2));
+        break;
+    case 6:
+        lo = get_u32(tile + 4 * k);
+        hi = get_u16(tile + 1024 + 2 * k);
+        for (j = 0; j < 8; ++j)
+            u[j] = (uint8_t)(((lo >> (4 * j)) & 0xF) | (((hi >> (2 * j)) & 0x3) << 4));
+        break;
+    }
+}
+
+int orc_pack_codes(int bits, const uint8_t *u, size_t ntiles, uint8_t *wire)
+{
+    if (!bits_ok(bits)) return -1;
+    size_t tb = orc_tile_bytes(bits);
+    for (size_t t = 0; t < ntiles; ++t)
+        for (int k = 0; k < NSLOT; ++k)
+            pack_slot(bits, u + t * TILE + 8 * (size_t)k, wire + t * tb, k);
+    return 0;
+}
+
+int orc_unpack_codes(int bits, const uint8_t *wire, size_t ntiles, uint8_t *u)
+{
+    if (!bits_ok(bits)) return -1;
+    size_t tb = orc_tile_bytes(bits);
+    for (size_t t = 0; t < ntiles; ++t)
+        for (int k = 0; k < NSLOT; ++k)
+            unpack_slot(bits, wire + t * tb, k, u + t * TILE + 8 * (size_t)k);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The block quantizer [QR Design Highlights; Quantization and               */
+/* Dequantization Paths]: absmax over the block -> fp16 scale -> scale,      */
+/* clip to [qmin, qmax], round, bias to unsigned.                            */
+/* ------------------------------------------------------------------------ */
+
+/* Round half to even of a float of small magnitude (|t| <= 128 here). */
+static float round_half_even(float t)
+{
+    double v = (double)t;
+    double fl = floor(v);
+    double frac = v - fl;
+    if (frac > 0.5) return (float)(fl + 1.0);
+    if (frac < 0.5) return (float)fl;
+    return (float)(fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0);
+}
+
+int orc_quantize_block(int bits, const float *x, uint8_t *u, uint16_t *scale)
+{
+    if (!bits_ok(bits)) return -1;
+    const int bias = 1 << (bits - 1);  /* |qmin|: [-4,+3] -> [0,7] for INT3 */
+    const float qmin = (float)(-bias);
+    const float qmax = (float)(bias - 1);
+    int i;
+
+    float A = 0.0f; /* block absolute maximum */
+    for (i = 0; i < BLOCK; ++i) {
+        if (!isfinite(x[i])) return -1; /* non-finite input is outside the contract */
+        float a = fabsf(x[i]);
+        if (a > A) A = a;
+    }
+    float d = A / (float)bias; /* power-of-two divide: exact unless it underflows */
+    uint16_t sh = orc_f32_to_f16(d);
+    if (sh == 0x7C00u) sh = 0x7BFFu; /* the fp16 scale saturates at 65504 */
+    float s = orc_f16_to_f32(sh);
+    if (s == 0.0f) { /* zero block, or a scale below the fp16 range */
+        *scale = 0;
+        for (i = 0; i < BLOCK; ++i) u[i] = (uint8_t)bias;
+        return 0;
+    }
+    float r = 1.0f / s; /* fp32 encode factor */
+    for (i = 0; i < BLOCK; ++i) {
+        float t = x[i] * r;
+        if (t < qmin) t = qmin;
+        if (t > qmax) t = qmax;
+        float q = round_half_even(t);
+        u[i] = (uint8_t)((int)q + bias);
+    }
+    *scale = sh;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Tiles: encode (send path) and decode (receive path)                       */
+/* ------------------------------------------------------------------------ */
+
+/* x: 2048 fp32 values (already zero-padded). */
+static int encode_tile(int bits, const float *x, uint8_t *tile)
+{
+    uint8_t u[TILE];
+    for (int g = 0; g < NBLOCK; ++g) {
+        uint16_t sh;
+        if (orc_quantize_block(bits, x + BLOCK * g, u + BLOCK * g, &sh) != 0) return -1;
+        put_u16(tile + scale_offset(bits) + 2 * (size_t)g, sh);
+    }
+    for (int k = 0; k < NSLOT; ++k) pack_slot(bits, u + 8 * k, tile, k);
+    return 0;
+}
+
+/* Recombine the bits, remove the bias, multiply by the block's decode scale.
+ * (u - bias) * s is exact in fp32: an 8-bit integer times an 11-bit
+ * significand. */
+static void decode_tile_f32(int bits, const uint8_t *tile, float *out)
+{
+    const int bias = 1 << (bits - 1);
+    uint8_t u[TILE];
+    for (int k = 0; k < NSLOT; ++k) unpack_slot(bits, tile, k, u + 8 * k);
+    for (int g = 0; g < NBLOCK; ++g) {
+        float s = orc_f16_to_f32((uint16_t)get_u16(tile + scale_offset(bits) + 2 * (size_t)g));
+        for (int i = 0; i < BLOCK; ++i) {
+            int q = (int)u[BLOCK * g + i] - bias;
+            out[BLOCK * g + i] = (float)q * s;
+        }
+    }
+}
+
+int orc_encode_f32(int bits, const float *x, size_t n, uint8_t *wire)
+{
+    if (!bits_ok(bits)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        for (size_t i = 0; i < TILE; ++i) {
+            size_t idx = t * TILE + i;
+            buf[i] = idx < n ? x[idx] : 0.0f; /* tail: zero padding */
+        }
+        if (encode_tile(bits, buf, wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+int orc_encode(int bits, int dtype, const uint16_t *x, size_t n, uint8_t *wire)
+{
+    if (!bits_ok(bits) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        for (size_t i = 0; i < TILE; ++i) {
+            size_t idx = t * TILE + i;
+            buf[i] = idx < n ? widen(dtype, x[idx]) : 0.0f;
+        }
+        if (encode_tile(bits, buf, wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+int orc_decode_f32(int bits, const uint8_t *wire, size_t n, float *out)
+{
+    if (!bits_ok(bits)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        decode_tile_f32(bits, wire + t * tb, buf);
+        for (size_t i = 0; i < TILE && t * TILE + i < n; ++i) out[t * TILE + i] = buf[i];
+    }
+    return 0;
+}
+
+int orc_decode(int bits, int dtype, const uint8_t *wire, size_t n, uint16_t *y)
+{
+    if (!bits_ok(bits) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        decode_tile_f32(bits, wire + t * tb, buf);
+        for (size_t i = 0; i < TILE && t * TILE + i < n; ++i)
+            y[t * TILE + i] = narrow(dtype, buf[i]); /* round half to even */
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Two-shot reduction [QR Quantization and Dequantization Paths: Phase-1B;   */
+/* FC key machinery: sum locally, re-quantize the partial sums]              */
+/* ------------------------------------------------------------------------ */
+
+/* Phase-1B: decode the R rank copies of each tile, add them in fp32 in rank
+ * order 0..R-1 (each add rounded to fp32), re-quantize the sums. */
+int orc_segment_reduce(int bits, int R, const uint8_t *const *wires, size_t n,
+                       uint8_t *out_wire)
+{
+    if (!bits_ok(bits) || R < 1) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_tile_bytes(bits);
+    float acc[TILE], y[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        decode_tile_f32(bits, wires[0] + t * tb, acc);
+        for (int r = 1; r < R; ++r) {
+            decode_tile_f32(bits, wires[r] + t * tb, y);
+            for (int i = 0; i < TILE; ++i) acc[i] = acc[i] + y[i];
+        }
+        if (encode_tile(bits, acc, out_wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+/* The whole two-shot all-reduce: quantize every rank (send), Phase-1B
+ * reduction with re-quantization, Phase-2 dequantization of the reduced
+ * wire.  Two quantization round trips in total [FC key machinery]. */
+int orc_allreduce(int bits, int dtype, int R, const uint16_t *const *x,
+                  size_t n, uint16_t *y)
+{
+    if (!bits_ok(bits) || R < 1 || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    size_t W = orc_wire_bytes(bits, n);
+    int rc = -1;
+    uint8_t **wires = (uint8_t **)calloc((size_t)R, sizeof *wires);
+    uint8_t *red = (uint8_t *)malloc(W ? W : 1);
+    if (!wires || !red) goto done;
+    for (int r = 0; r < R; ++r) {
+        wires[r] = (uint8_t *)malloc(W ? W : 1);
+        if (!wires[r]) goto done;
+        if (orc_encode(bits, dtype, x[r], n, wires[r]) != 0) goto done;
+    }
+    if (orc_segment_reduce(bits, R, (const uint8_t *const *)wires, n, red) != 0) goto done;
+    rc = orc_decode(bits, dtype, red, n, y);
+done:
+    if (wires)
+        for (int r = 0; r < R; ++r) free(wires[r]);
+    free(wires);
+    free(red);
+    return rc;
+}

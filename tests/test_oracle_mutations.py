@@ -1,0 +1,100 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case below plants one mistake in a temporary copy of the oracle's C
+source (a dropped term, a wrong sign, index or offset, a transposed bit
+order, the wrong rounding or denominator, ...), compiles it with gcc, and runs
+the pin battery of the other oracle test modules against it: at least one pin
+must fail.  Nothing here touches a GPU.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_formats as F
+import test_oracle_layout as L
+import test_oracle_quantizer as Q
+import test_oracle_reduce as Rd
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "qr_oracle.c")
+
+# (name, [(old, new), ...]) -- every `old` must occur in the source; all
+# occurrences are replaced.
+MUTATIONS = [
+    ("scale_over_qmax_not_qmin", [("float d = A / (float)bias;", "float d = A / (float)(bias - 1);")]),
+    ("round_half_up_not_even",
+     [("return (float)(fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0);", "return (float)(fl + 1.0);")]),
+    ("reduce_drops_rank0", [("decode_tile_f32(bits, wires[0] + t * tb, acc);", "memset(acc, 0, sizeof acc);")]),
+    ("reduce_drops_last_rank", [("for (int r = 1; r < R; ++r) {", "for (int r = 1; r < R - 1; ++r) {")]),
+    ("reduce_in_reverse_rank_order",
+     [("decode_tile_f32(bits, wires[0] + t * tb, acc);", "decode_tile_f32(bits, wires[R - 1] + t * tb, acc);"),
+      ("decode_tile_f32(bits, wires[r] + t * tb, y);", "decode_tile_f32(bits, wires[R - 1 - r] + t * tb, y);")]),
+    ("decode_bias_sign_flipped",
+     [("int q = (int)u[BLOCK * g + i] - bias;", "int q = bias - (int)u[BLOCK * g + i];")]),
+    ("nibble_order_reversed", [("(4 * j)", "(4 * (7 - j))")]),
+    ("q2w_order_reversed", [("(2 * j)", "(2 * (7 - j))")]),
+    ("q1w_at_wrong_offset", [("512 + k", "520 + k")]),
+    ("int6_high_bits_at_wrong_offset", [("1024 + 2 * k", "1026 + 2 * k")]),
+    ("no_lower_clip", [("if (t < qmin) t = qmin;", "")]),
+    ("no_upper_clip", [("if (t > qmax) t = qmax;", "")]),
+    ("no_scale_saturation", [("if (sh == 0x7C00u) sh = 0x7BFFu;", "")]),
+    ("absmax_without_abs", [("float a = fabsf(x[i]);", "float a = x[i];")]),
+    ("fp16_rounds_ties_up", [("return (fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0) * quantum;", "return (fl + 1.0) * quantum;")]),
+    ("scales_after_a_gap", [("static size_t scale_offset(int bits) { return (size_t)256 * (size_t)bits; }",
+                             "static size_t scale_offset(int bits) { return (size_t)256 * (size_t)bits + 2; }")]),
+    ("tail_padded_with_ones", [("buf[i] = idx < n ? widen(dtype, x[idx]) : 0.0f;",
+                                "buf[i] = idx < n ? widen(dtype, x[idx]) : 1.0f;")]),
+    ("bf16_subnormal_quantum_wrong", [("ldexp(1.0, -133) : ldexp(1.0, E - 7)", "ldexp(1.0, -132) : ldexp(1.0, E - 7)")]),
+    ("zero_scale_codes_not_bias", [("for (i = 0; i < BLOCK; ++i) u[i] = (uint8_t)bias;",
+                                    "for (i = 0; i < BLOCK; ++i) u[i] = 0;")]),
+]
+
+
+def _battery(orc):
+    golden = L._golden_cases()
+    yield lambda: L.test_tile_sizes_printed_on_the_page(orc)
+    for c in golden:
+        for d in (0, 1):
+            yield lambda c=c, d=d: L.test_known_answer_tiles(orc, c, d)
+    for b in (3, 4, 6, 8):
+        yield lambda b=b: Q.test_closed_form_all_equal_blocks(orc, b)
+        yield lambda b=b: Q.test_zero_block(orc, b, 1)
+        yield lambda b=b: Q.test_tail_is_zero_padded(orc, b, 0)
+        yield lambda b=b: Q.test_scale_saturates_and_underflows_bf16(orc, b)
+        yield lambda b=b: Rd.test_identical_ranks_scale_by_R(orc, b, 4, 1)
+        yield lambda b=b: Rd.test_error_bound_against_exact_sum(orc, b, 3)
+        yield lambda b=b: Q.test_codes_are_nearest_integers_clipped(orc, b)
+        yield lambda b=b: Q.test_error_bound(orc, b)
+    yield lambda: Q.test_int3_example_values(orc)
+    yield lambda: Rd.test_sum_runs_in_rank_order(orc, 0)
+    yield lambda: Rd.test_workload_c1_crafted_blocks(orc)
+    yield lambda: F.test_f16_widen_every_pattern(orc)
+    yield lambda: F.test_bf16_widen_every_pattern(orc)
+    for fmt in ("f16", "bf16"):
+        yield lambda fmt=fmt: F.test_narrow_ties_and_neighbours(orc, fmt)
+        yield lambda fmt=fmt: F.test_narrow_roundtrips_every_value(orc, fmt)
+
+
+@pytest.mark.parametrize("name,edits", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_fails_a_pin(tmp_path, name, edits):
+    src = open(SRC).read()
+    for old, new in edits:
+        assert old in src, f"mutation {name}: {old!r} not in the oracle source"
+        src = src.replace(old, new)
+    c = tmp_path / "qr_oracle.c"
+    c.write_text(src)
+    hdr = os.path.join(os.path.dirname(SRC), "qr_oracle.h")
+    (tmp_path / "qr_oracle.h").write_text(open(hdr).read())
+    so = tmp_path / f"lib_{name}.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                    str(c), "-o", str(so), "-lm"], check=True, capture_output=True)
+    caught = None
+    with oracle.using_library(str(so)):
+        for check in _battery(oracle):
+            try:
+                check()
+            except (AssertionError, ValueError) as e:  # a pin failed
+                caught = e
+                break
+    assert caught is not None, f"planted mistake {name!r} passed every pin"
