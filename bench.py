@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Benchmark of the fused quantize -> reduce -> dequantize all-reduce codec.
+
+Workload: R = 8 ranks, 2^27 bf16 values per rank (32 x 1024 x 4096, 256 MiB
+per rank, 2 GiB of input per call), N(0,1) with 8 seeded outlier channels x20.
+One step = one fused qr_allreduce at INT4 and one at INT3 over the same
+inputs (the whole hot path: send-path quantize, Phase-1B decode + fp32 sum +
+re-quantize, Phase-2 decode), two kernel launches.  The inputs (2 GiB) exceed
+the 129 MB L2, so no flush is needed between steps.
+
+Metric: input GB/s = R * N * 2 B per call / device time (1 GB = 1e9 B), and the
+dominant kernel's fraction of the measured HBM bandwidth, where its bytes are
+the algorithmic 2RN + 2N (every input read once, the output written once).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
+codec has no data-path exchange on one GPU, so there is no collective.
+`--impl reference` times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fused quant-reduce-dequant input GB/s & % of HBM roofline, R=8, INT4/INT3"
+R = 8
+N = 1 << 27
+DTYPE = workloads.BF16
+BITS = (4, 3)
+SEED = 5
+WORKLOAD = "allreduce R=8 x 32x1024x4096 bf16 per rank (256 MiB/rank), fused INT4 + INT3 per step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def set_values_per_rank(n: int) -> None:
+    global N, WORKLOAD
+    if n != N:
+        if n <= 0 or n % 2048:
+            raise SystemExit("--values-per-rank must be a positive multiple of 2048")
+        N = n
+        WORKLOAD = f"allreduce R=8 x {n} bf16 values per rank (profiling case), fused INT4 + INT3 per step"
+
+
+def tile_bytes(bits: int) -> int:
+    return 256 * bits + 128
+
+
+def config(extra=None) -> dict:
+    c = {"workload": WORKLOAD, "ranks": R, "values_per_rank": N, "storage": "bf16",
+         "bits": list(BITS), "data": "synthetic N(0,1) + 8 outlier channels x20, seed 5",
+         "l2": "inputs larger than L2 (2 GiB per call vs 129 MB L2): no flush",
+         "scaling_mode": "replicas (no data-path exchange on one GPU)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def host_inputs(n: int | None = None) -> list[np.ndarray]:
+    n = N if n is None else n
+    with cf.ThreadPoolExecutor(min(R, os.cpu_count() or 1)) as ex:
+        return list(ex.map(lambda r: workloads.sweep_rank(r, n, DTYPE, SEED), range(R)))
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_tiles(orc, xs, bits, t0, t1):
+    return orc.allreduce(bits, DTYPE, [x[t0 * 2048: t1 * 2048] for x in xs])
+
+
+def oracle_run(orc, xs, tiles, threads, start=0):
+    """All-reduce `tiles` consecutive tiles (from `start`, wrapping) at every
+    bit width, split across `threads` threads (ctypes releases the GIL)."""
+    T = N // 2048
+    chunks = []
+    per = -(-tiles // threads)
+    for i in range(threads):
+        a = i * per
+        b = min(tiles, a + per)
+        if a < b:
+            chunks.append(((start + a) % T, (start + a) % T + (b - a)))
+    chunks = [(a, min(b, T)) for a, b in chunks]
+
+    def work(c):
+        for bits in BITS:
+            _oracle_tiles(orc, xs, bits, c[0], c[1])
+
+    with cf.ThreadPoolExecutor(len(chunks)) as ex:
+        list(ex.map(work, chunks))
+    return sum(b - a for a, b in chunks)
+
+
+def oracle_calibrate(orc, xs, threads) -> float:
+    """Seconds of wall time per tile (all ranks, every bit width) on `threads` threads."""
+    tiles = 4 * threads
+    oracle_run(orc, xs, tiles, threads)
+    t = time.perf_counter()
+    done = oracle_run(orc, xs, tiles, threads, start=tiles)
+    return (time.perf_counter() - t) / done
+
+
+def cpu_baseline(xs, budget_s=12.0) -> dict:
+    import oracle as orc
+    orc.build()
+    threads = os.cpu_count() or 1
+    per_tile = oracle_calibrate(orc, xs, threads)
+    tiles = int(max(threads, min(N // 2048, budget_s / per_tile)))
+    t = time.perf_counter()
+    done = oracle_run(orc, xs, tiles, threads)
+    dt = time.perf_counter() - t
+    gbs = done * 2048 * R * 2 * len(BITS) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {done} of {N // 2048} tiles of every rank, INT4 and INT3, "
+                      f"{threads} threads, {dt:.1f} s wall"}
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle as orc
+    orc.build()
+    xs = host_inputs()
+    threads = os.cpu_count() or 1
+    per_tile = oracle_calibrate(orc, xs, threads)
+    budget_s = 150.0
+    step_tiles = int(max(1, min(N // 2048, budget_s / (args.steps + args.warmup) / per_tile)))
+    pos = 0
+    for _ in range(args.warmup):
+        pos += oracle_run(orc, xs, step_tiles, min(threads, step_tiles), start=pos)
+    t = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        k = oracle_run(orc, xs, step_tiles, min(threads, step_tiles), start=pos)
+        pos += k
+        done += k
+    dt = time.perf_counter() - t
+    gbs = done * 2048 * R * 2 * len(BITS) / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config({"reference_step": f"{step_tiles} tiles of every rank, INT4 and INT3"}),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{step_tiles} consecutive tiles per step (of {N // 2048}), "
+                                   f"{threads} threads"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.out = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [[c.strip() for c in ln.split(",")] for ln in out.splitlines() if ln.count(",") >= 7]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        smax = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)}
+
+
+def _gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+def measured_hbm() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: copy bandwidth)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "bit_quantized_all_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str) -> tuple[float | None, str]:
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None, "no ncu capture committed"
+    e = d.get(kernel)
+    if not e:
+        return None, f"no ncu capture of {kernel}"
+    if e.get("csrc_hash") != csrc_hash():
+        return None, "kernel sources changed since the ncu capture"
+    return float(e["dram_bytes_per_launch"]), e.get("source", "profiles/traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--values-per-rank", type=int, default=N,
+                    help="a smaller message for profiling captures (the default is the benchmark workload)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    set_values_per_rank(args.values_per_rank)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from bit_quantized_all_gb300 import build
+    build.build()
+    import bit_quantized_all_gb300 as qr
+
+    xs_host = host_inputs()
+    tdt = torch.bfloat16
+    pinned = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+    xs = [p.to(dev, non_blocking=True).view(tdt) for p in pinned]
+    ys = {b: torch.empty(N, dtype=tdt, device=dev) for b in BITS}
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for b in BITS:
+            qr.qr_allreduce(b, xs, y=ys[b], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: K steps, per-launch events on the launching stream
+    ev = {b: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for b in BITS}
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(_gpu_uuid(torch, dev))
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        for b in BITS:
+            ev[b][i][0].record(stream)
+            qr.qr_allreduce(b, xs, y=ys[b], stream=stream)
+            ev[b][i][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    in_bytes_call = R * N * 2
+    value = world * args.steps * len(BITS) * in_bytes_call / (elapsed_ms / 1e3) / 1e9
+
+    peak, peak_src = measured_hbm()
+    kernels = {}
+    for b in BITS:
+        d = [s.elapsed_time(e) for s, e in ev[b]]
+        avg = sum(d) / len(d)
+        alg = R * N * 2 + N * 2
+        kernels[b] = {"kernel": f"allreduce_kernel<{b},bf16>", "launches": len(d), "avg_ms": avg,
+                      "median_ms": statistics.median(d), "total_ms": sum(d),
+                      "input_gbs": in_bytes_call / (avg / 1e3) / 1e9,
+                      "achieved_gbs": alg / (avg / 1e3) / 1e9, "alg_bytes": alg}
+    dom = max(BITS, key=lambda b: kernels[b]["total_ms"])
+    k = kernels[dom]
+    traffic, traffic_src = profiled_traffic(k["kernel"])
+    roofline = {"bound": "hbm", "achieved": round(k["achieved_gbs"], 2), "peak": peak, "unit": "GB/s",
+                "frac": round(k["achieved_gbs"] / peak, 4), "traffic": traffic,
+                "kernel": k["kernel"], "alg_bytes_per_launch": k["alg_bytes"],
+                "avg_launch_ms": round(k["avg_ms"], 5), "peak_source": peak_src,
+                "traffic_source": traffic_src,
+                "all_kernels": {f"INT{b}": {"achieved_gbs": round(kernels[b]["achieved_gbs"], 2),
+                                            "frac": round(kernels[b]["achieved_gbs"] / peak, 4),
+                                            "input_gbs": round(kernels[b]["input_gbs"], 2),
+                                            "avg_ms": round(kernels[b]["avg_ms"], 5),
+                                            "median_ms": round(kernels[b]["median_ms"], 5),
+                                            "share": round(kernels[b]["total_ms"] /
+                                                           sum(kk["total_ms"] for kk in kernels.values()), 4)}
+                                for b in BITS}}
+
+    # ---- end to end through the public API: pinned host -> device, both
+    # all-reduces, device -> pinned host of both results, every step
+    host_out = {b: torch.empty(N, dtype=tdt).pin_memory() for b in BITS}
+
+    def e2e_step():
+        for r in range(R):
+            xs[r].view(torch.int16).copy_(pinned[r], non_blocking=True)
+        for b in BITS:
+            qr.qr_allreduce(b, xs, y=ys[b], stream=stream)
+            host_out[b].copy_(ys[b], non_blocking=True)
+
+    e2e = None
+    if args.e2e_steps > 0:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e_value = world * args.e2e_steps * len(BITS) * in_bytes_call / (e2e_ms / 1e3) / 1e9
+        e2e = {"value": round(e2e_value, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": R * N * 2, "d2h_bytes_per_step": len(BITS) * N * 2,
+               "steps": args.e2e_steps, "gpu_launches": args.e2e_steps * len(BITS),
+               "api": "qr_allreduce through the Python binding of the C ABI, pinned host buffers"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(xs_host)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config(),
+            "gpu_launches": args.steps * len(BITS),
+            "roofline": roofline,
+            "e2e": e2e,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

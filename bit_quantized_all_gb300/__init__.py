@@ -1,0 +1,302 @@
+"""Block-quantized two-shot all-reduce codec (QuickReduce / Flash
+Communication) for one GB300 GPU: Python binding of ``libqr.so``.
+
+The functions carry the names of the C ABI in ``include/qr.h``.  They only
+marshal arguments: check tensor dtypes, sizes, devices and contiguity, pick the
+caller's current stream, and call the library through ``ctypes``.  Every step
+of the codec runs in the library's CUDA kernels; there is no CPU path.  If
+``libqr.so`` has not been built, every call raises.
+
+Tensors: fp16 / bf16 messages are ``torch.float16`` / ``torch.bfloat16`` CUDA
+tensors (any shape, contiguous; n = numel); wires are ``torch.uint8`` CUDA
+tensors of at least ``qr_wire_bytes(bits, n)`` bytes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqr.so")
+
+QR_OK = 0
+QR_ERR_INVALID_ARG = 1
+QR_ERR_UNSUPPORTED = 2
+QR_ERR_MISALIGNED = 3
+QR_ERR_SIZE = 4
+QR_ERR_CUDA = 5
+
+QR_FP16 = 0
+QR_BF16 = 1
+QR_MAX_RANKS = 8
+BITS = (3, 4, 6, 8)
+
+EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_segment_reduce",
+           "qr_decode", "qr_allreduce", "qr_allreduce_emit", "qr_allreduce_ctas", "qr_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QRError(RuntimeError):
+    """A qr_* call returned a status other than QR_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libqr.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is not built; run bit_quantized_all_gb300.build.build() "
+                    "(needs nvcc). There is no CPU fallback.")
+            L = ctypes.CDLL(LIB_PATH)
+            vp = ctypes.c_void_p
+            sz = ctypes.c_size_t
+            i32 = ctypes.c_int
+            vpp = ctypes.POINTER(ctypes.c_void_p)
+            sig = {
+                "qr_tile_values": (sz, []),
+                "qr_tile_bytes": (sz, [i32]),
+                "qr_wire_bytes": (sz, [i32, sz]),
+                "qr_encode": (i32, [i32, i32, vp, sz, vp, vp]),
+                "qr_segment_reduce": (i32, [i32, i32, vpp, sz, vp, vp]),
+                "qr_decode": (i32, [i32, i32, vp, sz, vp, vp]),
+                "qr_allreduce": (i32, [i32, i32, i32, vpp, sz, vp, vp]),
+                "qr_allreduce_emit": (i32, [i32, i32, i32, vpp, sz, vp, vpp, vp, vp]),
+                "qr_allreduce_ctas": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
+                "qr_status_string": (ctypes.c_char_p, [i32]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().qr_status_string(status).decode()
+
+
+def _ptr_array(ptrs):
+    """A host array of device pointers (ints or None) for the C ABI."""
+    if ptrs is None:
+        return None
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+def _check(status: int, where: str) -> None:
+    if status != QR_OK:
+        raise QRError(status, where)
+
+
+# ---------------------------------------------------------------------------
+# raw C ABI: integer device pointers, integer stream handle, status returned
+# ---------------------------------------------------------------------------
+class capi:
+    """Direct calls of the C ABI with raw pointers; each returns the status."""
+
+    @staticmethod
+    def qr_encode(bits, dtype, x, n, wire, stream=None):
+        return lib().qr_encode(bits, dtype, x, n, wire, stream)
+
+    @staticmethod
+    def qr_decode(bits, dtype, wire, n, y, stream=None):
+        return lib().qr_decode(bits, dtype, wire, n, y, stream)
+
+    @staticmethod
+    def qr_segment_reduce(bits, R, wires, n, out, stream=None):
+        return lib().qr_segment_reduce(bits, R, _ptr_array(wires), n, out, stream)
+
+    @staticmethod
+    def qr_allreduce(bits, dtype, R, xs, n, y, stream=None):
+        return lib().qr_allreduce(bits, dtype, R, _ptr_array(xs), n, y, stream)
+
+    @staticmethod
+    def qr_allreduce_emit(bits, dtype, R, xs, n, y, wire_out, red_out, stream=None):
+        return lib().qr_allreduce_emit(bits, dtype, R, _ptr_array(xs), n, y, _ptr_array(wire_out),
+                                       red_out, stream)
+
+    @staticmethod
+    def qr_allreduce_ctas(bits, dtype, R, xs, n, y, ctas, stream=None):
+        return lib().qr_allreduce_ctas(bits, dtype, R, _ptr_array(xs), n, y, ctas, stream)
+
+
+# ---------------------------------------------------------------------------
+# sizes
+# ---------------------------------------------------------------------------
+def qr_tile_values() -> int:
+    return int(lib().qr_tile_values())
+
+
+def qr_tile_bytes(bits: int) -> int:
+    return int(lib().qr_tile_bytes(bits))
+
+
+def qr_wire_bytes(bits: int, n: int) -> int:
+    return int(lib().qr_wire_bytes(bits, n))
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor front end
+# ---------------------------------------------------------------------------
+_DTYPES = {torch.float16: QR_FP16, torch.bfloat16: QR_BF16}
+_TORCH = {QR_FP16: torch.float16, QR_BF16: torch.bfloat16}
+
+
+def _dtype_code(t: torch.Tensor, what: str) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"{what} must be torch.float16 or torch.bfloat16, got {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def _cuda_contig(t: torch.Tensor, what: str) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+
+
+def _wire_tensor(t: torch.Tensor, bits: int, n: int, what: str) -> None:
+    _cuda_contig(t, what)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{what} must be torch.uint8 (a packed wire), got {t.dtype}")
+    need = qr_wire_bytes(bits, n)
+    if t.numel() < need:
+        raise ValueError(f"{what} holds {t.numel()} bytes; {need} are needed for {n} values at INT{bits}")
+
+
+def _stream(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _same_device(ts, what):
+    dev = ts[0].device
+    for t in ts:
+        if t.device != dev:
+            raise ValueError(f"{what}: every tensor must be on {dev}")
+    return dev
+
+
+def new_wire(bits: int, n: int, device) -> torch.Tensor:
+    """An uninitialised wire buffer for an n-value message."""
+    return torch.empty(qr_wire_bytes(bits, n), dtype=torch.uint8, device=device)
+
+
+def qr_encode(bits: int, x: torch.Tensor, wire: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Send path: quantize x into a packed wire (returned)."""
+    _cuda_contig(x, "x")
+    dt = _dtype_code(x, "x")
+    n = x.numel()
+    if wire is None:
+        wire = new_wire(bits, n, x.device)
+    _wire_tensor(wire, bits, n, "wire")
+    _same_device([x, wire], "qr_encode")
+    _check(capi.qr_encode(bits, dt, x.data_ptr(), n, wire.data_ptr(), _stream(x.device, stream)), "qr_encode")
+    return wire
+
+
+def qr_decode(bits: int, wire: torch.Tensor, n: int, dtype: torch.dtype = torch.bfloat16,
+              y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Receive path: decode the first n values of a wire into fp16/bf16."""
+    _wire_tensor(wire, bits, n, "wire")
+    if y is None:
+        if dtype not in _DTYPES:
+            raise TypeError(f"dtype must be torch.float16 or torch.bfloat16, got {dtype}")
+        y = torch.empty(n, dtype=dtype, device=wire.device)
+    _cuda_contig(y, "y")
+    dt = _dtype_code(y, "y")
+    if y.numel() != n:
+        raise ValueError(f"y holds {y.numel()} values, expected {n}")
+    _same_device([wire, y], "qr_decode")
+    _check(capi.qr_decode(bits, dt, wire.data_ptr(), n, y.data_ptr(), _stream(y.device, stream)), "qr_decode")
+    return y
+
+
+def qr_segment_reduce(bits: int, wires, n: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Phase-1B: decode the R wires, sum in fp32 in rank order, re-quantize."""
+    wires = list(wires)
+    if not 1 <= len(wires) <= QR_MAX_RANKS:
+        raise ValueError(f"1 to {QR_MAX_RANKS} wires are supported, got {len(wires)}")
+    for i, w in enumerate(wires):
+        _wire_tensor(w, bits, n, f"wires[{i}]")
+    if out is None:
+        out = new_wire(bits, n, wires[0].device)
+    _wire_tensor(out, bits, n, "out")
+    dev = _same_device(wires + [out], "qr_segment_reduce")
+    _check(capi.qr_segment_reduce(bits, len(wires), [w.data_ptr() for w in wires], n, out.data_ptr(),
+                                  _stream(dev, stream)), "qr_segment_reduce")
+    return out
+
+
+def _check_inputs(xs):
+    xs = list(xs)
+    if not 1 <= len(xs) <= QR_MAX_RANKS:
+        raise ValueError(f"1 to {QR_MAX_RANKS} ranks are supported, got {len(xs)}")
+    for i, x in enumerate(xs):
+        _cuda_contig(x, f"xs[{i}]")
+    dt = _dtype_code(xs[0], "xs[0]")
+    for i, x in enumerate(xs):
+        if x.dtype != xs[0].dtype:
+            raise TypeError(f"xs[{i}] is {x.dtype}; every rank must be {xs[0].dtype}")
+        if x.numel() != xs[0].numel():
+            raise ValueError(f"xs[{i}] holds {x.numel()} values; every rank must hold {xs[0].numel()}")
+    return xs, dt, xs[0].numel()
+
+
+def qr_allreduce(bits: int, xs, y: torch.Tensor | None = None, stream=None, ctas: int = 0) -> torch.Tensor:
+    """The fused two-shot all-reduce of R rank tensors (one kernel)."""
+    xs, dt, n = _check_inputs(xs)
+    if y is None:
+        y = torch.empty_like(xs[0])
+    _cuda_contig(y, "y")
+    if y.dtype != xs[0].dtype or y.numel() != n:
+        raise ValueError("y must match the inputs' dtype and size")
+    dev = _same_device(xs + [y], "qr_allreduce")
+    ptrs = [x.data_ptr() for x in xs]
+    st = _stream(dev, stream)
+    if ctas:
+        status = capi.qr_allreduce_ctas(bits, dt, len(xs), ptrs, n, y.data_ptr(), ctas, st)
+    else:
+        status = capi.qr_allreduce(bits, dt, len(xs), ptrs, n, y.data_ptr(), st)
+    _check(status, "qr_allreduce")
+    return y
+
+
+def qr_allreduce_emit(bits: int, xs, y: torch.Tensor | None = None, wire_out=None,
+                      red_out: torch.Tensor | None = None, stream=None):
+    """qr_allreduce that also returns the R Phase-1 wires and the reduced wire."""
+    xs, dt, n = _check_inputs(xs)
+    dev = _same_device(xs, "qr_allreduce_emit")
+    if y is None:
+        y = torch.empty_like(xs[0])
+    if wire_out is None:
+        wire_out = [new_wire(bits, n, dev) for _ in xs]
+    if red_out is None:
+        red_out = new_wire(bits, n, dev)
+    _cuda_contig(y, "y")
+    if y.dtype != xs[0].dtype or y.numel() != n:
+        raise ValueError("y must match the inputs' dtype and size")
+    if len(wire_out) != len(xs):
+        raise ValueError("wire_out needs one wire per rank")
+    for i, w in enumerate(wire_out):
+        _wire_tensor(w, bits, n, f"wire_out[{i}]")
+    _wire_tensor(red_out, bits, n, "red_out")
+    _same_device(xs + [y, red_out] + list(wire_out), "qr_allreduce_emit")
+    _check(capi.qr_allreduce_emit(bits, dt, len(xs), [x.data_ptr() for x in xs], n, y.data_ptr(),
+                                  [w.data_ptr() for w in wire_out], red_out.data_ptr(),
+                                  _stream(dev, stream)), "qr_allreduce_emit")
+    return y, wire_out, red_out

@@ -1,0 +1,200 @@
+// qr_capi.cu -- the extern "C" entry points of libqr.so (declared in
+// include/qr.h): host-side argument validation, then a launch on the
+// caller's stream.  Validation runs before any CUDA call, so a rejected call
+// touches neither memory nor the device.
+//
+// Checks, in this order (the first failure is returned):
+//   1. null pointers, n == 0, R < 1                        -> QR_ERR_INVALID_ARG
+//   2. bits not in {3,4,6,8}, unknown dtype, R > 8         -> QR_ERR_UNSUPPORTED
+//   3. a byte count overflowing size_t                     -> QR_ERR_SIZE
+//   4. a device pointer not 16-byte aligned                -> QR_ERR_MISALIGNED
+//   5. an output partially overlapping another buffer      -> QR_ERR_INVALID_ARG
+// A launch error reported by the runtime                   -> QR_ERR_CUDA
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "../../include/qr.h"
+#include "qr_launch.h"
+
+#define QR_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr size_t kTile = 2048;
+
+bool bits_ok(int bits) { return bits == 3 || bits == 4 || bits == 6 || bits == 8; }
+bool dtype_ok(qr_dtype_t d) { return d == QR_FP16 || d == QR_BF16; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t tile_bytes(int bits) { return bits_ok(bits) ? size_t(256) * size_t(bits) + 128 : 0; }
+
+// ceil(n/2048) * tile_bytes, or 0 on overflow
+size_t wire_bytes(int bits, size_t n) {
+    const size_t tb = tile_bytes(bits);
+    if (tb == 0) return 0;
+    const size_t tiles = n / kTile + (n % kTile != 0);
+    if (tiles > SIZE_MAX / tb) return 0;
+    return tiles * tb;
+}
+
+// the 16-bit value buffers of n values: 2n bytes, and n must index as long long
+bool value_bytes_ok(size_t n) { return n <= (SIZE_MAX / 4); }
+
+// [a, a+na) and [b, b+nb) share a byte
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// an output may equal an input exactly (in place) but not overlap it partially
+bool bad_alias(const void *out, size_t nout, const void *in, size_t nin) {
+    return out != in && overlaps(out, nout, in, nin);
+}
+
+qr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_CUDA; }
+
+}  // namespace
+
+namespace qrk {
+
+int grid_for(const void *kernel, long long tiles, int ctas, cudaError_t *err) {
+    *err = cudaSuccess;
+    if (tiles <= 0) return 0;
+    if (ctas > 0) return static_cast<int>(tiles < ctas ? tiles : ctas);
+    int dev = 0;
+    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> resident;  // (device, kernel) -> CTAs per wave
+    int wave = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = resident.find({dev, kernel});
+        if (it != resident.end()) wave = it->second;
+    }
+    if (wave == 0) {
+        int sms = 0, per_sm = 0;
+        if ((*err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
+        if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0)) != cudaSuccess)
+            return 0;
+        wave = sms * (per_sm > 0 ? per_sm : 1);
+        std::lock_guard<std::mutex> lock(mu);
+        resident[{dev, kernel}] = wave;
+    }
+    return static_cast<int>(tiles < wave ? tiles : wave);
+}
+
+}  // namespace qrk
+
+QR_EXPORT size_t qr_tile_values(void) { return kTile; }
+
+QR_EXPORT size_t qr_tile_bytes(int bits) { return tile_bytes(bits); }
+
+QR_EXPORT size_t qr_wire_bytes(int bits, size_t n) { return wire_bytes(bits, n); }
+
+QR_EXPORT const char *qr_status_string(qr_status_t status) {
+    switch (status) {
+        case QR_OK: return "QR_OK";
+        case QR_ERR_INVALID_ARG: return "QR_ERR_INVALID_ARG: null pointer, zero size, R < 1 or partial aliasing";
+        case QR_ERR_UNSUPPORTED: return "QR_ERR_UNSUPPORTED: bits not in {3,4,6,8}, unknown dtype or R > 8";
+        case QR_ERR_MISALIGNED: return "QR_ERR_MISALIGNED: a device pointer is not 16-byte aligned";
+        case QR_ERR_SIZE: return "QR_ERR_SIZE: a byte count overflows size_t";
+        case QR_ERR_CUDA: return "QR_ERR_CUDA: the CUDA runtime reported an error";
+    }
+    return "QR_ERR_UNKNOWN: not a qr_status_t value";
+}
+
+QR_EXPORT qr_status_t qr_encode(int bits, qr_dtype_t dtype, const void *x, size_t n, void *wire,
+                                qr_stream_t stream) {
+    if (!x || !wire || n == 0) return QR_ERR_INVALID_ARG;
+    if (!bits_ok(bits) || !dtype_ok(dtype)) return QR_ERR_UNSUPPORTED;
+    const size_t W = wire_bytes(bits, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(x) || !aligned16(wire)) return QR_ERR_MISALIGNED;
+    if (overlaps(wire, W, x, 2 * n)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_encode(bits, dtype, x, static_cast<long long>(n), wire,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n, void *y,
+                                qr_stream_t stream) {
+    if (!wire || !y || n == 0) return QR_ERR_INVALID_ARG;
+    if (!bits_ok(bits) || !dtype_ok(dtype)) return QR_ERR_UNSUPPORTED;
+    const size_t W = wire_bytes(bits, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(wire) || !aligned16(y)) return QR_ERR_MISALIGNED;
+    if (overlaps(y, 2 * n, wire, W)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_decode(bits, dtype, wire, static_cast<long long>(n), y,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires, size_t n,
+                                        void *out_wire, qr_stream_t stream) {
+    if (!wires || !out_wire || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!wires[r]) return QR_ERR_INVALID_ARG;
+    if (!bits_ok(bits) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    const size_t W = wire_bytes(bits, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(out_wire)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(wires[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (bad_alias(out_wire, W, wires[r], W)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_reduce(bits, R, wires, static_cast<long long>(n), out_wire,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+qr_status_t allreduce_common(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n, void *y,
+                             void *const *wire_out, void *red_out, int ctas, qr_stream_t stream) {
+    if (!x || !y || n == 0 || R < 1 || ctas < 0) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r) {
+        if (!x[r]) return QR_ERR_INVALID_ARG;
+        if (wire_out && !wire_out[r]) return QR_ERR_INVALID_ARG;
+    }
+    if (!bits_ok(bits) || !dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    const size_t W = wire_bytes(bits, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    const size_t V = 2 * n;
+    if (!aligned16(y) || (red_out && !aligned16(red_out))) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(x[r]) || (wire_out && !aligned16(wire_out[r]))) return QR_ERR_MISALIGNED;
+    // outputs: y (may equal an input exactly), the R rank wires and the reduced wire
+    for (int r = 0; r < R; ++r) {
+        if (bad_alias(y, V, x[r], V)) return QR_ERR_INVALID_ARG;
+        if (wire_out) {
+            for (int i = 0; i < R; ++i)
+                if (overlaps(wire_out[r], W, x[i], V)) return QR_ERR_INVALID_ARG;
+            if (overlaps(wire_out[r], W, y, V)) return QR_ERR_INVALID_ARG;
+            for (int i = 0; i < r; ++i)
+                if (overlaps(wire_out[r], W, wire_out[i], W)) return QR_ERR_INVALID_ARG;
+            if (red_out && overlaps(wire_out[r], W, red_out, W)) return QR_ERR_INVALID_ARG;
+        }
+        if (red_out && overlaps(red_out, W, x[r], V)) return QR_ERR_INVALID_ARG;
+    }
+    if (red_out && overlaps(red_out, W, y, V)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_allreduce(bits, dtype, R, x, static_cast<long long>(n), y, wire_out, red_out,
+                                           ctas, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+QR_EXPORT qr_status_t qr_allreduce(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n, void *y,
+                                   qr_stream_t stream) {
+    return allreduce_common(bits, dtype, R, x, n, y, nullptr, nullptr, 0, stream);
+}
+
+QR_EXPORT qr_status_t qr_allreduce_emit(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                        void *y, void *const *wire_out, void *red_out, qr_stream_t stream) {
+    return allreduce_common(bits, dtype, R, x, n, y, wire_out, red_out, 0, stream);
+}
+
+QR_EXPORT qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                        void *y, int ctas, qr_stream_t stream) {
+    return allreduce_common(bits, dtype, R, x, n, y, nullptr, nullptr, ctas, stream);
+}

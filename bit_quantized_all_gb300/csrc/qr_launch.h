@@ -1,0 +1,24 @@
+// qr_launch.h -- internal host interface between the C ABI (qr_capi.cu) and
+// the per-kernel translation units.  Arguments arrive already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace qrk {
+
+// CTAs for a grid-stride launch over `tiles` tiles: `ctas` if positive, else
+// one full wave of resident CTAs of `kernel` on the current device; capped at
+// `tiles`.  Returns 0 (with *err set) if the device cannot be queried.
+int grid_for(const void *kernel, long long tiles, int ctas, cudaError_t *err);
+
+cudaError_t launch_encode(int bits, int dtype, const void *x, long long n, void *wire,
+                          cudaStream_t s);
+cudaError_t launch_decode(int bits, int dtype, const void *wire, long long n, void *y,
+                          cudaStream_t s);
+cudaError_t launch_reduce(int bits, int R, const void *const *wires, long long n, void *out,
+                          cudaStream_t s);
+cudaError_t launch_allreduce(int bits, int dtype, int R, const void *const *x, long long n,
+                             void *y, void *const *wire_out, void *red_out, int ctas,
+                             cudaStream_t s);
+
+}  // namespace qrk

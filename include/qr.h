@@ -1,0 +1,154 @@
+/*
+ * qr.h -- C ABI of libqr.so: the block-quantized two-shot all-reduce codec
+ * (QuickReduce / Flash Communication) on one GB300 GPU (sm_103a).
+ *
+ * R "ranks" are R buffers in the one GPU's memory.  Each rank's fp16/bf16
+ * message is cut into 2048-value tiles; every 32 values share one fp16 decode
+ * scale.  The send path quantizes a tile into a packed wire tile; Phase-1B
+ * decodes the R rank copies of a tile, sums them in fp32 and re-quantizes;
+ * Phase-2 decodes the reduced tile.  Sources:
+ *   [QR] "QuickReduce INT3 quantization and benchmarking on MI355" (AMD blog),
+ *        sections Design Highlights; Quantization and Dequantization Paths.
+ *   [FC] "Flash Communication" review record, arXiv 2412.04964, key
+ *        machinery (two quantization round trips: quantize, all-to-all, local
+ *        sum, re-quantize, all-gather, dequantize; one fused kernel).
+ *
+ * ---------------------------------------------------------------------------
+ * Arithmetic (fixed; GPU results are bit-exact against it):
+ *   per 32-value block: A = max|x|;  s = fp16_RNE(A / |qmin|), saturated at
+ *   65504, and if s == 0 every code is the bias and the stored scale is +0;
+ *   r = fp32_RN(1/s);  q = round_half_even(clip(fp32_RN(x*r), qmin, qmax));
+ *   code u = q + bias;  decode = (u - bias) * s (exact in fp32).
+ *   qmin = -2^(bits-1), qmax = 2^(bits-1) - 1, bias = 2^(bits-1).
+ *   Phase-1B: acc = sum over r = 0..R-1 (in that order, each add rounded to
+ *   fp32) of the decoded rank values; the reduced tile is the encode of acc.
+ *   Phase-2: out = fp16/bf16 round-half-even of the decoded reduced value
+ *   (an fp16 output that overflows becomes +-inf, as a native fp16 sum would).
+ *   Inputs must be finite; non-finite inputs give unspecified results.
+ *
+ * Wire format (part of the ABI): tile t of a wire starts at byte
+ * t * qr_tile_bytes(bits).  Slot k (0..255) = values 8k..8k+7 of the tile,
+ * lane j = value 8k+j; block g (0..63) = values 32g..32g+31.  Little-endian:
+ *   INT8 (2176 B): byte 8k+j = u;                              scales at 2048
+ *   INT6 (1664 B): u32 at 4k bits 4j..4j+3 = u & 15;
+ *                  u16 at 1024+2k bits 2j..2j+1 = u >> 4;      scales at 1536
+ *   INT4 (1152 B): u32 at 4k bits 4j..4j+3 = u;                scales at 1024
+ *   INT3  (896 B): u16 "q2w" at 2k bits 2j..2j+1 = u & 3;
+ *                  u8 "q1w" at 512+k bit j = u >> 2;           scales at 768
+ *   the fp16 decode scale of block g is at (scale offset) + 2g.
+ * A message of n values that is not a multiple of 2048 is zero-padded to
+ * whole tiles on the wire; decoded outputs are written for the first n values
+ * only (bytes of y past n are never touched).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions of every compute entry point:
+ *   - All pointers are DEVICE pointers on the current CUDA device, except the
+ *     arrays of R pointers (`x`, `wires`, `wire_out`), which are HOST arrays
+ *     holding R device pointers.  Every device pointer must be 16-byte aligned.
+ *   - fp16/bf16 values are raw 16-bit patterns, n values contiguous.
+ *   - The caller owns and allocates every buffer; the library allocates no
+ *     memory.  Work is enqueued asynchronously on `stream` (NULL = the legacy
+ *     default stream); buffers must stay alive until the stream has run it.
+ *   - Arguments are validated on the host before anything is enqueued; on any
+ *     error nothing is launched and no memory is read or written.
+ *   - An output may alias an input of the same call exactly (same pointer,
+ *     in-place) where noted; partial overlap is rejected.
+ *   - Calls are thread-safe.  The library keeps only a per-device cache of
+ *     launch limits (SM count, occupancy), filled on first use.
+ */
+#ifndef QR_H
+#define QR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same pointer type), declared here so that this header
+ * needs no CUDA header. */
+typedef struct CUstream_st *qr_stream_t;
+
+typedef enum {
+    QR_OK = 0,
+    QR_ERR_INVALID_ARG = 1, /* null pointer, n == 0, R < 1, partial aliasing */
+    QR_ERR_UNSUPPORTED = 2, /* bits not in {3,4,6,8}, unknown dtype, R > 8   */
+    QR_ERR_MISALIGNED = 3,  /* a device pointer not 16-byte aligned           */
+    QR_ERR_SIZE = 4,        /* a byte count overflows size_t                  */
+    QR_ERR_CUDA = 5         /* the CUDA runtime reported an error at launch   */
+} qr_status_t;
+
+typedef enum { QR_FP16 = 0, QR_BF16 = 1 } qr_dtype_t;
+
+#define QR_MAX_RANKS 8
+#define QR_TILE_VALUES 2048
+
+/* Values per tile: 2048 (the unit of [QR] Design Highlights' per-rank tile). */
+size_t qr_tile_values(void);
+
+/* Bytes of one wire tile: 256*bits + 128 (codes, then 64 fp16 scales);
+ * 1152 for INT4 and 896 for INT3 as printed in [QR] Design Highlights.
+ * 0 if bits is not one of 3, 4, 6, 8. */
+size_t qr_tile_bytes(int bits);
+
+/* Bytes of the wire of an n-value message: ceil(n/2048) * qr_tile_bytes(bits);
+ * 0 if bits is unsupported or the product overflows size_t. */
+size_t qr_wire_bytes(int bits, size_t n);
+
+/* Send path ([QR] Quantization and Dequantization Paths, CodecQ3::send and
+ * its INT4/INT6/INT8 counterparts): quantize n fp16/bf16 values `x` into
+ * `wire` (qr_wire_bytes(bits, n) bytes).  `wire` must not overlap `x`. */
+qr_status_t qr_encode(int bits, qr_dtype_t dtype, const void *x, size_t n,
+                      void *wire, qr_stream_t stream);
+
+/* Phase-1B in-segment reduction ([QR] Quantization and Dequantization Paths;
+ * [FC] key machinery "sums locally, re-quantizes the partial sums"): decode
+ * the R wires (host array of R device pointers, each qr_wire_bytes(bits, n)
+ * bytes), add them in fp32 in rank order, re-quantize into `out_wire`.
+ * 1 <= R <= 8.  `out_wire` may equal one of `wires` exactly. */
+qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires,
+                              size_t n, void *out_wire, qr_stream_t stream);
+
+/* Receive path / Phase-2 ([QR] Quantization and Dequantization Paths,
+ * CodecQ3::recv): decode the first n values of `wire` into fp16/bf16 `y`.
+ * The wire does not record its dtype; that is the caller's contract.
+ * `y` must not overlap `wire`. */
+qr_status_t qr_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n,
+                      void *y, qr_stream_t stream);
+
+/* The fused two-shot all-reduce ([FC] key machinery, a single fused kernel
+ * with two quantization round trips): y = decode(segment_reduce(encode(x[0]),
+ * ..., encode(x[R-1]))), in one pass over HBM with every intermediate on
+ * chip.  `x` is a host array of R device pointers to n values each; 1 <= R
+ * <= 8.  `y` (n values) may equal one of the x[r] exactly (in-place). */
+qr_status_t qr_allreduce(int bits, qr_dtype_t dtype, int R,
+                         const void *const *x, size_t n, void *y,
+                         qr_stream_t stream);
+
+/* qr_allreduce that also writes what a real two-shot exchange would send:
+ * `wire_out` (NULL, or a host array of R device pointers) receives each
+ * rank's Phase-1 wire, byte-identical to qr_encode; `red_out` (NULL or a
+ * device pointer) receives the reduced wire, byte-identical to
+ * qr_segment_reduce.  Each is qr_wire_bytes(bits, n) bytes and must not
+ * overlap any other buffer of the call. */
+qr_status_t qr_allreduce_emit(int bits, qr_dtype_t dtype, int R,
+                              const void *const *x, size_t n, void *y,
+                              void *const *wire_out, void *red_out,
+                              qr_stream_t stream);
+
+/* qr_allreduce with an explicit persistent-grid size: `ctas` CTAs of 256
+ * threads (0 = the library's choice, one full wave of resident CTAs).  The
+ * result does not depend on `ctas`; it is the SM-count knob of [FC] key
+ * machinery ("tuning the number of streaming multiprocessors"). */
+qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R,
+                              const void *const *x, size_t n, void *y,
+                              int ctas, qr_stream_t stream);
+
+/* A static string naming a status code (never NULL). */
+const char *qr_status_string(qr_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QR_H */

@@ -1,0 +1,165 @@
+"""The C ABI boundary, without a GPU.
+
+- libqr.so loads and exports every function include/qr.h declares;
+- the size functions follow their closed forms (1152 B INT4 and 896 B INT3
+  tiles, printed in "QuickReduce INT3 quantization and benchmarking on
+  MI355", Design Highlights);
+- each validation error is returned for invalid arguments.  Every call here
+  fails validation, which the library does on the host before any CUDA call,
+  so nothing is launched and no pointer is dereferenced (the pointers are
+  made-up addresses);
+- the binding fails loudly when the library is missing, and the product
+  package never touches the oracle.
+"""
+import os
+import re
+
+import pytest
+
+import bit_quantized_all_gb300 as qr
+from bit_quantized_all_gb300 import capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qr.h")
+
+A = 0x7F0000000000  # made-up, 16-byte aligned "device" addresses: never dereferenced
+B = 0x7F1000000000
+Y = 0x7F2000000000
+
+
+# The validation tests pass made-up addresses.  Where a GPU can be reached, a
+# validation bug would launch a kernel on them, so they run only where none can.
+no_gpu_only = pytest.mark.skipif(
+    __import__("torch").cuda.is_available(),
+    reason="made-up device addresses are only passed where no GPU can be reached")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bit_quantized_all_gb300 import build
+    build.build()
+    qr.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qr_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert "qr_allreduce" in names and "qr_encode" in names
+    L = qr.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(qr.EXPORTS)
+
+
+def test_sizes():
+    assert qr.qr_tile_values() == 2048
+    assert qr.qr_tile_bytes(4) == 1152 and qr.qr_tile_bytes(3) == 896
+    assert qr.qr_tile_bytes(8) == 2176 and qr.qr_tile_bytes(6) == 1664
+    for b in (0, 1, 2, 5, 7, 9, 16, -4):
+        assert qr.qr_tile_bytes(b) == 0
+        assert qr.qr_wire_bytes(b, 100) == 0
+    for b in (3, 4, 6, 8):
+        tb = qr.qr_tile_bytes(b)
+        assert qr.qr_wire_bytes(b, 0) == 0
+        assert qr.qr_wire_bytes(b, 1) == tb
+        assert qr.qr_wire_bytes(b, 2048) == tb
+        assert qr.qr_wire_bytes(b, 2049) == 2 * tb
+        assert qr.qr_wire_bytes(b, 2048 * 65536) == 65536 * tb
+        for n in (2**64 - 1, 2**62 + 5, 2**60):
+            tiles = -(-n // 2048)
+            exact = tiles * tb
+            assert qr.qr_wire_bytes(b, n) == (exact if exact < 2**64 else 0)  # 0 on size_t overflow
+
+
+def test_status_strings():
+    for code, stem in [(0, "QR_OK"), (1, "QR_ERR_INVALID_ARG"), (2, "QR_ERR_UNSUPPORTED"),
+                       (3, "QR_ERR_MISALIGNED"), (4, "QR_ERR_SIZE"), (5, "QR_ERR_CUDA")]:
+        assert qr.status_string(code).startswith(stem)
+    assert qr.status_string(99).startswith("QR_ERR_UNKNOWN")
+
+
+@no_gpu_only
+def test_encode_decode_validation():
+    n = 4096
+    assert capi.qr_encode(4, 0, A, 0, B) == qr.QR_ERR_INVALID_ARG          # n == 0
+    assert capi.qr_encode(4, 0, None, n, B) == qr.QR_ERR_INVALID_ARG       # null x
+    assert capi.qr_encode(4, 0, A, n, None) == qr.QR_ERR_INVALID_ARG       # null wire
+    assert capi.qr_encode(5, 0, A, n, B) == qr.QR_ERR_UNSUPPORTED          # bits
+    assert capi.qr_encode(4, 2, A, n, B) == qr.QR_ERR_UNSUPPORTED          # dtype
+    assert capi.qr_encode(4, 0, A, 2**63, B) == qr.QR_ERR_SIZE             # 2n overflows
+    assert capi.qr_encode(4, 0, A + 8, n, B) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_encode(4, 0, A, n, B + 2) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_encode(4, 0, A, n, A + 1024) == qr.QR_ERR_INVALID_ARG   # wire overlaps x
+    assert capi.qr_encode(4, 0, A, n, A) == qr.QR_ERR_INVALID_ARG          # even exactly
+    assert capi.qr_decode(3, 1, A, 0, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_decode(3, 1, None, n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_decode(2, 1, A, n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_decode(3, -1, A, n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_decode(3, 1, A + 4, n, Y) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_decode(3, 1, A, n, A + 16) == qr.QR_ERR_INVALID_ARG    # y overlaps wire
+
+
+@no_gpu_only
+def test_reduce_validation():
+    n = 2048 * 3
+    W = qr.qr_wire_bytes(4, n)
+    assert capi.qr_segment_reduce(4, 0, [A], n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_segment_reduce(4, 2, [A, None], n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_segment_reduce(4, 2, [A, B], n, None) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_segment_reduce(4, 2, None, n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_segment_reduce(4, 9, [A + 16 * i for i in range(9)], n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_segment_reduce(7, 2, [A, B], n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_segment_reduce(4, 2, [A, B + 8], n, Y) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_segment_reduce(4, 2, [A, B], n, A + W - 16) == qr.QR_ERR_INVALID_ARG  # partial overlap
+    assert capi.qr_segment_reduce(4, 2, [A, B], 2**62 * 3, Y) == qr.QR_ERR_SIZE
+
+
+@no_gpu_only
+def test_allreduce_validation():
+    n = 2048 * 2 + 37
+    V = 2 * n
+    W = qr.qr_wire_bytes(3, n)
+    xs = [A, B]
+    assert capi.qr_allreduce(3, 0, 2, xs, 0, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce(3, 0, 0, xs, n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce(3, 0, 2, [A, None], n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce(3, 0, 2, xs, n, None) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce(3, 0, 9, [A + 4096 * i for i in range(9)], n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_allreduce(1, 0, 2, xs, n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_allreduce(3, 5, 2, xs, n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_allreduce(3, 0, 2, [A, B + 2], n, Y) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_allreduce(3, 0, 2, xs, n, Y + 8) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_allreduce(3, 0, 2, xs, n, A + 16) == qr.QR_ERR_INVALID_ARG   # y partially overlaps x[0]
+    assert capi.qr_allreduce(3, 0, 2, xs, n, B - 4096) == qr.QR_ERR_INVALID_ARG  # y's end overlaps x[1]
+    assert capi.qr_allreduce(3, 0, 2, xs, 2**63, Y) == qr.QR_ERR_SIZE
+    assert capi.qr_allreduce_ctas(3, 0, 2, xs, n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    # emit: every output disjoint from every other buffer
+    wo = [Y + 2**20, Y + 2**21]
+    assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, [wo[0], None], None) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, [wo[0], A], None) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, [wo[0], wo[0] + W - 16], None) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, wo, wo[1]) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, wo, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, wo, Y + 2**22 + 8) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, [wo[0], wo[1] + 4], None) == qr.QR_ERR_MISALIGNED
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(qr, "LIB_PATH", str(tmp_path / "missing" / "libqr.so"))
+    monkeypatch.setattr(qr, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        qr.qr_tile_bytes(4)
+
+
+def test_product_package_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "bit_quantized_all_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\boracle\b|qr_oracle|liboracle|orc_", text), f

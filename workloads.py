@@ -84,8 +84,10 @@ def c4_rank(r: int) -> np.ndarray:
 def sweep_rank(r: int, n: int, dtype: int, seed: int = 5) -> np.ndarray:
     x = _rng(seed + 1000 * r).standard_normal(n, dtype=np.float32)
     ch = _rng(seed).choice(4096, size=8, replace=False)
-    col = np.arange(n) % 4096
-    x[np.isin(col, ch)] *= 20.0
+    full = (n // 4096) * 4096  # rows of 4096 channels; channel = value index mod 4096
+    x[:full].reshape(-1, 4096)[:, ch] *= 20.0
+    tail = x[full:]
+    tail[np.isin(np.arange(tail.size), ch)] *= 20.0
     return to_bits(x, dtype)
 
 
