@@ -218,6 +218,24 @@ def _gpu_uuid(torch, dev) -> str | None:
 
 
 # ---------------------------------------------------------------------------
+# replicas: every rank runs the whole workload on its own GPU; the job's time
+# is the slowest rank's, its throughput the units of all ranks over that time
+# ---------------------------------------------------------------------------
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, calls: int, bytes_per_call: int, elapsed_ms: float) -> float:
+    return world * calls * bytes_per_call / (elapsed_ms / 1e3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # roofline helpers
 # ---------------------------------------------------------------------------
 def measured_hbm() -> tuple[float, str]:
@@ -329,13 +347,9 @@ def main() -> None:
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), dev)
     in_bytes_call = R * N * 2
-    value = world * args.steps * len(BITS) * in_bytes_call / (elapsed_ms / 1e3) / 1e9
+    value = whole_job_gbs(world, args.steps * len(BITS), in_bytes_call, elapsed_ms)
 
     peak, peak_src = measured_hbm()
     kernels = {}
@@ -388,12 +402,8 @@ def main() -> None:
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e_value = world * args.e2e_steps * len(BITS) * in_bytes_call / (e2e_ms / 1e3) / 1e9
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e_value = whole_job_gbs(world, args.e2e_steps * len(BITS), in_bytes_call, e2e_ms)
         e2e = {"value": round(e2e_value, 2), "unit": "GB/s",
                "h2d_bytes_per_step": R * N * 2, "d2h_bytes_per_step": len(BITS) * N * 2,
                "steps": args.e2e_steps, "gpu_launches": args.e2e_steps * len(BITS),
