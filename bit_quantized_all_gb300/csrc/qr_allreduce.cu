@@ -1,4 +1,6 @@
 // qr_allreduce.cu -- launcher of the fused two-shot kernel (allreduce_kernel).
+#include <cstdint>
+
 #include "qr_kernels.cuh"
 #include "qr_launch.h"
 
@@ -15,9 +17,12 @@ static cudaError_t run_allreduce(int R, const void *const *x, long long n, void 
         wp.p[r] = wire_out ? wire_out[r] : nullptr;
     }
     const bool emit = (wire_out != nullptr) || (red_out != nullptr);
+    bool aligned32 = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
+    for (int r = 0; r < R; ++r) aligned32 = aligned32 && (reinterpret_cast<uintptr_t>(x[r]) & 31u) == 0;
+    if (!emit && aligned32) return run_allreduce16<B, DT>(R, xp, n, y, ctas, s);
     auto kern = emit ? allreduce_kernel<B, DT, true> : allreduce_kernel<B, DT, false>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), T, ctas, &err);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, ctas, &err);
     if (grid <= 0) return err;
     kern<<<grid, kThreads, 0, s>>>(xp, R, n, static_cast<uint16_t *>(y), wp, static_cast<uint8_t *>(red_out), T);
     return cudaGetLastError();

@@ -1,0 +1,38 @@
+// qr_allreduce16.cuh -- launcher of the 16-values-per-thread fused kernel
+// (allreduce16_kernel), dispatching R to a compile-time constant.  Each
+// qr_allreduce16_b<B>.cu instantiates it for one code width so that the
+// widths compile in parallel.
+#pragma once
+
+#include "qr_kernels.cuh"
+#include "qr_launch.h"
+
+namespace qrk {
+
+template <int B, int DT, int R>
+static cudaError_t run_allreduce16_r(const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s) {
+    const long long T = (n + kTileValues - 1) / kTileValues;
+    auto kern = allreduce16_kernel<B, DT, R>;
+    cudaError_t err = cudaSuccess;
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads16, T, ctas, &err);
+    if (grid <= 0) return err;
+    kern<<<grid, kThreads16, 0, s>>>(xp, n, static_cast<uint16_t *>(y), T);
+    return cudaGetLastError();
+}
+
+template <int B, int DT>
+cudaError_t run_allreduce16(int R, const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s) {
+    switch (R) {
+        case 1: return run_allreduce16_r<B, DT, 1>(xp, n, y, ctas, s);
+        case 2: return run_allreduce16_r<B, DT, 2>(xp, n, y, ctas, s);
+        case 3: return run_allreduce16_r<B, DT, 3>(xp, n, y, ctas, s);
+        case 4: return run_allreduce16_r<B, DT, 4>(xp, n, y, ctas, s);
+        case 5: return run_allreduce16_r<B, DT, 5>(xp, n, y, ctas, s);
+        case 6: return run_allreduce16_r<B, DT, 6>(xp, n, y, ctas, s);
+        case 7: return run_allreduce16_r<B, DT, 7>(xp, n, y, ctas, s);
+        case 8: return run_allreduce16_r<B, DT, 8>(xp, n, y, ctas, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qrk

@@ -1,0 +1,7 @@
+// qr_allreduce16_b8.cu -- INT8 instances of the 16-values-per-thread fused kernel.
+#include "qr_allreduce16.cuh"
+
+namespace qrk {
+template cudaError_t run_allreduce16<8, 0>(int, const ConstPtrs &, long long, void *, int, cudaStream_t);
+template cudaError_t run_allreduce16<8, 1>(int, const ConstPtrs &, long long, void *, int, cudaStream_t);
+}  // namespace qrk

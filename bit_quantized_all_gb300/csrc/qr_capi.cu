@@ -61,7 +61,7 @@ qr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_
 
 namespace qrk {
 
-int grid_for(const void *kernel, long long tiles, int ctas, cudaError_t *err) {
+int grid_for(const void *kernel, int threads, long long tiles, int ctas, cudaError_t *err) {
     *err = cudaSuccess;
     if (tiles <= 0) return 0;
     if (ctas > 0) return static_cast<int>(tiles < ctas ? tiles : ctas);
@@ -78,7 +78,7 @@ int grid_for(const void *kernel, long long tiles, int ctas, cudaError_t *err) {
     if (wave == 0) {
         int sms = 0, per_sm = 0;
         if ((*err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
-        if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0)) != cudaSuccess)
+        if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0)) != cudaSuccess)
             return 0;
         wave = sms * (per_sm > 0 ? per_sm : 1);
         std::lock_guard<std::mutex> lock(mu);

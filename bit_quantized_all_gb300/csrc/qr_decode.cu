@@ -9,7 +9,7 @@ static cudaError_t run_decode(const void *wire, long long n, void *y, cudaStream
     const long long T = (n + kTileValues - 1) / kTileValues;
     auto kern = decode_kernel<B, DT>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), T, 0, &err);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, 0, &err);
     if (grid <= 0) return err;
     kern<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t *>(wire), n, static_cast<uint16_t *>(y), T);
     return cudaGetLastError();

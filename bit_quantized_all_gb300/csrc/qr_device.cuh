@@ -361,6 +361,129 @@ __device__ __forceinline__ void store_scale(uint8_t *tile, int k, uint32_t bits)
 }
 
 // ---------------------------------------------------------------------------
+// 16 values per thread (two slots, 32 bytes of fp16/bf16): two threads per
+// block.  Used by the fused kernel when every pointer is 32-byte aligned.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void ld_stream32(const void *p, uint32_t (&w)[8]) {
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(p));
+}
+
+__device__ __forceinline__ void st_global32(void *p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// 16 values at `base` of an n-value message as 8 packed words; values at or
+// past n are +0.
+__device__ __forceinline__ void load16(const uint16_t *x, long long base, long long n, bool full,
+                                       uint32_t (&w)[8]) {
+    if (full) {
+        ld_stream32(x + base, w);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = (base + 2 * i < n) ? x[base + 2 * i] : 0u;
+            const uint32_t hi = (base + 2 * i + 1 < n) ? x[base + 2 * i + 1] : 0u;
+            w[i] = lo | (hi << 16);
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void widen16(const uint32_t (&w)[8], float2 (&v)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if constexpr (DT == 1) {
+            v[i].x = __uint_as_float(w[i] << 16);
+            v[i].y = __uint_as_float(w[i] & 0xFFFF0000u);
+        } else {
+            v[i] = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        }
+    }
+}
+
+// Absolute maximum of this thread's 16 values and its partner lane's.
+__device__ __forceinline__ float pair_absmax(const float2 (&v)[8]) {
+    float a = fmaxf(fabsf(v[0].x), fabsf(v[0].y));
+#pragma unroll
+    for (int i = 1; i < 8; ++i) a = fmaxf(a, fmaxf(fabsf(v[i].x), fabsf(v[i].y)));
+    return fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+}
+
+struct BlockScale2 {
+    float s, r;
+    uint32_t bits;
+    bool low_clip;  // the lower clip can change a code for this block (see below)
+};
+
+// The block scale of block_scale(), plus whether the lower clip at qmin can
+// matter.  For a normal, unsaturated fp16 scale, s = RN16(A/|qmin|) is within
+// 2^-11 (relative) of A/|qmin|, so every t = RN(x * RN(1/s)) with |x| <= A is
+// at least -|qmin|*(1 + 2^-10.9) > qmin - 1/2: it rounds to qmin or above and
+// only the upper clip is needed.  A zero scale gives t = 0.  Only a subnormal
+// scale (rounded far below A/|qmin|) or a saturated one (A/|qmin| > 65504)
+// can take t below qmin - 1/2.
+template <int B>
+__device__ __forceinline__ BlockScale2 block_scale2(float absmax) {
+    const float d = __fmul_rn(absmax, Codec<B>::kInvBias);
+    uint32_t h = __half_as_ushort(__float2half_rn(d));
+    BlockScale2 sc;
+    sc.low_clip = (h == 0x7C00u) || (h - 1u < 0x3FFu);  // saturated, or subnormal and nonzero
+    if (h == 0x7C00u) h = 0x7BFFu;
+    sc.bits = h;
+    sc.s = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+    sc.r = (h == 0u) ? 0.0f : __frcp_rn(sc.s);
+    return sc;
+}
+
+// q = RNE(clip(RN(v * r), qmin, qmax)) as exact integer floats, two at a time.
+// `low_clip` must be uniform across the warp.
+template <int B>
+__device__ __forceinline__ void quantize16(const float2 (&v)[8], float r, bool low_clip, float2 (&q)[8]) {
+    const float2 r2 = make_float2(r, r);
+    const float2 m2 = make_float2(kRoundMagic, kRoundMagic);
+    const float2 nm2 = make_float2(-kRoundMagic, -kRoundMagic);
+    if (low_clip) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float2 t = __fmul2_rn(v[i], r2);
+            t.x = fminf(fmaxf(t.x, Codec<B>::kQmin), Codec<B>::kQmax);
+            t.y = fminf(fmaxf(t.y, Codec<B>::kQmin), Codec<B>::kQmax);
+            q[i] = __fadd2_rn(__fadd2_rn(t, m2), nm2);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float2 t = __fmul2_rn(v[i], r2);
+            t.x = fminf(t.x, Codec<B>::kQmax);
+            t.y = fminf(t.y, Codec<B>::kQmax);
+            q[i] = __fadd2_rn(__fadd2_rn(t, m2), nm2);
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void store16(uint16_t *y, long long base, long long n, bool full,
+                                        const float2 (&o)[8]) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = narrow2<DT>(o[i].x, o[i].y);
+    if (full) {
+        st_global32(y + base, w);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (base + 2 * i < n) y[base + 2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+            if (base + 2 * i + 1 < n) y[base + 2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // kernel parameter blocks (R pointers travel by value)
 // ---------------------------------------------------------------------------
 struct ConstPtrs {

@@ -7,9 +7,10 @@
 namespace qrk {
 
 // CTAs for a grid-stride launch over `tiles` tiles: `ctas` if positive, else
-// one full wave of resident CTAs of `kernel` on the current device; capped at
-// `tiles`.  Returns 0 (with *err set) if the device cannot be queried.
-int grid_for(const void *kernel, long long tiles, int ctas, cudaError_t *err);
+// one full wave of resident CTAs of `kernel` (launched with `threads` threads
+// per CTA) on the current device; capped at `tiles`.  Returns 0 (with *err
+// set) if the device cannot be queried.
+int grid_for(const void *kernel, int threads, long long tiles, int ctas, cudaError_t *err);
 
 cudaError_t launch_encode(int bits, int dtype, const void *x, long long n, void *wire,
                           cudaStream_t s);
@@ -20,5 +21,12 @@ cudaError_t launch_reduce(int bits, int R, const void *const *wires, long long n
 cudaError_t launch_allreduce(int bits, int dtype, int R, const void *const *x, long long n,
                              void *y, void *const *wire_out, void *red_out, int ctas,
                              cudaStream_t s);
+
+struct ConstPtrs;
+
+// The 16-values-per-thread fused kernel (every pointer 32-byte aligned, no
+// wire emission), instantiated per width in qr_allreduce16_b<B>.cu.
+template <int B, int DT>
+cudaError_t run_allreduce16(int R, const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s);
 
 }  // namespace qrk

@@ -11,7 +11,7 @@ static cudaError_t run_reduce(int R, const void *const *wires, long long n, void
     for (int r = 0; r < R; ++r) w.p[r] = wires[r];
     auto kern = reduce_kernel<B>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), T, 0, &err);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, 0, &err);
     if (grid <= 0) return err;
     kern<<<grid, kThreads, 0, s>>>(w, R, static_cast<uint8_t *>(out), T);
     return cudaGetLastError();

@@ -103,6 +103,55 @@ def test_ragged_sizes(n, R):
             full_check(bits, dtype, xs, f"n={n} R={R} INT{bits} dt={dtype}")
 
 
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_every_rank_count(R):
+    n = 2048 * 3 + 37
+    for bits in BITS:
+        for dtype in (0, 1):
+            xs = _rand_ranks(R, n, dtype, seed=500 + 10 * R + bits + dtype)
+            full_check(bits, dtype, xs, f"R={R} INT{bits} dt={dtype}")
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_mixed_scale_ranges_in_one_warp(dtype):
+    """Neighbouring blocks with subnormal, normal and saturated fp16 scales,
+    so that some warps need the clip at qmin and others do not."""
+    n = 2048 * 8 + 37
+    rng = np.random.Generator(np.random.PCG64(31 + dtype))
+    lo, hi = (-27, 14) if dtype == 0 else (-40, 40)
+    for R in (1, 2, 5, 8):
+        xs = []
+        for r in range(R):
+            v = rng.standard_normal(n).astype(np.float32)
+            v *= np.repeat(np.exp2(rng.integers(lo, hi, size=-(-n // 32))), 32)[:n].astype(np.float32)
+            if dtype == 0:
+                v = np.clip(v, -60000.0 / R, 60000.0 / R)
+            xs.append(oracle.narrow(dtype, v))
+        for bits in BITS:
+            full_check(bits, dtype, xs, f"mixed scales R={R} INT{bits} dt={dtype}")
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_fused_with_16_byte_aligned_pointers(bits):
+    """Pointers that are 16- but not 32-byte aligned take the general fused
+    kernel; the result is the same."""
+    R, n, dtype = 3, 2048 * 5 + 37, 1
+    xs = _rand_ranks(R, n, dtype, seed=900 + bits)
+    bufs = []
+    for x in xs:
+        b = torch.zeros(2 * n + 64, dtype=torch.uint8, device="cuda")
+        b[16:16 + 2 * n] = torch.from_numpy(x.view(np.uint8)).cuda()
+        bufs.append(b)
+    yb = torch.zeros(2 * n + 64, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    ptrs = [b.data_ptr() + 16 for b in bufs]
+    assert all(p % 32 == 16 for p in ptrs)
+    assert capi.qr_allreduce(bits, dtype, R, ptrs, n, yb.data_ptr() + 16, st) == qr.QR_OK
+    torch.cuda.synchronize()
+    got = to_host_u8(yb)[16:16 + 2 * n].copy().view(np.uint16)
+    assert np.array_equal(got, oracle.allreduce(bits, dtype, xs))
+
+
 GUARD = 4096  # canary bytes before and after every buffer
 
 
