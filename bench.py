@@ -275,6 +275,80 @@ def profiled_traffic(kernel: str) -> tuple[float | None, str]:
 
 
 # ---------------------------------------------------------------------------
+# message-size sweep (not the headline line): fused and unfused arms
+# interleaved, median of `reps` launches, L2 flushed between launches when a
+# point's bytes are below 512 MiB
+# ---------------------------------------------------------------------------
+SWEEP_SIZES = [1 << 14, 1 << 16, 1 << 18, 1 << 20, (1 << 20) + 37, 1 << 22, 1 << 24, 1 << 26, 1 << 27,
+               1 << 28, 1 << 29, 1 << 30]
+
+
+def run_sweep(args) -> None:
+    import torch
+
+    from bit_quantized_all_gb300 import build
+    build.build()
+    import bit_quantized_all_gb300 as qr
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    peak, peak_src = measured_hbm()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sizes = [int(v) for v in args.sweep_sizes.split(",")] if args.sweep_sizes else SWEEP_SIZES
+    for dtype in (workloads.FP16, workloads.BF16):
+        tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
+        for Rs in (2, 4, 8):
+            for n in sizes:
+                xs = [x.view(tdt) for x in workloads.device_sweep(Rs, n, dtype, seed=SEED, device=dev)]
+                y = torch.empty(n, dtype=tdt, device=dev)
+                for bits in (8, 6, 4, 3):
+                    W = qr.qr_wire_bytes(bits, n)
+                    wires = [torch.empty(W, dtype=torch.uint8, device=dev) for _ in range(Rs)]
+                    red = torch.empty(W, dtype=torch.uint8, device=dev)
+                    yu = torch.empty(n, dtype=tdt, device=dev)
+                    fused_b = 2 * Rs * n + 2 * n
+                    unf_b = fused_b + 2 * (Rs + 1) * W
+                    do_flush = fused_b < (512 << 20)
+
+                    def fused():
+                        qr.qr_allreduce(bits, xs, y=y)
+
+                    def unfused():
+                        for r in range(Rs):
+                            qr.qr_encode(bits, xs[r], wire=wires[r])
+                        qr.qr_segment_reduce(bits, wires, n, out=red)
+                        qr.qr_decode(bits, red, n, y=yu)
+
+                    times = {"fused": [], "unfused": []}
+                    for _ in range(3):
+                        fused()
+                        unfused()
+                    for _ in range(args.reps):
+                        for name, fn in (("fused", fused), ("unfused", unfused)):
+                            if do_flush:
+                                flush.fill_(1)
+                            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            e0.record()
+                            fn()
+                            e1.record()
+                            e1.synchronize()
+                            times[name].append(e0.elapsed_time(e1))
+                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
+                    for name, alg in (("fused", fused_b), ("unfused", unf_b)):
+                        med = statistics.median(times[name])
+                        print(json.dumps({
+                            "sweep": name, "R": Rs, "values_per_rank": n, "storage": "fp16" if dtype == 0 else "bf16",
+                            "bits": bits, "median_ms": round(med, 5),
+                            "input_gbs": round(Rs * n * 2 / (med / 1e3) / 1e9, 2),
+                            "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
+                            "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
+                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps}), flush=True)
+                    del wires, red, yu
+                del xs, y
+                torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 def main() -> None:
@@ -287,7 +361,14 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--values-per-rank", type=int, default=N,
                     help="a smaller message for profiling captures (the default is the benchmark workload)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the message-size sweep (JSON line per point) instead of the benchmark")
+    ap.add_argument("--sweep-sizes", default="", help="comma-separated values per rank for --sweep")
+    ap.add_argument("--reps", type=int, default=100, help="launches per sweep point")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     set_values_per_rank(args.values_per_rank)
@@ -357,7 +438,7 @@ def main() -> None:
         d = [s.elapsed_time(e) for s, e in ev[b]]
         avg = sum(d) / len(d)
         alg = R * N * 2 + N * 2
-        kernels[b] = {"kernel": f"allreduce_kernel<{b},bf16>", "launches": len(d), "avg_ms": avg,
+        kernels[b] = {"kernel": f"allreduce16_kernel<{b},bf16,R={R}>", "launches": len(d), "avg_ms": avg,
                       "median_ms": statistics.median(d), "total_ms": sum(d),
                       "input_gbs": in_bytes_call / (avg / 1e3) / 1e9,
                       "achieved_gbs": alg / (avg / 1e3) / 1e9, "alg_bytes": alg}
