@@ -295,13 +295,16 @@ def run_sweep(args) -> None:
     peak, peak_src = measured_hbm()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     sizes = [int(v) for v in args.sweep_sizes.split(",")] if args.sweep_sizes else SWEEP_SIZES
-    for dtype in (workloads.FP16, workloads.BF16):
+    dtypes = [{"fp16": workloads.FP16, "bf16": workloads.BF16}[d] for d in args.sweep_dtypes.split(",")]
+    ranks = [int(r) for r in args.sweep_R.split(",")]
+    widths = [int(b) for b in args.sweep_bits.split(",")]
+    for dtype in dtypes:
         tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
-        for Rs in (2, 4, 8):
+        for Rs in ranks:
             for n in sizes:
                 xs = [x.view(tdt) for x in workloads.device_sweep(Rs, n, dtype, seed=SEED, device=dev)]
                 y = torch.empty(n, dtype=tdt, device=dev)
-                for bits in (8, 6, 4, 3):
+                for bits in widths:
                     W = qr.qr_wire_bytes(bits, n)
                     wires = [torch.empty(W, dtype=torch.uint8, device=dev) for _ in range(Rs)]
                     red = torch.empty(W, dtype=torch.uint8, device=dev)
@@ -319,12 +322,24 @@ def run_sweep(args) -> None:
                         qr.qr_segment_reduce(bits, wires, n, out=red)
                         qr.qr_decode(bits, red, n, y=yu)
 
-                    times = {"fused": [], "unfused": []}
+                    def encode_all():
+                        for r in range(Rs):
+                            qr.qr_encode(bits, xs[r], wire=wires[r])
+
+                    def reduce_only():
+                        qr.qr_segment_reduce(bits, wires, n, out=red)
+
+                    def decode_only():
+                        qr.qr_decode(bits, red, n, y=yu)
+
+                    arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all),
+                            ("reduce", reduce_only), ("decode", decode_only))
+                    times = {name: [] for name, _ in arms}
                     for _ in range(3):
                         fused()
                         unfused()
                     for _ in range(args.reps):
-                        for name, fn in (("fused", fused), ("unfused", unfused)):
+                        for name, fn in arms:
                             if do_flush:
                                 flush.fill_(1)
                             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -334,7 +349,9 @@ def run_sweep(args) -> None:
                             e1.synchronize()
                             times[name].append(e0.elapsed_time(e1))
                     same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
-                    for name, alg in (("fused", fused_b), ("unfused", unf_b)):
+                    kernel_b = {"fused": fused_b, "unfused": unf_b, "encode": Rs * (2 * n + W),
+                                "reduce": (Rs + 1) * W, "decode": W + 2 * n}
+                    for name, alg in kernel_b.items():
                         med = statistics.median(times[name])
                         print(json.dumps({
                             "sweep": name, "R": Rs, "values_per_rank": n, "storage": "fp16" if dtype == 0 else "bf16",
@@ -365,6 +382,9 @@ def main() -> None:
                     help="run the message-size sweep (JSON line per point) instead of the benchmark")
     ap.add_argument("--sweep-sizes", default="", help="comma-separated values per rank for --sweep")
     ap.add_argument("--reps", type=int, default=100, help="launches per sweep point")
+    ap.add_argument("--sweep-R", default="2,4,8", help="rank counts for --sweep")
+    ap.add_argument("--sweep-bits", default="8,6,4,3", help="code widths for --sweep")
+    ap.add_argument("--sweep-dtypes", default="fp16,bf16", help="storage types for --sweep")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

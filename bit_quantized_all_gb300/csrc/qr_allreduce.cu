@@ -22,7 +22,7 @@ static cudaError_t run_allreduce(int R, const void *const *x, long long n, void 
     if (!emit && aligned32) return run_allreduce16<B, DT>(R, xp, n, y, ctas, s);
     auto kern = emit ? allreduce_kernel<B, DT, true> : allreduce_kernel<B, DT, false>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, ctas, &err);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, ctas, 1, &err);
     if (grid <= 0) return err;
     kern<<<grid, kThreads, 0, s>>>(xp, R, n, static_cast<uint16_t *>(y), wp, static_cast<uint8_t *>(red_out), T);
     return cudaGetLastError();

@@ -14,7 +14,7 @@ static cudaError_t run_allreduce16_r(const ConstPtrs &xp, long long n, void *y, 
     const long long T = (n + kTileValues - 1) / kTileValues;
     auto kern = allreduce16_kernel<B, DT, R>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads16, T, ctas, &err);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads16, T, ctas, 4, &err);
     if (grid <= 0) return err;
     kern<<<grid, kThreads16, 0, s>>>(xp, n, static_cast<uint16_t *>(y), T);
     return cudaGetLastError();

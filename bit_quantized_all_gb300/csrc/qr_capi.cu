@@ -61,7 +61,7 @@ qr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_
 
 namespace qrk {
 
-int grid_for(const void *kernel, int threads, long long tiles, int ctas, cudaError_t *err) {
+int grid_for(const void *kernel, int threads, long long tiles, int ctas, int waves, cudaError_t *err) {
     *err = cudaSuccess;
     if (tiles <= 0) return 0;
     if (ctas > 0) return static_cast<int>(tiles < ctas ? tiles : ctas);
@@ -84,7 +84,8 @@ int grid_for(const void *kernel, int threads, long long tiles, int ctas, cudaErr
         std::lock_guard<std::mutex> lock(mu);
         resident[{dev, kernel}] = wave;
     }
-    return static_cast<int>(tiles < wave ? tiles : wave);
+    const long long want = static_cast<long long>(wave) * (waves > 0 ? waves : 1);
+    return static_cast<int>(tiles < want ? tiles : want);
 }
 
 }  // namespace qrk

@@ -1,17 +1,23 @@
-// qr_decode.cu -- launcher of the receive-path kernel (decode_kernel).
-#include "qr_kernels.cuh"
+// qr_decode.cu -- launcher of the receive-path kernel (decode16_kernel).
+#include <cstdint>
+
+#include "qr_kernels32.cuh"
 #include "qr_launch.h"
 
 namespace qrk {
 
+constexpr int kDecodeUnroll = 4;  // half-blocks per thread in flight (7-17 wire bytes each)
+
 template <int B, int DT>
 static cudaError_t run_decode(const void *wire, long long n, void *y, cudaStream_t s) {
-    const long long T = (n + kTileValues - 1) / kTileValues;
-    auto kern = decode_kernel<B, DT>;
+    const long long NH = 128 * ((n + kTileValues - 1) / kTileValues);  // half-blocks
+    const bool y32 = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
+    auto kern = y32 ? decode16_kernel<B, DT, kDecodeUnroll, true> : decode16_kernel<B, DT, kDecodeUnroll, false>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, 0, &err);
+    const long long units = (NH + kThreads32 * kDecodeUnroll - 1) / (kThreads32 * kDecodeUnroll);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t *>(wire), n, static_cast<uint16_t *>(y), T);
+    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint8_t *>(wire), n, static_cast<uint16_t *>(y), NH);
     return cudaGetLastError();
 }
 

@@ -318,10 +318,10 @@ __device__ __forceinline__ SlotCodes load_codes(const uint8_t *tile, int k) {
     return c;
 }
 
-// The 8 signed codes q = u - bias of a slot, as exact floats.
+// The codes of lanes 0,2,4,6 (`even`) and 1,3,5,7 (`odd`) of a slot, one
+// per byte.
 template <int B>
-__device__ __forceinline__ void unpack_q(const SlotCodes c, float (&q)[8]) {
-    uint32_t even, odd;  // lanes 0,2,4,6 / 1,3,5,7, one code per byte
+__device__ __forceinline__ void slot_even_odd_codes(const SlotCodes c, uint32_t &even, uint32_t &odd) {
     if constexpr (B == 8) {
         even = __byte_perm(c.a, c.b, 0x6420);
         odd = __byte_perm(c.a, c.b, 0x7531);
@@ -337,6 +337,13 @@ __device__ __forceinline__ void unpack_q(const SlotCodes c, float (&q)[8]) {
         even = (c.a & 0x0F0F0F0Fu) | ((hi & 0x03030303u) << 4);
         odd = ((c.a >> 4) & 0x0F0F0F0Fu) | (((hi >> 4) & 0x03030303u) << 4);
     }
+}
+
+// The 8 signed codes q = u - bias of a slot, as exact floats.
+template <int B>
+__device__ __forceinline__ void unpack_q(const SlotCodes c, float (&q)[8]) {
+    uint32_t even, odd;
+    slot_even_odd_codes<B>(c, even, odd);
     q[0] = magic_to_q<B>(byte_as_magic<0>(even));
     q[2] = magic_to_q<B>(byte_as_magic<1>(even));
     q[4] = magic_to_q<B>(byte_as_magic<2>(even));

@@ -1,17 +1,20 @@
-// qr_encode.cu -- launcher of the send-path kernel (encode_kernel).
-#include "qr_kernels.cuh"
+// qr_encode.cu -- launcher of the send-path kernel (encode32_kernel).
+#include "qr_kernels32.cuh"
 #include "qr_launch.h"
 
 namespace qrk {
 
+constexpr int kEncodeUnroll = 2;  // blocks per thread in flight (2 x 64 bytes of input)
+
 template <int B, int DT>
 static cudaError_t run_encode(const void *x, long long n, void *wire, cudaStream_t s) {
-    const long long T = (n + kTileValues - 1) / kTileValues;
-    auto kern = encode_kernel<B, DT>;
+    const long long NB = 64 * ((n + kTileValues - 1) / kTileValues);
+    auto kern = encode32_kernel<B, DT, kEncodeUnroll>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, 0, &err);
+    const long long units = (NB + kThreads32 * kEncodeUnroll - 1) / (kThreads32 * kEncodeUnroll);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t *>(x), n, static_cast<uint8_t *>(wire), T);
+    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint16_t *>(x), n, static_cast<uint8_t *>(wire), NB);
     return cudaGetLastError();
 }
 

@@ -1,99 +1,15 @@
-// qr_kernels.cuh -- the four kernels of the codec, templated on the code
-// width B and the storage type DT (0 = fp16, 1 = bf16).
+// qr_kernels.cuh -- the fused two-shot kernels, templated on the code width
+// B and the storage type DT (0 = fp16, 1 = bf16).  (The standalone encode,
+// reduce and decode kernels are in qr_kernels32.cuh.)
 //
-// Every kernel is a grid-stride loop over 2048-value tiles with 256 threads
-// per CTA (thread k = slot k); tiles are independent, so any grid size gives
-// the same bytes.  No kernel waits on another CTA, allocates, or uses global
-// scratch memory.
+// Every kernel is a grid-stride loop over 2048-value tiles; tiles are
+// independent, so any grid size gives the same bytes.  No kernel waits on
+// another CTA, allocates, or uses global scratch memory.
 #pragma once
 
 #include "qr_device.cuh"
 
 namespace qrk {
-
-// Send path [QR Quantization and Dequantization Paths, CodecQ3::send]:
-// absmax over the block -> fp16 scale -> scale / clip / round / bias -> pack;
-// the first lane of each quad (the block's leader) writes the scale.
-template <int B, int DT>
-__global__ void __launch_bounds__(kThreads) encode_kernel(const uint16_t *__restrict__ x, long long n,
-                                                          uint8_t *__restrict__ wire, long long T) {
-    const int k = threadIdx.x;
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        float v[8];
-        load_slot<DT>(x, t * kTileValues + 8 * k, n, v);
-        const BlockScale sc = block_scale<B>(quad_absmax(v));
-        float f[8];
-        quantize8<B>(v, sc.r, f);
-        uint8_t *tile = wire + t * Codec<B>::kTileBytes;
-        store_codes<B>(tile, k, f);
-        store_scale<B>(tile, k, sc.bits);
-    }
-}
-
-// Receive path / Phase-2 [QR Quantization and Dequantization Paths,
-// CodecQ3::recv]: recombine the bits, remove the bias, multiply by the
-// block's decode scale, round to fp16/bf16.
-template <int B, int DT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const uint8_t *__restrict__ wire, long long n,
-                                                          uint16_t *__restrict__ y, long long T) {
-    const int k = threadIdx.x;
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        const uint8_t *tile = wire + t * Codec<B>::kTileBytes;
-        const SlotCodes c = load_codes<B>(tile, k);
-        const float s = load_scale<B>(tile, k);
-        float q[8], v[8];
-        unpack_q<B>(c, q);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(q[j], s);
-        store_slot<DT>(y, t * kTileValues + 8 * k, n, v);
-    }
-}
-
-// Phase-1B in-segment reduction [QR Quantization and Dequantization Paths;
-// FC key machinery "sums locally, re-quantizes the partial sums"]: decode
-// the R rank tiles, add them in fp32 in rank order, re-quantize.
-// acc = fma(q, s, acc) equals fp32_RN(acc + q*s) because q*s is exact (an
-// 8-bit integer times an 11-bit significand).
-template <int B>
-__global__ void __launch_bounds__(kThreads) reduce_kernel(ConstPtrs wires, int R, uint8_t *out,
-                                                          long long T) {
-    const int k = threadIdx.x;
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        const long long off = t * Codec<B>::kTileBytes;
-        SlotCodes c[kMaxRanks];
-        float s[kMaxRanks];
-#pragma unroll
-        for (int r = 0; r < kMaxRanks; ++r) {
-            if (r < R) {
-                const uint8_t *tile = static_cast<const uint8_t *>(wires.p[r]) + off;
-                c[r] = load_codes<B>(tile, k);
-                s[r] = load_scale<B>(tile, k);
-            }
-        }
-        float acc[8];
-        {
-            float q[8];
-            unpack_q<B>(c[0], q);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = __fmul_rn(q[j], s[0]);
-        }
-#pragma unroll
-        for (int r = 1; r < kMaxRanks; ++r) {
-            if (r < R) {
-                float q[8];
-                unpack_q<B>(c[r], q);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] = __fmaf_rn(q[j], s[r], acc[j]);
-            }
-        }
-        const BlockScale sc = block_scale<B>(quad_absmax(acc));
-        float f[8];
-        quantize8<B>(acc, sc.r, f);
-        uint8_t *tile = out + off;
-        store_codes<B>(tile, k, f);
-        store_scale<B>(tile, k, sc.bits);
-    }
-}
 
 // The fused two-shot all-reduce [FC key machinery: one fused kernel, two
 // quantization round trips]: for each tile, quantize every rank's slot

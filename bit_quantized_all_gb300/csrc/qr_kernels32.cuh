@@ -1,0 +1,556 @@
+// qr_kernels32.cuh -- the standalone encode, Phase-1B reduce and decode
+// kernels: one 32-value block per thread (encode32, reduce32) or two threads
+// per block (decode16, reduce16).
+//
+// A block's codes are contiguous in each section of the wire tile (slots
+// 4g..4g+3), so a thread reads or writes them with one vector access per
+// section, computes the block absmax without shuffles, and the fp16 scale
+// once.  Each thread works on U blocks that lie a grid stride apart and
+// issues every load of all U before any arithmetic, to keep enough bytes in
+// flight for HBM.  Consecutive lanes own consecutive blocks of one tile.
+#pragma once
+
+#include "qr_device.cuh"
+
+namespace qrk {
+
+constexpr int kThreads32 = 256;
+
+// ---------------------------------------------------------------------------
+// values: 32 fp16/bf16 values of block `gb` (64 bytes)
+// ---------------------------------------------------------------------------
+
+// Values at or past n read as +0.  Full blocks use four 16-byte loads
+// (L1-cached: the four chunks of a thread share two 32-byte sectors).
+__device__ __forceinline__ void load_block_values(const uint16_t *x, long long base, long long n,
+                                                  uint32_t (&w)[16]) {
+    if (base + 32 <= n) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(x + base);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 c = p[i];
+            w[4 * i] = c.x;
+            w[4 * i + 1] = c.y;
+            w[4 * i + 2] = c.z;
+            w[4 * i + 3] = c.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t lo = (base + 2 * i < n) ? x[base + 2 * i] : 0u;
+            const uint32_t hi = (base + 2 * i + 1 < n) ? x[base + 2 * i + 1] : 0u;
+            w[i] = lo | (hi << 16);
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void widen_block(const uint32_t (&w)[16], float2 (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        if constexpr (DT == 1) {
+            v[i].x = __uint_as_float(w[i] << 16);
+            v[i].y = __uint_as_float(w[i] & 0xFFFF0000u);
+        } else {
+            v[i] = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        }
+    }
+}
+
+__device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
+    float a = fmaxf(fabsf(v[0].x), fabsf(v[0].y));
+#pragma unroll
+    for (int i = 1; i < 16; ++i) a = fmaxf(a, fmaxf(fabsf(v[i].x), fabsf(v[i].y)));
+    return a;
+}
+
+// f = clip(RN(v*r), qmin, qmax) + 1.5*2^23 + bias (the code in the low byte),
+// with the clip at qmin only where block_scale2 says it can matter.
+template <int B>
+__device__ __forceinline__ void quantize_block_magic(const float2 (&v)[16], float r, bool low_clip,
+                                                     float2 (&f)[16]) {
+    const float2 r2 = make_float2(r, r);
+    const float2 m2 = make_float2(Codec<B>::kMagic, Codec<B>::kMagic);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float2 t = __fmul2_rn(v[i], r2);
+        if (low_clip) {
+            t.x = fmaxf(t.x, Codec<B>::kQmin);
+            t.y = fmaxf(t.y, Codec<B>::kQmin);
+        }
+        t.x = fminf(t.x, Codec<B>::kQmax);
+        t.y = fminf(t.y, Codec<B>::kQmax);
+        f[i] = __fadd2_rn(t, m2);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// codes of one block: slot s = values 8s..8s+7 of the block = f[4s..4s+3]
+// ---------------------------------------------------------------------------
+
+// lanes 0,2,4,6 (the .x of the four pairs) and 1,3,5,7 (.y), one per byte
+__device__ __forceinline__ void slot_even_odd(const float2 (&f)[16], int s, uint32_t &even, uint32_t &odd) {
+    even = gather_low_bytes(__float_as_uint(f[4 * s].x), __float_as_uint(f[4 * s + 1].x),
+                            __float_as_uint(f[4 * s + 2].x), __float_as_uint(f[4 * s + 3].x));
+    odd = gather_low_bytes(__float_as_uint(f[4 * s].y), __float_as_uint(f[4 * s + 1].y),
+                           __float_as_uint(f[4 * s + 2].y), __float_as_uint(f[4 * s + 3].y));
+}
+
+// Raw words of one block's codes, section by section:
+//   B=8: w[0..7] (32 bytes at 32g)     B=4: w[0..3] (16 bytes at 16g)
+//   B=3: w[0..1] q2w (8 bytes at 8g), w[2] q1w (4 bytes at 512 + 4g)
+//   B=6: w[0..3] q4w (16 bytes at 16g), w[4..5] q2w (8 bytes at 1024 + 8g)
+template <int B>
+struct BlockWords {
+    static constexpr int kWords = (B == 8) ? 8 : (B == 4) ? 4 : (B == 3) ? 3 : 6;
+    uint32_t w[kWords];
+};
+
+template <int B>
+__device__ __forceinline__ void pack_block(const float2 (&f)[16], BlockWords<B> &c) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        uint32_t even, odd;
+        slot_even_odd(f, s, even, odd);
+        if constexpr (B == 8) {
+            c.w[2 * s] = __byte_perm(even, odd, 0x5140);
+            c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
+        } else if constexpr (B == 4) {
+            c.w[s] = even | (odd << 4);
+        } else if constexpr (B == 3) {
+            const uint32_t nib = even | (odd << 4);
+            const uint32_t q2 = compress_2_of_4(nib);
+            const uint32_t q1 = compress_1_of_4(nib >> 2);
+            if (s % 2 == 0) {
+                c.w[s / 2] = q2;
+            } else {
+                c.w[s / 2] |= q2 << 16;
+            }
+            if (s == 0) c.w[2] = q1;
+            else c.w[2] |= q1 << (8 * s);
+        } else {
+            c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
+            const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
+            const uint32_t q2 = compress_2_of_4(hi);
+            if (s % 2 == 0) {
+                c.w[4 + s / 2] = q2;
+            } else {
+                c.w[4 + s / 2] |= q2 << 16;
+            }
+        }
+    }
+}
+
+template <int B>
+__device__ __forceinline__ SlotCodes slot_codes(const BlockWords<B> &c, int s) {
+    SlotCodes sc;
+    if constexpr (B == 8) {
+        sc.a = c.w[2 * s];
+        sc.b = c.w[2 * s + 1];
+    } else if constexpr (B == 4) {
+        sc.a = c.w[s];
+        sc.b = 0;
+    } else if constexpr (B == 3) {
+        sc.a = (c.w[s / 2] >> (16 * (s % 2))) & 0xFFFFu;
+        sc.b = (c.w[2] >> (8 * s)) & 0xFFu;
+    } else {
+        sc.a = c.w[s];
+        sc.b = (c.w[4 + s / 2] >> (16 * (s % 2))) & 0xFFFFu;
+    }
+    return sc;
+}
+
+template <int B>
+__device__ __forceinline__ void store_block_codes(uint8_t *tile, int g, const BlockWords<B> &c) {
+    if constexpr (B == 8) {
+        uint4 *p = reinterpret_cast<uint4 *>(tile + 32 * g);
+        p[0] = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
+        p[1] = make_uint4(c.w[4], c.w[5], c.w[6], c.w[7]);
+    } else if constexpr (B == 4) {
+        *reinterpret_cast<uint4 *>(tile + 16 * g) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
+    } else if constexpr (B == 3) {
+        *reinterpret_cast<uint2 *>(tile + 8 * g) = make_uint2(c.w[0], c.w[1]);
+        *reinterpret_cast<uint32_t *>(tile + 512 + 4 * g) = c.w[2];
+    } else {
+        *reinterpret_cast<uint4 *>(tile + 16 * g) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
+        *reinterpret_cast<uint2 *>(tile + 1024 + 8 * g) = make_uint2(c.w[4], c.w[5]);
+    }
+}
+
+template <int B>
+__device__ __forceinline__ void load_block_codes(const uint8_t *tile, int g, BlockWords<B> &c) {
+    if constexpr (B == 8) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(tile + 32 * g);
+        const uint4 a = p[0], b = p[1];
+        c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+        c.w[4] = b.x; c.w[5] = b.y; c.w[6] = b.z; c.w[7] = b.w;
+    } else if constexpr (B == 4) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(tile + 16 * g);
+        c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+    } else if constexpr (B == 3) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(tile + 8 * g);
+        c.w[0] = a.x; c.w[1] = a.y;
+        c.w[2] = *reinterpret_cast<const uint32_t *>(tile + 512 + 4 * g);
+    } else {
+        const uint4 a = *reinterpret_cast<const uint4 *>(tile + 16 * g);
+        const uint2 b = *reinterpret_cast<const uint2 *>(tile + 1024 + 8 * g);
+        c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+        c.w[4] = b.x; c.w[5] = b.y;
+    }
+}
+
+// The 8 signed codes of a slot as exact floats, pairwise (lanes 2i, 2i+1):
+// each code goes into the low byte of 1.5*2^23 + bias by one byte permute,
+// and one packed add per pair removes the offset.
+template <int B>
+__device__ __forceinline__ void unpack_slot_q2(const SlotCodes c, float2 (&q)[4]) {
+    uint32_t even, odd;
+    slot_even_odd_codes<B>(c, even, odd);
+    const float2 nm = make_float2(-Codec<B>::kMagic, -Codec<B>::kMagic);
+    q[0] = __fadd2_rn(make_float2(byte_as_magic<0>(even), byte_as_magic<0>(odd)), nm);
+    q[1] = __fadd2_rn(make_float2(byte_as_magic<1>(even), byte_as_magic<1>(odd)), nm);
+    q[2] = __fadd2_rn(make_float2(byte_as_magic<2>(even), byte_as_magic<2>(odd)), nm);
+    q[3] = __fadd2_rn(make_float2(byte_as_magic<3>(even), byte_as_magic<3>(odd)), nm);
+}
+
+// The 32 signed codes of a block as exact floats, pairwise.
+template <int B>
+__device__ __forceinline__ void unpack_block_q(const BlockWords<B> &c, float2 (&q)[16]) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        float2 qs[4];
+        unpack_slot_q2<B>(slot_codes<B>(c, s), qs);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[4 * s + i] = qs[i];
+    }
+}
+
+template <int B>
+__device__ __forceinline__ uint32_t load_block_scale_bits(const uint8_t *tile, int g) {
+    return ld_u16(tile + Codec<B>::kCodeBytes + 2 * g);
+}
+
+template <int B>
+__device__ __forceinline__ void store_block_scale(uint8_t *tile, int g, uint32_t bits) {
+    *reinterpret_cast<uint16_t *>(tile + Codec<B>::kCodeBytes + 2 * g) = static_cast<uint16_t>(bits);
+}
+
+__device__ __forceinline__ float f16_bits_to_float(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// ---------------------------------------------------------------------------
+// kernels.  NB = number of blocks = 64 * tiles (the zero padding of the last
+// tile included); thread (CTA c, lane i) starts at block c*256 + i.
+// ---------------------------------------------------------------------------
+
+// Send path [QR Quantization and Dequantization Paths, CodecQ3::send].
+template <int B, int DT, int U>
+__global__ void __launch_bounds__(kThreads32) encode32_kernel(const uint16_t *__restrict__ x, long long n,
+                                                              uint8_t *__restrict__ wire, long long NB) {
+    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
+    for (long long gb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb0 < NB; gb0 += U * S) {
+        uint32_t raw[U][16];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long gb = gb0 + u * S;
+            if (gb < NB) load_block_values(x, gb * 32, n, raw[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long gb = gb0 + u * S;
+            if (gb < NB) {
+                float2 v[16], f[16];
+                widen_block<DT>(raw[u], v);
+                const BlockScale2 sc = block_scale2<B>(block_absmax(v));
+                quantize_block_magic<B>(v, sc.r, sc.low_clip, f);
+                BlockWords<B> c;
+                pack_block<B>(f, c);
+                uint8_t *tile = wire + (gb >> 6) * Codec<B>::kTileBytes;
+                store_block_codes<B>(tile, static_cast<int>(gb & 63), c);
+                store_block_scale<B>(tile, static_cast<int>(gb & 63), sc.bits);
+            }
+        }
+    }
+}
+
+// Receive path / Phase-2 [QR Quantization and Dequantization Paths,
+// CodecQ3::recv], with two threads per block (16 values, two slots each):
+// every lane writes 32 contiguous bytes of output and neighbouring lanes
+// write neighbouring bytes, so a warp's stores cover whole sectors once.
+// Work unit = half-block hb: block hb/2, slots 2*(hb%2) and 2*(hb%2)+1.
+template <int B>
+struct HalfWords {  // the codes of two slots
+    static constexpr int kWords = (B == 8) ? 4 : (B == 4) ? 2 : (B == 3) ? 2 : 3;
+    uint32_t w[kWords];
+};
+
+template <int B>
+__device__ __forceinline__ void load_half_codes(const uint8_t *tile, int g, int half, HalfWords<B> &c) {
+    if constexpr (B == 8) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(tile + 32 * g + 16 * half);
+        c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+    } else if constexpr (B == 4) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(tile + 16 * g + 8 * half);
+        c.w[0] = a.x; c.w[1] = a.y;
+    } else if constexpr (B == 3) {
+        c.w[0] = *reinterpret_cast<const uint32_t *>(tile + 8 * g + 4 * half);       // two q2w
+        c.w[1] = *reinterpret_cast<const uint16_t *>(tile + 512 + 4 * g + 2 * half); // two q1w
+    } else {
+        const uint2 a = *reinterpret_cast<const uint2 *>(tile + 16 * g + 8 * half);
+        c.w[0] = a.x; c.w[1] = a.y;
+        c.w[2] = *reinterpret_cast<const uint32_t *>(tile + 1024 + 8 * g + 4 * half);  // two q2w
+    }
+}
+
+template <int B>
+__device__ __forceinline__ SlotCodes half_slot_codes(const HalfWords<B> &c, int s) {
+    SlotCodes sc;
+    if constexpr (B == 8) {
+        sc.a = c.w[2 * s];
+        sc.b = c.w[2 * s + 1];
+    } else if constexpr (B == 4) {
+        sc.a = c.w[s];
+        sc.b = 0;
+    } else if constexpr (B == 3) {
+        sc.a = (c.w[0] >> (16 * s)) & 0xFFFFu;
+        sc.b = (c.w[1] >> (8 * s)) & 0xFFu;
+    } else {
+        sc.a = c.w[s];
+        sc.b = (c.w[2] >> (16 * s)) & 0xFFFFu;
+    }
+    return sc;
+}
+
+template <int B, int DT, int U, bool Y32>  // Y32: y is 32-byte aligned (one 256-bit store per unit)
+__global__ void __launch_bounds__(kThreads32) decode16_kernel(const uint8_t *__restrict__ wire, long long n,
+                                                              uint16_t *__restrict__ y, long long NH) {
+    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
+    for (long long hb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb0 < NH; hb0 += U * S) {
+        HalfWords<B> c[U];
+        uint32_t sb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long hb = hb0 + u * S;
+            if (hb < NH) {
+                const long long gb = hb >> 1;
+                const uint8_t *tile = wire + (gb >> 6) * Codec<B>::kTileBytes;
+                load_half_codes<B>(tile, static_cast<int>(gb & 63), static_cast<int>(hb & 1), c[u]);
+                sb[u] = load_block_scale_bits<B>(tile, static_cast<int>(gb & 63));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long hb = hb0 + u * S;
+            if (hb < NH) {
+                const float s = f16_bits_to_float(sb[u]);
+                const float2 s2 = make_float2(s, s);
+                float2 o[8];
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    float2 q[4];
+                    unpack_slot_q2<B>(half_slot_codes<B>(c[u], sl), q);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[4 * sl + i] = __fmul2_rn(q[i], s2);
+                }
+                const long long base = hb * 16;
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = narrow2<DT>(o[i].x, o[i].y);
+                if (base + 16 <= n) {
+                    if constexpr (Y32) {
+                        st_global32(y + base, w);
+                    } else {
+                        uint4 *p = reinterpret_cast<uint4 *>(y + base);
+                        p[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        p[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (base + 2 * i < n) y[base + 2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+                        if (base + 2 * i + 1 < n) y[base + 2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Codes of two slots (one half-block) from 16 magic floats f[0..7] (pairs).
+template <int B>
+__device__ __forceinline__ void pack_half(const float2 (&f)[8], HalfWords<B> &c) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const uint32_t even = gather_low_bytes(__float_as_uint(f[4 * s].x), __float_as_uint(f[4 * s + 1].x),
+                                               __float_as_uint(f[4 * s + 2].x), __float_as_uint(f[4 * s + 3].x));
+        const uint32_t odd = gather_low_bytes(__float_as_uint(f[4 * s].y), __float_as_uint(f[4 * s + 1].y),
+                                              __float_as_uint(f[4 * s + 2].y), __float_as_uint(f[4 * s + 3].y));
+        if constexpr (B == 8) {
+            c.w[2 * s] = __byte_perm(even, odd, 0x5140);
+            c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
+        } else if constexpr (B == 4) {
+            c.w[s] = even | (odd << 4);
+        } else if constexpr (B == 3) {
+            const uint32_t nib = even | (odd << 4);
+            const uint32_t q2 = compress_2_of_4(nib), q1 = compress_1_of_4(nib >> 2);
+            if (s == 0) {
+                c.w[0] = q2;
+                c.w[1] = q1;
+            } else {
+                c.w[0] |= q2 << 16;
+                c.w[1] |= q1 << 8;
+            }
+        } else {
+            c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
+            const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
+            const uint32_t q2 = compress_2_of_4(hi);
+            if (s == 0) c.w[2] = q2;
+            else c.w[2] |= q2 << 16;
+        }
+    }
+}
+
+template <int B>
+__device__ __forceinline__ void store_half_codes(uint8_t *tile, int g, int half, const HalfWords<B> &c) {
+    if constexpr (B == 8) {
+        *reinterpret_cast<uint4 *>(tile + 32 * g + 16 * half) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
+    } else if constexpr (B == 4) {
+        *reinterpret_cast<uint2 *>(tile + 16 * g + 8 * half) = make_uint2(c.w[0], c.w[1]);
+    } else if constexpr (B == 3) {
+        *reinterpret_cast<uint32_t *>(tile + 8 * g + 4 * half) = c.w[0];
+        *reinterpret_cast<uint16_t *>(tile + 512 + 4 * g + 2 * half) = static_cast<uint16_t>(c.w[1]);
+    } else {
+        *reinterpret_cast<uint2 *>(tile + 16 * g + 8 * half) = make_uint2(c.w[0], c.w[1]);
+        *reinterpret_cast<uint32_t *>(tile + 1024 + 8 * g + 4 * half) = c.w[2];
+    }
+}
+
+// Phase-1B in-segment reduction [QR Quantization and Dequantization Paths;
+// FC key machinery], with two threads per block (lanes 2k and 2k+1 own the
+// two halves of one block, so the pair shares the absmax by one shuffle):
+// decode the R rank copies, add them in fp32 in rank order (fma(q, s, acc) =
+// RN(acc + q*s): q*s is exact), re-quantize.  Half-blocks hb and hb^1 are
+// always both in or both out of range, and every lane reaches the shuffle.
+template <int B, int R, int U>
+__global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, uint8_t *out, long long NH) {
+    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
+    for (long long hb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb0 - (threadIdx.x & 31) < NH;
+         hb0 += U * S) {
+        HalfWords<B> c[U][R];
+        uint32_t sb[U][R];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long hb = hb0 + u * S;
+            if (hb < NH) {
+                const long long gb = hb >> 1;
+                const long long off = (gb >> 6) * Codec<B>::kTileBytes;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint8_t *tile = static_cast<const uint8_t *>(wires.p[r]) + off;
+                    load_half_codes<B>(tile, static_cast<int>(gb & 63), static_cast<int>(hb & 1), c[u][r]);
+                    sb[u][r] = load_block_scale_bits<B>(tile, static_cast<int>(gb & 63));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long hb = hb0 + u * S;
+            const bool valid = hb < NH;
+            float2 acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
+            if (valid) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float s = f16_bits_to_float(sb[u][r]);
+                    const float2 s2 = make_float2(s, s);
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        float2 q[4];
+                        unpack_slot_q2<B>(half_slot_codes<B>(c[u][r], sl), q);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            acc[4 * sl + i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[4 * sl + i]);
+                    }
+                }
+            }
+            const BlockScale2 sc = block_scale2<B>(pair_absmax(acc));
+            if (valid) {
+                float2 f[8];
+                const float2 r2 = make_float2(sc.r, sc.r);
+                const float2 m2 = make_float2(Codec<B>::kMagic, Codec<B>::kMagic);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float2 t = __fmul2_rn(acc[i], r2);
+                    if (sc.low_clip) {
+                        t.x = fmaxf(t.x, Codec<B>::kQmin);
+                        t.y = fmaxf(t.y, Codec<B>::kQmin);
+                    }
+                    t.x = fminf(t.x, Codec<B>::kQmax);
+                    t.y = fminf(t.y, Codec<B>::kQmax);
+                    f[i] = __fadd2_rn(t, m2);
+                }
+                HalfWords<B> cw;
+                pack_half<B>(f, cw);
+                const long long gb = hb >> 1;
+                uint8_t *tile = out + (gb >> 6) * Codec<B>::kTileBytes;
+                store_half_codes<B>(tile, static_cast<int>(gb & 63), static_cast<int>(hb & 1), cw);
+                if ((hb & 1) == 0) store_block_scale<B>(tile, static_cast<int>(gb & 63), sc.bits);
+            }
+        }
+    }
+}
+
+// Phase-1B in-segment reduction with one thread per block (fewer
+// instructions than reduce16_kernel, which wins where the 8-rank loads need
+// more warps to hide their latency): decode the R rank copies of the block,
+// add them in fp32 in rank order (fma(q, s, acc) = RN(acc + q*s): q*s is
+// exact), re-quantize.
+template <int B, int R, int U>
+__global__ void __launch_bounds__(kThreads32) reduce32_kernel(ConstPtrs wires, uint8_t *out, long long NB) {
+    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
+    for (long long gb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb0 < NB; gb0 += U * S) {
+        BlockWords<B> c[U][R];
+        uint32_t sb[U][R];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long gb = gb0 + u * S;
+            if (gb < NB) {
+                const long long off = (gb >> 6) * Codec<B>::kTileBytes;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint8_t *tile = static_cast<const uint8_t *>(wires.p[r]) + off;
+                    load_block_codes<B>(tile, static_cast<int>(gb & 63), c[u][r]);
+                    sb[u][r] = load_block_scale_bits<B>(tile, static_cast<int>(gb & 63));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long gb = gb0 + u * S;
+            if (gb < NB) {
+                float2 acc[16];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float s = f16_bits_to_float(sb[u][r]);
+                    const float2 s2 = make_float2(s, s);
+                    float2 q[16];
+                    unpack_block_q<B>(c[u][r], q);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
+                }
+                const BlockScale2 sc = block_scale2<B>(block_absmax(acc));
+                float2 f[16];
+                quantize_block_magic<B>(acc, sc.r, sc.low_clip, f);
+                BlockWords<B> cw;
+                pack_block<B>(f, cw);
+                uint8_t *tile = out + (gb >> 6) * Codec<B>::kTileBytes;
+                store_block_codes<B>(tile, static_cast<int>(gb & 63), cw);
+                store_block_scale<B>(tile, static_cast<int>(gb & 63), sc.bits);
+            }
+        }
+    }
+}
+
+}  // namespace qrk

@@ -6,11 +6,11 @@
 
 namespace qrk {
 
-// CTAs for a grid-stride launch over `tiles` tiles: `ctas` if positive, else
-// one full wave of resident CTAs of `kernel` (launched with `threads` threads
-// per CTA) on the current device; capped at `tiles`.  Returns 0 (with *err
-// set) if the device cannot be queried.
-int grid_for(const void *kernel, int threads, long long tiles, int ctas, cudaError_t *err);
+// CTAs for a grid-stride launch over `tiles` work units: `ctas` if positive,
+// else `waves` full waves of resident CTAs of `kernel` (launched with
+// `threads` threads per CTA) on the current device; capped at `tiles`.
+// Returns 0 (with *err set) if the device cannot be queried.
+int grid_for(const void *kernel, int threads, long long tiles, int ctas, int waves, cudaError_t *err);
 
 cudaError_t launch_encode(int bits, int dtype, const void *x, long long n, void *wire,
                           cudaStream_t s);

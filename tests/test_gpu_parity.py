@@ -147,9 +147,24 @@ def test_fused_with_16_byte_aligned_pointers(bits):
     ptrs = [b.data_ptr() + 16 for b in bufs]
     assert all(p % 32 == 16 for p in ptrs)
     assert capi.qr_allreduce(bits, dtype, R, ptrs, n, yb.data_ptr() + 16, st) == qr.QR_OK
+    # the unfused kernels on the same 16-byte-aligned pointers
+    W = qr.qr_wire_bytes(bits, n)
+    wb = [torch.zeros(W + 64, dtype=torch.uint8, device="cuda") for _ in range(R + 1)]
+    yu = torch.zeros(2 * n + 64, dtype=torch.uint8, device="cuda")
+    wp = [b.data_ptr() + 16 for b in wb]
+    for r in range(R):
+        assert capi.qr_encode(bits, dtype, ptrs[r], n, wp[r], st) == qr.QR_OK
+    assert capi.qr_segment_reduce(bits, R, wp[:R], n, wp[R], st) == qr.QR_OK
+    assert capi.qr_decode(bits, dtype, wp[R], n, yu.data_ptr() + 16, st) == qr.QR_OK
     torch.cuda.synchronize()
+    w_ref = [oracle.encode(bits, dtype, x) for x in xs]
+    for r in range(R):
+        assert_wire_equal(to_host_u8(wb[r])[16:16 + W], w_ref[r], bits, f"16B-aligned encode {r}")
+    assert_wire_equal(to_host_u8(wb[R])[16:16 + W], oracle.segment_reduce(bits, w_ref, n), bits, "16B reduce")
+    y_ref = oracle.allreduce(bits, dtype, xs)
     got = to_host_u8(yb)[16:16 + 2 * n].copy().view(np.uint16)
-    assert np.array_equal(got, oracle.allreduce(bits, dtype, xs))
+    assert np.array_equal(got, y_ref)
+    assert np.array_equal(to_host_u8(yu)[16:16 + 2 * n].copy().view(np.uint16), y_ref)
 
 
 GUARD = 4096  # canary bytes before and after every buffer
