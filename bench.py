@@ -248,10 +248,15 @@ def measured_hbm() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
-def csrc_hash() -> str:
+# The sources that determine the benchmarked kernel's code and launch shape.
+FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_allreduce16.cuh", "qr_allreduce16_b3.cu",
+                   "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_launch.h", "qr_capi.cu")
+
+
+def csrc_hash(files=FUSED16_SOURCES) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "bit_quantized_all_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -75,6 +75,15 @@ def _bind(path: str) -> ctypes.CDLL:
         "orc_decode": (i32, [i32, i32, u8p, sz, u16p]),
         "orc_segment_reduce": (i32, [i32, i32, ctypes.POINTER(u8p), sz, u8p]),
         "orc_allreduce": (i32, [i32, i32, i32, ctypes.POINTER(u16p), sz, u16p]),
+        "orc_fc_tile_bytes": (sz, [i32]),
+        "orc_fc_wire_bytes": (sz, [i32, sz]),
+        "orc_fc_quantize_group": (i32, [i32, f32p, u8p, f32p, f32p]),
+        "orc_fc_encode_f32": (i32, [i32, f32p, sz, u8p]),
+        "orc_fc_encode": (i32, [i32, i32, u16p, sz, u8p]),
+        "orc_fc_decode_f32": (i32, [i32, u8p, sz, f32p]),
+        "orc_fc_decode": (i32, [i32, i32, u8p, sz, u16p]),
+        "orc_fc_segment_reduce": (i32, [i32, i32, i32, ctypes.POINTER(u8p), sz, u8p]),
+        "orc_fc_allreduce": (i32, [i32, i32, i32, i32, ctypes.POINTER(u16p), sz, u16p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -257,4 +266,81 @@ def allreduce(bits: int, dtype: int, xs) -> np.ndarray:
     arr = (ctypes.POINTER(ctypes.c_uint16) * len(xs))(*[_p(x, ctypes.c_uint16) for x in xs])
     y = np.empty(n, np.uint16)
     _check(lib().orc_allreduce(bits, dtype, len(xs), arr, n, _p(y, ctypes.c_uint16)), "allreduce")
+    return y
+
+
+# ---- the Flash Communication codec (asymmetric, groups of 128) -------------
+
+FC_BITS = (4, 8)
+
+
+def fc_tile_bytes(bits: int) -> int:
+    return int(lib().orc_fc_tile_bytes(bits))
+
+
+def fc_wire_bytes(bits: int, n: int) -> int:
+    return int(lib().orc_fc_wire_bytes(bits, n))
+
+
+def fc_quantize_group(bits: int, x):
+    """x: 128 fp32 values -> (codes uint8[128], scale, zero point)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.size == 128
+    u = np.empty(128, np.uint8)
+    s = np.zeros(1, np.float32)
+    z = np.zeros(1, np.float32)
+    _check(lib().orc_fc_quantize_group(bits, _p(x, ctypes.c_float), _p(u, ctypes.c_uint8),
+                                       _p(s, ctypes.c_float), _p(z, ctypes.c_float)), "fc_quantize_group")
+    return u, float(s[0]), float(z[0])
+
+
+def fc_encode_f32(bits: int, x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    w = np.empty(fc_wire_bytes(bits, x.size), np.uint8)
+    _check(lib().orc_fc_encode_f32(bits, _p(x, ctypes.c_float), x.size, _p(w, ctypes.c_uint8)), "fc_encode_f32")
+    return w
+
+
+def fc_encode(bits: int, dtype: int, x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.uint16).reshape(-1)
+    w = np.empty(fc_wire_bytes(bits, x.size), np.uint8)
+    _check(lib().orc_fc_encode(bits, dtype, _p(x, ctypes.c_uint16), x.size, _p(w, ctypes.c_uint8)), "fc_encode")
+    return w
+
+
+def fc_decode_f32(bits: int, wire, n: int) -> np.ndarray:
+    wire = np.ascontiguousarray(wire, dtype=np.uint8)
+    assert wire.size >= fc_wire_bytes(bits, n)
+    out = np.empty(n, np.float32)
+    _check(lib().orc_fc_decode_f32(bits, _p(wire, ctypes.c_uint8), n, _p(out, ctypes.c_float)), "fc_decode_f32")
+    return out
+
+
+def fc_decode(bits: int, dtype: int, wire, n: int) -> np.ndarray:
+    wire = np.ascontiguousarray(wire, dtype=np.uint8)
+    assert wire.size >= fc_wire_bytes(bits, n)
+    y = np.empty(n, np.uint16)
+    _check(lib().orc_fc_decode(bits, dtype, _p(wire, ctypes.c_uint8), n, _p(y, ctypes.c_uint16)), "fc_decode")
+    return y
+
+
+def fc_segment_reduce(bits_in: int, bits_out: int, wires, n: int) -> np.ndarray:
+    ws = [np.ascontiguousarray(w, dtype=np.uint8) for w in wires]
+    for w in ws:
+        assert w.size >= fc_wire_bytes(bits_in, n)
+    arr = (ctypes.POINTER(ctypes.c_uint8) * len(ws))(*[_p(w, ctypes.c_uint8) for w in ws])
+    out = np.empty(fc_wire_bytes(bits_out, n), np.uint8)
+    _check(lib().orc_fc_segment_reduce(bits_in, bits_out, len(ws), arr, n, _p(out, ctypes.c_uint8)),
+           "fc_segment_reduce")
+    return out
+
+
+def fc_allreduce(bits_rs: int, bits_ag: int, dtype: int, xs) -> np.ndarray:
+    xs = [np.ascontiguousarray(x, dtype=np.uint16).reshape(-1) for x in xs]
+    n = xs[0].size
+    assert all(x.size == n for x in xs)
+    arr = (ctypes.POINTER(ctypes.c_uint16) * len(xs))(*[_p(x, ctypes.c_uint16) for x in xs])
+    y = np.empty(n, np.uint16)
+    _check(lib().orc_fc_allreduce(bits_rs, bits_ag, dtype, len(xs), arr, n, _p(y, ctypes.c_uint16)),
+           "fc_allreduce")
     return y

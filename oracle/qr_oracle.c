@@ -466,3 +466,207 @@ done:
     free(red);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The Flash Communication codec: asymmetric quantization in groups of 128   */
+/* [FC key machinery "asymmetric group-128 scaling"; pith summary "group     */
+/* size 128", "INT4 for the reduce stage and INT8 for the gather stage";     */
+/* minor comments on "INT6" and Algorithm 1's Dequantize(M_q, z, s)].        */
+/* ------------------------------------------------------------------------ */
+
+#define FC_GROUP 128
+#define FC_NGROUP (TILE / FC_GROUP)
+
+static int fc_bits_ok(int bits) { return bits == 4 || bits == 8; }
+
+size_t orc_fc_tile_bytes(int bits)
+{
+    return fc_bits_ok(bits) ? (size_t)256 * (size_t)bits + 128 : 0;
+}
+
+size_t orc_fc_wire_bytes(int bits, size_t n)
+{
+    return ((n + TILE - 1) / TILE) * orc_fc_tile_bytes(bits);
+}
+
+static void put_f32(uint8_t *p, float f)
+{
+    uint32_t v;
+    memcpy(&v, &f, sizeof v);
+    put_u32(p, v);
+}
+
+static float get_f32(const uint8_t *p)
+{
+    uint32_t v = get_u32(p);
+    float f;
+    memcpy(&f, &v, sizeof f);
+    return f;
+}
+
+/* One group of 128 values: zero point = minimum, scale = range / (2^b - 1),
+ * codes = nearest integer of (x - z) / s, ties to even, at most 2^b - 1. */
+int orc_fc_quantize_group(int bits, const float *x, uint8_t *u, float *scale, float *zero)
+{
+    if (!fc_bits_ok(bits)) return -1;
+    const int umax = (1 << bits) - 1;
+    float lo = x[0], hi = x[0];
+    int i;
+    for (i = 0; i < FC_GROUP; ++i) {
+        if (!isfinite(x[i])) return -1;
+        if (x[i] < lo) lo = x[i];
+        if (x[i] > hi) hi = x[i];
+    }
+    float range = hi - lo;
+    if (!isfinite(range)) return -1; /* a range beyond fp32 is outside the contract */
+    float s = range / (float)umax;
+    if (!(s >= 0x1p-126f)) s = 0.0f; /* zero or subnormal: every code 0 */
+    *zero = lo;
+    *scale = s;
+    if (s == 0.0f) {
+        for (i = 0; i < FC_GROUP; ++i) u[i] = 0;
+        return 0;
+    }
+    float r = 1.0f / s;
+    for (i = 0; i < FC_GROUP; ++i) {
+        float t = (x[i] - lo) * r;
+        float q = round_half_even(t); /* t >= 0 */
+        if (q > (float)umax) q = (float)umax;
+        u[i] = (uint8_t)q;
+    }
+    return 0;
+}
+
+static int fc_encode_tile(int bits, const float *x, uint8_t *tile)
+{
+    uint8_t u[TILE];
+    const size_t meta = (size_t)256 * (size_t)bits;
+    for (int g = 0; g < FC_NGROUP; ++g) {
+        float s, z;
+        if (orc_fc_quantize_group(bits, x + FC_GROUP * g, u + FC_GROUP * g, &s, &z) != 0) return -1;
+        put_f32(tile + meta + 4 * (size_t)g, s);
+        put_f32(tile + meta + 64 + 4 * (size_t)g, z);
+    }
+    for (int k = 0; k < NSLOT; ++k) pack_slot(bits, u + 8 * k, tile, k);
+    return 0;
+}
+
+/* decode = u*s + z with one rounding */
+static void fc_decode_tile_f32(int bits, const uint8_t *tile, float *out)
+{
+    uint8_t u[TILE];
+    const size_t meta = (size_t)256 * (size_t)bits;
+    for (int k = 0; k < NSLOT; ++k) unpack_slot(bits, tile, k, u + 8 * k);
+    for (int g = 0; g < FC_NGROUP; ++g) {
+        float s = get_f32(tile + meta + 4 * (size_t)g);
+        float z = get_f32(tile + meta + 64 + 4 * (size_t)g);
+        for (int i = 0; i < FC_GROUP; ++i) out[FC_GROUP * g + i] = fmaf((float)u[FC_GROUP * g + i], s, z);
+    }
+}
+
+int orc_fc_encode_f32(int bits, const float *x, size_t n, uint8_t *wire)
+{
+    if (!fc_bits_ok(bits)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        for (size_t i = 0; i < TILE; ++i) {
+            size_t idx = t * TILE + i;
+            buf[i] = idx < n ? x[idx] : 0.0f;
+        }
+        if (fc_encode_tile(bits, buf, wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+int orc_fc_encode(int bits, int dtype, const uint16_t *x, size_t n, uint8_t *wire)
+{
+    if (!fc_bits_ok(bits) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        for (size_t i = 0; i < TILE; ++i) {
+            size_t idx = t * TILE + i;
+            buf[i] = idx < n ? widen(dtype, x[idx]) : 0.0f;
+        }
+        if (fc_encode_tile(bits, buf, wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+int orc_fc_decode_f32(int bits, const uint8_t *wire, size_t n, float *out)
+{
+    if (!fc_bits_ok(bits)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        fc_decode_tile_f32(bits, wire + t * tb, buf);
+        for (size_t i = 0; i < TILE && t * TILE + i < n; ++i) out[t * TILE + i] = buf[i];
+    }
+    return 0;
+}
+
+int orc_fc_decode(int bits, int dtype, const uint8_t *wire, size_t n, uint16_t *y)
+{
+    if (!fc_bits_ok(bits) || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fc_tile_bytes(bits);
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        fc_decode_tile_f32(bits, wire + t * tb, buf);
+        for (size_t i = 0; i < TILE && t * TILE + i < n; ++i) y[t * TILE + i] = narrow(dtype, buf[i]);
+    }
+    return 0;
+}
+
+/* Phase-1B: decode the R rank copies (bits_in), add in fp32 in rank order,
+ * re-quantize the sums (bits_out: 8 for the pages' "INT6" mixed scheme).
+ * Values at or past n are zero in every phase: an asymmetric code does not
+ * decode a padded zero back to exactly 0, so the sums there are set to 0
+ * again before re-quantization. */
+int orc_fc_segment_reduce(int bits_in, int bits_out, int R, const uint8_t *const *wires,
+                          size_t n, uint8_t *out_wire)
+{
+    if (!fc_bits_ok(bits_in) || !fc_bits_ok(bits_out) || R < 1) return -1;
+    size_t T = (n + TILE - 1) / TILE;
+    size_t tbi = orc_fc_tile_bytes(bits_in), tbo = orc_fc_tile_bytes(bits_out);
+    float acc[TILE], y[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        fc_decode_tile_f32(bits_in, wires[0] + t * tbi, acc);
+        for (int r = 1; r < R; ++r) {
+            fc_decode_tile_f32(bits_in, wires[r] + t * tbi, y);
+            for (int i = 0; i < TILE; ++i) acc[i] = acc[i] + y[i];
+        }
+        for (size_t i = 0; i < TILE; ++i)
+            if (t * TILE + i >= n) acc[i] = 0.0f;
+        if (fc_encode_tile(bits_out, acc, out_wire + t * tbo) != 0) return -1;
+    }
+    return 0;
+}
+
+/* quantize (bits_rs) -> all-to-all -> local sum -> re-quantize (bits_ag) ->
+ * all-gather -> dequantize: two quantization round trips. */
+int orc_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, const uint16_t *const *x,
+                     size_t n, uint16_t *y)
+{
+    if (!fc_bits_ok(bits_rs) || !fc_bits_ok(bits_ag) || R < 1 ||
+        (dtype != ORC_FP16 && dtype != ORC_BF16))
+        return -1;
+    size_t W = orc_fc_wire_bytes(bits_rs, n), W2 = orc_fc_wire_bytes(bits_ag, n);
+    int rc = -1;
+    uint8_t **wires = (uint8_t **)calloc((size_t)R, sizeof *wires);
+    uint8_t *red = (uint8_t *)malloc(W2 ? W2 : 1);
+    if (!wires || !red) goto done;
+    for (int r = 0; r < R; ++r) {
+        wires[r] = (uint8_t *)malloc(W ? W : 1);
+        if (!wires[r]) goto done;
+        if (orc_fc_encode(bits_rs, dtype, x[r], n, wires[r]) != 0) goto done;
+    }
+    if (orc_fc_segment_reduce(bits_rs, bits_ag, R, (const uint8_t *const *)wires, n, red) != 0) goto done;
+    rc = orc_fc_decode(bits_ag, dtype, red, n, y);
+done:
+    if (wires)
+        for (int r = 0; r < R; ++r) free(wires[r]);
+    free(wires);
+    free(red);
+    return rc;
+}

@@ -101,6 +101,39 @@ int orc_segment_reduce(int bits, int R, const uint8_t *const *wires, size_t n,
 int orc_allreduce(int bits, int dtype, int R, const uint16_t *const *x,
                   size_t n, uint16_t *y);
 
+/* ---- the Flash Communication codec (asymmetric, groups of 128) ----------
+ * "Flash Communication" review record (arXiv 2412.04964): activations are
+ * quantized "with asymmetric group-128 scaling" to 4-8 bits, exchanged,
+ * summed locally, "re-quantizes the partial sums to INT8", all-gathered and
+ * dequantized; "INT6" names the mixed scheme INT4 for the reduce-scatter and
+ * INT8 for the all-gather; Algorithm 1 dequantizes from the codes, a zero
+ * point z and a scale s.  Readings (the pages fix no more than that):
+ *   per group of 128: lo = min x, hi = max x (fp32, exact);
+ *   s = fp32_RN(fp32_RN(hi - lo) / (2^b - 1));  z = lo;
+ *   s below 2^-126 (zero or subnormal) is stored as 0 and every code is 0;
+ *   r = fp32_RN(1/s);  u = min(RNE(fp32_RN(fp32_RN(x - z) * r)), 2^b - 1);
+ *   decode = fp32_RN(u*s + z) (one rounding, a fused multiply-add);
+ *   Phase-1B: acc = decode_0, acc = fp32_RN(acc + decode_r), r = 1..R-1;
+ *   values at or past n are zero in every phase (Phase-1B sets the sums
+ *   there back to 0: a padded zero does not decode to exactly 0);
+ *   s and z are stored as fp32 (every fp16/bf16 input and every fp32 partial
+ *   sum fits); b is 4 or 8.
+ * Tile of 2048 values = 16 groups: codes as in the symmetric codec (INT4
+ * nibbles lane j at bits 4j of the u32 at 4k; INT8 bytes), then 16 fp32
+ * scales at 256*b, then 16 fp32 zero points at 256*b + 64: 256*b + 128 bytes.
+ */
+size_t orc_fc_tile_bytes(int bits);           /* 256*bits + 128, 0 unless bits is 4 or 8 */
+size_t orc_fc_wire_bytes(int bits, size_t n);
+int orc_fc_quantize_group(int bits, const float *x, uint8_t *u, float *scale, float *zero);
+int orc_fc_encode_f32(int bits, const float *x, size_t n, uint8_t *wire);
+int orc_fc_encode(int bits, int dtype, const uint16_t *x, size_t n, uint8_t *wire);
+int orc_fc_decode_f32(int bits, const uint8_t *wire, size_t n, float *out);
+int orc_fc_decode(int bits, int dtype, const uint8_t *wire, size_t n, uint16_t *y);
+int orc_fc_segment_reduce(int bits_in, int bits_out, int R, const uint8_t *const *wires,
+                          size_t n, uint8_t *out_wire);
+int orc_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, const uint16_t *const *x,
+                     size_t n, uint16_t *y);
+
 #ifdef __cplusplus
 }
 #endif

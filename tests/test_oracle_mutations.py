@@ -15,6 +15,7 @@ import oracle
 import test_oracle_formats as F
 import test_oracle_layout as L
 import test_oracle_quantizer as Q
+import test_oracle_fc as FC
 import test_oracle_reduce as Rd
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "qr_oracle.c")
@@ -48,6 +49,25 @@ MUTATIONS = [
     ("bf16_subnormal_quantum_wrong", [("ldexp(1.0, -133) : ldexp(1.0, E - 7)", "ldexp(1.0, -132) : ldexp(1.0, E - 7)")]),
     ("zero_scale_codes_not_bias", [("for (i = 0; i < BLOCK; ++i) u[i] = (uint8_t)bias;",
                                     "for (i = 0; i < BLOCK; ++i) u[i] = 0;")]),
+    # the Flash Communication codec
+    ("fc_zero_point_is_max", [("    *zero = lo;", "    *zero = hi;")]),
+    ("fc_scale_over_2b", [("float s = range / (float)umax;", "float s = range / (float)(umax + 1);")]),
+    # (Removing the cap at 2^b - 1 is not a mistake the pins could catch: it
+    # never fires, since t <= range * RN(1/RN(range/umax)) <= umax*(1+2^-24)^3
+    # < umax + 1/2.)
+    ("fc_decode_two_roundings", [("fmaf((float)u[FC_GROUP * g + i], s, z)", "(float)u[FC_GROUP * g + i] * s + z")]),
+    ("fc_truncate_not_round", [("        float q = round_half_even(t); /* t >= 0 */", "        float q = floorf(t);")]),
+    ("fc_reduce_drops_rank0", [("fc_decode_tile_f32(bits_in, wires[0] + t * tbi, acc);",
+                                "memset(acc, 0, sizeof acc);")]),
+    ("fc_reduce_reverse_order",
+     [("fc_decode_tile_f32(bits_in, wires[0] + t * tbi, acc);",
+       "fc_decode_tile_f32(bits_in, wires[R - 1] + t * tbi, acc);"),
+      ("fc_decode_tile_f32(bits_in, wires[r] + t * tbi, y);",
+       "fc_decode_tile_f32(bits_in, wires[R - 1 - r] + t * tbi, y);")]),
+    ("fc_tail_not_repadded", [("            if (t * TILE + i >= n) acc[i] = 0.0f;", "            ;")]),
+    ("fc_zero_points_at_wrong_offset", [("meta + 64 + 4 * (size_t)g", "meta + 60 + 4 * (size_t)g")]),
+    ("fc_reduce_reencodes_at_input_width", [("if (fc_encode_tile(bits_out, acc, out_wire + t * tbo) != 0) return -1;",
+                                             "if (fc_encode_tile(bits_in, acc, out_wire + t * tbo) != 0) return -1;")]),
 ]
 
 
@@ -74,6 +94,21 @@ def _battery(orc):
     for fmt in ("f16", "bf16"):
         yield lambda fmt=fmt: F.test_narrow_ties_and_neighbours(orc, fmt)
         yield lambda fmt=fmt: F.test_narrow_roundtrips_every_value(orc, fmt)
+    # the Flash Communication codec
+    for c in FC._cases():
+        for d in (0, 1):
+            yield lambda c=c, d=d: FC.test_known_answer_tiles(orc, c, d)
+    yield lambda: FC.test_decode_is_one_fused_rounding(orc)
+    for b in (4, 8):
+        yield lambda b=b: FC.test_constant_groups_are_exact(orc, b)
+        yield lambda b=b: FC.test_min_decodes_exactly_and_codes_span_the_range(orc, b)
+        yield lambda b=b: FC.test_codes_are_nearest_integers(orc, b)
+        yield lambda b=b: FC.test_error_bound(orc, b)
+        yield lambda b=b: FC.test_one_rank_and_mixed_widths(orc, b, 1)
+        yield lambda b=b: FC.test_identical_ranks_on_exact_grids(orc, b, 4)
+    yield lambda: FC.test_two_ranks_commute_and_rank_order(orc)
+    for brs, bag in ((4, 8), (8, 8)):
+        yield lambda brs=brs, bag=bag: FC.test_error_bound_against_exact_sum(orc, brs, bag, 3)
 
 
 @pytest.mark.parametrize("name,edits", MUTATIONS, ids=[m[0] for m in MUTATIONS])
