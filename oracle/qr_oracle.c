@@ -521,7 +521,11 @@ int orc_fc_quantize_group(int bits, const float *x, uint8_t *u, float *scale, fl
     if (!isfinite(range)) return -1; /* a range beyond fp32 is outside the contract */
     float s = range / (float)umax;
     if (!(s >= 0x1p-126f)) s = 0.0f; /* zero or subnormal: every code 0 */
-    *zero = lo;
+    /* The zero point is the minimum as a value: -0 and +0 are the same value,
+     * and a zero minimum is stored as +0 (lo + 0 turns -0 into +0 and leaves
+     * every other value unchanged). */
+    float z = lo + 0.0f;
+    *zero = z;
     *scale = s;
     if (s == 0.0f) {
         for (i = 0; i < FC_GROUP; ++i) u[i] = 0;
@@ -529,7 +533,7 @@ int orc_fc_quantize_group(int bits, const float *x, uint8_t *u, float *scale, fl
     }
     float r = 1.0f / s;
     for (i = 0; i < FC_GROUP; ++i) {
-        float t = (x[i] - lo) * r;
+        float t = (x[i] - z) * r;
         float q = round_half_even(t); /* t >= 0 */
         if (q > (float)umax) q = (float)umax;
         u[i] = (uint8_t)q;

@@ -109,7 +109,8 @@ int orc_allreduce(int bits, int dtype, int R, const uint16_t *const *x,
  * INT8 for the all-gather; Algorithm 1 dequantizes from the codes, a zero
  * point z and a scale s.  Readings (the pages fix no more than that):
  *   per group of 128: lo = min x, hi = max x (fp32, exact);
- *   s = fp32_RN(fp32_RN(hi - lo) / (2^b - 1));  z = lo;
+ *   s = fp32_RN(fp32_RN(hi - lo) / (2^b - 1));  z = lo (a zero minimum, of
+ *   either sign, stored as +0);
  *   s below 2^-126 (zero or subnormal) is stored as 0 and every code is 0;
  *   r = fp32_RN(1/s);  u = min(RNE(fp32_RN(fp32_RN(x - z) * r)), 2^b - 1);
  *   decode = fp32_RN(u*s + z) (one rounding, a fused multiply-add);

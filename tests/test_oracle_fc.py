@@ -129,6 +129,21 @@ def test_error_bound(orc, bits):
     assert np.all(np.abs(xd - y) <= bound)
 
 
+def test_zero_minimum_is_stored_as_plus_zero(orc):
+    """-0 and +0 are the same value: a group whose minimum is zero stores the
+    zero point +0 whichever sign its zeros carry, and its code-0 values
+    decode to +0."""
+    for first in (-0.0, 0.0):
+        g = np.zeros(128, np.float32)
+        g[0], g[1], g[5] = first, -0.0, 2.5
+        u, s, z = orc.fc_quantize_group(4, g)
+        assert np.float32(z).view(np.uint32) == 0
+        x = np.zeros(2048, np.float32)
+        x[:128] = g
+        y = orc.fc_decode(4, 1, orc.fc_encode_f32(4, x), 2048)
+        assert y[0] == 0 and y[1] == 0  # +0 bit patterns
+
+
 def test_decode_is_one_fused_rounding(orc):
     """INT4 group with minimum -1 and maximum 4: s = RN(5/15) = RN(1/3) =
     0.3333333432674408, r = RN(1/s) = 3, and the value 0 gets code 3.  With one

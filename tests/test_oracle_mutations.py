@@ -50,7 +50,8 @@ MUTATIONS = [
     ("zero_scale_codes_not_bias", [("for (i = 0; i < BLOCK; ++i) u[i] = (uint8_t)bias;",
                                     "for (i = 0; i < BLOCK; ++i) u[i] = 0;")]),
     # the Flash Communication codec
-    ("fc_zero_point_is_max", [("    *zero = lo;", "    *zero = hi;")]),
+    ("fc_zero_point_is_max", [("    float z = lo + 0.0f;", "    float z = hi + 0.0f;")]),
+    ("fc_zero_point_sign_kept", [("    float z = lo + 0.0f;", "    float z = lo;")]),
     ("fc_scale_over_2b", [("float s = range / (float)umax;", "float s = range / (float)(umax + 1);")]),
     # (Removing the cap at 2^b - 1 is not a mistake the pins could catch: it
     # never fires, since t <= range * RN(1/RN(range/umax)) <= umax*(1+2^-24)^3
@@ -99,6 +100,7 @@ def _battery(orc):
         for d in (0, 1):
             yield lambda c=c, d=d: FC.test_known_answer_tiles(orc, c, d)
     yield lambda: FC.test_decode_is_one_fused_rounding(orc)
+    yield lambda: FC.test_zero_minimum_is_stored_as_plus_zero(orc)
     for b in (4, 8):
         yield lambda b=b: FC.test_constant_groups_are_exact(orc, b)
         yield lambda b=b: FC.test_min_decodes_exactly_and_codes_span_the_range(orc, b)
