@@ -35,7 +35,11 @@ QR_MAX_RANKS = 8
 BITS = (3, 4, 6, 8)
 
 EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_segment_reduce",
-           "qr_decode", "qr_allreduce", "qr_allreduce_emit", "qr_allreduce_ctas", "qr_status_string")
+           "qr_decode", "qr_allreduce", "qr_allreduce_emit", "qr_allreduce_ctas", "qr_status_string",
+           "qr_fc_tile_bytes", "qr_fc_wire_bytes", "qr_fc_encode", "qr_fc_segment_reduce", "qr_fc_decode",
+           "qr_fc_allreduce")
+FC_BITS = (4, 8)
+FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +78,12 @@ def lib() -> ctypes.CDLL:
                 "qr_allreduce_emit": (i32, [i32, i32, i32, vpp, sz, vp, vpp, vp, vp]),
                 "qr_allreduce_ctas": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_status_string": (ctypes.c_char_p, [i32]),
+                "qr_fc_tile_bytes": (sz, [i32]),
+                "qr_fc_wire_bytes": (sz, [i32, sz]),
+                "qr_fc_encode": (i32, [i32, i32, vp, sz, vp, vp]),
+                "qr_fc_segment_reduce": (i32, [i32, i32, i32, vpp, sz, vp, vp]),
+                "qr_fc_decode": (i32, [i32, i32, vp, sz, vp, vp]),
+                "qr_fc_allreduce": (i32, [i32, i32, i32, i32, vpp, sz, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -129,6 +139,22 @@ class capi:
     @staticmethod
     def qr_allreduce_ctas(bits, dtype, R, xs, n, y, ctas, stream=None):
         return lib().qr_allreduce_ctas(bits, dtype, R, _ptr_array(xs), n, y, ctas, stream)
+
+    @staticmethod
+    def qr_fc_encode(bits, dtype, x, n, wire, stream=None):
+        return lib().qr_fc_encode(bits, dtype, x, n, wire, stream)
+
+    @staticmethod
+    def qr_fc_decode(bits, dtype, wire, n, y, stream=None):
+        return lib().qr_fc_decode(bits, dtype, wire, n, y, stream)
+
+    @staticmethod
+    def qr_fc_segment_reduce(bits_in, bits_out, R, wires, n, out, stream=None):
+        return lib().qr_fc_segment_reduce(bits_in, bits_out, R, _ptr_array(wires), n, out, stream)
+
+    @staticmethod
+    def qr_fc_allreduce(bits_rs, bits_ag, dtype, R, xs, n, y, stream=None):
+        return lib().qr_fc_allreduce(bits_rs, bits_ag, dtype, R, _ptr_array(xs), n, y, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -300,3 +326,83 @@ def qr_allreduce_emit(bits: int, xs, y: torch.Tensor | None = None, wire_out=Non
                                   [w.data_ptr() for w in wire_out], red_out.data_ptr(),
                                   _stream(dev, stream)), "qr_allreduce_emit")
     return y, wire_out, red_out
+
+
+# ---------------------------------------------------------------------------
+# the Flash Communication codec (asymmetric groups of 128)
+# ---------------------------------------------------------------------------
+def qr_fc_tile_bytes(bits: int) -> int:
+    return int(lib().qr_fc_tile_bytes(bits))
+
+
+def qr_fc_wire_bytes(bits: int, n: int) -> int:
+    return int(lib().qr_fc_wire_bytes(bits, n))
+
+
+def _fc_wire_tensor(t: torch.Tensor, bits: int, n: int, what: str) -> None:
+    _cuda_contig(t, what)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{what} must be torch.uint8 (a packed wire), got {t.dtype}")
+    need = qr_fc_wire_bytes(bits, n)
+    if t.numel() < need:
+        raise ValueError(f"{what} holds {t.numel()} bytes; {need} are needed for {n} values at INT{bits}")
+
+
+def qr_fc_encode(bits: int, x: torch.Tensor, wire: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Send path of the asymmetric group-128 codec."""
+    _cuda_contig(x, "x")
+    dt = _dtype_code(x, "x")
+    n = x.numel()
+    if wire is None:
+        wire = torch.empty(qr_fc_wire_bytes(bits, n), dtype=torch.uint8, device=x.device)
+    _fc_wire_tensor(wire, bits, n, "wire")
+    _same_device([x, wire], "qr_fc_encode")
+    _check(capi.qr_fc_encode(bits, dt, x.data_ptr(), n, wire.data_ptr(), _stream(x.device, stream)), "qr_fc_encode")
+    return wire
+
+
+def qr_fc_decode(bits: int, wire: torch.Tensor, n: int, dtype: torch.dtype = torch.bfloat16,
+                 y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _fc_wire_tensor(wire, bits, n, "wire")
+    if y is None:
+        if dtype not in _DTYPES:
+            raise TypeError(f"dtype must be torch.float16 or torch.bfloat16, got {dtype}")
+        y = torch.empty(n, dtype=dtype, device=wire.device)
+    _cuda_contig(y, "y")
+    dt = _dtype_code(y, "y")
+    if y.numel() != n:
+        raise ValueError(f"y holds {y.numel()} values, expected {n}")
+    _same_device([wire, y], "qr_fc_decode")
+    _check(capi.qr_fc_decode(bits, dt, wire.data_ptr(), n, y.data_ptr(), _stream(y.device, stream)), "qr_fc_decode")
+    return y
+
+
+def qr_fc_segment_reduce(bits_in: int, bits_out: int, wires, n: int, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    wires = list(wires)
+    if not 1 <= len(wires) <= QR_MAX_RANKS:
+        raise ValueError(f"1 to {QR_MAX_RANKS} wires are supported, got {len(wires)}")
+    for i, w in enumerate(wires):
+        _fc_wire_tensor(w, bits_in, n, f"wires[{i}]")
+    if out is None:
+        out = torch.empty(qr_fc_wire_bytes(bits_out, n), dtype=torch.uint8, device=wires[0].device)
+    _fc_wire_tensor(out, bits_out, n, "out")
+    dev = _same_device(wires + [out], "qr_fc_segment_reduce")
+    _check(capi.qr_fc_segment_reduce(bits_in, bits_out, len(wires), [w.data_ptr() for w in wires], n,
+                                     out.data_ptr(), _stream(dev, stream)), "qr_fc_segment_reduce")
+    return out
+
+
+def qr_fc_allreduce(bits_rs: int, bits_ag: int, xs, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The fused two-shot all-reduce with the asymmetric group-128 codec:
+    reduce-scatter at bits_rs, all-gather at bits_ag ((4, 8) is "INT6")."""
+    xs, dt, n = _check_inputs(xs)
+    if y is None:
+        y = torch.empty_like(xs[0])
+    _cuda_contig(y, "y")
+    if y.dtype != xs[0].dtype or y.numel() != n:
+        raise ValueError("y must match the inputs' dtype and size")
+    dev = _same_device(xs + [y], "qr_fc_allreduce")
+    _check(capi.qr_fc_allreduce(bits_rs, bits_ag, dt, len(xs), [x.data_ptr() for x in xs], n, y.data_ptr(),
+                                _stream(dev, stream)), "qr_fc_allreduce")
+    return y

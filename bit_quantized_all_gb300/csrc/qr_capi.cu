@@ -96,6 +96,86 @@ QR_EXPORT size_t qr_tile_bytes(int bits) { return tile_bytes(bits); }
 
 QR_EXPORT size_t qr_wire_bytes(int bits, size_t n) { return wire_bytes(bits, n); }
 
+namespace {
+
+bool fc_bits_ok(int bits) { return bits == 4 || bits == 8; }
+bool fc_pair_ok(int rs, int ag) { return (rs == 4 && ag == 4) || (rs == 4 && ag == 8) || (rs == 8 && ag == 8); }
+
+size_t fc_wire_bytes(int bits, size_t n) {
+    if (!fc_bits_ok(bits)) return 0;
+    const size_t tb = size_t(256) * size_t(bits) + 128;
+    const size_t tiles = n / kTile + (n % kTile != 0);
+    if (tiles > SIZE_MAX / tb) return 0;
+    return tiles * tb;
+}
+
+}  // namespace
+
+QR_EXPORT size_t qr_fc_tile_bytes(int bits) { return fc_bits_ok(bits) ? size_t(256) * size_t(bits) + 128 : 0; }
+
+QR_EXPORT size_t qr_fc_wire_bytes(int bits, size_t n) { return fc_wire_bytes(bits, n); }
+
+QR_EXPORT qr_status_t qr_fc_encode(int bits, qr_dtype_t dtype, const void *x, size_t n, void *wire,
+                                   qr_stream_t stream) {
+    if (!x || !wire || n == 0) return QR_ERR_INVALID_ARG;
+    if (!fc_bits_ok(bits) || !dtype_ok(dtype)) return QR_ERR_UNSUPPORTED;
+    const size_t W = fc_wire_bytes(bits, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(x) || !aligned16(wire)) return QR_ERR_MISALIGNED;
+    if (overlaps(wire, W, x, 2 * n)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_fc_encode(bits, dtype, x, static_cast<long long>(n), wire,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_fc_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n, void *y,
+                                   qr_stream_t stream) {
+    if (!wire || !y || n == 0) return QR_ERR_INVALID_ARG;
+    if (!fc_bits_ok(bits) || !dtype_ok(dtype)) return QR_ERR_UNSUPPORTED;
+    const size_t W = fc_wire_bytes(bits, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(wire) || !aligned16(y)) return QR_ERR_MISALIGNED;
+    if (overlaps(y, 2 * n, wire, W)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_fc_decode(bits, dtype, wire, static_cast<long long>(n), y,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R, const void *const *wires, size_t n,
+                                           void *out_wire, qr_stream_t stream) {
+    if (!wires || !out_wire || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!wires[r]) return QR_ERR_INVALID_ARG;
+    if (!fc_pair_ok(bits_in, bits_out) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    const size_t Wi = fc_wire_bytes(bits_in, n), Wo = fc_wire_bytes(bits_out, n);
+    if (!value_bytes_ok(n) || Wi == 0 || Wo == 0) return QR_ERR_SIZE;
+    if (!aligned16(out_wire)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(wires[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r) {
+        // in place only when the widths match (the tiles then line up)
+        if (bits_in == bits_out ? bad_alias(out_wire, Wo, wires[r], Wi) : overlaps(out_wire, Wo, wires[r], Wi))
+            return QR_ERR_INVALID_ARG;
+    }
+    return from_cuda(qrk::launch_fc_reduce(bits_in, bits_out, R, wires, static_cast<long long>(n), out_wire,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_fc_allreduce(int bits_rs, int bits_ag, qr_dtype_t dtype, int R, const void *const *x,
+                                      size_t n, void *y, qr_stream_t stream) {
+    if (!x || !y || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!x[r]) return QR_ERR_INVALID_ARG;
+    if (!fc_pair_ok(bits_rs, bits_ag) || !dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    if (!value_bytes_ok(n) || fc_wire_bytes(bits_rs, n) == 0) return QR_ERR_SIZE;
+    const size_t V = 2 * n;
+    if (!aligned16(y)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(x[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (bad_alias(y, V, x[r], V)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_fc_allreduce(bits_rs, bits_ag, dtype, R, x, static_cast<long long>(n), y, 0,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QR_EXPORT const char *qr_status_string(qr_status_t status) {
     switch (status) {
         case QR_OK: return "QR_OK";

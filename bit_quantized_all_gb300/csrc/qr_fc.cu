@@ -1,0 +1,101 @@
+// qr_fc.cu -- launchers of the Flash Communication codec's encode, Phase-1B
+// reduce and decode kernels, and the width-pair dispatch of its fused
+// all-reduce.
+#include <cstdint>
+
+#include "qr_kernels_fc.cuh"
+#include "qr_launch.h"
+
+namespace qrk {
+
+template <int B, int DT, bool A32>
+static cudaError_t run_fc_encode_t(const void *x, long long n, void *wire, cudaStream_t s) {
+    const long long T = (n + kTileValues - 1) / kTileValues;
+    auto kern = fc_encode_kernel<B, DT, A32>;
+    cudaError_t err = cudaSuccess;
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, 4, &err);
+    if (grid <= 0) return err;
+    kern<<<grid, kThreadsFc, 0, s>>>(static_cast<const uint16_t *>(x), n, static_cast<uint8_t *>(wire), T);
+    return cudaGetLastError();
+}
+
+template <int B, int DT, bool A32>
+static cudaError_t run_fc_decode_t(const void *wire, long long n, void *y, cudaStream_t s) {
+    const long long T = (n + kTileValues - 1) / kTileValues;
+    auto kern = fc_decode_kernel<B, DT, A32>;
+    cudaError_t err = cudaSuccess;
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, 4, &err);
+    if (grid <= 0) return err;
+    kern<<<grid, kThreadsFc, 0, s>>>(static_cast<const uint8_t *>(wire), n, static_cast<uint16_t *>(y), T);
+    return cudaGetLastError();
+}
+
+template <int BIN, int BOUT, int R>
+static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
+    const long long T = (n + kTileValues - 1) / kTileValues;
+    auto kern = fc_reduce_kernel<BIN, BOUT, R>;
+    cudaError_t err = cudaSuccess;
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, 4, &err);
+    if (grid <= 0) return err;
+    kern<<<grid, kThreadsFc, 0, s>>>(w, n, static_cast<uint8_t *>(out), T);
+    return cudaGetLastError();
+}
+
+template <int B, int DT>
+static cudaError_t fc_encode_dt(const void *x, long long n, void *wire, cudaStream_t s) {
+    return (reinterpret_cast<uintptr_t>(x) & 31u) == 0 ? run_fc_encode_t<B, DT, true>(x, n, wire, s)
+                                                        : run_fc_encode_t<B, DT, false>(x, n, wire, s);
+}
+
+template <int B, int DT>
+static cudaError_t fc_decode_dt(const void *wire, long long n, void *y, cudaStream_t s) {
+    return (reinterpret_cast<uintptr_t>(y) & 31u) == 0 ? run_fc_decode_t<B, DT, true>(wire, n, y, s)
+                                                        : run_fc_decode_t<B, DT, false>(wire, n, y, s);
+}
+
+cudaError_t launch_fc_encode(int bits, int dtype, const void *x, long long n, void *wire, cudaStream_t s) {
+    if (bits == 4) return dtype ? fc_encode_dt<4, 1>(x, n, wire, s) : fc_encode_dt<4, 0>(x, n, wire, s);
+    if (bits == 8) return dtype ? fc_encode_dt<8, 1>(x, n, wire, s) : fc_encode_dt<8, 0>(x, n, wire, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fc_decode(int bits, int dtype, const void *wire, long long n, void *y, cudaStream_t s) {
+    if (bits == 4) return dtype ? fc_decode_dt<4, 1>(wire, n, y, s) : fc_decode_dt<4, 0>(wire, n, y, s);
+    if (bits == 8) return dtype ? fc_decode_dt<8, 1>(wire, n, y, s) : fc_decode_dt<8, 0>(wire, n, y, s);
+    return cudaErrorInvalidValue;
+}
+
+template <int BIN, int BOUT>
+static cudaError_t fc_reduce_r(int R, const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
+    switch (R) {
+        case 1: return run_fc_reduce_t<BIN, BOUT, 1>(w, n, out, s);
+        case 2: return run_fc_reduce_t<BIN, BOUT, 2>(w, n, out, s);
+        case 3: return run_fc_reduce_t<BIN, BOUT, 3>(w, n, out, s);
+        case 4: return run_fc_reduce_t<BIN, BOUT, 4>(w, n, out, s);
+        case 5: return run_fc_reduce_t<BIN, BOUT, 5>(w, n, out, s);
+        case 6: return run_fc_reduce_t<BIN, BOUT, 6>(w, n, out, s);
+        case 7: return run_fc_reduce_t<BIN, BOUT, 7>(w, n, out, s);
+        case 8: return run_fc_reduce_t<BIN, BOUT, 8>(w, n, out, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fc_reduce(int bits_in, int bits_out, int R, const void *const *wires, long long n, void *out,
+                             cudaStream_t s) {
+    ConstPtrs w{};
+    for (int r = 0; r < R; ++r) w.p[r] = wires[r];
+    if (bits_in == 4 && bits_out == 4) return fc_reduce_r<4, 4>(R, w, n, out, s);
+    if (bits_in == 4 && bits_out == 8) return fc_reduce_r<4, 8>(R, w, n, out, s);
+    if (bits_in == 8 && bits_out == 8) return fc_reduce_r<8, 8>(R, w, n, out, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, const void *const *x, long long n,
+                                void *y, int ctas, cudaStream_t s) {
+    if (bits_rs == 4 && bits_ag == 4) return run_fc_allreduce<4, 4>(dtype, R, x, n, y, ctas, s);
+    if (bits_rs == 4 && bits_ag == 8) return run_fc_allreduce<4, 8>(dtype, R, x, n, y, ctas, s);
+    if (bits_rs == 8 && bits_ag == 8) return run_fc_allreduce<8, 8>(dtype, R, x, n, y, ctas, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qrk

@@ -1,0 +1,7 @@
+// qr_fc_allreduce_48.cu -- the INT4 reduce-scatter / INT8 all-gather instances of
+// the fused Flash Communication all-reduce.
+#include "qr_fc_allreduce.cuh"
+
+namespace qrk {
+template cudaError_t run_fc_allreduce<4, 8>(int, int, const void *const *, long long, void *, int, cudaStream_t);
+}  // namespace qrk

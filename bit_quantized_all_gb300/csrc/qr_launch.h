@@ -29,4 +29,15 @@ struct ConstPtrs;
 template <int B, int DT>
 cudaError_t run_allreduce16(int R, const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s);
 
+// The Flash Communication codec (asymmetric groups of 128): widths 4 and 8;
+// the (reduce-scatter, all-gather) width pairs (4,4), (4,8) and (8,8).
+cudaError_t launch_fc_encode(int bits, int dtype, const void *x, long long n, void *wire, cudaStream_t s);
+cudaError_t launch_fc_decode(int bits, int dtype, const void *wire, long long n, void *y, cudaStream_t s);
+cudaError_t launch_fc_reduce(int bits_in, int bits_out, int R, const void *const *wires, long long n, void *out,
+                             cudaStream_t s);
+cudaError_t launch_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, const void *const *x, long long n,
+                                void *y, int ctas, cudaStream_t s);
+template <int BRS, int BAG>
+cudaError_t run_fc_allreduce(int dtype, int R, const void *const *x, long long n, void *y, int ctas, cudaStream_t s);
+
 }  // namespace qrk

@@ -137,13 +137,58 @@ qr_status_t qr_allreduce_emit(int bits, qr_dtype_t dtype, int R,
                               void *const *wire_out, void *red_out,
                               qr_stream_t stream);
 
-/* qr_allreduce with an explicit persistent-grid size: `ctas` CTAs of 256
- * threads (0 = the library's choice, one full wave of resident CTAs).  The
+/* qr_allreduce with an explicit grid size: `ctas` CTAs in the grid-stride
+ * loop over tiles (0 = the library's choice, four waves of resident CTAs).  The
  * result does not depend on `ctas`; it is the SM-count knob of [FC] key
  * machinery ("tuning the number of streaming multiprocessors"). */
 qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R,
                               const void *const *x, size_t n, void *y,
                               int ctas, qr_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The Flash Communication codec ([FC] key machinery "asymmetric group-128
+ * scaling"; pith summary "group size 128", "INT4 for the reduce stage and
+ * INT8 for the gather stage"; minor comments: "INT6" is that mixed scheme;
+ * Algorithm 1 dequantizes from codes, a zero point z and a scale s).
+ * Per group of 128 values: lo = min x, hi = max x; s = fp32_RN(fp32_RN(hi -
+ * lo) / (2^b - 1)), stored as 0 below 2^-126; z = lo (a zero minimum stored
+ * as +0); r = fp32_RN(1/s) (0 when s = 0); u = RNE(fp32_RN(fp32_RN(x - z) *
+ * r)) (never above 2^b - 1); decode = fp32_RN(u*s + z) (one rounding).
+ * Phase-1B: fp32 rank-order sum of the decoded ranks, values at or past n
+ * reset to 0 (a padded zero does not decode to exactly 0), re-quantized at
+ * the all-gather width.  bits is 4 or 8.
+ * Wire tile (2048 values = 16 groups, 256*bits + 128 bytes, little-endian):
+ * codes as INT4 / INT8 above, then 16 fp32 scales at 256*bits, then 16 fp32
+ * zero points at 256*bits + 64.  Same conventions as the entry points above.
+ * ------------------------------------------------------------------------ */
+
+/* 256*bits + 128 for bits 4 and 8, else 0. */
+size_t qr_fc_tile_bytes(int bits);
+
+/* ceil(n/2048) * qr_fc_tile_bytes(bits); 0 if unsupported or on overflow. */
+size_t qr_fc_wire_bytes(int bits, size_t n);
+
+/* Send path: quantize n fp16/bf16 values into a bits-wide wire. */
+qr_status_t qr_fc_encode(int bits, qr_dtype_t dtype, const void *x, size_t n,
+                         void *wire, qr_stream_t stream);
+
+/* Phase-1B: decode R bits_in-wide wires (host array of R device pointers),
+ * sum in fp32 in rank order, re-quantize into a bits_out-wide wire.
+ * (bits_in, bits_out) is (4,4), (4,8) or (8,8). */
+qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R,
+                                 const void *const *wires, size_t n,
+                                 void *out_wire, qr_stream_t stream);
+
+/* Receive path / Phase-2: decode the first n values into fp16/bf16. */
+qr_status_t qr_fc_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n,
+                         void *y, qr_stream_t stream);
+
+/* The fused two-shot all-reduce with this codec: reduce-scatter wires at
+ * bits_rs, all-gather at bits_ag -- (4,4) INT4, (8,8) INT8, (4,8) the mixed
+ * "INT6".  y may equal one of the x[r] exactly (in-place). */
+qr_status_t qr_fc_allreduce(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
+                            const void *const *x, size_t n, void *y,
+                            qr_stream_t stream);
 
 /* A static string naming a status code (never NULL). */
 const char *qr_status_string(qr_status_t status);

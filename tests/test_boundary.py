@@ -149,6 +149,37 @@ def test_allreduce_validation():
     assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, [wo[0], wo[1] + 4], None) == qr.QR_ERR_MISALIGNED
 
 
+def test_fc_sizes():
+    assert qr.qr_fc_tile_bytes(4) == 1152 and qr.qr_fc_tile_bytes(8) == 2176
+    for b in (3, 6, 0, 16):
+        assert qr.qr_fc_tile_bytes(b) == 0 and qr.qr_fc_wire_bytes(b, 10) == 0
+    assert qr.qr_fc_wire_bytes(4, 2049) == 2 * 1152
+
+
+@no_gpu_only
+def test_fc_validation():
+    n = 2048 + 5
+    assert capi.qr_fc_encode(4, 0, A, 0, B) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_encode(3, 0, A, n, B) == qr.QR_ERR_UNSUPPORTED    # FC is INT4 / INT8 only
+    assert capi.qr_fc_encode(6, 1, A, n, B) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_fc_encode(4, 0, A + 2, n, B) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_fc_encode(8, 0, A, n, A + 32) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_decode(8, 1, None, n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_decode(5, 1, A, n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_fc_decode(4, 1, A, n, A + 16) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_segment_reduce(8, 4, 2, [A, B], n, Y) == qr.QR_ERR_UNSUPPORTED  # (8,4) is not a scheme
+    assert capi.qr_fc_segment_reduce(4, 8, 0, [A], n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_segment_reduce(4, 8, 9, [A + 4096 * i for i in range(9)], n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_fc_segment_reduce(4, 8, 2, [A, B], n, A) == qr.QR_ERR_INVALID_ARG  # widths differ: no in-place
+    assert capi.qr_fc_segment_reduce(4, 4, 2, [A, B], n, A + 16) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_allreduce(8, 4, 0, 2, [A, B], n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_fc_allreduce(4, 8, 2, 2, [A, B], n, Y) == qr.QR_ERR_UNSUPPORTED     # dtype
+    assert capi.qr_fc_allreduce(4, 8, 0, 2, [A, None], n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_allreduce(4, 8, 0, 2, [A, B], n, A + 16) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_allreduce(4, 8, 0, 2, [A, B + 8], n, Y) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_fc_allreduce(4, 8, 0, 2, [A, B], 2**63, Y) == qr.QR_ERR_SIZE
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qr, "LIB_PATH", str(tmp_path / "missing" / "libqr.so"))
     monkeypatch.setattr(qr, "_lib", None)
