@@ -533,9 +533,13 @@ int orc_fc_quantize_group(int bits, const float *x, uint8_t *u, float *scale, fl
     }
     float r = 1.0f / s;
     for (i = 0; i < FC_GROUP; ++i) {
-        float t = (x[i] - z) * r;
-        float q = round_half_even(t); /* t >= 0 */
-        if (q > (float)umax) q = (float)umax;
+        /* the nearest integer (ties to even) to the exact product (x - z) * r;
+         * a double holds the product of two floats exactly */
+        float d = x[i] - z;
+        double t = (double)d * (double)r; /* >= 0 */
+        double fl = floor(t), frac = t - fl;
+        double q = frac > 0.5 ? fl + 1.0 : frac < 0.5 ? fl : (fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0);
+        if (q > (double)umax) q = (double)umax;
         u[i] = (uint8_t)q;
     }
     return 0;

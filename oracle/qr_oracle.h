@@ -112,7 +112,8 @@ int orc_allreduce(int bits, int dtype, int R, const uint16_t *const *x,
  *   s = fp32_RN(fp32_RN(hi - lo) / (2^b - 1));  z = lo (a zero minimum, of
  *   either sign, stored as +0);
  *   s below 2^-126 (zero or subnormal) is stored as 0 and every code is 0;
- *   r = fp32_RN(1/s);  u = min(RNE(fp32_RN(fp32_RN(x - z) * r)), 2^b - 1);
+ *   r = fp32_RN(1/s);  u = min(RNE(fp32_RN(x - z) * r), 2^b - 1), the
+ *   product taken exactly (the nearest integer to it, one rounding);
  *   decode = fp32_RN(u*s + z) (one rounding, a fused multiply-add);
  *   Phase-1B: acc = decode_0, acc = fp32_RN(acc + decode_r), r = 1..R-1;
  *   values at or past n are zero in every phase (Phase-1B sets the sums

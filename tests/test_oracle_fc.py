@@ -159,6 +159,21 @@ def test_decode_is_one_fused_rounding(orc):
     assert y[2] == 2.0**-25
 
 
+def test_code_is_nearest_integer_of_exact_product(orc):
+    """The code is the nearest integer to the exact product (x - z) * r, one
+    rounding.  Group with minimum -4.0053387 (0xc0802bbc) and maximum 2.8191404
+    (0x40346ccc): s = 0.45496526 (0x3ee8f135), r = 2.19797 (0x400cab8a); for
+    x = -0.593099 (0xbf17d556), d = x - z = 3.4122396 (0x405a6222) and the exact
+    product d*r = 7.49999987... gives code 7, while rounding the product to fp32
+    first (7.5, a tie) would give 8."""
+    bits = np.array([0xc0802bbc, 0x40346ccc, 0xbf17d556], np.uint32).view(np.float32)
+    g = np.full(128, bits[2], np.float32)
+    g[0], g[1] = bits[0], bits[1]
+    u, s, z = orc.fc_quantize_group(4, g)
+    assert np.float32(s).view(np.uint32) == 0x3ee8f135
+    assert u[0] == 0 and u[1] == 15 and np.all(u[2:] == 7)
+
+
 def test_non_finite_or_overflowing_range_is_rejected(orc):
     g = np.zeros(128, np.float32)
     g[0] = np.inf

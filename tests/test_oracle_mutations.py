@@ -57,7 +57,10 @@ MUTATIONS = [
     # never fires, since t <= range * RN(1/RN(range/umax)) <= umax*(1+2^-24)^3
     # < umax + 1/2.)
     ("fc_decode_two_roundings", [("fmaf((float)u[FC_GROUP * g + i], s, z)", "(float)u[FC_GROUP * g + i] * s + z")]),
-    ("fc_truncate_not_round", [("        float q = round_half_even(t); /* t >= 0 */", "        float q = floorf(t);")]),
+    ("fc_truncate_not_round", [("double q = frac > 0.5 ? fl + 1.0 : frac < 0.5 ? fl : (fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0);",
+                                "double q = fl;")]),
+    ("fc_product_rounded_to_fp32_first", [("double t = (double)d * (double)r; /* >= 0 */",
+                                           "double t = (double)(d * r); /* >= 0 */")]),
     ("fc_reduce_drops_rank0", [("fc_decode_tile_f32(bits_in, wires[0] + t * tbi, acc);",
                                 "memset(acc, 0, sizeof acc);")]),
     ("fc_reduce_reverse_order",
@@ -101,6 +104,7 @@ def _battery(orc):
             yield lambda c=c, d=d: FC.test_known_answer_tiles(orc, c, d)
     yield lambda: FC.test_decode_is_one_fused_rounding(orc)
     yield lambda: FC.test_zero_minimum_is_stored_as_plus_zero(orc)
+    yield lambda: FC.test_code_is_nearest_integer_of_exact_product(orc)
     for b in (4, 8):
         yield lambda b=b: FC.test_constant_groups_are_exact(orc, b)
         yield lambda b=b: FC.test_min_decodes_exactly_and_codes_span_the_range(orc, b)
