@@ -303,6 +303,9 @@ def run_sweep(args) -> None:
     dtypes = [{"fp16": workloads.FP16, "bf16": workloads.BF16}[d] for d in args.sweep_dtypes.split(",")]
     ranks = [int(r) for r in args.sweep_R.split(",")]
     widths = [int(b) for b in args.sweep_bits.split(",")]
+    if args.sweep_codec == "fc":
+        run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks)
+        return
     for dtype in dtypes:
         tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
         for Rs in ranks:
@@ -370,6 +373,76 @@ def run_sweep(args) -> None:
                 torch.cuda.empty_cache()
 
 
+def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
+    """The sweep for the Flash Communication codec: width pairs (4,4), (4,8)
+    (the mixed "INT6") and (8,8), fused and unfused arms interleaved."""
+    import torch
+
+    for dtype in dtypes:
+        tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
+        for Rs in ranks:
+            for n in sizes:
+                xs = [x.view(tdt) for x in workloads.device_sweep(Rs, n, dtype, seed=SEED, device=dev)]
+                y = torch.empty(n, dtype=tdt, device=dev)
+                yu = torch.empty(n, dtype=tdt, device=dev)
+                for brs, bag in qr.FC_PAIRS:
+                    Wi, Wo = qr.qr_fc_wire_bytes(brs, n), qr.qr_fc_wire_bytes(bag, n)
+                    wires = [torch.empty(Wi, dtype=torch.uint8, device=dev) for _ in range(Rs)]
+                    red = torch.empty(Wo, dtype=torch.uint8, device=dev)
+                    fused_b = 2 * Rs * n + 2 * n
+                    kernel_b = {"fused": fused_b, "unfused": fused_b + 2 * Rs * Wi + 2 * Wo,
+                                "encode": Rs * (2 * n + Wi), "reduce": Rs * Wi + Wo, "decode": Wo + 2 * n}
+                    do_flush = fused_b < (512 << 20)
+
+                    def fused():
+                        qr.qr_fc_allreduce(brs, bag, xs, y=y)
+
+                    def encode_all():
+                        for r in range(Rs):
+                            qr.qr_fc_encode(brs, xs[r], wire=wires[r])
+
+                    def reduce_only():
+                        qr.qr_fc_segment_reduce(brs, bag, wires, n, out=red)
+
+                    def decode_only():
+                        qr.qr_fc_decode(bag, red, n, y=yu)
+
+                    def unfused():
+                        encode_all()
+                        reduce_only()
+                        decode_only()
+
+                    arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all),
+                            ("reduce", reduce_only), ("decode", decode_only))
+                    times = {name: [] for name, _ in arms}
+                    for _ in range(3):
+                        fused()
+                        unfused()
+                    for _ in range(args.reps):
+                        for name, fn in arms:
+                            if do_flush:
+                                flush.fill_(1)
+                            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            e0.record()
+                            fn()
+                            e1.record()
+                            e1.synchronize()
+                            times[name].append(e0.elapsed_time(e1))
+                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
+                    for name, alg in kernel_b.items():
+                        med = statistics.median(times[name])
+                        print(json.dumps({
+                            "sweep": name, "codec": "fc", "R": Rs, "values_per_rank": n,
+                            "storage": "fp16" if dtype == 0 else "bf16", "bits_rs": brs, "bits_ag": bag,
+                            "median_ms": round(med, 5), "input_gbs": round(Rs * n * 2 / (med / 1e3) / 1e9, 2),
+                            "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
+                            "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
+                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps}), flush=True)
+                    del wires, red
+                del xs, y, yu
+                torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -390,6 +463,8 @@ def main() -> None:
     ap.add_argument("--sweep-R", default="2,4,8", help="rank counts for --sweep")
     ap.add_argument("--sweep-bits", default="8,6,4,3", help="code widths for --sweep")
     ap.add_argument("--sweep-dtypes", default="fp16,bf16", help="storage types for --sweep")
+    ap.add_argument("--sweep-codec", choices=["qr", "fc"], default="qr",
+                    help="qr: symmetric 32-value blocks; fc: asymmetric groups of 128")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

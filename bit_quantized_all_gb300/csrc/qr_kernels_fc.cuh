@@ -6,16 +6,12 @@
 // Arithmetic (the same steps as the library's reference definition):
 //   per group: lo = min x, hi = max x; s = RN(RN(hi - lo) / (2^b - 1)), 0 if
 //   below 2^-126; z = lo + 0 (a zero minimum is +0); r = RN(1/s) (0 if s = 0);
-//   u = RNE(RN(RN(x - z) * r)); decode = RN(u*s + z) (one fma);
+//   u = RNE(RN(x - z) * r), the product taken exactly (one rounding: a fused
+//   multiply-add with 1.5*2^23); decode = RN(u*s + z) (one fma);
 //   Phase-1B: acc = decode_0, acc = RN(acc + decode_r), values past n reset to
 //   0, re-quantized at the all-gather width.
-// u never exceeds 2^b - 1 (t <= range * RN(1/RN(range/umax)) <= umax *
-// (1 + 2^-24)^3 < umax + 1/2), but the cap min(t, 2^b - 1) is applied anyway,
-// between the multiply and the rounding add: the toolchain fuses a packed
-// multiply whose result feeds only a packed add into one rounding, even with
-// explicit round-to-nearest modifiers, which would move values that land
-// exactly on a half (RN(d*r) = k + 1/2) to the other side.  The min is exact
-// (the cap is an integer) and cannot be fused across.
+// u never exceeds 2^b - 1: d <= range and d*r <= range * RN(1/RN(range/umax))
+// <= umax * (1 + 2^-24) / (1 - 2^-24) < umax + 1/2, so no cap is applied.
 //
 // Tile (2048 values = 16 groups): codes as in the symmetric codec (INT4 /
 // INT8), then 16 fp32 scales at 256*b and 16 fp32 zero points at 256*b + 64.
@@ -40,6 +36,18 @@ struct FcParams {
     float s, r, z;
 };
 
+// three-input minimum / maximum (sm_100+)
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Group minimum and maximum across the 8 lanes of a group (every lane of the
 // warp must call it).
 __device__ __forceinline__ void group_minmax(const float2 (&v)[8], float &lo, float &hi) {
@@ -47,8 +55,8 @@ __device__ __forceinline__ void group_minmax(const float2 (&v)[8], float &lo, fl
     hi = fmaxf(v[0].x, v[0].y);
 #pragma unroll
     for (int i = 1; i < 8; ++i) {
-        lo = fminf(lo, fminf(v[i].x, v[i].y));
-        hi = fmaxf(hi, fmaxf(v[i].x, v[i].y));
+        lo = fmin3(lo, v[i].x, v[i].y);
+        hi = fmax3(hi, v[i].x, v[i].y);
     }
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1) {
@@ -68,20 +76,16 @@ __device__ __forceinline__ FcParams fc_params(float lo, float hi) {
     return p;
 }
 
-// f = RNE(min(RN(RN(x - z) * r), 2^b - 1)) + 1.5*2^23: the code in the low byte.
+// f = RN(d*r + 1.5*2^23) = RNE(d*r) + 1.5*2^23 with d = RN(x - z): the exact
+// product rounded once to an integer (0 <= d*r < 2^22, and the fp32 spacing
+// in [2^23, 2^24) is 1); the code is in the low byte.
 template <int B>
 __device__ __forceinline__ void fc_quantize16(const float2 (&v)[8], const FcParams &p, float2 (&f)[8]) {
     const float2 nz = make_float2(-p.z, -p.z);
     const float2 r2 = make_float2(p.r, p.r);
     const float2 m2 = make_float2(kRoundMagic, kRoundMagic);
-    constexpr float cap = static_cast<float>(FcCodec<B>::kUmax);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float2 t = __fmul2_rn(__fadd2_rn(v[i], nz), r2);
-        t.x = fminf(t.x, cap);
-        t.y = fminf(t.y, cap);
-        f[i] = __fadd2_rn(t, m2);
-    }
+    for (int i = 0; i < 8; ++i) f[i] = __ffma2_rn(__fadd2_rn(v[i], nz), r2, m2);
 }
 
 // decode of magic floats: RN(u*s + z)
