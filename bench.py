@@ -250,7 +250,7 @@ def measured_hbm() -> tuple[float, str]:
 
 # The sources that determine the benchmarked kernel's code and launch shape.
 FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_allreduce16.cuh", "qr_allreduce16_b3.cu",
-                   "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_launch.h", "qr_capi.cu")
+                   "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_grid.cu")
 
 
 def csrc_hash(files=FUSED16_SOURCES) -> str:
@@ -340,12 +340,19 @@ def run_sweep(args) -> None:
                     def decode_only():
                         qr.qr_decode(bits, red, n, y=yu)
 
+                    ws = torch.empty(qr.qr_twoshot_workspace_bytes(bits, Rs, n), dtype=torch.uint8, device=dev)
+                    ys2 = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
+
+                    def twoshot():
+                        qr.qr_allreduce_twoshot(bits, xs, ys=ys2, workspace=ws)
+
                     arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all),
-                            ("reduce", reduce_only), ("decode", decode_only))
+                            ("reduce", reduce_only), ("decode", decode_only), ("twoshot", twoshot))
                     times = {name: [] for name, _ in arms}
                     for _ in range(3):
                         fused()
                         unfused()
+                        twoshot()
                     for _ in range(args.reps):
                         for name, fn in arms:
                             if do_flush:
@@ -356,9 +363,13 @@ def run_sweep(args) -> None:
                             e1.record()
                             e1.synchronize()
                             times[name].append(e0.elapsed_time(e1))
-                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
+                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and all(
+                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in ys2)
+                    # two-shot: R sends (2N in, W out each), R*W + W for the owners'
+                    # reductions, R decodes (W in, 2N out each)
                     kernel_b = {"fused": fused_b, "unfused": unf_b, "encode": Rs * (2 * n + W),
-                                "reduce": (Rs + 1) * W, "decode": W + 2 * n}
+                                "reduce": (Rs + 1) * W, "decode": W + 2 * n,
+                                "twoshot": 4 * Rs * n + (3 * Rs + 1) * W}
                     for name, alg in kernel_b.items():
                         med = statistics.median(times[name])
                         print(json.dumps({
@@ -368,7 +379,7 @@ def run_sweep(args) -> None:
                             "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
                             "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps}), flush=True)
-                    del wires, red, yu
+                    del wires, red, yu, ws, ys2
                 del xs, y
                 torch.cuda.empty_cache()
 

@@ -37,7 +37,7 @@ BITS = (3, 4, 6, 8)
 EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_segment_reduce",
            "qr_decode", "qr_allreduce", "qr_allreduce_emit", "qr_allreduce_ctas", "qr_status_string",
            "qr_fc_tile_bytes", "qr_fc_wire_bytes", "qr_fc_encode", "qr_fc_segment_reduce", "qr_fc_decode",
-           "qr_fc_allreduce")
+           "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot")
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
 
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
                 "qr_fc_segment_reduce": (i32, [i32, i32, i32, vpp, sz, vp, vp]),
                 "qr_fc_decode": (i32, [i32, i32, vp, sz, vp, vp]),
                 "qr_fc_allreduce": (i32, [i32, i32, i32, i32, vpp, sz, vp, vp]),
+                "qr_twoshot_workspace_bytes": (sz, [i32, i32, sz]),
+                "qr_allreduce_twoshot": (i32, [i32, i32, i32, vpp, sz, vpp, vp, sz, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -139,6 +141,11 @@ class capi:
     @staticmethod
     def qr_allreduce_ctas(bits, dtype, R, xs, n, y, ctas, stream=None):
         return lib().qr_allreduce_ctas(bits, dtype, R, _ptr_array(xs), n, y, ctas, stream)
+
+    @staticmethod
+    def qr_allreduce_twoshot(bits, dtype, R, xs, n, ys, workspace, workspace_bytes, stream=None):
+        return lib().qr_allreduce_twoshot(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), workspace,
+                                          workspace_bytes, stream)
 
     @staticmethod
     def qr_fc_encode(bits, dtype, x, n, wire, stream=None):
@@ -326,6 +333,38 @@ def qr_allreduce_emit(bits: int, xs, y: torch.Tensor | None = None, wire_out=Non
                                   [w.data_ptr() for w in wire_out], red_out.data_ptr(),
                                   _stream(dev, stream)), "qr_allreduce_emit")
     return y, wire_out, red_out
+
+
+def qr_twoshot_workspace_bytes(bits: int, R: int, n: int) -> int:
+    return int(lib().qr_twoshot_workspace_bytes(bits, R, n))
+
+
+def qr_allreduce_twoshot(bits: int, xs, ys=None, workspace: torch.Tensor | None = None, stream=None):
+    """The two-shot all-reduce with its exchange laid out per rank and per
+    owner in `workspace`: returns (the R outputs, the workspace)."""
+    xs, dt, n = _check_inputs(xs)
+    R = len(xs)
+    dev = _same_device(xs, "qr_allreduce_twoshot")
+    if ys is None:
+        ys = [torch.empty_like(xs[0]) for _ in range(R)]
+    ys = list(ys)
+    if len(ys) != R:
+        raise ValueError("one output per rank is needed")
+    for i, y in enumerate(ys):
+        _cuda_contig(y, f"ys[{i}]")
+        if y.dtype != xs[0].dtype or y.numel() != n:
+            raise ValueError(f"ys[{i}] must match the inputs' dtype and size")
+    need = qr_twoshot_workspace_bytes(bits, R, n)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _cuda_contig(workspace, "workspace")
+    if workspace.dtype != torch.uint8:
+        raise TypeError(f"workspace must be torch.uint8, got {workspace.dtype}")
+    _same_device(xs + ys + [workspace], "qr_allreduce_twoshot")
+    _check(capi.qr_allreduce_twoshot(bits, dt, R, [x.data_ptr() for x in xs], n, [y.data_ptr() for y in ys],
+                                     workspace.data_ptr(), workspace.numel(), _stream(dev, stream)),
+           "qr_allreduce_twoshot")
+    return ys, workspace
 
 
 # ---------------------------------------------------------------------------

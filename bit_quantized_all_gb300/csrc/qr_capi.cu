@@ -11,9 +11,6 @@
 //   5. an output partially overlapping another buffer      -> QR_ERR_INVALID_ARG
 // A launch error reported by the runtime                   -> QR_ERR_CUDA
 #include <cstdint>
-#include <map>
-#include <mutex>
-#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -59,42 +56,56 @@ qr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_
 
 }  // namespace
 
-namespace qrk {
-
-int grid_for(const void *kernel, int threads, long long tiles, int ctas, int waves, cudaError_t *err) {
-    *err = cudaSuccess;
-    if (tiles <= 0) return 0;
-    if (ctas > 0) return static_cast<int>(tiles < ctas ? tiles : ctas);
-    int dev = 0;
-    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
-    static std::mutex mu;
-    static std::map<std::pair<int, const void *>, int> resident;  // (device, kernel) -> CTAs per wave
-    int wave = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        auto it = resident.find({dev, kernel});
-        if (it != resident.end()) wave = it->second;
-    }
-    if (wave == 0) {
-        int sms = 0, per_sm = 0;
-        if ((*err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
-        if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0)) != cudaSuccess)
-            return 0;
-        wave = sms * (per_sm > 0 ? per_sm : 1);
-        std::lock_guard<std::mutex> lock(mu);
-        resident[{dev, kernel}] = wave;
-    }
-    const long long want = static_cast<long long>(wave) * (waves > 0 ? waves : 1);
-    return static_cast<int>(tiles < want ? tiles : want);
-}
-
-}  // namespace qrk
 
 QR_EXPORT size_t qr_tile_values(void) { return kTile; }
 
 QR_EXPORT size_t qr_tile_bytes(int bits) { return tile_bytes(bits); }
 
 QR_EXPORT size_t qr_wire_bytes(int bits, size_t n) { return wire_bytes(bits, n); }
+
+namespace {
+
+// R*(R+1)*ceil(ceil(n/2048)/R) tiles, 0 on overflow or bad arguments
+size_t twoshot_ws_bytes(int bits, int R, size_t n) {
+    const size_t tb = tile_bytes(bits);
+    if (tb == 0 || R < 1 || R > QR_MAX_RANKS) return 0;
+    const size_t tiles = n / kTile + (n % kTile != 0);
+    const size_t seg = tiles / size_t(R) + (tiles % size_t(R) != 0);
+    const size_t bufs = size_t(R) * size_t(R + 1);
+    if (seg > SIZE_MAX / bufs || seg * bufs > SIZE_MAX / tb) return 0;
+    return seg * bufs * tb;
+}
+
+}  // namespace
+
+QR_EXPORT size_t qr_twoshot_workspace_bytes(int bits, int R, size_t n) { return twoshot_ws_bytes(bits, R, n); }
+
+QR_EXPORT qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                           void *const *y, void *workspace, size_t workspace_bytes,
+                                           qr_stream_t stream) {
+    if (!x || !y || !workspace || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!x[r] || !y[r]) return QR_ERR_INVALID_ARG;
+    if (!bits_ok(bits) || !dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    const size_t need = twoshot_ws_bytes(bits, R, n);
+    if (!value_bytes_ok(n) || need == 0 || wire_bytes(bits, n) == 0) return QR_ERR_SIZE;
+    if (workspace_bytes < need) return QR_ERR_SIZE;
+    const size_t V = 2 * n;
+    if (!aligned16(workspace)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(x[r]) || !aligned16(y[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r) {
+        if (overlaps(workspace, need, x[r], V) || overlaps(workspace, need, y[r], V)) return QR_ERR_INVALID_ARG;
+        for (int i = 0; i < R; ++i) {
+            // every input is read in Phase-1, before any output is written: an
+            // output may be an input exactly (in place), never partly
+            if (bad_alias(y[r], V, x[i], V)) return QR_ERR_INVALID_ARG;
+            if (i < r && overlaps(y[r], V, y[i], V)) return QR_ERR_INVALID_ARG;
+        }
+    }
+    return from_cuda(qrk::launch_twoshot(bits, dtype, R, x, static_cast<long long>(n), y, workspace,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
 
 namespace {
 

@@ -244,10 +244,30 @@ __device__ __forceinline__ float f16_bits_to_float(uint32_t h) {
 // tile included); thread (CTA c, lane i) starts at block c*256 + i.
 // ---------------------------------------------------------------------------
 
+// Where tile t of a wire goes: contiguously (a plain wire) ...
+struct ContigTiles {
+    uint8_t *base;
+    int tile_bytes;
+    __device__ __forceinline__ uint8_t *operator()(long long t) const { return base + t * tile_bytes; }
+};
+
+// ... or into owner k's receive buffer for sender j (the two-shot exchange
+// on one GPU): owner k = t / seg owns tiles [k*seg, (k+1)*seg); the R
+// buffers of owner k sit back to back, each `seg` tiles long.
+struct OwnerTiles {
+    uint8_t *ws;
+    long long seg;
+    int ranks, sender, tile_bytes;
+    __device__ __forceinline__ uint8_t *operator()(long long t) const {
+        const long long k = t / seg;
+        return ws + ((k * ranks + sender) * seg + (t - k * seg)) * tile_bytes;
+    }
+};
+
 // Send path [QR Quantization and Dequantization Paths, CodecQ3::send].
-template <int B, int DT, int U>
+template <int B, int DT, int U, class Addr = ContigTiles>
 __global__ void __launch_bounds__(kThreads32) encode32_kernel(const uint16_t *__restrict__ x, long long n,
-                                                              uint8_t *__restrict__ wire, long long NB) {
+                                                              Addr wire, long long NB) {
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long gb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb0 < NB; gb0 += U * S) {
         uint32_t raw[U][16];
@@ -266,7 +286,7 @@ __global__ void __launch_bounds__(kThreads32) encode32_kernel(const uint16_t *__
                 quantize_block_magic<B>(v, sc.r, sc.low_clip, f);
                 BlockWords<B> c;
                 pack_block<B>(f, c);
-                uint8_t *tile = wire + (gb >> 6) * Codec<B>::kTileBytes;
+                uint8_t *tile = wire(gb >> 6);
                 store_block_codes<B>(tile, static_cast<int>(gb & 63), c);
                 store_block_scale<B>(tile, static_cast<int>(gb & 63), sc.bits);
             }

@@ -29,6 +29,13 @@ struct ConstPtrs;
 template <int B, int DT>
 cudaError_t run_allreduce16(int R, const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s);
 
+// The two-shot all-reduce with its exchange laid out per rank and per owner in
+// a workspace of R*(R+1)*seg tiles, seg = twoshot_segment_tiles(T, R)
+// (qr_twoshot.cu): R sends, R owner reductions, R decodes into y[0..R-1].
+long long twoshot_segment_tiles(long long tiles, int R);
+cudaError_t launch_twoshot(int bits, int dtype, int R, const void *const *x, long long n, void *const *y, void *ws,
+                           cudaStream_t s);
+
 // The Flash Communication codec (asymmetric groups of 128): widths 4 and 8;
 // the (reduce-scatter, all-gather) width pairs (4,4), (4,8) and (8,8).
 cudaError_t launch_fc_encode(int bits, int dtype, const void *x, long long n, void *wire, cudaStream_t s);

@@ -75,7 +75,8 @@ typedef enum {
     QR_ERR_INVALID_ARG = 1, /* null pointer, n == 0, R < 1, partial aliasing */
     QR_ERR_UNSUPPORTED = 2, /* bits not in {3,4,6,8}, unknown dtype, R > 8   */
     QR_ERR_MISALIGNED = 3,  /* a device pointer not 16-byte aligned           */
-    QR_ERR_SIZE = 4,        /* a byte count overflows size_t                  */
+    QR_ERR_SIZE = 4,        /* a byte count overflows size_t, or a workspace
+                               is smaller than the call needs                */
     QR_ERR_CUDA = 5         /* the CUDA runtime reported an error at launch   */
 } qr_status_t;
 
@@ -144,6 +145,35 @@ qr_status_t qr_allreduce_emit(int bits, qr_dtype_t dtype, int R,
 qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R,
                               const void *const *x, size_t n, void *y,
                               int ctas, qr_stream_t stream);
+
+/* The two-shot all-reduce with its exchange laid out as across R GPUs
+ * ([QR] Design Highlights and Quantization and Dequantization Paths: Phase-1
+ * sends, Phase-1B in-segment reduction by the segment's owner, Phase-2
+ * gather; [FC] key machinery: one all-to-all, local sum and re-quantization,
+ * one all-gather).  The T tiles are cut into R segments of seg = ceil(T/R)
+ * tiles, owner k holding tiles [k*seg, (k+1)*seg).  Rank j quantizes its
+ * message and writes segment k into owner k's receive buffer; owner k
+ * reduces the R copies of its segment into the gathered wire; every rank
+ * decodes the whole gathered wire into its own output y[j].  Each rank's and
+ * each owner's work is a separate launch on `stream`, in that order.  Every
+ * y[j] equals qr_allreduce's output.
+ * `workspace` (device, 16-byte aligned, at least
+ * qr_twoshot_workspace_bytes(bits, R, n) bytes, owned by the caller) holds
+ *   recv[k][j] at byte ((k*R + j) * seg) * qr_tile_bytes(bits): owner k's
+ *              copy of sender j's segment, seg tiles each;
+ *   the gathered reduced wire at byte (R*R*seg) * qr_tile_bytes(bits), in
+ *              tile order (byte-identical to qr_segment_reduce's output).
+ * Every byte the call reads from the workspace is written by the same call
+ * first.  `y` is a host array of R device pointers; outputs must not overlap
+ * each other or the workspace; y[j] may equal an input exactly (every input
+ * is read before any output is written).  A workspace smaller than needed
+ * returns QR_ERR_SIZE. */
+size_t qr_twoshot_workspace_bytes(int bits, int R, size_t n); /* R*(R+1)*seg tiles; 0 if invalid */
+
+qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R,
+                                 const void *const *x, size_t n, void *const *y,
+                                 void *workspace, size_t workspace_bytes,
+                                 qr_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * The Flash Communication codec ([FC] key machinery "asymmetric group-128

@@ -180,6 +180,42 @@ def test_fc_validation():
     assert capi.qr_fc_allreduce(4, 8, 0, 2, [A, B], 2**63, Y) == qr.QR_ERR_SIZE
 
 
+def test_twoshot_workspace_bytes():
+    for bits in (3, 4, 6, 8):
+        tb = qr.qr_tile_bytes(bits)
+        for R in (1, 2, 3, 8):
+            for n in (1, 2048, 2049, 2048 * 17 + 5, 2**27):
+                T = -(-n // 2048)
+                seg = -(-T // R)
+                assert qr.qr_twoshot_workspace_bytes(bits, R, n) == R * (R + 1) * seg * tb
+    assert qr.qr_twoshot_workspace_bytes(5, 2, 100) == 0
+    assert qr.qr_twoshot_workspace_bytes(4, 0, 100) == 0
+    assert qr.qr_twoshot_workspace_bytes(4, 9, 100) == 0
+    assert qr.qr_twoshot_workspace_bytes(8, 8, 2**64 - 1) == 0
+
+
+@no_gpu_only
+def test_twoshot_validation():
+    n = 2048 * 5 + 3
+    need = qr.qr_twoshot_workspace_bytes(4, 2, n)
+    WS = 0x7F3000000000
+    V = 2 * n
+    xs, ys = [A, B], [Y, Y + 2**24]
+    call = capi.qr_allreduce_twoshot
+    assert call(4, 0, 2, xs, n, ys, None, need) == qr.QR_ERR_INVALID_ARG
+    assert call(4, 0, 2, xs, n, [Y, None], WS, need) == qr.QR_ERR_INVALID_ARG
+    assert call(4, 0, 2, xs, 0, ys, WS, need) == qr.QR_ERR_INVALID_ARG
+    assert call(5, 0, 2, xs, n, ys, WS, need) == qr.QR_ERR_UNSUPPORTED
+    assert call(4, 0, 9, [A + 4096 * i for i in range(9)], n, [Y + 2**22 * i for i in range(9)], WS,
+                need) == qr.QR_ERR_UNSUPPORTED
+    assert call(4, 0, 2, xs, n, ys, WS, need - 1) == qr.QR_ERR_SIZE            # workspace too small
+    assert call(4, 0, 2, xs, n, ys, WS + 8, need) == qr.QR_ERR_MISALIGNED
+    assert call(4, 0, 2, xs, n, [Y, Y + 4096], WS, need) == qr.QR_ERR_INVALID_ARG   # outputs overlap
+    assert call(4, 0, 2, xs, n, [Y, Y], WS, need) == qr.QR_ERR_INVALID_ARG
+    assert call(4, 0, 2, xs, n, [A + 16, Y], WS, need) == qr.QR_ERR_INVALID_ARG      # partial in-place
+    assert call(4, 0, 2, xs, n, ys, A, need) == qr.QR_ERR_INVALID_ARG              # workspace over an input
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qr, "LIB_PATH", str(tmp_path / "missing" / "libqr.so"))
     monkeypatch.setattr(qr, "_lib", None)

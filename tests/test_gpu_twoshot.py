@@ -1,0 +1,127 @@
+"""Parity of the two-shot all-reduce whose exchange is laid out as across R
+GPUs (qr_allreduce_twoshot) against the oracle.
+
+Every rank's output equals the oracle's all-reduce bit for bit; the
+workspace holds, byte for byte, each owner's received copies of every
+sender's quantized segment (the oracle's encode of that sender, cut at the
+segment) and the gathered reduced wire (the oracle's Phase-1B output).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_quantized_all_gb300 as qr
+import oracle
+import workloads
+from qr_testlib import assert_outputs_match, assert_wire_equal, to_dev, to_host_u8, to_host_u16, xmax_of
+
+pytestmark = pytest.mark.gpu
+
+BITS = [3, 4, 6, 8]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from bit_quantized_all_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    qr.lib()
+
+
+def twoshot_check(bits, dtype, xs, what):
+    R, n = len(xs), xs[0].size
+    xs_dev = [to_dev(x, dtype) for x in xs]
+    ys, ws = qr.qr_allreduce_twoshot(bits, xs_dev)
+    torch.cuda.synchronize()
+    w_ref = [oracle.encode(bits, dtype, x) for x in xs]
+    red_ref = oracle.segment_reduce(bits, w_ref, n)
+    y_ref = oracle.decode(bits, dtype, red_ref, n)
+    xmax = xmax_of(xs, dtype)
+    for j, y in enumerate(ys):
+        assert_outputs_match(to_host_u16(y), y_ref, dtype, xmax, f"{what} rank {j} output")
+    tb = qr.qr_tile_bytes(bits)
+    T = -(-n // 2048)
+    seg = -(-T // R)
+    wsh = to_host_u8(ws)
+    for k in range(R):
+        t0, t1 = k * seg, min(T, (k + 1) * seg)
+        if t0 >= T:
+            break
+        for j in range(R):
+            off = (k * R + j) * seg * tb
+            assert_wire_equal(wsh[off: off + (t1 - t0) * tb], w_ref[j][t0 * tb: t1 * tb], bits,
+                              f"{what} owner {k} copy from rank {j}")
+    red_off = R * R * seg * tb
+    assert_wire_equal(wsh[red_off: red_off + T * tb], red_ref, bits, f"{what} gathered wire")
+    # the fused kernel gives the same bytes
+    yf = qr.qr_allreduce(bits, xs_dev)
+    assert torch.equal(yf.view(torch.int16), ys[0].view(torch.int16))
+
+
+def _rand_ranks(R, n, dtype, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for r in range(R):
+        v = rng.standard_normal(n).astype(np.float32) * np.float32(1 + r)
+        v[rng.integers(0, n, size=max(1, n // 300))] *= 25.0
+        out.append(oracle.narrow(dtype, v))
+    return out
+
+
+@pytest.mark.parametrize("cfg", [workloads.C1, workloads.C2, workloads.C3], ids=lambda c: c["name"])
+def test_workloads(cfg):
+    xs = workloads.ranks(cfg)
+    for bits in cfg["bits"]:
+        twoshot_check(bits, cfg["dtype"], xs, f"{cfg['name']} INT{bits}")
+
+
+@pytest.mark.parametrize("n", [1, 37, 2048, 2049, 2048 * 3, 2048 * 5 + 37, 2048 * 9 + 1])
+@pytest.mark.parametrize("R", [1, 2, 3, 8])
+def test_segment_shapes(n, R):
+    """Fewer tiles than ranks (empty owners), uneven last segments, ragged tails."""
+    for bits in BITS:
+        for dtype in (0, 1):
+            twoshot_check(bits, dtype, _rand_ranks(R, n, dtype, 40 * n + R + bits), f"n={n} R={R} INT{bits}")
+
+
+@pytest.mark.parametrize("R", [4, 5, 6, 7])
+def test_other_rank_counts(R):
+    n = 2048 * 11 + 100
+    for bits in BITS:
+        twoshot_check(bits, 1, _rand_ranks(R, n, 1, 700 + R + bits), f"R={R} INT{bits}")
+
+
+def test_in_place_and_repeat():
+    n = 2048 * 64 + 5
+    R = 4
+    xs_dev = [to_dev(x, 0) for x in _rand_ranks(R, n, 0, 5)]
+    y0 = qr.qr_allreduce(4, xs_dev)
+    ys, ws = qr.qr_allreduce_twoshot(4, xs_dev)
+    ys2, _ = qr.qr_allreduce_twoshot(4, xs_dev, workspace=ws)  # the same workspace again
+    for a, b in zip(ys, ys2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    xs2 = [x.clone() for x in xs_dev]
+    out, _ = qr.qr_allreduce_twoshot(4, xs2, ys=xs2)  # every rank in place
+    for y in out:
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+def test_large_sampled():
+    """The benchmark's size class: R=8, 2^27 values per rank; outputs equal
+    the fused kernel's (which is checked against the oracle elsewhere) and a
+    sample of gathered tiles equals the oracle's reduction of those tiles."""
+    n, R = 1 << 27, 8
+    xs_dev = [x.view(torch.bfloat16) for x in workloads.device_sweep(R, n, 1, seed=11, device="cuda")]
+    yf = qr.qr_allreduce(4, xs_dev)
+    ys, ws = qr.qr_allreduce_twoshot(4, xs_dev)
+    for y in ys:
+        assert torch.equal(y.view(torch.int16), yf.view(torch.int16))
+    T, tb = n // 2048, qr.qr_tile_bytes(4)
+    seg = -(-T // R)
+    red_off = R * R * seg * tb
+    rng = np.random.Generator(np.random.PCG64(3))
+    for t in rng.choice(T, size=64, replace=False).tolist() + [0, T - 1]:
+        xt = [x[t * 2048:(t + 1) * 2048].contiguous().view(torch.int16).cpu().numpy().view(np.uint16) for x in xs_dev]
+        red_t = oracle.segment_reduce(4, [oracle.encode(4, 1, v) for v in xt], 2048)
+        got = ws[red_off + t * tb: red_off + (t + 1) * tb].cpu().numpy()
+        assert_wire_equal(got, red_t, 4, f"gathered tile {t}")
