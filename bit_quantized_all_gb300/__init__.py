@@ -37,7 +37,9 @@ BITS = (3, 4, 6, 8)
 EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_segment_reduce",
            "qr_decode", "qr_allreduce", "qr_allreduce_emit", "qr_allreduce_ctas", "qr_status_string",
            "qr_fc_tile_bytes", "qr_fc_wire_bytes", "qr_fc_encode", "qr_fc_segment_reduce", "qr_fc_decode",
-           "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot")
+           "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot",
+           "qr_allreduce_twoshot_static")
+TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
 
@@ -86,6 +88,7 @@ def lib() -> ctypes.CDLL:
                 "qr_fc_allreduce": (i32, [i32, i32, i32, i32, vpp, sz, vp, vp]),
                 "qr_twoshot_workspace_bytes": (sz, [i32, i32, sz]),
                 "qr_allreduce_twoshot": (i32, [i32, i32, i32, vpp, sz, vpp, vp, sz, vp]),
+                "qr_allreduce_twoshot_static": (i32, [i32, i32, i32, vpp, sz, vpp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -146,6 +149,10 @@ class capi:
     def qr_allreduce_twoshot(bits, dtype, R, xs, n, ys, workspace, workspace_bytes, stream=None):
         return lib().qr_allreduce_twoshot(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), workspace,
                                           workspace_bytes, stream)
+
+    @staticmethod
+    def qr_allreduce_twoshot_static(bits, dtype, R, xs, n, ys, stream=None):
+        return lib().qr_allreduce_twoshot_static(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), stream)
 
     @staticmethod
     def qr_fc_encode(bits, dtype, x, n, wire, stream=None):

@@ -175,6 +175,36 @@ qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R,
                                  void *workspace, size_t workspace_bytes,
                                  qr_stream_t stream);
 
+/* qr_allreduce_twoshot for callers that cannot allocate device memory (no
+ * counterpart on the source pages; a convenience of this library).  Some
+ * callers cannot call cudaMalloc: code running inside someone else's memory
+ * budget or caching allocator, code in a phase where allocating is not
+ * allowed or would synchronize the device, plain C callers without an
+ * allocator.  This entry point computes exactly what qr_allreduce_twoshot
+ * computes, with its workspace taken from one buffer of
+ * QR_TWOSHOT_STATIC_WORKSPACE_BYTES that the library itself holds in device
+ * memory: every GPU that loads the library keeps that buffer until the
+ * process exits.  The caller still passes the inputs `x` and the outputs `y`.
+ *   - Sizes: a call whose qr_twoshot_workspace_bytes(bits, R, n) exceeds
+ *     QR_TWOSHOT_STATIC_WORKSPACE_BYTES returns QR_ERR_SIZE and does nothing
+ *     (32 MiB holds, for example, R=8 at INT4 up to 6.6 M values per rank, at
+ *     INT8 up to 3.5 M).
+ *   - The first call made while a device is current looks up the buffer's
+ *     device address on that device (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.  It allocates nothing, and neither does
+ *     any later call.
+ *   - All calls share the one buffer, and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (every byte a call reads is
+ *     written by that call first), but calls that overlap on the GPU (on two
+ *     streams, or from two threads without ordering) race on it.
+ * Arguments and errors are those of qr_allreduce_twoshot without the
+ * workspace. */
+#define QR_TWOSHOT_STATIC_WORKSPACE_BYTES (32u << 20)
+
+qr_status_t qr_allreduce_twoshot_static(int bits, qr_dtype_t dtype, int R,
+                                        const void *const *x, size_t n,
+                                        void *const *y, qr_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * The Flash Communication codec ([FC] key machinery "asymmetric group-128
  * scaling"; pith summary "group size 128", "INT4 for the reduce stage and
