@@ -265,9 +265,10 @@ struct OwnerTiles {
 };
 
 // Send path [QR Quantization and Dequantization Paths, CodecQ3::send].
-template <int B, int DT, int U, class Addr = ContigTiles>
-__global__ void __launch_bounds__(kThreads32) encode32_kernel(const uint16_t *__restrict__ x, long long n,
-                                                              Addr wire, long long NB) {
+// The body of each kernel below is a device function so that the two-shot
+// path can run it once per rank (blockIdx.y) inside a single launch.
+template <int B, int DT, int U, class Addr>
+__device__ __forceinline__ void encode32_run(const uint16_t *__restrict__ x, long long n, Addr wire, long long NB) {
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long gb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb0 < NB; gb0 += U * S) {
         uint32_t raw[U][16];
@@ -292,6 +293,12 @@ __global__ void __launch_bounds__(kThreads32) encode32_kernel(const uint16_t *__
             }
         }
     }
+}
+
+template <int B, int DT, int U, class Addr = ContigTiles>
+__global__ void __launch_bounds__(kThreads32) encode32_kernel(const uint16_t *__restrict__ x, long long n,
+                                                              Addr wire, long long NB) {
+    encode32_run<B, DT, U, Addr>(x, n, wire, NB);
 }
 
 // Receive path / Phase-2 [QR Quantization and Dequantization Paths,
@@ -343,8 +350,8 @@ __device__ __forceinline__ SlotCodes half_slot_codes(const HalfWords<B> &c, int 
 }
 
 template <int B, int DT, int U, bool Y32>  // Y32: y is 32-byte aligned (one 256-bit store per unit)
-__global__ void __launch_bounds__(kThreads32) decode16_kernel(const uint8_t *__restrict__ wire, long long n,
-                                                              uint16_t *__restrict__ y, long long NH) {
+__device__ __forceinline__ void decode16_run(const uint8_t *__restrict__ wire, long long n, uint16_t *__restrict__ y,
+                                             long long NH) {
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long hb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb0 < NH; hb0 += U * S) {
         HalfWords<B> c[U];
@@ -395,6 +402,12 @@ __global__ void __launch_bounds__(kThreads32) decode16_kernel(const uint8_t *__r
             }
         }
     }
+}
+
+template <int B, int DT, int U, bool Y32>
+__global__ void __launch_bounds__(kThreads32) decode16_kernel(const uint8_t *__restrict__ wire, long long n,
+                                                              uint16_t *__restrict__ y, long long NH) {
+    decode16_run<B, DT, U, Y32>(wire, n, y, NH);
 }
 
 // Codes of two slots (one half-block) from 16 magic floats f[0..7] (pairs).
@@ -453,7 +466,7 @@ __device__ __forceinline__ void store_half_codes(uint8_t *tile, int g, int half,
 // RN(acc + q*s): q*s is exact), re-quantize.  Half-blocks hb and hb^1 are
 // always both in or both out of range, and every lane reaches the shuffle.
 template <int B, int R, int U>
-__global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, uint8_t *out, long long NH) {
+__device__ __forceinline__ void reduce16_run(ConstPtrs wires, uint8_t *out, long long NH) {
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long hb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb0 - (threadIdx.x & 31) < NH;
          hb0 += U * S) {
@@ -522,13 +535,18 @@ __global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, u
     }
 }
 
+template <int B, int R, int U>
+__global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, uint8_t *out, long long NH) {
+    reduce16_run<B, R, U>(wires, out, NH);
+}
+
 // Phase-1B in-segment reduction with one thread per block (fewer
 // instructions than reduce16_kernel, which wins where the 8-rank loads need
 // more warps to hide their latency): decode the R rank copies of the block,
 // add them in fp32 in rank order (fma(q, s, acc) = RN(acc + q*s): q*s is
 // exact), re-quantize.
 template <int B, int R, int U>
-__global__ void __launch_bounds__(kThreads32) reduce32_kernel(ConstPtrs wires, uint8_t *out, long long NB) {
+__device__ __forceinline__ void reduce32_run(ConstPtrs wires, uint8_t *out, long long NB) {
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long gb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb0 < NB; gb0 += U * S) {
         BlockWords<B> c[U][R];
@@ -572,5 +590,19 @@ __global__ void __launch_bounds__(kThreads32) reduce32_kernel(ConstPtrs wires, u
         }
     }
 }
+
+template <int B, int R, int U>
+__global__ void __launch_bounds__(kThreads32) reduce32_kernel(ConstPtrs wires, uint8_t *out, long long NB) {
+    reduce32_run<B, R, U>(wires, out, NB);
+}
+
+// Which Phase-1B kernel: measured on GB300 at 2^24..2^30 values per rank, the
+// two-threads-per-block kernel is faster for INT4/INT6 with six or more
+// ranks (latency-bound there); one thread per block needs fewer
+// instructions and wins everywhere else (INT3 and small R are ALU-bound).
+template <int B, int R>
+__host__ __device__ constexpr bool reduce_two_threads_per_block() { return (B == 4 || B == 6) && R >= 6; }
+template <int R>
+__host__ __device__ constexpr int reduce_units_per_thread() { return (R <= 2) ? 2 : 1; }
 
 }  // namespace qrk

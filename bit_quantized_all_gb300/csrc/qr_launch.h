@@ -31,7 +31,8 @@ cudaError_t run_allreduce16(int R, const ConstPtrs &xp, long long n, void *y, in
 
 // The two-shot all-reduce with its exchange laid out per rank and per owner in
 // a workspace of R*(R+1)*seg tiles, seg = twoshot_segment_tiles(T, R)
-// (qr_twoshot.cu): R sends, R owner reductions, R decodes into y[0..R-1].
+// (qr_twoshot.cu): one launch each for the R sends, the R owner reductions
+// and the R decodes into y[0..R-1].
 long long twoshot_segment_tiles(long long tiles, int R);
 cudaError_t launch_twoshot(int bits, int dtype, int R, const void *const *x, long long n, void *const *y, void *ws,
                            cudaStream_t s);

@@ -5,16 +5,12 @@
 
 namespace qrk {
 
-// Which reduce kernel: measured on GB300 at 2^24..2^30 values per rank, the
-// two-threads-per-block kernel is faster for INT4/INT6 with six or more
-// ranks (latency-bound there); one thread per block needs fewer
-// instructions and wins everywhere else (INT3 and small R are ALU-bound).
 template <int B, int R>
 static cudaError_t run_reduce_r(const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
-    constexpr int U = (R <= 2) ? 2 : 1;  // work units per thread in flight
+    constexpr int U = reduce_units_per_thread<R>();  // work units per thread in flight
     const long long T = (n + kTileValues - 1) / kTileValues;
     cudaError_t err = cudaSuccess;
-    if constexpr ((B == 4 || B == 6) && R >= 6) {
+    if constexpr (reduce_two_threads_per_block<B, R>()) {
         const long long NH = 128 * T;
         auto kern = reduce16_kernel<B, R, U>;
         const long long units = (NH + kThreads32 * U - 1) / (kThreads32 * U);

@@ -9,10 +9,12 @@
 //   recv[k][j] at ((k*R + j) * seg) tiles: owner k's copy of sender j's
 //              quantized segment (seg tiles each; R*R buffers);
 //   red        at (R*R*seg) tiles: the gathered reduced wire, tile order.
-// Every rank's send, every owner's reduction and every rank's decode is its
-// own launch, on the caller's stream in that order, so the data each rank
-// would move is moved: R*(2N + W) for the sends, R*W + W for the owners'
-// reductions, R*(W + 2N) for the decodes (W = wire bytes).
+// Each phase is one launch on the caller's stream whose grid has one row
+// (blockIdx.y) per rank or owner, and each row does exactly what that rank
+// would do on its own GPU, so the data each rank would move is moved:
+// R*(2N + W) for the sends, R*W + W for the owners' reductions, R*(W + 2N)
+// for the decodes (W = wire bytes).  The three launches run in order, which
+// is the synchronisation a real exchange needs between its phases.
 #include <cstdint>
 
 #include "qr_kernels32.cuh"
@@ -20,28 +22,142 @@
 
 namespace qrk {
 
+// p[i] for a run-time i without indexing the kernel-parameter array (which
+// would copy it to local memory): one select per rank.
+template <class P>
+__device__ __forceinline__ P row_pointer(const P (&p)[kMaxRanks], int i) {
+    P v = p[0];
+#pragma unroll
+    for (int r = 1; r < kMaxRanks; ++r) v = (i == r) ? p[r] : v;
+    return v;
+}
+
 long long twoshot_segment_tiles(long long tiles, int R) { return (tiles + R - 1) / R; }
 
+// Phase-1: sender j = blockIdx.y quantizes its whole message straight into
+// the owners' receive buffers (segment k of the wire lands in recv[k][j]).
+template <int B, int DT, int U>
+__global__ void __launch_bounds__(kThreads32) twoshot_send_kernel(ConstPtrs x, long long n, uint8_t *ws,
+                                                                  long long seg, long long NB) {
+    const int j = static_cast<int>(blockIdx.y);
+    encode32_run<B, DT, U>(static_cast<const uint16_t *>(row_pointer(x.p, j)), n,
+                           OwnerTiles{ws, seg, static_cast<int>(gridDim.y), j, Codec<B>::kTileBytes}, NB);
+}
+
+// Phase-1B: owner k = blockIdx.y reduces the R received copies of its
+// segment, in sender order, into its segment of the gathered wire.
+template <int B, int R, int U>
+__global__ void __launch_bounds__(kThreads32) twoshot_reduce_kernel(uint8_t *ws, long long T, long long seg) {
+    const long long k = blockIdx.y;
+    const long long t0 = k * seg;
+    const long long tiles = (T < t0 + seg ? T : t0 + seg) - t0;
+    if (tiles <= 0) return;  // more owners than tiles: nothing to reduce
+    constexpr long long tb = Codec<B>::kTileBytes;
+    ConstPtrs w;
+#pragma unroll
+    for (int j = 0; j < R; ++j) w.p[j] = ws + (k * R + j) * seg * tb;
+    uint8_t *red = ws + static_cast<long long>(R) * R * seg * tb + t0 * tb;
+    if constexpr (reduce_two_threads_per_block<B, R>())
+        reduce16_run<B, R, U>(w, red, 128 * tiles);
+    else
+        reduce32_run<B, R, U>(w, red, 64 * tiles);
+}
+
+// Phase-2: rank j = blockIdx.y decodes the gathered wire into its output.
+template <int B, int DT, int U, bool Y32>
+__global__ void __launch_bounds__(kThreads32) twoshot_decode_kernel(const uint8_t *__restrict__ red, long long n,
+                                                                    MutPtrs y, long long NH) {
+    decode16_run<B, DT, U, Y32>(red, n, static_cast<uint16_t *>(row_pointer(y.p, static_cast<int>(blockIdx.y))), NH);
+}
+
+// CTAs per row: four waves of resident CTAs over all rows together, split
+// evenly between the rows, at most one per work unit of a row.
+static int row_ctas(const void *kern, long long units_per_row, int rows, cudaError_t *err) {
+    const int g = grid_for(kern, kThreads32, units_per_row * rows, 0, 4, err);
+    if (g <= 0) return 0;
+    long long per_row = (g + rows - 1) / rows;
+    if (per_row > units_per_row) per_row = units_per_row;
+    return static_cast<int>(per_row < 1 ? 1 : per_row);
+}
+
 template <int B, int DT>
-static cudaError_t send_rank(const void *x, long long n, uint8_t *ws, long long seg, int R, int j,
-                             cudaStream_t s) {
+static cudaError_t send_all(int R, const void *const *x, long long n, uint8_t *ws, long long seg, cudaStream_t s) {
     constexpr int U = 2;
     const long long NB = 64 * ((n + kTileValues - 1) / kTileValues);
-    auto kern = encode32_kernel<B, DT, U, OwnerTiles>;
+    ConstPtrs xp{};
+    for (int j = 0; j < R; ++j) xp.p[j] = x[j];
+    auto kern = twoshot_send_kernel<B, DT, U>;
     cudaError_t err = cudaSuccess;
-    const long long units = (NB + kThreads32 * U - 1) / (kThreads32 * U);
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
-    if (grid <= 0) return err;
-    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint16_t *>(x), n,
-                                     OwnerTiles{ws, seg, R, j, Codec<B>::kTileBytes}, NB);
+    const int gx = row_ctas(reinterpret_cast<const void *>(kern), (NB + kThreads32 * U - 1) / (kThreads32 * U), R, &err);
+    if (gx <= 0) return err;
+    kern<<<dim3(gx, R), kThreads32, 0, s>>>(xp, n, ws, seg, NB);
     return cudaGetLastError();
 }
 
-static cudaError_t send(int bits, int dtype, const void *x, long long n, uint8_t *ws, long long seg, int R, int j,
-                        cudaStream_t s) {
+template <int B, int R>
+static cudaError_t reduce_all_r(uint8_t *ws, long long T, long long seg, cudaStream_t s) {
+    constexpr int U = reduce_units_per_thread<R>();
+    const long long per_row = (reduce_two_threads_per_block<B, R>() ? 128 : 64) * seg;
+    auto kern = twoshot_reduce_kernel<B, R, U>;
+    cudaError_t err = cudaSuccess;
+    const int gx = row_ctas(reinterpret_cast<const void *>(kern), (per_row + kThreads32 * U - 1) / (kThreads32 * U), R,
+                            &err);
+    if (gx <= 0) return err;
+    kern<<<dim3(gx, R), kThreads32, 0, s>>>(ws, T, seg);
+    return cudaGetLastError();
+}
+
+template <int B>
+static cudaError_t reduce_all(int R, uint8_t *ws, long long T, long long seg, cudaStream_t s) {
+    switch (R) {
+        case 1: return reduce_all_r<B, 1>(ws, T, seg, s);
+        case 2: return reduce_all_r<B, 2>(ws, T, seg, s);
+        case 3: return reduce_all_r<B, 3>(ws, T, seg, s);
+        case 4: return reduce_all_r<B, 4>(ws, T, seg, s);
+        case 5: return reduce_all_r<B, 5>(ws, T, seg, s);
+        case 6: return reduce_all_r<B, 6>(ws, T, seg, s);
+        case 7: return reduce_all_r<B, 7>(ws, T, seg, s);
+        case 8: return reduce_all_r<B, 8>(ws, T, seg, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int B, int DT>
+static cudaError_t decode_all(int R, const uint8_t *red, long long n, void *const *y, cudaStream_t s) {
+    constexpr int U = 4;  // half-blocks per thread in flight, as in the standalone decode
+    const long long NH = 128 * ((n + kTileValues - 1) / kTileValues);
+    MutPtrs yp{};
+    bool y32 = true;
+    for (int j = 0; j < R; ++j) {
+        yp.p[j] = y[j];
+        y32 = y32 && (reinterpret_cast<uintptr_t>(y[j]) & 31u) == 0;
+    }
+    auto kern = y32 ? twoshot_decode_kernel<B, DT, U, true> : twoshot_decode_kernel<B, DT, U, false>;
+    cudaError_t err = cudaSuccess;
+    const int gx = row_ctas(reinterpret_cast<const void *>(kern), (NH + kThreads32 * U - 1) / (kThreads32 * U), R, &err);
+    if (gx <= 0) return err;
+    kern<<<dim3(gx, R), kThreads32, 0, s>>>(red, n, yp, NH);
+    return cudaGetLastError();
+}
+
+template <int B, int DT>
+static cudaError_t run_twoshot(int R, const void *const *x, long long n, void *const *y, uint8_t *ws,
+                               cudaStream_t s) {
+    const long long T = (n + kTileValues - 1) / kTileValues;
+    const long long seg = twoshot_segment_tiles(T, R);
+    cudaError_t err;
+    if ((err = send_all<B, DT>(R, x, n, ws, seg, s)) != cudaSuccess) return err;
+    if ((err = reduce_all<B>(R, ws, T, seg, s)) != cudaSuccess) return err;
+    const uint8_t *red = ws + static_cast<long long>(R) * R * seg * Codec<B>::kTileBytes;
+    return decode_all<B, DT>(R, red, n, y, s);
+}
+
+cudaError_t launch_twoshot(int bits, int dtype, int R, const void *const *x, long long n, void *const *y, void *ws,
+                           cudaStream_t s) {
+    uint8_t *w = static_cast<uint8_t *>(ws);
 #define QR_CASE(B)                                                                                  \
     case B:                                                                                         \
-        return dtype ? send_rank<B, 1>(x, n, ws, seg, R, j, s) : send_rank<B, 0>(x, n, ws, seg, R, j, s);
+        return dtype ? run_twoshot<B, 1>(R, x, n, y, w, s) : run_twoshot<B, 0>(R, x, n, y, w, s);
     switch (bits) {
         QR_CASE(3)
         QR_CASE(4)
@@ -50,33 +166,6 @@ static cudaError_t send(int bits, int dtype, const void *x, long long n, uint8_t
     }
 #undef QR_CASE
     return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_twoshot(int bits, int dtype, int R, const void *const *x, long long n, void *const *y, void *ws,
-                           cudaStream_t s) {
-    const long long T = (n + kTileValues - 1) / kTileValues;
-    const long long seg = twoshot_segment_tiles(T, R);
-    const long long tb = 256LL * bits + 128;
-    uint8_t *w = static_cast<uint8_t *>(ws);
-    cudaError_t err;
-    // Phase-1: every rank sends segment k of its quantized message to owner k
-    for (int j = 0; j < R; ++j)
-        if ((err = send(bits, dtype, x[j], n, w, seg, R, j, s)) != cudaSuccess) return err;
-    // Phase-1B: owner k reduces the R copies of its segment into the gathered wire
-    uint8_t *red = w + static_cast<long long>(R) * R * seg * tb;
-    for (int k = 0; k < R; ++k) {
-        const long long t0 = k * seg;
-        if (t0 >= T) break;
-        const long long end = (k + 1) * seg * kTileValues;
-        const long long nk = (end < n ? end : n) - t0 * kTileValues;
-        const void *copies[kMaxRanks];
-        for (int j = 0; j < R; ++j) copies[j] = w + (static_cast<long long>(k) * R + j) * seg * tb;
-        if ((err = launch_reduce(bits, R, copies, nk, red + t0 * tb, s)) != cudaSuccess) return err;
-    }
-    // Phase-2: every rank decodes the gathered wire into its own output
-    for (int j = 0; j < R; ++j)
-        if ((err = launch_decode(bits, dtype, red, n, y[j], s)) != cudaSuccess) return err;
-    return cudaSuccess;
 }
 
 }  // namespace qrk

@@ -154,9 +154,10 @@ qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R,
  * tiles, owner k holding tiles [k*seg, (k+1)*seg).  Rank j quantizes its
  * message and writes segment k into owner k's receive buffer; owner k
  * reduces the R copies of its segment into the gathered wire; every rank
- * decodes the whole gathered wire into its own output y[j].  Each rank's and
- * each owner's work is a separate launch on `stream`, in that order.  Every
- * y[j] equals qr_allreduce's output.
+ * decodes the whole gathered wire into its own output y[j].  Each phase is
+ * one launch on `stream` (the sends, then the owners' reductions, then the
+ * decodes), with one grid row per rank or owner doing that rank's or owner's
+ * work alone.  Every y[j] equals qr_allreduce's output.
  * `workspace` (device, 16-byte aligned, at least
  * qr_twoshot_workspace_bytes(bits, R, n) bytes, owned by the caller) holds
  *   recv[k][j] at byte ((k*R + j) * seg) * qr_tile_bytes(bits): owner k's
