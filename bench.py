@@ -249,8 +249,8 @@ def measured_hbm() -> tuple[float, str]:
 
 
 # The sources that determine the benchmarked kernel's code and launch shape.
-FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_allreduce16.cuh", "qr_allreduce16_b3.cu",
-                   "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_grid.cu")
+FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_pipeline.cuh", "qr_allreduce16.cuh",
+                   "qr_allreduce16_b3.cu", "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_grid.cu")
 
 
 def csrc_hash(files=FUSED16_SOURCES) -> str:
@@ -306,12 +306,14 @@ def run_sweep(args) -> None:
     if args.sweep_codec == "fc":
         run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks)
         return
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for dtype in dtypes:
         tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
         for Rs in ranks:
             for n in sizes:
                 xs = [x.view(tdt) for x in workloads.device_sweep(Rs, n, dtype, seed=SEED, device=dev)]
                 y = torch.empty(n, dtype=tdt, device=dev)
+                y2 = torch.empty(n, dtype=tdt, device=dev)
                 for bits in widths:
                     W = qr.qr_wire_bytes(bits, n)
                     wires = [torch.empty(W, dtype=torch.uint8, device=dev) for _ in range(Rs)]
@@ -346,8 +348,14 @@ def run_sweep(args) -> None:
                     def twoshot():
                         qr.qr_allreduce_twoshot(bits, xs, ys=ys2, workspace=ws)
 
-                    arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all),
-                            ("reduce", reduce_only), ("decode", decode_only), ("twoshot", twoshot))
+                    regs_ctas = 4 * 4 * sms  # forces the register-fed fused kernel (four waves)
+
+                    def fused_regs():
+                        qr.qr_allreduce(bits, xs, y=y2, ctas=regs_ctas)
+
+                    arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
+                            ("encode", encode_all), ("reduce", reduce_only), ("decode", decode_only),
+                            ("twoshot", twoshot))
                     times = {name: [] for name, _ in arms}
                     for _ in range(3):
                         fused()
@@ -363,11 +371,12 @@ def run_sweep(args) -> None:
                             e1.record()
                             e1.synchronize()
                             times[name].append(e0.elapsed_time(e1))
-                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and all(
+                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
+                        torch.equal(y.view(torch.int16), y2.view(torch.int16))) and all(
                         torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in ys2)
                     # two-shot: R sends (2N in, W out each), R*W + W for the owners'
                     # reductions, R decodes (W in, 2N out each)
-                    kernel_b = {"fused": fused_b, "unfused": unf_b, "encode": Rs * (2 * n + W),
+                    kernel_b = {"fused": fused_b, "fused_regs": fused_b, "unfused": unf_b, "encode": Rs * (2 * n + W),
                                 "reduce": (Rs + 1) * W, "decode": W + 2 * n,
                                 "twoshot": 4 * Rs * n + (3 * Rs + 1) * W}
                     for name, alg in kernel_b.items():
@@ -549,7 +558,8 @@ def main() -> None:
         d = [s.elapsed_time(e) for s, e in ev[b]]
         avg = sum(d) / len(d)
         alg = R * N * 2 + N * 2
-        kernels[b] = {"kernel": f"allreduce16_kernel<{b},bf16,R={R}>", "launches": len(d), "avg_ms": avg,
+        kernels[b] = {"kernel": f"allreduce16_staged_kernel<{b},bf16,R={R},G=5,SG=1>", "launches": len(d),
+                      "avg_ms": avg,
                       "median_ms": statistics.median(d), "total_ms": sum(d),
                       "input_gbs": in_bytes_call / (avg / 1e3) / 1e9,
                       "achieved_gbs": alg / (avg / 1e3) / 1e9, "alg_bytes": alg}

@@ -38,7 +38,8 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_decode", "qr_allreduce", "qr_allreduce_emit", "qr_allreduce_ctas", "qr_status_string",
            "qr_fc_tile_bytes", "qr_fc_wire_bytes", "qr_fc_encode", "qr_fc_segment_reduce", "qr_fc_decode",
            "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot",
-           "qr_allreduce_twoshot_static")
+           "qr_allreduce_twoshot_static", "qr_wait_timeouts", "qr_selftest_bounded_wait",
+           "qr_allreduce_staged")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -89,6 +90,9 @@ def lib() -> ctypes.CDLL:
                 "qr_twoshot_workspace_bytes": (sz, [i32, i32, sz]),
                 "qr_allreduce_twoshot": (i32, [i32, i32, i32, vpp, sz, vpp, vp, sz, vp]),
                 "qr_allreduce_twoshot_static": (i32, [i32, i32, i32, vpp, sz, vpp, vp]),
+                "qr_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint)]),
+                "qr_allreduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
+                "qr_selftest_bounded_wait": (i32, [vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -146,6 +150,10 @@ class capi:
         return lib().qr_allreduce_ctas(bits, dtype, R, _ptr_array(xs), n, y, ctas, stream)
 
     @staticmethod
+    def qr_allreduce_staged(bits, dtype, R, xs, n, y, ctas, stream=None):
+        return lib().qr_allreduce_staged(bits, dtype, R, _ptr_array(xs), n, y, ctas, stream)
+
+    @staticmethod
     def qr_allreduce_twoshot(bits, dtype, R, xs, n, ys, workspace, workspace_bytes, stream=None):
         return lib().qr_allreduce_twoshot(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), workspace,
                                           workspace_bytes, stream)
@@ -153,6 +161,17 @@ class capi:
     @staticmethod
     def qr_allreduce_twoshot_static(bits, dtype, R, xs, n, ys, stream=None):
         return lib().qr_allreduce_twoshot_static(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), stream)
+
+    @staticmethod
+    def qr_wait_timeouts():
+        """(status, count) -- reads and clears the device's wait-timeout counter."""
+        c = ctypes.c_uint(0)
+        st = lib().qr_wait_timeouts(ctypes.byref(c))
+        return st, c.value
+
+    @staticmethod
+    def qr_selftest_bounded_wait(stream=None):
+        return lib().qr_selftest_bounded_wait(stream)
 
     @staticmethod
     def qr_fc_encode(bits, dtype, x, n, wire, stream=None):
@@ -316,6 +335,22 @@ def qr_allreduce(bits: int, xs, y: torch.Tensor | None = None, stream=None, ctas
     return y
 
 
+def qr_allreduce_staged(bits: int, xs, y: torch.Tensor | None = None, stream=None, ctas: int = 0) -> torch.Tensor:
+    """qr_allreduce on the staged kernel (bulk copies into shared memory, one
+    persistent CTA per SM) at any size; every tensor 32-byte aligned."""
+    xs, dt, n = _check_inputs(xs)
+    if y is None:
+        y = torch.empty_like(xs[0])
+    _cuda_contig(y, "y")
+    if y.dtype != xs[0].dtype or y.numel() != n:
+        raise ValueError("y must match the inputs' dtype and size")
+    dev = _same_device(xs + [y], "qr_allreduce_staged")
+    status = capi.qr_allreduce_staged(bits, dt, len(xs), [x.data_ptr() for x in xs], n, y.data_ptr(), ctas,
+                                      _stream(dev, stream))
+    _check(status, "qr_allreduce_staged")
+    return y
+
+
 def qr_allreduce_emit(bits: int, xs, y: torch.Tensor | None = None, wire_out=None,
                       red_out: torch.Tensor | None = None, stream=None):
     """qr_allreduce that also returns the R Phase-1 wires and the reduced wire."""
@@ -340,6 +375,14 @@ def qr_allreduce_emit(bits: int, xs, y: torch.Tensor | None = None, wire_out=Non
                                   [w.data_ptr() for w in wire_out], red_out.data_ptr(),
                                   _stream(dev, stream)), "qr_allreduce_emit")
     return y, wire_out, red_out
+
+
+def qr_wait_timeouts() -> int:
+    """Device-side waits that ran out on the current device since the last
+    call (0 in a correct run); resets the count.  Synchronizes the device."""
+    st, count = capi.qr_wait_timeouts()
+    _check(st, "qr_wait_timeouts")
+    return count
 
 
 def qr_twoshot_workspace_bytes(bits: int, R: int, n: int) -> int:

@@ -1,4 +1,5 @@
-// qr_allreduce.cu -- launcher of the fused two-shot kernel (allreduce_kernel).
+// qr_allreduce.cu -- launchers of the fused two-shot kernels: the choice between
+// allreduce_kernel and the 16-values-per-thread kernels, and the staged entry.
 #include <cstdint>
 
 #include "qr_kernels.cuh"
@@ -26,6 +27,24 @@ static cudaError_t run_allreduce(int R, const void *const *x, long long n, void 
     if (grid <= 0) return err;
     kern<<<grid, kThreads, 0, s>>>(xp, R, n, static_cast<uint16_t *>(y), wp, static_cast<uint8_t *>(red_out), T);
     return cudaGetLastError();
+}
+
+cudaError_t launch_allreduce_staged(int bits, int dtype, int R, const void *const *x, long long n, void *y, int ctas,
+                                    cudaStream_t s) {
+    ConstPtrs xp{};
+    for (int r = 0; r < R; ++r) xp.p[r] = x[r];
+#define QR_CASE(B)                                                                                  \
+    case B:                                                                                         \
+        return dtype ? run_allreduce16_staged<B, 1>(R, xp, n, y, ctas, s)                          \
+                     : run_allreduce16_staged<B, 0>(R, xp, n, y, ctas, s);
+    switch (bits) {
+        QR_CASE(3)
+        QR_CASE(4)
+        QR_CASE(6)
+        QR_CASE(8)
+    }
+#undef QR_CASE
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_allreduce(int bits, int dtype, int R, const void *const *x, long long n, void *y,

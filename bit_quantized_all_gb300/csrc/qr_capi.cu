@@ -243,7 +243,8 @@ QR_EXPORT qr_status_t qr_segment_reduce(int bits, int R, const void *const *wire
 namespace {
 
 qr_status_t allreduce_common(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n, void *y,
-                             void *const *wire_out, void *red_out, int ctas, qr_stream_t stream) {
+                             void *const *wire_out, void *red_out, int ctas, qr_stream_t stream,
+                             bool staged = false) {
     if (!x || !y || n == 0 || R < 1 || ctas < 0) return QR_ERR_INVALID_ARG;
     for (int r = 0; r < R && r < QR_MAX_RANKS; ++r) {
         if (!x[r]) return QR_ERR_INVALID_ARG;
@@ -270,6 +271,14 @@ qr_status_t allreduce_common(int bits, qr_dtype_t dtype, int R, const void *cons
         if (red_out && overlaps(red_out, W, x[r], V)) return QR_ERR_INVALID_ARG;
     }
     if (red_out && overlaps(red_out, W, y, V)) return QR_ERR_INVALID_ARG;
+    if (staged) {
+        const auto a32 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+        if (!a32(y)) return QR_ERR_MISALIGNED;
+        for (int r = 0; r < R; ++r)
+            if (!a32(x[r])) return QR_ERR_MISALIGNED;
+        return from_cuda(qrk::launch_allreduce_staged(bits, dtype, R, x, static_cast<long long>(n), y, ctas,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(qrk::launch_allreduce(bits, dtype, R, x, static_cast<long long>(n), y, wire_out, red_out,
                                            ctas, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -284,6 +293,11 @@ QR_EXPORT qr_status_t qr_allreduce(int bits, qr_dtype_t dtype, int R, const void
 QR_EXPORT qr_status_t qr_allreduce_emit(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
                                         void *y, void *const *wire_out, void *red_out, qr_stream_t stream) {
     return allreduce_common(bits, dtype, R, x, n, y, wire_out, red_out, 0, stream);
+}
+
+QR_EXPORT qr_status_t qr_allreduce_staged(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                          void *y, int ctas, qr_stream_t stream) {
+    return allreduce_common(bits, dtype, R, x, n, y, nullptr, nullptr, ctas, stream, true);
 }
 
 QR_EXPORT qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,

@@ -38,4 +38,33 @@ int grid_for(const void *kernel, int threads, long long tiles, int ctas, int wav
     return static_cast<int>(tiles < want ? tiles : want);
 }
 
+int sm_count(cudaError_t *err) {
+    *err = cudaSuccess;
+    int dev = 0;
+    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+    static std::mutex mu;
+    static std::map<int, int> sms;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = sms.find(dev);
+    if (it != sms.end()) return it->second;
+    int v = 0;
+    if ((*err = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
+    sms[dev] = v;
+    return v;
+}
+
+cudaError_t allow_dynamic_smem(const void *kernel, int bytes) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> done;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({dev, kernel});
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess) done[{dev, kernel}] = bytes;
+    return err;
+}
+
 }  // namespace qrk

@@ -4,10 +4,12 @@
 //
 // Every kernel is a grid-stride loop over 2048-value tiles; tiles are
 // independent, so any grid size gives the same bytes.  No kernel waits on
-// another CTA, allocates, or uses global scratch memory.
+// another CTA, allocates, or uses global scratch memory; the staged kernel's
+// threads wait only on their own CTA's shared-memory barriers.
 #pragma once
 
 #include "qr_device.cuh"
+#include "qr_pipeline.cuh"
 
 namespace qrk {
 
@@ -83,6 +85,32 @@ __global__ void __launch_bounds__(kThreads) allreduce_kernel(ConstPtrs x, int R,
 // saturated scale (block_scale2).
 constexpr int kThreads16 = 128;
 
+// One tile for one thread: raw[r] holds this thread's 16 values of rank r
+// (values base..base+15); the result goes to y[base..].  Called by whole
+// warps (the absmax of a block is shared by a lane pair).
+template <int B, int DT, int R>
+__device__ __forceinline__ void allreduce16_tile(const uint32_t (&raw)[R][8], uint16_t *y, long long base,
+                                                 long long n, bool full) {
+    float2 acc[8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float2 v[8], q[8];
+        widen16<DT>(raw[r], v);
+        const BlockScale2 sc = block_scale2<B>(pair_absmax(v));
+        quantize16<B>(v, sc.r, __any_sync(0xFFFFFFFFu, sc.low_clip), q);
+        const float2 s2 = make_float2(sc.s, sc.s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
+    }
+    const BlockScale2 sc = block_scale2<B>(pair_absmax(acc));
+    float2 q[8], o[8];
+    quantize16<B>(acc, sc.r, __any_sync(0xFFFFFFFFu, sc.low_clip), q);
+    const float2 s2 = make_float2(sc.s, sc.s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __fmul2_rn(q[i], s2);
+    store16<DT>(y, base, n, full, o);
+}
+
 template <int B, int DT, int R>
 __global__ void __launch_bounds__(kThreads16, 4) allreduce16_kernel(ConstPtrs x, long long n, uint16_t *y,
                                                                     long long T) {
@@ -93,24 +121,95 @@ __global__ void __launch_bounds__(kThreads16, 4) allreduce16_kernel(ConstPtrs x,
         uint32_t raw[R][8];
 #pragma unroll
         for (int r = 0; r < R; ++r) load16(static_cast<const uint16_t *>(x.p[r]), base, n, full, raw[r]);
-        float2 acc[8];
+        allreduce16_tile<B, DT, R>(raw, y, base, n, full);
+    }
+}
+
+// The same computation with the inputs staged through shared memory by the
+// bulk-copy engine, so that HBM reads stay in flight while the warps compute
+// (a register-fed kernel at 100+ registers per thread has too few warps per
+// SM to keep enough loads outstanding).  Persistent: one CTA per SM made of
+// G groups of 128 threads; each group is an independent pipeline over its
+// own tiles t = blockIdx.x + gridDim.x * (g + G * j), j = 0, 1, ..., with a
+// private ring of SG stages (stage = the R ranks' 4 KiB slices of one tile).
+//   - The group's leader thread fills a stage with R bulk copies whose
+//     completion is counted on the stage's mbarrier; the first SG tiles are
+//     issued up front.
+//   - For tile j the group waits on stage j % SG, copies its 32 bytes per
+//     rank per thread into registers, and meets at a named barrier that also
+//     ANDs every thread's "my wait completed" (so the group leaves the loop
+//     together, never stranding a thread in a hardware barrier); the leader
+//     then refills the stage with tile j + SG and the group computes while
+//     that copy is in flight.
+//   - A stage is only ever filled and drained by its own group, in order, so
+//     every parity wait refers to an unambiguous phase.
+//   - The ragged last tile (n not a multiple of 2048) is not staged: group 0
+//     of CTA 0 reads it with bounds-checked loads after its loop.
+// Every mbarrier wait gives up after one second; the group then adds one to
+// *timeouts, its leader waits (bounded again) for the copies it issued, and
+// the group returns.
+template <int B, int DT, int R, int G, int SG>
+__global__ void __launch_bounds__(128 * G, 1) allreduce16_staged_kernel(ConstPtrs x, long long n, uint16_t *y,
+                                                                        long long full_tiles, unsigned *timeouts) {
+    static_assert(G >= 1 && G <= 15 && SG >= 1, "named barriers 1..G, at least one stage per group");
+    constexpr uint32_t kSlice = kTileValues * 2;  // bytes of one rank's tile
+    extern __shared__ __align__(128) uint8_t ring[];  // G * SG * R * kSlice bytes
+    __shared__ __align__(8) uint64_t full[G * SG];
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G * SG; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    const int g = threadIdx.x / 128, k = threadIdx.x & 127;
+    const bool leader = k == 0;
+    const long long first = blockIdx.x + static_cast<long long>(gridDim.x) * g;  // tile of j = 0
+    const long long stride = static_cast<long long>(gridDim.x) * G;
+    const long long tiles = full_tiles > first ? (full_tiles - first + stride - 1) / stride : 0;
+    uint8_t *my_ring = ring + static_cast<size_t>(g) * SG * R * kSlice;
+    uint64_t *my_full = full + g * SG;
+
+    auto issue = [&](long long j) {  // leader only: stage j % SG <- tile j
+        const int s = static_cast<int>(j % SG);
+        const long long t = first + j * stride;
+        mbar_arrive_expect_tx(&my_full[s], R * kSlice);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float2 v[8], q[8];
-            widen16<DT>(raw[r], v);
-            const BlockScale2 sc = block_scale2<B>(pair_absmax(v));
-            quantize16<B>(v, sc.r, __any_sync(0xFFFFFFFFu, sc.low_clip), q);
-            const float2 s2 = make_float2(sc.s, sc.s);
+        for (int r = 0; r < R; ++r)
+            bulk_copy_g2s(my_ring + (static_cast<size_t>(s) * R + r) * kSlice,
+                          static_cast<const uint8_t *>(x.p[r]) + t * kSlice, kSlice, &my_full[s]);
+    };
+
+    long long issued = 0;
+    if (leader)
+        for (; issued < tiles && issued < SG; ++issued) issue(issued);
+
+    long long j = 0;
+    for (; j < tiles; ++j) {
+        const int s = static_cast<int>(j % SG);
+        const bool ok = mbar_wait(&my_full[s], static_cast<uint32_t>((j / SG) & 1));
+        uint32_t raw[R][8];
+        const uint8_t *stage = my_ring + static_cast<size_t>(s) * R * kSlice + 32 * k;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
+        for (int r = 0; r < R; ++r) lds32(stage + r * kSlice, raw[r]);
+        if (!group_all(1 + g, ok)) break;  // also: every thread is done reading stage s
+        if (leader && issued < tiles) issue(issued++);
+        allreduce16_tile<B, DT, R>(raw, y, (first + j * stride) * kTileValues + 16 * k, n, true);
+    }
+    if (j < tiles) {  // a wait ran out
+        if (leader) {
+            atomicAdd(timeouts, 1u);
+            for (long long i = j; i < issued; ++i)  // copies still in flight into this group's stages
+                if (!mbar_wait(&my_full[i % SG], static_cast<uint32_t>((i / SG) & 1))) break;
         }
-        const BlockScale2 sc = block_scale2<B>(pair_absmax(acc));
-        float2 q[8], o[8];
-        quantize16<B>(acc, sc.r, __any_sync(0xFFFFFFFFu, sc.low_clip), q);
-        const float2 s2 = make_float2(sc.s, sc.s);
+        return;
+    }
+    if (blockIdx.x == 0 && g == 0 && full_tiles * kTileValues < n) {
+        const long long base = full_tiles * kTileValues + 16 * k;
+        uint32_t raw[R][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = __fmul2_rn(q[i], s2);
-        store16<DT>(y, base, n, full, o);
+        for (int r = 0; r < R; ++r) load16(static_cast<const uint16_t *>(x.p[r]), base, n, false, raw[r]);
+        allreduce16_tile<B, DT, R>(raw, y, base, n, false);
     }
 }
 

@@ -12,6 +12,17 @@ namespace qrk {
 // Returns 0 (with *err set) if the device cannot be queried.
 int grid_for(const void *kernel, int threads, long long tiles, int ctas, int waves, cudaError_t *err);
 
+// Streaming multiprocessors of the current device (cached); 0 on error.
+int sm_count(cudaError_t *err);
+
+// Raises the dynamic shared-memory limit of `kernel` to `bytes` on the
+// current device (once per device and kernel).
+cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
+
+// Device address of the library's wait-timeout counter on the current
+// device (qr_timeouts.cu); nullptr with *err set on failure.
+unsigned *wait_timeout_counter(cudaError_t *err);
+
 cudaError_t launch_encode(int bits, int dtype, const void *x, long long n, void *wire,
                           cudaStream_t s);
 cudaError_t launch_decode(int bits, int dtype, const void *wire, long long n, void *y,
@@ -28,6 +39,14 @@ struct ConstPtrs;
 // wire emission), instantiated per width in qr_allreduce16_b<B>.cu.
 template <int B, int DT>
 cudaError_t run_allreduce16(int R, const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s);
+
+// The staged fused kernel (bulk copies into shared memory, one persistent
+// CTA per SM; every pointer 32-byte aligned) with min(ctas or #SMs, #SMs,
+// full tiles) CTAs, at least one.
+template <int B, int DT>
+cudaError_t run_allreduce16_staged(int R, const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s);
+cudaError_t launch_allreduce_staged(int bits, int dtype, int R, const void *const *x, long long n, void *y, int ctas,
+                                    cudaStream_t s);
 
 // The two-shot all-reduce with its exchange laid out per rank and per owner in
 // a workspace of R*(R+1)*seg tiles, seg = twoshot_segment_tiles(T, R)

@@ -54,7 +54,9 @@
  *   - An output may alias an input of the same call exactly (same pointer,
  *     in-place) where noted; partial overlap is rejected.
  *   - Calls are thread-safe.  The library keeps only a per-device cache of
- *     launch limits (SM count, occupancy), filled on first use.
+ *     launch limits (SM count, occupancy), filled on first use, and a
+ *     per-device counter of device-side waits that ran out
+ *     (qr_wait_timeouts).
  */
 #ifndef QR_H
 #define QR_H
@@ -122,7 +124,11 @@ qr_status_t qr_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n,
  * with two quantization round trips): y = decode(segment_reduce(encode(x[0]),
  * ..., encode(x[R-1]))), in one pass over HBM with every intermediate on
  * chip.  `x` is a host array of R device pointers to n values each; 1 <= R
- * <= 8.  `y` (n values) may equal one of the x[r] exactly (in-place). */
+ * <= 8.  `y` (n values) may equal one of the x[r] exactly (in-place).
+ * Kernel choice (the result is the same bytes either way): with every
+ * pointer 32-byte aligned, R >= 4 and at least 48 full tiles per SM (R = 3:
+ * 128), the staged kernel of qr_allreduce_staged; otherwise a grid-stride
+ * kernel that loads the inputs straight into registers. */
 qr_status_t qr_allreduce(int bits, qr_dtype_t dtype, int R,
                          const void *const *x, size_t n, void *y,
                          qr_stream_t stream);
@@ -138,10 +144,24 @@ qr_status_t qr_allreduce_emit(int bits, qr_dtype_t dtype, int R,
                               void *const *wire_out, void *red_out,
                               qr_stream_t stream);
 
-/* qr_allreduce with an explicit grid size: `ctas` CTAs in the grid-stride
- * loop over tiles (0 = the library's choice, four waves of resident CTAs).  The
- * result does not depend on `ctas`; it is the SM-count knob of [FC] key
- * machinery ("tuning the number of streaming multiprocessors"). */
+/* qr_allreduce on the staged kernel, whatever the size: a persistent kernel
+ * (one CTA per SM) whose CTAs bring every rank's slice of a tile into shared
+ * memory with bulk asynchronous copies, several tiles ahead, and run the
+ * arithmetic from there.  `ctas` = 0 for one CTA per SM, else min(ctas,
+ * #SMs) CTAs (at least one, at most one per full tile); the result does not
+ * depend on it.  Every x[r] and y must be 32-byte aligned
+ * (QR_ERR_MISALIGNED otherwise); ctas < 0 is QR_ERR_INVALID_ARG.  The
+ * kernel's waits on its shared-memory barriers are bounded (see
+ * qr_wait_timeouts).  Same other arguments and errors as qr_allreduce. */
+qr_status_t qr_allreduce_staged(int bits, qr_dtype_t dtype, int R,
+                                const void *const *x, size_t n, void *y,
+                                int ctas, qr_stream_t stream);
+
+/* qr_allreduce with an explicit grid size: `ctas` > 0 runs the grid-stride
+ * kernel with `ctas` CTAs over the tiles; 0 = the library's choice (what
+ * qr_allreduce does).  The result does not depend on `ctas`; it is the
+ * SM-count knob of [FC] key machinery ("tuning the number of streaming
+ * multiprocessors"). */
 qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R,
                               const void *const *x, size_t n, void *y,
                               int ctas, qr_stream_t stream);
@@ -205,6 +225,23 @@ qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R,
 qr_status_t qr_allreduce_twoshot_static(int bits, qr_dtype_t dtype, int R,
                                         const void *const *x, size_t n,
                                         void *const *y, qr_stream_t stream);
+
+/* Device-side waits that ran out (no counterpart on the source pages; a
+ * safety property of this library).  A kernel that waits on a shared-memory
+ * barrier gives each wait one second; if a wait runs out (which a correct
+ * launch never does) the kernel adds one to a per-device counter, stops
+ * issuing work, waits (again bounded) for its own copies in flight and
+ * returns, leaving the context usable; its outputs are then incomplete.
+ * qr_wait_timeouts stores the current device's count in *count and resets
+ * it to zero; it synchronizes with the device (a blocking copy), so call it
+ * between steps, not inside a stream capture.  QR_ERR_INVALID_ARG for a
+ * null `count`, QR_ERR_CUDA if the copy fails. */
+qr_status_t qr_wait_timeouts(unsigned *count);
+
+/* Self-test of the bounded wait: enqueues one single-thread kernel on
+ * `stream` that waits on a barrier nothing completes; after one second it
+ * gives up and adds one to the qr_wait_timeouts counter.  Only for tests. */
+qr_status_t qr_selftest_bounded_wait(qr_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * The Flash Communication codec ([FC] key machinery "asymmetric group-128

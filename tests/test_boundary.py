@@ -138,6 +138,16 @@ def test_allreduce_validation():
     assert capi.qr_allreduce(3, 0, 2, xs, n, B - 4096) == qr.QR_ERR_INVALID_ARG  # y's end overlaps x[1]
     assert capi.qr_allreduce(3, 0, 2, xs, 2**63, Y) == qr.QR_ERR_SIZE
     assert capi.qr_allreduce_ctas(3, 0, 2, xs, n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    # the staged kernel: the same checks, ctas >= 0, and 32-byte alignment
+    assert capi.qr_allreduce_staged(3, 0, 2, xs, n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_staged(3, 0, 2, xs, 0, Y, 0) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_staged(1, 0, 2, xs, n, Y, 0) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_allreduce_staged(3, 0, 2, [A, B + 16], n, Y, 0) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_allreduce_staged(3, 0, 2, xs, n, Y + 16, 0) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_allreduce_staged(3, 0, 2, xs, n, A + 32, 0) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_allreduce_staged(3, 0, 2, xs, 2**63, Y, 0) == qr.QR_ERR_SIZE
+    # the timeout counter's reader rejects a null destination without touching the device
+    assert qr.lib().qr_wait_timeouts(None) == qr.QR_ERR_INVALID_ARG
     # emit: every output disjoint from every other buffer
     wo = [Y + 2**20, Y + 2**21]
     assert capi.qr_allreduce_emit(3, 0, 2, xs, n, Y, [wo[0], None], None) == qr.QR_ERR_INVALID_ARG

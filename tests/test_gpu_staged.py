@@ -1,0 +1,153 @@
+"""The staged fused kernel (inputs brought into shared memory by bulk
+asynchronous copies, one persistent CTA per SM) against the oracle and
+against the register-fed fused kernel.
+
+qr_allreduce_staged always runs the staged kernel; qr_allreduce takes it
+when every pointer is 32-byte aligned, R >= 3 and the message is long
+enough; qr_allreduce_ctas with ctas > 0 always takes the register-fed
+kernel.  Both must give the oracle's
+bytes.  The staged kernel's shared-memory waits are bounded: a correct run
+leaves the library's wait-timeout counter at zero, and the self-test that
+makes a wait run out on purpose moves it by exactly one while later work
+still runs correctly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_quantized_all_gb300 as qr
+import oracle
+from bit_quantized_all_gb300 import capi
+from qr_testlib import assert_outputs_match, to_dev, to_host_u16, xmax_of
+
+pytestmark = pytest.mark.gpu
+
+BITS = [3, 4, 6, 8]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from bit_quantized_all_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    qr.lib()
+    qr.qr_wait_timeouts()  # start from zero
+
+
+def _sms():
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
+def _threshold_tiles(R):
+    """Full tiles from which qr_allreduce takes the staged kernel (none for R <= 2)."""
+    return {3: 128}.get(R, 48) * _sms() if R >= 3 else None
+
+
+def _ranks(R, n, dtype, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for r in range(R):
+        v = rng.standard_normal(n).astype(np.float32) * np.float32(1 + 0.5 * r)
+        v[rng.integers(0, n, size=max(1, n // 500))] *= 40.0
+        out.append(oracle.narrow(dtype, v))
+    return out
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_against_the_oracle(R):
+    """Three CTAs (15 groups) over 100 full tiles and a ragged tail: every
+    group runs through its ring of stages several times (each barrier's
+    parity flips), every width, both types."""
+    n = 100 * 2048 + 777
+    for dtype in (0, 1):
+        xs = _ranks(R, n, dtype, 900 + 10 * R + dtype)
+        xs_dev = [to_dev(x, dtype) for x in xs]
+        xmax = xmax_of(xs, dtype)
+        for bits in BITS:
+            y = qr.qr_allreduce_staged(bits, xs_dev, ctas=3)
+            y_ref = oracle.allreduce(bits, dtype, xs)
+            assert_outputs_match(to_host_u16(y), y_ref, dtype, xmax, f"staged R={R} INT{bits} dt={dtype}")
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("n", [1, 37, 2047, 2048, 2049, 2048 * 5, 2048 * 5 + 1999])
+@pytest.mark.parametrize("R", [1, 3, 8])
+def test_short_messages(n, R):
+    """Messages of no full tile (only the ragged one), exactly one tile, and a few."""
+    for bits in BITS:
+        xs = _ranks(R, n, 1, 31 * n + R + bits)
+        y = qr.qr_allreduce_staged(bits, [to_dev(x, 1) for x in xs])
+        assert_outputs_match(to_host_u16(y), oracle.allreduce(bits, 1, xs), 1, xmax_of(xs, 1),
+                             f"n={n} R={R} INT{bits}")
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("ctas", [0, 1, 2, 5, 151, 152, 153, 100000])
+def test_grid_size_does_not_change_the_result(ctas):
+    R, n = 8, (5 * 152 * 2 + 3) * 2048 + 9  # two tiles per group at one CTA per SM, and a tail
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(17)
+    xs = [(torch.randn(n, device="cuda", generator=gen) * (r + 1)).to(torch.bfloat16) for r in range(R)]
+    for bits in (4, 3):
+        y_regs = qr.qr_allreduce(bits, xs, ctas=1000)
+        y_st = qr.qr_allreduce_staged(bits, xs, ctas=ctas)
+        assert torch.equal(y_st.view(torch.int16), y_regs.view(torch.int16)), (bits, ctas)
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 8])
+@pytest.mark.parametrize("offset", [-1, 0, 1])
+def test_dispatch_around_the_threshold(R, offset):
+    """qr_allreduce (library's choice) == the register-fed kernel == the
+    staged kernel, one tile below, at and above the threshold, ragged."""
+    base = _threshold_tiles(R) or 48 * _sms()
+    n = (base + offset) * 2048 + 100
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(n + R)
+    xs = [(torch.randn(n, device="cuda", generator=gen) * (r + 1)).to(torch.bfloat16) for r in range(R)]
+    y_default = qr.qr_allreduce(4, xs)
+    y_regs = qr.qr_allreduce(4, xs, ctas=4 * 4 * _sms())
+    y_st = qr.qr_allreduce_staged(4, xs)
+    assert torch.equal(y_default.view(torch.int16), y_regs.view(torch.int16))
+    assert torch.equal(y_st.view(torch.int16), y_regs.view(torch.int16))
+    assert qr.qr_wait_timeouts() == 0
+
+
+def test_in_place_and_repeat():
+    R = 4
+    n = 300 * 2048 + 3
+    xs = [to_dev(x, 0) for x in _ranks(R, n, 0, 77)]
+    y0 = qr.qr_allreduce_staged(4, xs)
+    y1 = qr.qr_allreduce_staged(4, xs)
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    xs2 = [x.clone() for x in xs]
+    qr.qr_allreduce_staged(4, xs2, y=xs2[2])  # output over one of the inputs
+    assert torch.equal(xs2[2].view(torch.int16), y0.view(torch.int16))
+    assert qr.qr_wait_timeouts() == 0
+
+
+def test_misaligned_for_the_staged_kernel():
+    """16-byte aligned but not 32: rejected by the staged entry, accepted
+    (other kernel) by qr_allreduce."""
+    n = 4096
+    bufs = [torch.zeros(n + 16, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    xs = [b[8:8 + n] for b in bufs]  # 16 bytes past a 512-byte boundary
+    with pytest.raises(qr.QRError):
+        qr.qr_allreduce_staged(4, xs)
+    y = qr.qr_allreduce(4, xs)
+    assert y.numel() == n
+
+
+def test_bounded_wait_runs_out_and_is_reported():
+    """A wait on a barrier nothing completes gives up after one second,
+    counts once, and leaves the context usable."""
+    assert qr.qr_wait_timeouts() == 0
+    assert capi.qr_selftest_bounded_wait(torch.cuda.current_stream().cuda_stream) == qr.QR_OK
+    torch.cuda.synchronize()
+    assert qr.qr_wait_timeouts() == 1
+    assert qr.qr_wait_timeouts() == 0  # reading clears it
+    R, n = 2, 50 * 2048 + 1
+    xs = _ranks(R, n, 1, 5)
+    y = qr.qr_allreduce_staged(3, [to_dev(x, 1) for x in xs], ctas=2)
+    assert_outputs_match(to_host_u16(y), oracle.allreduce(3, 1, xs), 1, xmax_of(xs, 1), "after the self-test")
+    assert qr.qr_wait_timeouts() == 0
