@@ -10,19 +10,24 @@
 namespace qrk {
 
 // Launch shape of the staged kernel for R ranks: five groups of 128 threads
-// (20 warps; at 96 registers a thread, the most the SM's register quadrants
-// allow for five warps each), each with as many stages (at most 4) as fit in
-// 224 KiB of shared memory at R * 4 KiB per stage.  Measured on GB300 at
-// R=8 (2^27 bf16 values per rank, INT4/INT3): 4 groups 6.74 TB/s, 5 groups
-// 6.93 TB/s, 6 and 7 groups 6.38 and 5.97 TB/s (register spills), one to
-// three groups with more stages each 4.4-5.5 TB/s (too few warps to issue
-// the arithmetic); the register-fed kernel 6.36 TB/s.
+// (20 warps: at 96 registers a thread, the most that five warps in each of
+// the SM's four register quadrants allow), each with as many stages (at most
+// 4) as fit in 224 KiB of shared memory at R * 4 KiB per stage; each group
+// sums the first R/2 ranks straight from shared memory and copies the other
+// R/2 into registers before it releases the stage.  Measured on GB300 at
+// R=8 (2^27 bf16 values per rank, INT4 and INT3, back-to-back launches):
+//   groups x early ranks:  5 x 0: 6.65 TB/s   5 x 2: 6.92   5 x 4: 6.99
+//                          5 x 6: 6.84        6 x 4: 6.75   6 x 6: 6.98
+//                          7 x 4: 6.50        7 x 6: 6.65   4 x 4: 6.75
+// (one to three groups with deeper rings: 4.4-5.5 TB/s, too few warps to
+// issue the arithmetic); the register-fed kernel 6.36 TB/s.
 template <int R>
 struct StagedShape {
     static constexpr int kGroups = 5;
     static constexpr int kFit = (224 * 1024) / (kGroups * R * kTileValues * 2);
     static constexpr int kStages = kFit >= 4 ? 4 : kFit;  // per group
     static constexpr int kSmemBytes = kGroups * kStages * R * kTileValues * 2;
+    static constexpr int kEarlyRanks = R / 2;  // summed from shared memory before the stage is released
     static_assert(kStages >= 1, "at least one stage per group");
 };
 
@@ -40,7 +45,7 @@ constexpr long long staged_min_tiles_per_sm() {
 template <int B, int DT, int R>
 static cudaError_t run_allreduce16_staged_r(const ConstPtrs &xp, long long n, void *y, int ctas, cudaStream_t s) {
     using Shape = StagedShape<R>;
-    auto kern = allreduce16_staged_kernel<B, DT, R, Shape::kGroups, Shape::kStages>;
+    auto kern = allreduce16_staged_kernel<B, DT, R, Shape::kGroups, Shape::kStages, Shape::kEarlyRanks>;
     cudaError_t err = cudaSuccess;
     const int sms = sm_count(&err);
     if (sms <= 0) return err;

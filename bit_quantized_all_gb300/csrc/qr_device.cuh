@@ -384,6 +384,13 @@ __device__ __forceinline__ void st_global32(void *p, const uint32_t (&w)[8]) {
                  : "memory");
 }
 
+// 32 bytes = w[4..7] then w[0..3].
+__device__ __forceinline__ void st_global32_swapped(void *p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[4]), "r"(w[5]),
+                 "r"(w[6]), "r"(w[7]), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                 : "memory");
+}
+
 // 16 values at `base` of an n-value message as 8 packed words; values at or
 // past n are +0.
 __device__ __forceinline__ void load16(const uint16_t *x, long long base, long long n, bool full,
@@ -475,12 +482,15 @@ __device__ __forceinline__ void quantize16(const float2 (&v)[8], float r, bool l
 
 template <int DT>
 __device__ __forceinline__ void store16(uint16_t *y, long long base, long long n, bool full,
-                                        const float2 (&o)[8]) {
+                                        const float2 (&o)[8], bool swapped_halves = false) {
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = narrow2<DT>(o[i].x, o[i].y);
     if (full) {
-        st_global32(y + base, w);
+        if (swapped_halves)  // o[0..3] are values 8..15, o[4..7] values 0..7
+            st_global32_swapped(y + base, w);
+        else
+            st_global32(y + base, w);
     } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {

@@ -85,30 +85,44 @@ __global__ void __launch_bounds__(kThreads) allreduce_kernel(ConstPtrs x, int R,
 // saturated scale (block_scale2).
 constexpr int kThreads16 = 128;
 
-// One tile for one thread: raw[r] holds this thread's 16 values of rank r
-// (values base..base+15); the result goes to y[base..].  Called by whole
-// warps (the absmax of a block is shared by a lane pair).
-template <int B, int DT, int R>
-__device__ __forceinline__ void allreduce16_tile(const uint32_t (&raw)[R][8], uint16_t *y, long long base,
-                                                 long long n, bool full) {
-    float2 acc[8];
+// Phase-1 and Phase-1B of one rank for one thread: quantize the thread's 16
+// values of rank r (w; values base..base+15, or with their two 8-value
+// halves exchanged -- the same way for every rank, since every step here is
+// per value or over the whole block) and add their dequantized values into
+// acc in rank order (acc = q*s for the first rank).  Called by whole warps
+// (the absmax of a block is shared by a lane pair).
+template <int B, int DT>
+__device__ __forceinline__ void accumulate_rank(const uint32_t (&w)[8], float2 (&acc)[8], bool first) {
+    float2 v[8], q[8];
+    widen16<DT>(w, v);
+    const BlockScale2 sc = block_scale2<B>(pair_absmax(v));
+    quantize16<B>(v, sc.r, __any_sync(0xFFFFFFFFu, sc.low_clip), q);
+    const float2 s2 = make_float2(sc.s, sc.s);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        float2 v[8], q[8];
-        widen16<DT>(raw[r], v);
-        const BlockScale2 sc = block_scale2<B>(pair_absmax(v));
-        quantize16<B>(v, sc.r, __any_sync(0xFFFFFFFFu, sc.low_clip), q);
-        const float2 s2 = make_float2(sc.s, sc.s);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
-    }
+    for (int i = 0; i < 8; ++i) acc[i] = first ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
+}
+
+// Requantize the sums and write the dequantized result (Phase-2) to y[base..].
+template <int B, int DT>
+__device__ __forceinline__ void finish_tile(const float2 (&acc)[8], uint16_t *y, long long base, long long n,
+                                            bool full, bool swapped = false) {
     const BlockScale2 sc = block_scale2<B>(pair_absmax(acc));
     float2 q[8], o[8];
     quantize16<B>(acc, sc.r, __any_sync(0xFFFFFFFFu, sc.low_clip), q);
     const float2 s2 = make_float2(sc.s, sc.s);
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = __fmul2_rn(q[i], s2);
-    store16<DT>(y, base, n, full, o);
+    store16<DT>(y, base, n, full, o, swapped);
+}
+
+// One tile for one thread: raw[r] holds this thread's 16 values of rank r.
+template <int B, int DT, int R>
+__device__ __forceinline__ void allreduce16_tile(const uint32_t (&raw)[R][8], uint16_t *y, long long base,
+                                                 long long n, bool full) {
+    float2 acc[8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) accumulate_rank<B, DT>(raw[r], acc, r == 0);
+    finish_tile<B, DT>(acc, y, base, n, full);
 }
 
 template <int B, int DT, int R>
@@ -135,8 +149,12 @@ __global__ void __launch_bounds__(kThreads16, 4) allreduce16_kernel(ConstPtrs x,
 //   - The group's leader thread fills a stage with R bulk copies whose
 //     completion is counted on the stage's mbarrier; the first SG tiles are
 //     issued up front.
-//   - For tile j the group waits on stage j % SG, copies its 32 bytes per
-//     rank per thread into registers, and meets at a named barrier that also
+//   - For tile j the group waits on stage j % SG, quantizes and sums ranks
+//     0..K-1 straight from the stage, copies the other R-K ranks' 32 bytes
+//     per thread into registers (lanes with bit 2 set read the two 16-byte
+//     halves in the other order, so that every 8 lanes cover the 32 banks
+//     once; their values stay exchanged up to the store), and meets at a
+//     named barrier that also
 //     ANDs every thread's "my wait completed" (so the group leaves the loop
 //     together, never stranding a thread in a hardware barrier); the leader
 //     then refills the stage with tile j + SG and the group computes while
@@ -148,69 +166,94 @@ __global__ void __launch_bounds__(kThreads16, 4) allreduce16_kernel(ConstPtrs x,
 // Every mbarrier wait gives up after one second; the group then adds one to
 // *timeouts, its leader waits (bounded again) for the copies it issued, and
 // the group returns.
-template <int B, int DT, int R, int G, int SG>
+// The ragged last tile for the staged kernel, read with bounds-checked loads.
+// Not inlined: its 8R conditional loads would otherwise set the register
+// budget of the whole kernel and push the main loop into spills.
+template <int B, int DT, int R>
+__device__ __noinline__ void allreduce16_ragged_tile(const ConstPtrs &x, long long n, uint16_t *y, long long base) {
+    uint32_t raw[R][8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) load16(static_cast<const uint16_t *>(x.p[r]), base, n, false, raw[r]);
+    allreduce16_tile<B, DT, R>(raw, y, base, n, false);
+}
+
+template <int B, int DT, int R, int G, int SG, int K>
 __global__ void __launch_bounds__(128 * G, 1) allreduce16_staged_kernel(ConstPtrs x, long long n, uint16_t *y,
                                                                         long long full_tiles, unsigned *timeouts) {
     static_assert(G >= 1 && G <= 15 && SG >= 1, "named barriers 1..G, at least one stage per group");
+    static_assert(K >= 0 && K < R, "ranks taken from shared memory before the stage is released");
     constexpr uint32_t kSlice = kTileValues * 2;  // bytes of one rank's tile
+    constexpr uint32_t kStageBytes = R * kSlice;
     extern __shared__ __align__(128) uint8_t ring[];  // G * SG * R * kSlice bytes
     __shared__ __align__(8) uint64_t full[G * SG];
+    __shared__ const uint8_t *src[R];  // the ranks' inputs, read by the leaders at each refill
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G * SG; ++s) mbar_init(&full[s], 1);
+        for (int r = 0; r < R; ++r) src[r] = static_cast<const uint8_t *>(x.p[r]);
         mbar_init_fence();
     }
     __syncthreads();
 
     const int g = threadIdx.x / 128, k = threadIdx.x & 127;
     const bool leader = k == 0;
-    const long long first = blockIdx.x + static_cast<long long>(gridDim.x) * g;  // tile of j = 0
+    // this group's tiles: t = first + j * stride, j < tiles (32-bit: a group
+    // never has 2^31 tiles)
+    const long long first = blockIdx.x + static_cast<long long>(gridDim.x) * g;
     const long long stride = static_cast<long long>(gridDim.x) * G;
-    const long long tiles = full_tiles > first ? (full_tiles - first + stride - 1) / stride : 0;
-    uint8_t *my_ring = ring + static_cast<size_t>(g) * SG * R * kSlice;
+    const int tiles = full_tiles > first ? static_cast<int>((full_tiles - first + stride - 1) / stride) : 0;
+    uint8_t *my_ring = ring + static_cast<size_t>(g) * SG * kStageBytes;
     uint64_t *my_full = full + g * SG;
+    // this thread's 32 bytes in a stage, first and second 16-byte half
+    // (exchanged in lanes with bit 2 set: see lds32)
+    const bool swap = (k >> 2) & 1;
+    const uint32_t mine = smem_addr(my_ring) + 32u * k;
+    const uint32_t half_a = mine + (swap ? 16u : 0u), half_b = mine + (swap ? 0u : 16u);
 
-    auto issue = [&](long long j) {  // leader only: stage j % SG <- tile j
-        const int s = static_cast<int>(j % SG);
-        const long long t = first + j * stride;
-        mbar_arrive_expect_tx(&my_full[s], R * kSlice);
+    auto issue = [&](int j) {  // leader only: stage j % SG <- tile j
+        const int s = j % SG;
+        const long long off = (first + j * stride) * kSlice;
+        uint8_t *dst = my_ring + static_cast<size_t>(s) * kStageBytes;
+        mbar_arrive_expect_tx(&my_full[s], kStageBytes);
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-            bulk_copy_g2s(my_ring + (static_cast<size_t>(s) * R + r) * kSlice,
-                          static_cast<const uint8_t *>(x.p[r]) + t * kSlice, kSlice, &my_full[s]);
+        for (int r = 0; r < R; ++r) bulk_copy_g2s(dst + r * kSlice, src[r] + off, kSlice, &my_full[s]);
     };
 
-    long long issued = 0;
+    int issued = 0;
     if (leader)
         for (; issued < tiles && issued < SG; ++issued) issue(issued);
 
-    long long j = 0;
+    int j = 0;
     for (; j < tiles; ++j) {
-        const int s = static_cast<int>(j % SG);
+        const int s = j % SG;
         const bool ok = mbar_wait(&my_full[s], static_cast<uint32_t>((j / SG) & 1));
-        uint32_t raw[R][8];
-        const uint8_t *stage = my_ring + static_cast<size_t>(s) * R * kSlice + 32 * k;
+        const uint32_t at = static_cast<uint32_t>(s) * kStageBytes;
+        float2 acc[8];
 #pragma unroll
-        for (int r = 0; r < R; ++r) lds32(stage + r * kSlice, raw[r]);
+        for (int r = 0; r < K; ++r) {  // straight from the stage (garbage if !ok: never stored)
+            uint32_t w[8];
+            lds_rank<kSlice>(half_a + at, half_b + at, r, w);
+            accumulate_rank<B, DT>(w, acc, r == 0);
+        }
+        uint32_t rest[R - K][8];
+#pragma unroll
+        for (int r = K; r < R; ++r) lds_rank<kSlice>(half_a + at, half_b + at, r, rest[r - K]);
         if (!group_all(1 + g, ok)) break;  // also: every thread is done reading stage s
         if (leader && issued < tiles) issue(issued++);
-        allreduce16_tile<B, DT, R>(raw, y, (first + j * stride) * kTileValues + 16 * k, n, true);
+#pragma unroll
+        for (int r = K; r < R; ++r) accumulate_rank<B, DT>(rest[r - K], acc, r == 0);
+        finish_tile<B, DT>(acc, y, (first + j * stride) * kTileValues + 16 * k, n, true, swap);
     }
     if (j < tiles) {  // a wait ran out
         if (leader) {
             atomicAdd(timeouts, 1u);
-            for (long long i = j; i < issued; ++i)  // copies still in flight into this group's stages
+            for (int i = j; i < issued; ++i)  // copies still in flight into this group's stages
                 if (!mbar_wait(&my_full[i % SG], static_cast<uint32_t>((i / SG) & 1))) break;
         }
         return;
     }
-    if (blockIdx.x == 0 && g == 0 && full_tiles * kTileValues < n) {
-        const long long base = full_tiles * kTileValues + 16 * k;
-        uint32_t raw[R][8];
-#pragma unroll
-        for (int r = 0; r < R; ++r) load16(static_cast<const uint16_t *>(x.p[r]), base, n, false, raw[r]);
-        allreduce16_tile<B, DT, R>(raw, y, base, n, false);
-    }
+    if (blockIdx.x == 0 && g == 0 && full_tiles * kTileValues < n)
+        allreduce16_ragged_tile<B, DT, R>(x, n, y, full_tiles * kTileValues + 16 * k);
 }
 
 }  // namespace qrk

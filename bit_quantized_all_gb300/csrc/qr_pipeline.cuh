@@ -89,15 +89,41 @@ __device__ __forceinline__ bool group_all(int id, bool pred) {
     return out != 0;
 }
 
-// 32 bytes from shared memory (two 16-byte loads).  Plain loads: the
-// "memory" clobbers of the barrier wait before them and the arrive after
-// them keep them between the two, and the compiler schedules them freely
-// there.
-__device__ __forceinline__ void lds32(const void *p, uint32_t (&w)[8]) {
-    const uint4 a = static_cast<const uint4 *>(p)[0];
-    const uint4 b = static_cast<const uint4 *>(p)[1];
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+// 32 bytes of rank slice `r` of a stage (two 16-byte shared loads) for a
+// thread whose bytes start at shared address `lo` (first 16 bytes) and `hi`
+// (second 16), the slice offset an immediate: with the halves exchanged
+// (lo = start + 16, hi = start) w[0..3] holds bytes 16..31 and w[4..7] bytes
+// 0..15.  Lanes that read 32 contiguous bytes each touch every bank twice
+// per 16-byte access (lanes k and k+4 meet in the same banks); exchanging the
+// order in lanes with bit 2 set makes each 8-lane phase cover all 32 banks
+// once.  Two base registers and immediate offsets: R address registers kept
+// live across the loop would cost as many registers as a rank's data.
+template <int kOffset>
+__device__ __forceinline__ void lds32(uint32_t lo, uint32_t hi, uint32_t (&w)[8]) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(lo), "n"(kOffset)
+                 : "memory");
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "r"(hi), "n"(kOffset)
+                 : "memory");
+}
+
+// lds32 of rank slice r (0 <= r < 8) of a stage, the slice offset
+// r * kSlice as an immediate.
+template <uint32_t kSlice>
+__device__ __forceinline__ void lds_rank(uint32_t lo, uint32_t hi, int r, uint32_t (&w)[8]) {
+    switch (r) {
+        case 0: lds32<0 * kSlice>(lo, hi, w); break;
+        case 1: lds32<1 * kSlice>(lo, hi, w); break;
+        case 2: lds32<2 * kSlice>(lo, hi, w); break;
+        case 3: lds32<3 * kSlice>(lo, hi, w); break;
+        case 4: lds32<4 * kSlice>(lo, hi, w); break;
+        case 5: lds32<5 * kSlice>(lo, hi, w); break;
+        case 6: lds32<6 * kSlice>(lo, hi, w); break;
+        default: lds32<7 * kSlice>(lo, hi, w); break;
+    }
 }
 
 }  // namespace qrk
