@@ -249,7 +249,7 @@ def measured_hbm() -> tuple[float, str]:
 
 
 # The sources that determine the benchmarked kernel's code and launch shape.
-FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_pipeline.cuh", "qr_allreduce16.cuh",
+FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_pipeline.cuh", "qr_staged.cuh", "qr_allreduce16.cuh",
                    "qr_allreduce16_b3.cu", "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_grid.cu")
 
 
@@ -356,21 +356,7 @@ def run_sweep(args) -> None:
                     arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
                             ("encode", encode_all), ("reduce", reduce_only), ("decode", decode_only),
                             ("twoshot", twoshot))
-                    times = {name: [] for name, _ in arms}
-                    for _ in range(3):
-                        fused()
-                        unfused()
-                        twoshot()
-                    for _ in range(args.reps):
-                        for name, fn in arms:
-                            if do_flush:
-                                flush.fill_(1)
-                            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                            e0.record()
-                            fn()
-                            e1.record()
-                            e1.synchronize()
-                            times[name].append(e0.elapsed_time(e1))
+                    times = time_arms(arms, args, flush if do_flush else None, warm=(fused, fused_regs, unfused, twoshot))
                     same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
                         torch.equal(y.view(torch.int16), y2.view(torch.int16))) and all(
                         torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in ys2)
@@ -387,10 +373,39 @@ def run_sweep(args) -> None:
                             "input_gbs": round(Rs * n * 2 / (med / 1e3) / 1e9, 2),
                             "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
-                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps}), flush=True)
+                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps,
+                            "burst": 1 if do_flush else args.burst}), flush=True)
                     del wires, red, yu, ws, ys2
                 del xs, y
                 torch.cuda.empty_cache()
+
+
+def time_arms(arms, args, flush, warm=()):
+    """Per-arm CUDA-event times (ms per launch sequence), arms interleaved.
+    With `flush` (a buffer larger than L2) it is rewritten before every
+    timed sample and each sample is one launch sequence; without it each
+    sample is `args.burst` back-to-back sequences of the same arm (their mean),
+    which keeps a kernel's shared-memory configuration from being switched
+    by the other arms between launches."""
+    import torch
+
+    for _ in range(3):
+        for fn in warm:
+            fn()
+    times = {name: [] for name, _ in arms}
+    burst = 1 if flush is not None else max(1, args.burst)
+    for _ in range(args.reps):
+        for name, fn in arms:
+            if flush is not None:
+                flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(burst):
+                fn()
+            e1.record()
+            e1.synchronize()
+            times[name].append(e0.elapsed_time(e1) / burst)
+    return times
 
 
 def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
@@ -398,6 +413,7 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
     (the mixed "INT6") and (8,8), fused and unfused arms interleaved."""
     import torch
 
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for dtype in dtypes:
         tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
         for Rs in ranks:
@@ -405,17 +421,21 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                 xs = [x.view(tdt) for x in workloads.device_sweep(Rs, n, dtype, seed=SEED, device=dev)]
                 y = torch.empty(n, dtype=tdt, device=dev)
                 yu = torch.empty(n, dtype=tdt, device=dev)
+                y2 = torch.empty(n, dtype=tdt, device=dev)
                 for brs, bag in qr.FC_PAIRS:
                     Wi, Wo = qr.qr_fc_wire_bytes(brs, n), qr.qr_fc_wire_bytes(bag, n)
                     wires = [torch.empty(Wi, dtype=torch.uint8, device=dev) for _ in range(Rs)]
                     red = torch.empty(Wo, dtype=torch.uint8, device=dev)
                     fused_b = 2 * Rs * n + 2 * n
-                    kernel_b = {"fused": fused_b, "unfused": fused_b + 2 * Rs * Wi + 2 * Wo,
+                    kernel_b = {"fused": fused_b, "fused_regs": fused_b, "unfused": fused_b + 2 * Rs * Wi + 2 * Wo,
                                 "encode": Rs * (2 * n + Wi), "reduce": Rs * Wi + Wo, "decode": Wo + 2 * n}
                     do_flush = fused_b < (512 << 20)
 
                     def fused():
                         qr.qr_fc_allreduce(brs, bag, xs, y=y)
+
+                    def fused_regs():  # the register-fed fused kernel (four waves)
+                        qr.qr_fc_allreduce(brs, bag, xs, y=y2, ctas=4 * 4 * sms)
 
                     def encode_all():
                         for r in range(Rs):
@@ -432,23 +452,11 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                         reduce_only()
                         decode_only()
 
-                    arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all),
-                            ("reduce", reduce_only), ("decode", decode_only))
-                    times = {name: [] for name, _ in arms}
-                    for _ in range(3):
-                        fused()
-                        unfused()
-                    for _ in range(args.reps):
-                        for name, fn in arms:
-                            if do_flush:
-                                flush.fill_(1)
-                            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                            e0.record()
-                            fn()
-                            e1.record()
-                            e1.synchronize()
-                            times[name].append(e0.elapsed_time(e1))
-                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
+                    arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
+                            ("encode", encode_all), ("reduce", reduce_only), ("decode", decode_only))
+                    times = time_arms(arms, args, flush if do_flush else None, warm=(fused, fused_regs, unfused))
+                    same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
+                        torch.equal(y.view(torch.int16), y2.view(torch.int16)))
                     for name, alg in kernel_b.items():
                         med = statistics.median(times[name])
                         print(json.dumps({
@@ -457,9 +465,10 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                             "median_ms": round(med, 5), "input_gbs": round(Rs * n * 2 / (med / 1e3) / 1e9, 2),
                             "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
-                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps}), flush=True)
+                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps,
+                            "burst": 1 if do_flush else args.burst}), flush=True)
                     del wires, red
-                del xs, y, yu
+                del xs, y, yu, y2
                 torch.cuda.empty_cache()
 
 
@@ -480,6 +489,8 @@ def main() -> None:
                     help="run the message-size sweep (JSON line per point) instead of the benchmark")
     ap.add_argument("--sweep-sizes", default="", help="comma-separated values per rank for --sweep")
     ap.add_argument("--reps", type=int, default=100, help="launches per sweep point")
+    ap.add_argument("--burst", type=int, default=1,
+                    help="sweep: back-to-back launches of one arm per timed sample where L2 is not flushed")
     ap.add_argument("--sweep-R", default="2,4,8", help="rank counts for --sweep")
     ap.add_argument("--sweep-bits", default="8,6,4,3", help="code widths for --sweep")
     ap.add_argument("--sweep-dtypes", default="fp16,bf16", help="storage types for --sweep")
@@ -558,7 +569,7 @@ def main() -> None:
         d = [s.elapsed_time(e) for s, e in ev[b]]
         avg = sum(d) / len(d)
         alg = R * N * 2 + N * 2
-        kernels[b] = {"kernel": f"allreduce16_staged_kernel<{b},bf16,R={R},G=5,SG=1>", "launches": len(d),
+        kernels[b] = {"kernel": f"staged_allreduce_kernel<QrTile<{b},bf16>,R={R},G=5,SG=1,K=4>", "launches": len(d),
                       "avg_ms": avg,
                       "median_ms": statistics.median(d), "total_ms": sum(d),
                       "input_gbs": in_bytes_call / (avg / 1e3) / 1e9,

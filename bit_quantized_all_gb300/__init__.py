@@ -39,7 +39,7 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_fc_tile_bytes", "qr_fc_wire_bytes", "qr_fc_encode", "qr_fc_segment_reduce", "qr_fc_decode",
            "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot",
            "qr_allreduce_twoshot_static", "qr_wait_timeouts", "qr_selftest_bounded_wait",
-           "qr_allreduce_staged")
+           "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
                 "qr_allreduce_twoshot_static": (i32, [i32, i32, i32, vpp, sz, vpp, vp]),
                 "qr_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint)]),
                 "qr_allreduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
+                "qr_fc_allreduce_staged": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
+                "qr_fc_allreduce_ctas": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_selftest_bounded_wait": (i32, [vp]),
             }
             for name, (res, args) in sig.items():
@@ -184,6 +186,14 @@ class capi:
     @staticmethod
     def qr_fc_segment_reduce(bits_in, bits_out, R, wires, n, out, stream=None):
         return lib().qr_fc_segment_reduce(bits_in, bits_out, R, _ptr_array(wires), n, out, stream)
+
+    @staticmethod
+    def qr_fc_allreduce_ctas(bits_rs, bits_ag, dtype, R, xs, n, y, ctas, stream=None):
+        return lib().qr_fc_allreduce_ctas(bits_rs, bits_ag, dtype, R, _ptr_array(xs), n, y, ctas, stream)
+
+    @staticmethod
+    def qr_fc_allreduce_staged(bits_rs, bits_ag, dtype, R, xs, n, y, ctas, stream=None):
+        return lib().qr_fc_allreduce_staged(bits_rs, bits_ag, dtype, R, _ptr_array(xs), n, y, ctas, stream)
 
     @staticmethod
     def qr_fc_allreduce(bits_rs, bits_ag, dtype, R, xs, n, y, stream=None):
@@ -482,7 +492,8 @@ def qr_fc_segment_reduce(bits_in: int, bits_out: int, wires, n: int, out: torch.
     return out
 
 
-def qr_fc_allreduce(bits_rs: int, bits_ag: int, xs, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+def qr_fc_allreduce(bits_rs: int, bits_ag: int, xs, y: torch.Tensor | None = None, stream=None,
+                    ctas: int = 0) -> torch.Tensor:
     """The fused two-shot all-reduce with the asymmetric group-128 codec:
     reduce-scatter at bits_rs, all-gather at bits_ag ((4, 8) is "INT6")."""
     xs, dt, n = _check_inputs(xs)
@@ -492,6 +503,27 @@ def qr_fc_allreduce(bits_rs: int, bits_ag: int, xs, y: torch.Tensor | None = Non
     if y.dtype != xs[0].dtype or y.numel() != n:
         raise ValueError("y must match the inputs' dtype and size")
     dev = _same_device(xs + [y], "qr_fc_allreduce")
-    _check(capi.qr_fc_allreduce(bits_rs, bits_ag, dt, len(xs), [x.data_ptr() for x in xs], n, y.data_ptr(),
-                                _stream(dev, stream)), "qr_fc_allreduce")
+    ptrs = [x.data_ptr() for x in xs]
+    if ctas:
+        status = capi.qr_fc_allreduce_ctas(bits_rs, bits_ag, dt, len(xs), ptrs, n, y.data_ptr(), ctas,
+                                           _stream(dev, stream))
+    else:
+        status = capi.qr_fc_allreduce(bits_rs, bits_ag, dt, len(xs), ptrs, n, y.data_ptr(), _stream(dev, stream))
+    _check(status, "qr_fc_allreduce")
+    return y
+
+
+def qr_fc_allreduce_staged(bits_rs: int, bits_ag: int, xs, y: torch.Tensor | None = None, stream=None,
+                           ctas: int = 0) -> torch.Tensor:
+    """qr_fc_allreduce on the staged kernel (bulk copies into shared memory,
+    one persistent CTA per SM) at any size; every tensor 32-byte aligned."""
+    xs, dt, n = _check_inputs(xs)
+    if y is None:
+        y = torch.empty_like(xs[0])
+    _cuda_contig(y, "y")
+    if y.dtype != xs[0].dtype or y.numel() != n:
+        raise ValueError("y must match the inputs' dtype and size")
+    dev = _same_device(xs + [y], "qr_fc_allreduce_staged")
+    _check(capi.qr_fc_allreduce_staged(bits_rs, bits_ag, dt, len(xs), [x.data_ptr() for x in xs], n, y.data_ptr(),
+                                       ctas, _stream(dev, stream)), "qr_fc_allreduce_staged")
     return y

@@ -170,9 +170,11 @@ QR_EXPORT qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R, con
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
-QR_EXPORT qr_status_t qr_fc_allreduce(int bits_rs, int bits_ag, qr_dtype_t dtype, int R, const void *const *x,
-                                      size_t n, void *y, qr_stream_t stream) {
-    if (!x || !y || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+namespace {
+
+qr_status_t fc_allreduce_common(int bits_rs, int bits_ag, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                void *y, int ctas, bool staged, qr_stream_t stream) {
+    if (!x || !y || n == 0 || R < 1 || ctas < 0) return QR_ERR_INVALID_ARG;
     for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
         if (!x[r]) return QR_ERR_INVALID_ARG;
     if (!fc_pair_ok(bits_rs, bits_ag) || !dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
@@ -183,8 +185,33 @@ QR_EXPORT qr_status_t qr_fc_allreduce(int bits_rs, int bits_ag, qr_dtype_t dtype
         if (!aligned16(x[r])) return QR_ERR_MISALIGNED;
     for (int r = 0; r < R; ++r)
         if (bad_alias(y, V, x[r], V)) return QR_ERR_INVALID_ARG;
-    return from_cuda(qrk::launch_fc_allreduce(bits_rs, bits_ag, dtype, R, x, static_cast<long long>(n), y, 0,
+    if (staged) {
+        const auto a32 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+        if (!a32(y)) return QR_ERR_MISALIGNED;
+        for (int r = 0; r < R; ++r)
+            if (!a32(x[r])) return QR_ERR_MISALIGNED;
+        return from_cuda(qrk::launch_fc_allreduce_staged(bits_rs, bits_ag, dtype, R, x, static_cast<long long>(n), y,
+                                                         ctas, reinterpret_cast<cudaStream_t>(stream)));
+    }
+    return from_cuda(qrk::launch_fc_allreduce(bits_rs, bits_ag, dtype, R, x, static_cast<long long>(n), y, ctas,
                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+QR_EXPORT qr_status_t qr_fc_allreduce(int bits_rs, int bits_ag, qr_dtype_t dtype, int R, const void *const *x,
+                                      size_t n, void *y, qr_stream_t stream) {
+    return fc_allreduce_common(bits_rs, bits_ag, dtype, R, x, n, y, 0, false, stream);
+}
+
+QR_EXPORT qr_status_t qr_fc_allreduce_ctas(int bits_rs, int bits_ag, qr_dtype_t dtype, int R, const void *const *x,
+                                           size_t n, void *y, int ctas, qr_stream_t stream) {
+    return fc_allreduce_common(bits_rs, bits_ag, dtype, R, x, n, y, ctas, false, stream);
+}
+
+QR_EXPORT qr_status_t qr_fc_allreduce_staged(int bits_rs, int bits_ag, qr_dtype_t dtype, int R, const void *const *x,
+                                             size_t n, void *y, int ctas, qr_stream_t stream) {
+    return fc_allreduce_common(bits_rs, bits_ag, dtype, R, x, n, y, ctas, true, stream);
 }
 
 QR_EXPORT const char *qr_status_string(qr_status_t status) {

@@ -98,4 +98,12 @@ cudaError_t launch_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, cons
     return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_fc_allreduce_staged(int bits_rs, int bits_ag, int dtype, int R, const void *const *x, long long n,
+                                       void *y, int ctas, cudaStream_t s) {
+    if (bits_rs == 4 && bits_ag == 4) return run_fc_allreduce_staged<4, 4>(dtype, R, x, n, y, ctas, s);
+    if (bits_rs == 4 && bits_ag == 8) return run_fc_allreduce_staged<4, 8>(dtype, R, x, n, y, ctas, s);
+    if (bits_rs == 8 && bits_ag == 8) return run_fc_allreduce_staged<8, 8>(dtype, R, x, n, y, ctas, s);
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace qrk

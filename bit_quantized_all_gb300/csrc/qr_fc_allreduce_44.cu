@@ -4,4 +4,6 @@
 
 namespace qrk {
 template cudaError_t run_fc_allreduce<4, 4>(int, int, const void *const *, long long, void *, int, cudaStream_t);
+template cudaError_t run_fc_allreduce_staged<4, 4>(int, int, const void *const *, long long, void *, int,
+                                                              cudaStream_t);
 }  // namespace qrk

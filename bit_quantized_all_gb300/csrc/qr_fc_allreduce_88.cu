@@ -4,4 +4,6 @@
 
 namespace qrk {
 template cudaError_t run_fc_allreduce<8, 8>(int, int, const void *const *, long long, void *, int, cudaStream_t);
+template cudaError_t run_fc_allreduce_staged<8, 8>(int, int, const void *const *, long long, void *, int,
+                                                              cudaStream_t);
 }  // namespace qrk

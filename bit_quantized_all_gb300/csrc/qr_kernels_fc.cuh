@@ -225,6 +225,61 @@ __global__ void __launch_bounds__(kThreadsFc, 4) fc_allreduce_kernel(ConstPtrs x
     }
 }
 
+// The per-tile steps of fc_allreduce_kernel as a policy for the staged kernel
+// (staged_allreduce_kernel in qr_staged.cuh).  Every step before the store
+// is per value or over a whole group of 128, so a thread may hold its two
+// 8-value halves exchanged; values past n only occur in the ragged tile.
+template <int BRS, int BAG, int DT>
+struct FcTile {
+    static __device__ __forceinline__ void accumulate(const uint32_t (&w)[8], float2 (&acc)[8], bool first) {
+        float2 v[8], f[8], d[8];
+        widen16<DT>(w, v);
+        float lo, hi;
+        group_minmax(v, lo, hi);
+        const FcParams p = fc_params<BRS>(lo, hi);
+        fc_quantize16<BRS>(v, p, f);
+        fc_dequant16(f, p, d);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = first ? d[k] : __fadd2_rn(acc[k], d[k]);
+    }
+    static __device__ __forceinline__ void finish(const float2 (&acc)[8], uint16_t *y, long long base, long long,
+                                                  bool swapped) {
+        float lo, hi;
+        group_minmax(acc, lo, hi);
+        const FcParams p = fc_params<BAG>(lo, hi);
+        float2 f[8], o[8];
+        fc_quantize16<BAG>(acc, p, f);
+        fc_dequant16(f, p, o);
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = narrow2<DT>(o[k].x, o[k].y);
+        if (swapped)
+            st_global32_swapped(y + base, w);
+        else
+            st_global32(y + base, w);
+    }
+    // The last, partial tile with bounds-checked loads (not inlined, so that
+    // it does not set the register budget of the staged kernel's main loop).
+    template <int R>
+    static __device__ __noinline__ void ragged(const ConstPtrs &x, long long n, uint16_t *y, long long base) {
+        float2 acc[8];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            uint32_t w[8];
+            load16v<true>(static_cast<const uint16_t *>(x.p[r]), base, n, w);
+            accumulate(w, acc, r == 0);
+        }
+        if (base + 16 > n) zero_past_n(acc, base, n);
+        float lo, hi;
+        group_minmax(acc, lo, hi);
+        const FcParams p = fc_params<BAG>(lo, hi);
+        float2 f[8], o[8];
+        fc_quantize16<BAG>(acc, p, f);
+        fc_dequant16(f, p, o);
+        store16v<DT, true>(y, base, n, o);
+    }
+};
+
 // Send path: quantize into a BITS-wide Flash Communication wire.
 template <int B, int DT, bool A32>
 __global__ void __launch_bounds__(kThreadsFc) fc_encode_kernel(const uint16_t *__restrict__ x, long long n,

@@ -66,5 +66,12 @@ cudaError_t launch_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, cons
                                 void *y, int ctas, cudaStream_t s);
 template <int BRS, int BAG>
 cudaError_t run_fc_allreduce(int dtype, int R, const void *const *x, long long n, void *y, int ctas, cudaStream_t s);
+// The staged kernel with the Flash Communication codec at any size (every
+// pointer 32-byte aligned).
+cudaError_t launch_fc_allreduce_staged(int bits_rs, int bits_ag, int dtype, int R, const void *const *x, long long n,
+                                       void *y, int ctas, cudaStream_t s);
+template <int BRS, int BAG>
+cudaError_t run_fc_allreduce_staged(int dtype, int R, const void *const *x, long long n, void *y, int ctas,
+                                    cudaStream_t s);
 
 }  // namespace qrk

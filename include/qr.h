@@ -283,10 +283,27 @@ qr_status_t qr_fc_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n,
 
 /* The fused two-shot all-reduce with this codec: reduce-scatter wires at
  * bits_rs, all-gather at bits_ag -- (4,4) INT4, (8,8) INT8, (4,8) the mixed
- * "INT6".  y may equal one of the x[r] exactly (in-place). */
+ * "INT6".  y may equal one of the x[r] exactly (in-place).  Kernel choice as
+ * for qr_allreduce (the staged kernel for R >= 4 and at least 48 full tiles
+ * per SM, R = 3: 128, with every pointer 32-byte aligned). */
 qr_status_t qr_fc_allreduce(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
                             const void *const *x, size_t n, void *y,
                             qr_stream_t stream);
+
+/* qr_fc_allreduce with an explicit grid size, as qr_allreduce_ctas: `ctas` >
+ * 0 runs the grid-stride (register-fed) kernel with `ctas` CTAs; 0 = the
+ * library's choice.  The result does not depend on it. */
+qr_status_t qr_fc_allreduce_ctas(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
+                                 const void *const *x, size_t n, void *y,
+                                 int ctas, qr_stream_t stream);
+
+/* qr_fc_allreduce on the staged kernel at any size, as qr_allreduce_staged:
+ * `ctas` = 0 for one CTA per SM, else min(ctas, #SMs); every x[r] and y
+ * 32-byte aligned (QR_ERR_MISALIGNED otherwise); ctas < 0 is
+ * QR_ERR_INVALID_ARG. */
+qr_status_t qr_fc_allreduce_staged(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
+                                   const void *const *x, size_t n, void *y,
+                                   int ctas, qr_stream_t stream);
 
 /* A static string naming a status code (never NULL). */
 const char *qr_status_string(qr_status_t status);

@@ -146,6 +146,10 @@ def test_allreduce_validation():
     assert capi.qr_allreduce_staged(3, 0, 2, xs, n, Y + 16, 0) == qr.QR_ERR_MISALIGNED
     assert capi.qr_allreduce_staged(3, 0, 2, xs, n, A + 32, 0) == qr.QR_ERR_INVALID_ARG
     assert capi.qr_allreduce_staged(3, 0, 2, xs, 2**63, Y, 0) == qr.QR_ERR_SIZE
+    assert capi.qr_fc_allreduce_staged(4, 8, 0, 2, xs, n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_allreduce_ctas(4, 8, 0, 2, xs, n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_allreduce_staged(4, 4, 0, 2, [A, B + 16], n, Y, 0) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_fc_allreduce_staged(3, 8, 0, 2, xs, n, Y, 0) == qr.QR_ERR_UNSUPPORTED
     # the timeout counter's reader rejects a null destination without touching the device
     assert qr.lib().qr_wait_timeouts(None) == qr.QR_ERR_INVALID_ARG
     # emit: every output disjoint from every other buffer

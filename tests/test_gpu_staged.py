@@ -134,8 +134,59 @@ def test_misaligned_for_the_staged_kernel():
     xs = [b[8:8 + n] for b in bufs]  # 16 bytes past a 512-byte boundary
     with pytest.raises(qr.QRError):
         qr.qr_allreduce_staged(4, xs)
+    with pytest.raises(qr.QRError):
+        qr.qr_fc_allreduce_staged(4, 8, xs)
     y = qr.qr_allreduce(4, xs)
     assert y.numel() == n
+
+
+FC_PAIRS = [(4, 4), (4, 8), (8, 8)]
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_flash_communication_codec_against_the_oracle(R):
+    """The staged kernel with the asymmetric group-128 codec: three CTAs over
+    100 full tiles and a ragged tail, every width pair, both types."""
+    n = 100 * 2048 + 777
+    for dtype in (0, 1):
+        xs = _ranks(R, n, dtype, 700 + 10 * R + dtype)
+        xs_dev = [to_dev(x, dtype) for x in xs]
+        xmax = xmax_of(xs, dtype)
+        for brs, bag in FC_PAIRS:
+            y = qr.qr_fc_allreduce_staged(brs, bag, xs_dev, ctas=3)
+            y_ref = oracle.fc_allreduce(brs, bag, dtype, xs)
+            assert_outputs_match(to_host_u16(y), y_ref, dtype, xmax, f"fc staged R={R} ({brs},{bag}) dt={dtype}")
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 2048 * 7 + 129])
+def test_flash_communication_short_messages(n):
+    R = 8
+    xs = _ranks(R, n, 1, 13 * n)
+    for brs, bag in FC_PAIRS:
+        y = qr.qr_fc_allreduce_staged(brs, bag, [to_dev(x, 1) for x in xs])
+        assert_outputs_match(to_host_u16(y), oracle.fc_allreduce(brs, bag, 1, xs), 1, xmax_of(xs, 1),
+                             f"fc n={n} ({brs},{bag})")
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("R", [3, 8])
+@pytest.mark.parametrize("tiles_per_sm", [3, 60])
+def test_flash_communication_equals_the_register_kernel(R, tiles_per_sm):
+    """The staged kernel, the register-fed kernel (ctas > 0) and the
+    library's choice give the same bytes (below and above the threshold,
+    several tiles per group, a tail)."""
+    n = (tiles_per_sm * 152 + 11) * 2048 + 5
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(R)
+    xs = [(torch.randn(n, device="cuda", generator=gen) * (r + 1)).to(torch.bfloat16) for r in range(R)]
+    for brs, bag in FC_PAIRS:
+        y_regs = qr.qr_fc_allreduce(brs, bag, xs, ctas=1000)
+        y_st = qr.qr_fc_allreduce_staged(brs, bag, xs)
+        y_default = qr.qr_fc_allreduce(brs, bag, xs)
+        assert torch.equal(y_st.view(torch.int16), y_regs.view(torch.int16)), (brs, bag)
+        assert torch.equal(y_default.view(torch.int16), y_regs.view(torch.int16)), (brs, bag)
+    assert qr.qr_wait_timeouts() == 0
 
 
 def test_bounded_wait_runs_out_and_is_reported():
