@@ -153,12 +153,35 @@ __device__ __forceinline__ void store_slot(uint16_t *y, long long base, long lon
 // Dequantization Paths: absmax -> fp16 scale -> scale, clip, round, bias]
 // ---------------------------------------------------------------------------
 
+// three-input minimum / maximum (sm_100+): one instruction for what two
+// two-input ones do; exact, so the order of the operands does not matter.
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// max |v[i]| over N values with three-input maxima.
+template <int N>
+__device__ __forceinline__ float absmax_n(const float *v) {
+    static_assert(N >= 3, "at least three values");
+    float a = fmax3(fabsf(v[0]), fabsf(v[1]), fabsf(v[2]));
+    int i = 3;
+#pragma unroll
+    for (; i + 1 < N; i += 2) a = fmax3(a, fabsf(v[i]), fabsf(v[i + 1]));
+    if (i < N) a = fmaxf(a, fabsf(v[i]));
+    return a;
+}
+
 // Absolute maximum of the 32 values of this thread's block (4 lanes x 8).
 // Every lane of the warp must call it (full-mask shuffles).
 __device__ __forceinline__ float quad_absmax(const float (&v)[8]) {
-    float a = fabsf(v[0]);
-#pragma unroll
-    for (int j = 1; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+    float a = absmax_n<8>(v);
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
     return a;
@@ -422,9 +445,7 @@ __device__ __forceinline__ void widen16(const uint32_t (&w)[8], float2 (&v)[8]) 
 
 // Absolute maximum of this thread's 16 values and its partner lane's.
 __device__ __forceinline__ float pair_absmax(const float2 (&v)[8]) {
-    float a = fmaxf(fabsf(v[0].x), fabsf(v[0].y));
-#pragma unroll
-    for (int i = 1; i < 8; ++i) a = fmaxf(a, fmaxf(fabsf(v[i].x), fabsf(v[i].y)));
+    const float a = absmax_n<16>(reinterpret_cast<const float *>(v));
     return fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
 }
 

@@ -58,10 +58,7 @@ __device__ __forceinline__ void widen_block(const uint32_t (&w)[16], float2 (&v)
 }
 
 __device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
-    float a = fmaxf(fabsf(v[0].x), fabsf(v[0].y));
-#pragma unroll
-    for (int i = 1; i < 16; ++i) a = fmaxf(a, fmaxf(fabsf(v[i].x), fabsf(v[i].y)));
-    return a;
+    return absmax_n<32>(reinterpret_cast<const float *>(v));
 }
 
 // f = clip(RN(v*r), qmin, qmax) + 1.5*2^23 + bias (the code in the low byte),

@@ -36,18 +36,6 @@ struct FcParams {
     float s, r, z;
 };
 
-// three-input minimum / maximum (sm_100+)
-__device__ __forceinline__ float fmin3(float a, float b, float c) {
-    float d;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 // Group minimum and maximum across the 8 lanes of a group (every lane of the
 // warp must call it).
 __device__ __forceinline__ void group_minmax(const float2 (&v)[8], float &lo, float &hi) {
