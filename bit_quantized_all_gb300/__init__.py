@@ -39,7 +39,8 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_fc_tile_bytes", "qr_fc_wire_bytes", "qr_fc_encode", "qr_fc_segment_reduce", "qr_fc_decode",
            "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot",
            "qr_allreduce_twoshot_static", "qr_wait_timeouts", "qr_selftest_bounded_wait",
-           "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas")
+           "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas",
+           "qr_segment_reduce_staged")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
                 "qr_allreduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_fc_allreduce_staged": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_fc_allreduce_ctas": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
+                "qr_segment_reduce_staged": (i32, [i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_selftest_bounded_wait": (i32, [vp]),
             }
             for name, (res, args) in sig.items():
@@ -137,6 +139,10 @@ class capi:
     @staticmethod
     def qr_segment_reduce(bits, R, wires, n, out, stream=None):
         return lib().qr_segment_reduce(bits, R, _ptr_array(wires), n, out, stream)
+
+    @staticmethod
+    def qr_segment_reduce_staged(bits, R, wires, n, out, ctas, stream=None):
+        return lib().qr_segment_reduce_staged(bits, R, _ptr_array(wires), n, out, ctas, stream)
 
     @staticmethod
     def qr_allreduce(bits, dtype, R, xs, n, y, stream=None):
@@ -295,8 +301,10 @@ def qr_decode(bits: int, wire: torch.Tensor, n: int, dtype: torch.dtype = torch.
     return y
 
 
-def qr_segment_reduce(bits: int, wires, n: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Phase-1B: decode the R wires, sum in fp32 in rank order, re-quantize."""
+def qr_segment_reduce(bits: int, wires, n: int, out: torch.Tensor | None = None, stream=None,
+                      staged: bool = False, ctas: int = 0) -> torch.Tensor:
+    """Phase-1B: decode the R wires, sum in fp32 in rank order, re-quantize.
+    `staged` runs the staged kernel (qr_segment_reduce_staged) at any size."""
     wires = list(wires)
     if not 1 <= len(wires) <= QR_MAX_RANKS:
         raise ValueError(f"1 to {QR_MAX_RANKS} wires are supported, got {len(wires)}")
@@ -306,8 +314,12 @@ def qr_segment_reduce(bits: int, wires, n: int, out: torch.Tensor | None = None,
         out = new_wire(bits, n, wires[0].device)
     _wire_tensor(out, bits, n, "out")
     dev = _same_device(wires + [out], "qr_segment_reduce")
-    _check(capi.qr_segment_reduce(bits, len(wires), [w.data_ptr() for w in wires], n, out.data_ptr(),
-                                  _stream(dev, stream)), "qr_segment_reduce")
+    ptrs = [w.data_ptr() for w in wires]
+    if staged:
+        status = capi.qr_segment_reduce_staged(bits, len(wires), ptrs, n, out.data_ptr(), ctas, _stream(dev, stream))
+    else:
+        status = capi.qr_segment_reduce(bits, len(wires), ptrs, n, out.data_ptr(), _stream(dev, stream))
+    _check(status, "qr_segment_reduce")
     return out
 
 

@@ -250,9 +250,11 @@ QR_EXPORT qr_status_t qr_decode(int bits, qr_dtype_t dtype, const void *wire, si
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
-QR_EXPORT qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires, size_t n,
-                                        void *out_wire, qr_stream_t stream) {
-    if (!wires || !out_wire || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+namespace {
+
+qr_status_t segment_reduce_common(int bits, int R, const void *const *wires, size_t n, void *out_wire, int ctas,
+                                  bool staged, qr_stream_t stream) {
+    if (!wires || !out_wire || n == 0 || R < 1 || ctas < 0) return QR_ERR_INVALID_ARG;
     for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
         if (!wires[r]) return QR_ERR_INVALID_ARG;
     if (!bits_ok(bits) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
@@ -263,8 +265,23 @@ QR_EXPORT qr_status_t qr_segment_reduce(int bits, int R, const void *const *wire
         if (!aligned16(wires[r])) return QR_ERR_MISALIGNED;
     for (int r = 0; r < R; ++r)
         if (bad_alias(out_wire, W, wires[r], W)) return QR_ERR_INVALID_ARG;
+    if (staged)
+        return from_cuda(qrk::launch_reduce_staged(bits, R, wires, static_cast<long long>(n), out_wire, ctas,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(qrk::launch_reduce(bits, R, wires, static_cast<long long>(n), out_wire,
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+QR_EXPORT qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires, size_t n,
+                                        void *out_wire, qr_stream_t stream) {
+    return segment_reduce_common(bits, R, wires, n, out_wire, 0, false, stream);
+}
+
+QR_EXPORT qr_status_t qr_segment_reduce_staged(int bits, int R, const void *const *wires, size_t n,
+                                               void *out_wire, int ctas, qr_stream_t stream) {
+    return segment_reduce_common(bits, R, wires, n, out_wire, ctas, true, stream);
 }
 
 namespace {

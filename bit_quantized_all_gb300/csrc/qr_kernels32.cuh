@@ -11,6 +11,7 @@
 #pragma once
 
 #include "qr_device.cuh"
+#include "qr_pipeline.cuh"
 
 namespace qrk {
 
@@ -542,6 +543,32 @@ __global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, u
 // more warps to hide their latency): decode the R rank copies of the block,
 // add them in fp32 in rank order (fma(q, s, acc) = RN(acc + q*s): q*s is
 // exact), re-quantize.
+// Phase-1B of one 32-value block from its R ranks' codes c[r] and fp16 scale
+// bits sb[r]: decode, add in fp32 in rank order (fma(q, s, acc) =
+// RN(acc + q*s): q*s is exact), re-quantize, and write the block's codes
+// and scale into `tile` (block g).
+template <int B, int R>
+__device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
+                                             int g) {
+    float2 acc[16];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float s = f16_bits_to_float(sb[r]);
+        const float2 s2 = make_float2(s, s);
+        float2 q[16];
+        unpack_block_q<B>(c[r], q);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
+    }
+    const BlockScale2 sc = block_scale2<B>(block_absmax(acc));
+    float2 f[16];
+    quantize_block_magic<B>(acc, sc.r, sc.low_clip, f);
+    BlockWords<B> cw;
+    pack_block<B>(f, cw);
+    store_block_codes<B>(tile, g, cw);
+    store_block_scale<B>(tile, g, sc.bits);
+}
+
 template <int B, int R, int U>
 __device__ __forceinline__ void reduce32_run(ConstPtrs wires, uint8_t *out, long long NB) {
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
@@ -564,26 +591,8 @@ __device__ __forceinline__ void reduce32_run(ConstPtrs wires, uint8_t *out, long
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const long long gb = gb0 + u * S;
-            if (gb < NB) {
-                float2 acc[16];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float s = f16_bits_to_float(sb[u][r]);
-                    const float2 s2 = make_float2(s, s);
-                    float2 q[16];
-                    unpack_block_q<B>(c[u][r], q);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
-                }
-                const BlockScale2 sc = block_scale2<B>(block_absmax(acc));
-                float2 f[16];
-                quantize_block_magic<B>(acc, sc.r, sc.low_clip, f);
-                BlockWords<B> cw;
-                pack_block<B>(f, cw);
-                uint8_t *tile = out + (gb >> 6) * Codec<B>::kTileBytes;
-                store_block_codes<B>(tile, static_cast<int>(gb & 63), cw);
-                store_block_scale<B>(tile, static_cast<int>(gb & 63), sc.bits);
-            }
+            if (gb < NB)
+                reduce_block<B, R>(c[u], sb[u], out + (gb >> 6) * Codec<B>::kTileBytes, static_cast<int>(gb & 63));
         }
     }
 }
@@ -601,5 +610,94 @@ template <int B, int R>
 __host__ __device__ constexpr bool reduce_two_threads_per_block() { return (B == 4 || B == 6) && R >= 6; }
 template <int R>
 __host__ __device__ constexpr int reduce_units_per_thread() { return (R <= 2) ? 2 : 1; }
+
+// Phase-1B with the R ranks' wire tiles staged through shared memory by the
+// bulk-copy engine (the same pipeline as the staged fused kernel in
+// qr_staged.cuh): persistent, one CTA per SM of G groups of 64 threads, one
+// tile per group at a time and one 32-value block per thread.  Each group
+// owns a ring of SG stages of R * tile-bytes; its leader fills stage j % SG
+// with the group's tile j (R bulk copies counted on the stage's mbarrier).
+// The group copies its blocks' codes and scales into registers, meets at a
+// named barrier that also ANDs "my wait completed", the leader refills the
+// stage with tile j + SG, and the group reduces and writes the block while
+// that copy is in flight.  A wire is whole tiles, so there is no ragged
+// tile.  Every wait gives up after one second (the group then counts one
+// timeout, its leader waits, bounded again, for its copies, and it returns).
+template <int B, int R, int G, int SG>
+__global__ void __launch_bounds__(64 * G, 1) staged_reduce_kernel(ConstPtrs wires, uint8_t *out, long long T,
+                                                                  unsigned *timeouts) {
+    static_assert(G >= 1 && G <= 15 && SG >= 1, "named barriers 1..G, at least one stage per group");
+    constexpr uint32_t kTile = Codec<B>::kTileBytes;
+    constexpr uint32_t kStageBytes = R * kTile;
+    extern __shared__ __align__(128) uint8_t ring[];  // G * SG * R * kTile bytes
+    __shared__ __align__(8) uint64_t full[G * SG];
+    __shared__ const uint8_t *src[R];
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G * SG; ++s) mbar_init(&full[s], 1);
+        for (int r = 0; r < R; ++r) src[r] = static_cast<const uint8_t *>(wires.p[r]);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    const int g = threadIdx.x / 64, k = threadIdx.x & 63;
+    const bool leader = k == 0;
+    const long long first = blockIdx.x + static_cast<long long>(gridDim.x) * g;
+    const long long stride = static_cast<long long>(gridDim.x) * G;
+    const int tiles = T > first ? static_cast<int>((T - first + stride - 1) / stride) : 0;
+    uint8_t *my_ring = ring + static_cast<size_t>(g) * SG * kStageBytes;
+    uint64_t *my_full = full + g * SG;
+
+    auto issue = [&](int j) {  // leader only: stage j % SG <- tile j of every rank
+        const int s = j % SG;
+        const long long off = (first + j * stride) * kTile;
+        uint8_t *dst = my_ring + static_cast<size_t>(s) * kStageBytes;
+        mbar_arrive_expect_tx(&my_full[s], kStageBytes);
+#pragma unroll
+        for (int r = 0; r < R; ++r) bulk_copy_g2s(dst + r * kTile, src[r] + off, kTile, &my_full[s]);
+    };
+
+    int issued = 0;
+    if (leader)
+        for (; issued < tiles && issued < SG; ++issued) issue(issued);
+
+    int j = 0;
+    for (; j < tiles; ++j) {
+        const int s = j % SG;
+        const bool ok = mbar_wait(&my_full[s], static_cast<uint32_t>((j / SG) & 1));
+        const uint8_t *stage = my_ring + static_cast<size_t>(s) * kStageBytes;
+        BlockWords<B> c[R];
+        uint32_t sb[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            load_block_codes<B>(stage + r * kTile, k, c[r]);
+            sb[r] = load_block_scale_bits<B>(stage + r * kTile, k);
+        }
+        if (!group_all<64>(1 + g, ok)) break;  // also: every thread is done reading stage s
+        if (leader && issued < tiles) issue(issued++);
+        reduce_block<B, R>(c, sb, out + (first + j * stride) * kTile, k);
+    }
+    if (j < tiles && leader) {  // a wait ran out
+        atomicAdd(timeouts, 1u);
+        for (int i = j; i < issued; ++i)
+            if (!mbar_wait(&my_full[i % SG], static_cast<uint32_t>((i / SG) & 1))) break;
+    }
+}
+
+// Launch shape of the staged Phase-1B kernel: eight groups of 64 threads,
+// each with as many stages (at most 4) as fit in 200 KiB of shared memory at
+// R * tile-bytes per stage.  Measured on GB300 at 2^27 bf16 values per rank
+// against the register-fed kernels (fraction of the measured HBM bandwidth,
+// 4 / 8 / 12 groups): INT8 R=8 0.96 -> 0.93 / 1.00 / 0.83, R=2 0.76 -> 0.69 /
+// 0.92 / 0.89; INT6 R=8 0.64 -> 0.63 / 0.76 / 0.72; INT4 R=8 0.60 -> 0.54 /
+// 0.67 / 0.69; INT3 R=8 0.34 -> 0.29 / 0.34 / 0.34 (bound by the integer
+// pipe, not by memory: it stays on reduce32_kernel).
+template <int B, int R>
+struct StagedReduceShape {
+    static constexpr int kGroups = 8;
+    static constexpr int kFit = (200 * 1024) / (kGroups * R * Codec<B>::kTileBytes);
+    static constexpr int kStages = kFit >= 4 ? 4 : (kFit < 1 ? 1 : kFit);
+    static constexpr int kSmemBytes = kGroups * kStages * R * Codec<B>::kTileBytes;
+};
 
 }  // namespace qrk

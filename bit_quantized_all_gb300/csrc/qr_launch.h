@@ -29,6 +29,10 @@ cudaError_t launch_decode(int bits, int dtype, const void *wire, long long n, vo
                           cudaStream_t s);
 cudaError_t launch_reduce(int bits, int R, const void *const *wires, long long n, void *out,
                           cudaStream_t s);
+// Phase-1B on the staged kernel (bulk copies of the R wire tiles into shared
+// memory; min(ctas or #SMs, #SMs, tiles) persistent CTAs).
+cudaError_t launch_reduce_staged(int bits, int R, const void *const *wires, long long n, void *out, int ctas,
+                                 cudaStream_t s);
 cudaError_t launch_allreduce(int bits, int dtype, int R, const void *const *x, long long n,
                              void *y, void *const *wire_out, void *red_out, int ctas,
                              cudaStream_t s);

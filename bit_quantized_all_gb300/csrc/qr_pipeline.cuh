@@ -74,17 +74,20 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
-// Named barrier `id` over the 128 threads of one group, returning whether
-// `pred` holds in all of them.  Every thread of the group must arrive.
+// Named barrier `id` over the kThreads threads of one group (a multiple of
+// 32), returning whether `pred` holds in all of them.  Every thread of the
+// group must arrive.
+template <int kThreads>
 __device__ __forceinline__ bool group_all(int id, bool pred) {
+    static_assert(kThreads % 32 == 0, "whole warps");
     uint32_t out;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, 128, p;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(out)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "n"(kThreads)
         : "memory");
     return out != 0;
 }

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(128 * G, 1) staged_allreduce_kernel(ConstPtrs 
         uint32_t rest[R - K][8];
 #pragma unroll
         for (int r = K; r < R; ++r) lds_rank<kSlice>(half_a + at, half_b + at, r, rest[r - K]);
-        if (!group_all(1 + g, ok)) break;  // also: every thread is done reading stage s
+        if (!group_all<128>(1 + g, ok)) break;  // also: every thread is done reading stage s
         if (leader && issued < tiles) issue(issued++);
 #pragma unroll
         for (int r = K; r < R; ++r) Tile::accumulate(rest[r - K], acc, r == 0);

@@ -189,6 +189,54 @@ def test_flash_communication_equals_the_register_kernel(R, tiles_per_sm):
     assert qr.qr_wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+def test_staged_reduce_against_the_oracle(R):
+    """Phase-1B on the staged kernel: three CTAs (24 groups) over 100 tiles
+    (a ragged message, so the last tile is zero-padded on the wire), every
+    width: the reduced wire equals the oracle's byte for byte."""
+    n = 100 * 2048 + 777
+    xs = _ranks(R, n, 1, 500 + R)
+    for bits in BITS:
+        w_ref = [oracle.encode(bits, 1, x) for x in xs]
+        wires = [torch.from_numpy(w).cuda() for w in w_ref]
+        red = qr.qr_segment_reduce(bits, wires, n, staged=True, ctas=3)
+        assert np.array_equal(red.cpu().numpy(), oracle.segment_reduce(bits, w_ref, n)), (bits, R)
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("n", [1, 2048, 2049, 2048 * 9])
+def test_staged_reduce_short_messages(n):
+    R = 4
+    xs = _ranks(R, n, 0, 71 * n)
+    for bits in BITS:
+        w_ref = [oracle.encode(bits, 0, x) for x in xs]
+        wires = [torch.from_numpy(w).cuda() for w in w_ref]
+        red = qr.qr_segment_reduce(bits, wires, n, staged=True)
+        assert np.array_equal(red.cpu().numpy(), oracle.segment_reduce(bits, w_ref, n)), (bits, n)
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("R", [2, 8])
+def test_staged_reduce_equals_the_register_kernels_and_in_place(R):
+    """Above the threshold (the default takes the staged kernel for INT4/6/8)
+    and below it: default == staged == staged with a small grid; in place."""
+    for tiles_per_sm in (3, 50):
+        n = (tiles_per_sm * 152 + 7) * 2048 + 100
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(tiles_per_sm + R)
+        xs = [(torch.randn(n, device="cuda", generator=gen) * (r + 1)).to(torch.bfloat16) for r in range(R)]
+        for bits in BITS:
+            wires = [qr.qr_encode(bits, x) for x in xs]
+            red0 = qr.qr_segment_reduce(bits, wires, n)
+            red1 = qr.qr_segment_reduce(bits, wires, n, staged=True)
+            red2 = qr.qr_segment_reduce(bits, wires, n, staged=True, ctas=7)
+            assert torch.equal(red0, red1) and torch.equal(red0, red2), (bits, R, tiles_per_sm)
+            w2 = [w.clone() for w in wires]
+            qr.qr_segment_reduce(bits, w2, n, out=w2[0], staged=True)  # in place over rank 0's wire
+            assert torch.equal(w2[0], red0)
+    assert qr.qr_wait_timeouts() == 0
+
+
 def test_bounded_wait_runs_out_and_is_reported():
     """A wait on a barrier nothing completes gives up after one second,
     counts once, and leaves the context usable."""
