@@ -211,15 +211,55 @@ __device__ __forceinline__ void unpack_slot_q2(const SlotCodes c, float2 (&q)[4]
     q[3] = __fadd2_rn(make_float2(byte_as_magic<3>(even), byte_as_magic<3>(odd)), nm);
 }
 
+// The 16 signed INT3 codes of two consecutive slots as exact floats,
+// pairwise (q[4i + m] = lanes 2m, 2m+1 of slot i).  W: the two slots' q2w
+// (slot 0 in bits 0..15); X: their q1w (slot 0 in bits 0..7, slot 1 in
+// 8..15; bits above 15 are ignored).  The q1 bits are spread to every fourth
+// bit (three shift-and-mask steps) and merged with the q2 fields into
+// 3-bit codes in nibbles, even lanes in one word and odd lanes in another;
+// each code's byte then goes into a magic float by one byte permute (which
+// can take any byte, so the codes need no further ordering).  18 integer
+// operations per 16 values where spreading each slot's fields apart takes
+// about twice as many.
+__device__ __forceinline__ void unpack_pair_q3(uint32_t W, uint32_t X, float2 (&q)[8]) {
+    uint32_t x = (X & 0xFFu) | ((X << 8) & 0x00FF0000u);  // slot i's q1 byte at bits 16i
+    x = (x | (x << 4)) & 0x0F0F0F0Fu;
+    x = (x | (x << 2)) & 0x33333333u;  // lane j = 4a+2b+c of slot i at bit 16i + 8a + 4b + c
+    const uint32_t e = (W & 0x33333333u) | ((x << 2) & 0x44444444u);           // nibble 4i+m: lane 2m
+    const uint32_t o = ((W >> 2) & 0x33333333u) | ((x << 1) & 0x44444444u);    // nibble 4i+m: lane 2m+1
+    const uint32_t el = e & 0x0F0F0F0Fu, eh = (e >> 4) & 0x0F0F0F0Fu;          // byte t: nibble 2t / 2t+1
+    const uint32_t ol = o & 0x0F0F0F0Fu, oh = (o >> 4) & 0x0F0F0F0Fu;
+    const float2 nm = make_float2(-Codec<3>::kMagic, -Codec<3>::kMagic);
+    q[0] = __fadd2_rn(make_float2(byte_as_magic<0>(el), byte_as_magic<0>(ol)), nm);  // slot 0 lanes 0, 1
+    q[1] = __fadd2_rn(make_float2(byte_as_magic<0>(eh), byte_as_magic<0>(oh)), nm);  // lanes 2, 3
+    q[2] = __fadd2_rn(make_float2(byte_as_magic<1>(el), byte_as_magic<1>(ol)), nm);  // lanes 4, 5
+    q[3] = __fadd2_rn(make_float2(byte_as_magic<1>(eh), byte_as_magic<1>(oh)), nm);  // lanes 6, 7
+    q[4] = __fadd2_rn(make_float2(byte_as_magic<2>(el), byte_as_magic<2>(ol)), nm);  // slot 1
+    q[5] = __fadd2_rn(make_float2(byte_as_magic<2>(eh), byte_as_magic<2>(oh)), nm);
+    q[6] = __fadd2_rn(make_float2(byte_as_magic<3>(el), byte_as_magic<3>(ol)), nm);
+    q[7] = __fadd2_rn(make_float2(byte_as_magic<3>(eh), byte_as_magic<3>(oh)), nm);
+}
+
 // The 32 signed codes of a block as exact floats, pairwise.
 template <int B>
 __device__ __forceinline__ void unpack_block_q(const BlockWords<B> &c, float2 (&q)[16]) {
+    if constexpr (B == 3) {
+        float2 lo[8], hi[8];
+        unpack_pair_q3(c.w[0], c.w[2], lo);        // slots 0, 1
+        unpack_pair_q3(c.w[1], c.w[2] >> 16, hi);  // slots 2, 3
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        float2 qs[4];
-        unpack_slot_q2<B>(slot_codes<B>(c, s), qs);
+        for (int i = 0; i < 8; ++i) {
+            q[i] = lo[i];
+            q[8 + i] = hi[i];
+        }
+    } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q[4 * s + i] = qs[i];
+        for (int s = 0; s < 4; ++s) {
+            float2 qs[4];
+            unpack_slot_q2<B>(slot_codes<B>(c, s), qs);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[4 * s + i] = qs[i];
+        }
     }
 }
 
@@ -371,12 +411,19 @@ __device__ __forceinline__ void decode16_run(const uint8_t *__restrict__ wire, l
                 const float s = f16_bits_to_float(sb[u]);
                 const float2 s2 = make_float2(s, s);
                 float2 o[8];
+                if constexpr (B == 3) {
+                    float2 q[8];
+                    unpack_pair_q3(c[u].w[0], c[u].w[1], q);
 #pragma unroll
-                for (int sl = 0; sl < 2; ++sl) {
-                    float2 q[4];
-                    unpack_slot_q2<B>(half_slot_codes<B>(c[u], sl), q);
+                    for (int i = 0; i < 8; ++i) o[i] = __fmul2_rn(q[i], s2);
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) o[4 * sl + i] = __fmul2_rn(q[i], s2);
+                    for (int sl = 0; sl < 2; ++sl) {
+                        float2 q[4];
+                        unpack_slot_q2<B>(half_slot_codes<B>(c[u], sl), q);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o[4 * sl + i] = __fmul2_rn(q[i], s2);
+                    }
                 }
                 const long long base = hb * 16;
                 uint32_t w[8];
