@@ -104,36 +104,54 @@ struct BlockWords {
     uint32_t w[kWords];
 };
 
+// The INT3 fields of slots 2h and 2h+1 from their 16 magic floats (f[4s + m]
+// = lanes 2m, 2m+1 of slot s; the code is each float's low byte): W = the two
+// slots' q2w (slot 2h in bits 0..15), X = their q1w (slot 2h in bits 0..7,
+// slot 2h+1 in 8..15).  The inverse of unpack_pair_q3: the codes go into
+// bytes (even / odd lanes, first / second half of each slot), merge into
+// nibbles, the q2 fields come out with one mask, and the q1 bits, masked to
+// every fourth bit, are gathered by three shift-and-mask steps.
+__device__ __forceinline__ void pack_pair_q3(const float2 (&f)[16], int h, uint32_t &W, uint32_t &X) {
+    const int a = 8 * h, b = 8 * h + 4;  // f index of lane 0 of slot 2h, of slot 2h+1
+    const auto u = [](float v) { return __float_as_uint(v); };
+    const uint32_t el = gather_low_bytes(u(f[a].x), u(f[a + 2].x), u(f[b].x), u(f[b + 2].x));          // lanes 0, 4
+    const uint32_t eh = gather_low_bytes(u(f[a + 1].x), u(f[a + 3].x), u(f[b + 1].x), u(f[b + 3].x));  // lanes 2, 6
+    const uint32_t ol = gather_low_bytes(u(f[a].y), u(f[a + 2].y), u(f[b].y), u(f[b + 2].y));          // lanes 1, 5
+    const uint32_t oh = gather_low_bytes(u(f[a + 1].y), u(f[a + 3].y), u(f[b + 1].y), u(f[b + 3].y));  // lanes 3, 7
+    const uint32_t e = el | (eh << 4), o = ol | (oh << 4);  // nibble 4i+m: lane 2m / 2m+1 of slot 2h+i
+    W = (e & 0x33333333u) | ((o << 2) & 0xCCCCCCCCu);
+    uint32_t x = ((e >> 2) & 0x11111111u) | ((o >> 1) & 0x22222222u);
+    x = (x | (x >> 2)) & 0x0F0F0F0Fu;
+    x = (x | (x >> 4)) & 0x00FF00FFu;
+    X = (x & 0xFFu) | ((x >> 8) & 0xFF00u);
+}
+
 template <int B>
 __device__ __forceinline__ void pack_block(const float2 (&f)[16], BlockWords<B> &c) {
+    if constexpr (B == 3) {
+        uint32_t x01, x23;
+        pack_pair_q3(f, 0, c.w[0], x01);
+        pack_pair_q3(f, 1, c.w[1], x23);
+        c.w[2] = x01 | (x23 << 16);
+    } else {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        uint32_t even, odd;
-        slot_even_odd(f, s, even, odd);
-        if constexpr (B == 8) {
-            c.w[2 * s] = __byte_perm(even, odd, 0x5140);
-            c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
-        } else if constexpr (B == 4) {
-            c.w[s] = even | (odd << 4);
-        } else if constexpr (B == 3) {
-            const uint32_t nib = even | (odd << 4);
-            const uint32_t q2 = compress_2_of_4(nib);
-            const uint32_t q1 = compress_1_of_4(nib >> 2);
-            if (s % 2 == 0) {
-                c.w[s / 2] = q2;
+        for (int s = 0; s < 4; ++s) {
+            uint32_t even, odd;
+            slot_even_odd(f, s, even, odd);
+            if constexpr (B == 8) {
+                c.w[2 * s] = __byte_perm(even, odd, 0x5140);
+                c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
+            } else if constexpr (B == 4) {
+                c.w[s] = even | (odd << 4);
             } else {
-                c.w[s / 2] |= q2 << 16;
-            }
-            if (s == 0) c.w[2] = q1;
-            else c.w[2] |= q1 << (8 * s);
-        } else {
-            c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
-            const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
-            const uint32_t q2 = compress_2_of_4(hi);
-            if (s % 2 == 0) {
-                c.w[4 + s / 2] = q2;
-            } else {
-                c.w[4 + s / 2] |= q2 << 16;
+                c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
+                const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
+                const uint32_t q2 = compress_2_of_4(hi);
+                if (s % 2 == 0) {
+                    c.w[4 + s / 2] = q2;
+                } else {
+                    c.w[4 + s / 2] |= q2 << 16;
+                }
             }
         }
     }
