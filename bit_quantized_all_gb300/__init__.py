@@ -40,7 +40,7 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot",
            "qr_allreduce_twoshot_static", "qr_wait_timeouts", "qr_selftest_bounded_wait",
            "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas",
-           "qr_segment_reduce_staged")
+           "qr_segment_reduce_staged", "qr_fc_segment_reduce_staged")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
                 "qr_fc_allreduce_staged": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_fc_allreduce_ctas": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_segment_reduce_staged": (i32, [i32, i32, vpp, sz, vp, i32, vp]),
+                "qr_fc_segment_reduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_selftest_bounded_wait": (i32, [vp]),
             }
             for name, (res, args) in sig.items():
@@ -192,6 +193,10 @@ class capi:
     @staticmethod
     def qr_fc_segment_reduce(bits_in, bits_out, R, wires, n, out, stream=None):
         return lib().qr_fc_segment_reduce(bits_in, bits_out, R, _ptr_array(wires), n, out, stream)
+
+    @staticmethod
+    def qr_fc_segment_reduce_staged(bits_in, bits_out, R, wires, n, out, ctas, stream=None):
+        return lib().qr_fc_segment_reduce_staged(bits_in, bits_out, R, _ptr_array(wires), n, out, ctas, stream)
 
     @staticmethod
     def qr_fc_allreduce_ctas(bits_rs, bits_ag, dtype, R, xs, n, y, ctas, stream=None):
@@ -489,7 +494,7 @@ def qr_fc_decode(bits: int, wire: torch.Tensor, n: int, dtype: torch.dtype = tor
 
 
 def qr_fc_segment_reduce(bits_in: int, bits_out: int, wires, n: int, out: torch.Tensor | None = None,
-                         stream=None) -> torch.Tensor:
+                         stream=None, staged: bool = False, ctas: int = 0) -> torch.Tensor:
     wires = list(wires)
     if not 1 <= len(wires) <= QR_MAX_RANKS:
         raise ValueError(f"1 to {QR_MAX_RANKS} wires are supported, got {len(wires)}")
@@ -499,8 +504,14 @@ def qr_fc_segment_reduce(bits_in: int, bits_out: int, wires, n: int, out: torch.
         out = torch.empty(qr_fc_wire_bytes(bits_out, n), dtype=torch.uint8, device=wires[0].device)
     _fc_wire_tensor(out, bits_out, n, "out")
     dev = _same_device(wires + [out], "qr_fc_segment_reduce")
-    _check(capi.qr_fc_segment_reduce(bits_in, bits_out, len(wires), [w.data_ptr() for w in wires], n,
-                                     out.data_ptr(), _stream(dev, stream)), "qr_fc_segment_reduce")
+    ptrs = [w.data_ptr() for w in wires]
+    if staged:
+        status = capi.qr_fc_segment_reduce_staged(bits_in, bits_out, len(wires), ptrs, n, out.data_ptr(), ctas,
+                                                  _stream(dev, stream))
+    else:
+        status = capi.qr_fc_segment_reduce(bits_in, bits_out, len(wires), ptrs, n, out.data_ptr(),
+                                           _stream(dev, stream))
+    _check(status, "qr_fc_segment_reduce")
     return out
 
 

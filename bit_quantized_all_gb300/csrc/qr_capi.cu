@@ -150,9 +150,11 @@ QR_EXPORT qr_status_t qr_fc_decode(int bits, qr_dtype_t dtype, const void *wire,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
-QR_EXPORT qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R, const void *const *wires, size_t n,
-                                           void *out_wire, qr_stream_t stream) {
-    if (!wires || !out_wire || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+namespace {
+
+qr_status_t fc_segment_reduce_common(int bits_in, int bits_out, int R, const void *const *wires, size_t n,
+                                     void *out_wire, int ctas, bool staged, qr_stream_t stream) {
+    if (!wires || !out_wire || n == 0 || R < 1 || ctas < 0) return QR_ERR_INVALID_ARG;
     for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
         if (!wires[r]) return QR_ERR_INVALID_ARG;
     if (!fc_pair_ok(bits_in, bits_out) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
@@ -166,8 +168,23 @@ QR_EXPORT qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R, con
         if (bits_in == bits_out ? bad_alias(out_wire, Wo, wires[r], Wi) : overlaps(out_wire, Wo, wires[r], Wi))
             return QR_ERR_INVALID_ARG;
     }
+    if (staged)
+        return from_cuda(qrk::launch_fc_reduce_staged(bits_in, bits_out, R, wires, static_cast<long long>(n), out_wire,
+                                                      ctas, reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(qrk::launch_fc_reduce(bits_in, bits_out, R, wires, static_cast<long long>(n), out_wire,
                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+QR_EXPORT qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R, const void *const *wires, size_t n,
+                                           void *out_wire, qr_stream_t stream) {
+    return fc_segment_reduce_common(bits_in, bits_out, R, wires, n, out_wire, 0, false, stream);
+}
+
+QR_EXPORT qr_status_t qr_fc_segment_reduce_staged(int bits_in, int bits_out, int R, const void *const *wires,
+                                                  size_t n, void *out_wire, int ctas, qr_stream_t stream) {
+    return fc_segment_reduce_common(bits_in, bits_out, R, wires, n, out_wire, ctas, true, stream);
 }
 
 namespace {

@@ -30,9 +30,47 @@ static cudaError_t run_fc_decode_t(const void *wire, long long n, void *y, cudaS
     return cudaGetLastError();
 }
 
+// Phase-1B on the staged kernel (the R wire tiles brought into shared memory
+// by bulk copies) with min(ctas or #SMs, #SMs, tiles) persistent CTAs.
+template <int BIN, int BOUT, int R>
+static cudaError_t run_fc_reduce_staged_t(const ConstPtrs &w, long long n, void *out, int ctas, cudaStream_t s) {
+    using P = FcReduce<BIN, BOUT>;
+    using Shape = StagedReduceShape<P, R>;
+    auto kern = staged_reduce_kernel<P, R, Shape::kGroups, Shape::kStages>;
+    const long long T = (n + kTileValues - 1) / kTileValues;
+    cudaError_t err = cudaSuccess;
+    const int sms = sm_count(&err);
+    if (sms <= 0) return err;
+    if ((err = allow_dynamic_smem(reinterpret_cast<const void *>(kern), Shape::kSmemBytes)) != cudaSuccess)
+        return err;
+    unsigned *timeouts = wait_timeout_counter(&err);
+    if (!timeouts) return err;
+    long long grid = ctas > 0 ? ctas : sms;
+    if (grid > sms) grid = sms;
+    if (grid > T) grid = T;
+    kern<<<static_cast<int>(grid), P::kThreads * Shape::kGroups, Shape::kSmemBytes, s>>>(
+        w, static_cast<uint8_t *>(out), T, n, timeouts);
+    return cudaGetLastError();
+}
+
+// Where the default takes the staged Phase-1B kernel: from 48 tiles per SM,
+// for R >= 6, or R >= 4 with 8-bit input wires.  Measured on GB300 at 2^27
+// bf16 values per rank (fraction of the measured HBM bandwidth, register-fed
+// -> staged): R=8 4->4 0.38 -> 0.47, 4->8 0.45 -> 0.53, 8->8 0.72 -> 0.94;
+// R=4 4->4 0.44 -> 0.41, 4->8 0.49 -> 0.49, 8->8 0.73 -> 0.79; R=2 4->4 0.47
+// -> 0.34, 8->8 0.79 -> 0.66 (with few ranks the decode arithmetic, not the
+// memory latency, bounds the kernel, and the register-fed grid has more warps).
+constexpr long long kStagedFcReduceMinTilesPerSm = 48;
+
 template <int BIN, int BOUT, int R>
 static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
     const long long T = (n + kTileValues - 1) / kTileValues;
+    if constexpr (R >= 6 || (BIN == 8 && R >= 4)) {
+        cudaError_t e = cudaSuccess;
+        const int sms = sm_count(&e);
+        if (sms <= 0) return e;
+        if (T >= kStagedFcReduceMinTilesPerSm * sms) return run_fc_reduce_staged_t<BIN, BOUT, R>(w, n, out, 0, s);
+    }
     auto kern = fc_reduce_kernel<BIN, BOUT, R>;
     cudaError_t err = cudaSuccess;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, 4, &err);
@@ -87,6 +125,31 @@ cudaError_t launch_fc_reduce(int bits_in, int bits_out, int R, const void *const
     if (bits_in == 4 && bits_out == 4) return fc_reduce_r<4, 4>(R, w, n, out, s);
     if (bits_in == 4 && bits_out == 8) return fc_reduce_r<4, 8>(R, w, n, out, s);
     if (bits_in == 8 && bits_out == 8) return fc_reduce_r<8, 8>(R, w, n, out, s);
+    return cudaErrorInvalidValue;
+}
+
+template <int BIN, int BOUT>
+static cudaError_t fc_reduce_staged_r(int R, const ConstPtrs &w, long long n, void *out, int ctas, cudaStream_t s) {
+    switch (R) {
+        case 1: return run_fc_reduce_staged_t<BIN, BOUT, 1>(w, n, out, ctas, s);
+        case 2: return run_fc_reduce_staged_t<BIN, BOUT, 2>(w, n, out, ctas, s);
+        case 3: return run_fc_reduce_staged_t<BIN, BOUT, 3>(w, n, out, ctas, s);
+        case 4: return run_fc_reduce_staged_t<BIN, BOUT, 4>(w, n, out, ctas, s);
+        case 5: return run_fc_reduce_staged_t<BIN, BOUT, 5>(w, n, out, ctas, s);
+        case 6: return run_fc_reduce_staged_t<BIN, BOUT, 6>(w, n, out, ctas, s);
+        case 7: return run_fc_reduce_staged_t<BIN, BOUT, 7>(w, n, out, ctas, s);
+        case 8: return run_fc_reduce_staged_t<BIN, BOUT, 8>(w, n, out, ctas, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fc_reduce_staged(int bits_in, int bits_out, int R, const void *const *wires, long long n, void *out,
+                                    int ctas, cudaStream_t s) {
+    ConstPtrs w{};
+    for (int r = 0; r < R; ++r) w.p[r] = wires[r];
+    if (bits_in == 4 && bits_out == 4) return fc_reduce_staged_r<4, 4>(R, w, n, out, ctas, s);
+    if (bits_in == 4 && bits_out == 8) return fc_reduce_staged_r<4, 8>(R, w, n, out, ctas, s);
+    if (bits_in == 8 && bits_out == 8) return fc_reduce_staged_r<8, 8>(R, w, n, out, ctas, s);
     return cudaErrorInvalidValue;
 }
 

@@ -676,25 +676,51 @@ __host__ __device__ constexpr bool reduce_two_threads_per_block() { return (B ==
 template <int R>
 __host__ __device__ constexpr int reduce_units_per_thread() { return (R <= 2) ? 2 : 1; }
 
+// The symmetric codec's Phase-1B as a policy for staged_reduce_kernel: one
+// 32-value block per thread, 64 threads per tile.
+template <int B>
+struct QrReduce {
+    static constexpr int kThreads = 64;
+    static constexpr uint32_t kTileIn = Codec<B>::kTileBytes, kTileOut = Codec<B>::kTileBytes;
+    template <int R>
+    struct Regs {
+        BlockWords<B> c[R];
+        uint32_t sb[R];
+    };
+    template <int R>
+    static __device__ __forceinline__ void load(const uint8_t *stage, int k, Regs<R> &g) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            load_block_codes<B>(stage + r * kTileIn, k, g.c[r]);
+            g.sb[r] = load_block_scale_bits<B>(stage + r * kTileIn, k);
+        }
+    }
+    template <int R>
+    static __device__ __forceinline__ void reduce(const Regs<R> &g, uint8_t *tile_out, int k, long long, long long) {
+        reduce_block<B, R>(g.c, g.sb, tile_out, k);
+    }
+};
+
 // Phase-1B with the R ranks' wire tiles staged through shared memory by the
 // bulk-copy engine (the same pipeline as the staged fused kernel in
-// qr_staged.cuh): persistent, one CTA per SM of G groups of 64 threads, one
-// tile per group at a time and one 32-value block per thread.  Each group
-// owns a ring of SG stages of R * tile-bytes; its leader fills stage j % SG
-// with the group's tile j (R bulk copies counted on the stage's mbarrier).
-// The group copies its blocks' codes and scales into registers, meets at a
-// named barrier that also ANDs "my wait completed", the leader refills the
-// stage with tile j + SG, and the group reduces and writes the block while
-// that copy is in flight.  A wire is whole tiles, so there is no ragged
-// tile.  Every wait gives up after one second (the group then counts one
-// timeout, its leader waits, bounded again, for its copies, and it returns).
-template <int B, int R, int G, int SG>
-__global__ void __launch_bounds__(64 * G, 1) staged_reduce_kernel(ConstPtrs wires, uint8_t *out, long long T,
-                                                                  unsigned *timeouts) {
+// qr_staged.cuh), generic over the codec (a policy P: QrReduce, FcReduce):
+// persistent, one CTA per SM of G groups of P::kThreads threads, one tile
+// per group at a time.  Each group owns a ring of SG stages of R input
+// tiles; its leader fills stage j % SG with the group's tile j (R bulk
+// copies counted on the stage's mbarrier).  The group copies its share of
+// the stage into registers, meets at a named barrier that also ANDs "my
+// wait completed", the leader refills the stage with tile j + SG, and the
+// group reduces and writes its part of the output tile while that copy is
+// in flight.  A wire is whole tiles, so there is no ragged tile.  Every
+// wait gives up after one second (the group then counts one timeout, its
+// leader waits, bounded again, for its copies, and it returns).
+template <class P, int R, int G, int SG>
+__global__ void __launch_bounds__(P::kThreads * G, 1) staged_reduce_kernel(ConstPtrs wires, uint8_t *out,
+                                                                          long long T, long long n,
+                                                                          unsigned *timeouts) {
     static_assert(G >= 1 && G <= 15 && SG >= 1, "named barriers 1..G, at least one stage per group");
-    constexpr uint32_t kTile = Codec<B>::kTileBytes;
-    constexpr uint32_t kStageBytes = R * kTile;
-    extern __shared__ __align__(128) uint8_t ring[];  // G * SG * R * kTile bytes
+    constexpr uint32_t kStageBytes = R * P::kTileIn;
+    extern __shared__ __align__(128) uint8_t ring[];  // G * SG * R * P::kTileIn bytes
     __shared__ __align__(8) uint64_t full[G * SG];
     __shared__ const uint8_t *src[R];
 
@@ -705,7 +731,7 @@ __global__ void __launch_bounds__(64 * G, 1) staged_reduce_kernel(ConstPtrs wire
     }
     __syncthreads();
 
-    const int g = threadIdx.x / 64, k = threadIdx.x & 63;
+    const int g = threadIdx.x / P::kThreads, k = threadIdx.x % P::kThreads;
     const bool leader = k == 0;
     const long long first = blockIdx.x + static_cast<long long>(gridDim.x) * g;
     const long long stride = static_cast<long long>(gridDim.x) * G;
@@ -715,11 +741,11 @@ __global__ void __launch_bounds__(64 * G, 1) staged_reduce_kernel(ConstPtrs wire
 
     auto issue = [&](int j) {  // leader only: stage j % SG <- tile j of every rank
         const int s = j % SG;
-        const long long off = (first + j * stride) * kTile;
+        const long long off = (first + j * stride) * P::kTileIn;
         uint8_t *dst = my_ring + static_cast<size_t>(s) * kStageBytes;
         mbar_arrive_expect_tx(&my_full[s], kStageBytes);
 #pragma unroll
-        for (int r = 0; r < R; ++r) bulk_copy_g2s(dst + r * kTile, src[r] + off, kTile, &my_full[s]);
+        for (int r = 0; r < R; ++r) bulk_copy_g2s(dst + r * P::kTileIn, src[r] + off, P::kTileIn, &my_full[s]);
     };
 
     int issued = 0;
@@ -730,17 +756,12 @@ __global__ void __launch_bounds__(64 * G, 1) staged_reduce_kernel(ConstPtrs wire
     for (; j < tiles; ++j) {
         const int s = j % SG;
         const bool ok = mbar_wait(&my_full[s], static_cast<uint32_t>((j / SG) & 1));
-        const uint8_t *stage = my_ring + static_cast<size_t>(s) * kStageBytes;
-        BlockWords<B> c[R];
-        uint32_t sb[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            load_block_codes<B>(stage + r * kTile, k, c[r]);
-            sb[r] = load_block_scale_bits<B>(stage + r * kTile, k);
-        }
-        if (!group_all<64>(1 + g, ok)) break;  // also: every thread is done reading stage s
+        typename P::template Regs<R> regs;
+        P::template load<R>(my_ring + static_cast<size_t>(s) * kStageBytes, k, regs);
+        if (!group_all<P::kThreads>(1 + g, ok)) break;  // also: every thread is done reading stage s
         if (leader && issued < tiles) issue(issued++);
-        reduce_block<B, R>(c, sb, out + (first + j * stride) * kTile, k);
+        const long long t = first + j * stride;
+        P::template reduce<R>(regs, out + t * P::kTileOut, k, t, n);
     }
     if (j < tiles && leader) {  // a wait ran out
         atomicAdd(timeouts, 1u);
@@ -749,7 +770,8 @@ __global__ void __launch_bounds__(64 * G, 1) staged_reduce_kernel(ConstPtrs wire
     }
 }
 
-// Launch shape of the staged Phase-1B kernel: eight groups of 64 threads,
+// Launch shape of the staged Phase-1B kernel: 512 threads (eight groups of 64
+// threads for the symmetric codec),
 // each with as many stages (at most 4) as fit in 200 KiB of shared memory at
 // R * tile-bytes per stage.  Measured on GB300 at 2^27 bf16 values per rank
 // against the register-fed kernels (fraction of the measured HBM bandwidth,
@@ -757,12 +779,12 @@ __global__ void __launch_bounds__(64 * G, 1) staged_reduce_kernel(ConstPtrs wire
 // 0.92 / 0.89; INT6 R=8 0.64 -> 0.63 / 0.76 / 0.72; INT4 R=8 0.60 -> 0.54 /
 // 0.67 / 0.69; INT3 R=8 0.34 -> 0.29 / 0.34 / 0.34 (bound by the integer
 // pipe, not by memory: it stays on reduce32_kernel).
-template <int B, int R>
+template <class P, int R>
 struct StagedReduceShape {
-    static constexpr int kGroups = 8;
-    static constexpr int kFit = (200 * 1024) / (kGroups * R * Codec<B>::kTileBytes);
+    static constexpr int kGroups = 512 / P::kThreads;  // 16 warps
+    static constexpr int kFit = (200 * 1024) / (kGroups * R * P::kTileIn);
     static constexpr int kStages = kFit >= 4 ? 4 : (kFit < 1 ? 1 : kFit);
-    static constexpr int kSmemBytes = kGroups * kStages * R * Codec<B>::kTileBytes;
+    static constexpr int kSmemBytes = kGroups * kStages * R * P::kTileIn;
 };
 
 }  // namespace qrk

@@ -307,6 +307,34 @@ __global__ void __launch_bounds__(kThreadsFc) fc_decode_kernel(const uint8_t *__
 
 // Phase-1B: decode R BIN-wide wires, add in rank order, reset values past n,
 // re-quantize into a BOUT-wide wire.
+// Phase-1B of one tile for thread i (values base..base+15): decode the R
+// ranks' codes c[r] with their group scale s[r] and zero point z[r], add in
+// rank order, reset values past n, re-quantize at BOUT bits into tile_out.
+// Called by whole warps (the group min / max spans 8 lanes).
+template <int BIN, int BOUT, int R>
+__device__ __forceinline__ void fc_reduce_tile(const HalfWords<BIN> (&c)[R], const float (&s)[R], const float (&z)[R],
+                                               uint8_t *tile_out, int i, long long base, long long n) {
+    float2 acc[8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float2 u[8];
+        fc_unpack16<BIN>(c[r], u);
+        const float2 s2 = make_float2(s[r], s[r]), z2 = make_float2(z[r], z[r]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 d = __ffma2_rn(u[k], s2, z2);
+            acc[k] = (r == 0) ? d : __fadd2_rn(acc[k], d);
+        }
+    }
+    if (base + 16 > n) zero_past_n(acc, base, n);
+    float lo, hi;
+    group_minmax(acc, lo, hi);
+    const FcParams p = fc_params<BOUT>(lo, hi);
+    float2 f[8];
+    fc_quantize16<BOUT>(acc, p, f);
+    fc_store16<BOUT>(tile_out, i, f, p);
+}
+
 template <int BIN, int BOUT, int R>
 __global__ void __launch_bounds__(kThreadsFc) fc_reduce_kernel(ConstPtrs wires, long long n, uint8_t *out,
                                                                long long T) {
@@ -318,27 +346,31 @@ __global__ void __launch_bounds__(kThreadsFc) fc_reduce_kernel(ConstPtrs wires, 
         for (int r = 0; r < R; ++r)
             fc_load16<BIN>(static_cast<const uint8_t *>(wires.p[r]) + t * FcCodec<BIN>::kTileBytes, i, c[r], s[r],
                            z[r]);
-        float2 acc[8];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float2 u[8];
-            fc_unpack16<BIN>(c[r], u);
-            const float2 s2 = make_float2(s[r], s[r]), z2 = make_float2(z[r], z[r]);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float2 d = __ffma2_rn(u[k], s2, z2);
-                acc[k] = (r == 0) ? d : __fadd2_rn(acc[k], d);
-            }
-        }
-        const long long base = t * kTileValues + 16 * i;
-        if (base + 16 > n) zero_past_n(acc, base, n);
-        float lo, hi;
-        group_minmax(acc, lo, hi);
-        const FcParams p = fc_params<BOUT>(lo, hi);
-        float2 f[8];
-        fc_quantize16<BOUT>(acc, p, f);
-        fc_store16<BOUT>(out + t * FcCodec<BOUT>::kTileBytes, i, f, p);
+        fc_reduce_tile<BIN, BOUT, R>(c, s, z, out + t * FcCodec<BOUT>::kTileBytes, i, t * kTileValues + 16 * i, n);
     }
 }
+
+// The Flash Communication Phase-1B as a policy for staged_reduce_kernel
+// (qr_kernels32.cuh): 16 values per thread, 128 threads per tile.
+template <int BIN, int BOUT>
+struct FcReduce {
+    static constexpr int kThreads = kThreadsFc;
+    static constexpr uint32_t kTileIn = FcCodec<BIN>::kTileBytes, kTileOut = FcCodec<BOUT>::kTileBytes;
+    template <int R>
+    struct Regs {
+        HalfWords<BIN> c[R];
+        float s[R], z[R];
+    };
+    template <int R>
+    static __device__ __forceinline__ void load(const uint8_t *stage, int k, Regs<R> &g) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) fc_load16<BIN>(stage + r * kTileIn, k, g.c[r], g.s[r], g.z[r]);
+    }
+    template <int R>
+    static __device__ __forceinline__ void reduce(const Regs<R> &g, uint8_t *tile_out, int k, long long t,
+                                                  long long n) {
+        fc_reduce_tile<BIN, BOUT, R>(g.c, g.s, g.z, tile_out, k, t * kTileValues + 16 * k, n);
+    }
+};
 
 }  // namespace qrk

@@ -66,6 +66,8 @@ cudaError_t launch_fc_encode(int bits, int dtype, const void *x, long long n, vo
 cudaError_t launch_fc_decode(int bits, int dtype, const void *wire, long long n, void *y, cudaStream_t s);
 cudaError_t launch_fc_reduce(int bits_in, int bits_out, int R, const void *const *wires, long long n, void *out,
                              cudaStream_t s);
+cudaError_t launch_fc_reduce_staged(int bits_in, int bits_out, int R, const void *const *wires, long long n, void *out,
+                                    int ctas, cudaStream_t s);
 cudaError_t launch_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, const void *const *x, long long n,
                                 void *y, int ctas, cudaStream_t s);
 template <int BRS, int BAG>

@@ -9,8 +9,8 @@ namespace qrk {
 // The staged kernel with min(ctas or #SMs, #SMs, tiles) persistent CTAs.
 template <int B, int R>
 static cudaError_t run_reduce_staged_r(const ConstPtrs &w, long long n, void *out, int ctas, cudaStream_t s) {
-    using Shape = StagedReduceShape<B, R>;
-    auto kern = staged_reduce_kernel<B, R, Shape::kGroups, Shape::kStages>;
+    using Shape = StagedReduceShape<QrReduce<B>, R>;
+    auto kern = staged_reduce_kernel<QrReduce<B>, R, Shape::kGroups, Shape::kStages>;
     const long long T = (n + kTileValues - 1) / kTileValues;
     cudaError_t err = cudaSuccess;
     const int sms = sm_count(&err);
@@ -22,8 +22,8 @@ static cudaError_t run_reduce_staged_r(const ConstPtrs &w, long long n, void *ou
     long long grid = ctas > 0 ? ctas : sms;
     if (grid > sms) grid = sms;
     if (grid > T) grid = T;
-    kern<<<static_cast<int>(grid), 64 * Shape::kGroups, Shape::kSmemBytes, s>>>(w, static_cast<uint8_t *>(out), T,
-                                                                                 timeouts);
+    kern<<<static_cast<int>(grid), QrReduce<B>::kThreads * Shape::kGroups, Shape::kSmemBytes, s>>>(
+        w, static_cast<uint8_t *>(out), T, n, timeouts);
     return cudaGetLastError();
 }
 

@@ -290,6 +290,14 @@ qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R,
                                  const void *const *wires, size_t n,
                                  void *out_wire, qr_stream_t stream);
 
+/* qr_fc_segment_reduce on the staged Phase-1B kernel at any size, as
+ * qr_segment_reduce_staged (`ctas` = 0 for one CTA per SM, else min(ctas,
+ * #SMs); ctas < 0 is QR_ERR_INVALID_ARG).  qr_fc_segment_reduce itself
+ * takes it from 48 tiles per SM when R >= 6, or R >= 4 with bits_in = 8. */
+qr_status_t qr_fc_segment_reduce_staged(int bits_in, int bits_out, int R,
+                                        const void *const *wires, size_t n,
+                                        void *out_wire, int ctas, qr_stream_t stream);
+
 /* Receive path / Phase-2: decode the first n values into fp16/bf16. */
 qr_status_t qr_fc_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n,
                          void *y, qr_stream_t stream);

@@ -118,6 +118,8 @@ def test_reduce_validation():
     assert capi.qr_segment_reduce(4, 2, [A, B], n, A + W - 16) == qr.QR_ERR_INVALID_ARG  # partial overlap
     assert capi.qr_segment_reduce(4, 2, [A, B], 2**62 * 3, Y) == qr.QR_ERR_SIZE
     assert capi.qr_segment_reduce_staged(4, 2, [A, B], n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_segment_reduce_staged(4, 8, 2, [A, B], n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fc_segment_reduce_staged(8, 4, 2, [A, B], n, Y, 0) == qr.QR_ERR_UNSUPPORTED
     assert capi.qr_segment_reduce_staged(4, 2, [A, B + 8], n, Y, 0) == qr.QR_ERR_MISALIGNED
     assert capi.qr_segment_reduce_staged(7, 2, [A, B], n, Y, 0) == qr.QR_ERR_UNSUPPORTED
     assert capi.qr_segment_reduce_staged(4, 2, [A, B], n, A + W - 16, 0) == qr.QR_ERR_INVALID_ARG

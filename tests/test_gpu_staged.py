@@ -237,6 +237,36 @@ def test_staged_reduce_equals_the_register_kernels_and_in_place(R):
     assert qr.qr_wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("R", [1, 3, 8])
+def test_staged_fc_reduce_against_the_oracle(R):
+    """The Flash Communication Phase-1B on the staged kernel: three CTAs over
+    60 tiles of a ragged message (values past n reset to zero), every width
+    pair; byte for byte the oracle's reduced wire."""
+    n = 60 * 2048 + 333
+    xs = _ranks(R, n, 1, 300 + R)
+    for brs, bag in FC_PAIRS:
+        w_ref = [oracle.fc_encode(brs, 1, x) for x in xs]
+        wires = [torch.from_numpy(w).cuda() for w in w_ref]
+        red = qr.qr_fc_segment_reduce(brs, bag, wires, n, staged=True, ctas=3)
+        assert np.array_equal(red.cpu().numpy(), oracle.fc_segment_reduce(brs, bag, w_ref, n)), (brs, bag, R)
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("tiles_per_sm", [3, 50])
+def test_staged_fc_reduce_equals_the_default(tiles_per_sm):
+    R = 8
+    n = (tiles_per_sm * 152 + 7) * 2048 + 100
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(tiles_per_sm)
+    xs = [(torch.randn(n, device="cuda", generator=gen) * (r + 1)).to(torch.bfloat16) for r in range(R)]
+    for brs, bag in FC_PAIRS:
+        wires = [qr.qr_fc_encode(brs, x) for x in xs]
+        red0 = qr.qr_fc_segment_reduce(brs, bag, wires, n)
+        red1 = qr.qr_fc_segment_reduce(brs, bag, wires, n, staged=True, ctas=11)
+        assert torch.equal(red0, red1), (brs, bag, tiles_per_sm)
+    assert qr.qr_wait_timeouts() == 0
+
+
 def test_bounded_wait_runs_out_and_is_reported():
     """A wait on a barrier nothing completes gives up after one second,
     counts once, and leaves the context usable."""
