@@ -54,9 +54,11 @@
  *   - An output may alias an input of the same call exactly (same pointer,
  *     in-place) where noted; partial overlap is rejected.
  *   - Calls are thread-safe.  The library keeps only a per-device cache of
- *     launch limits (SM count, occupancy), filled on first use, and a
- *     per-device counter of device-side waits that ran out
- *     (qr_wait_timeouts).
+ *     launch limits (SM count, occupancy, the staged kernels' shared-memory
+ *     limits), filled on first use, and a per-device counter of device-side
+ *     waits that ran out (qr_wait_timeouts).  The first launch of each
+ *     staged kernel on a device does this setup (a function attribute and a
+ *     symbol address); make it before any stream capture.
  */
 #ifndef QR_H
 #define QR_H
