@@ -280,3 +280,54 @@ def test_bounded_wait_runs_out_and_is_reported():
     y = qr.qr_allreduce_staged(3, [to_dev(x, 1) for x in xs], ctas=2)
     assert_outputs_match(to_host_u16(y), oracle.allreduce(3, 1, xs), 1, xmax_of(xs, 1), "after the self-test")
     assert qr.qr_wait_timeouts() == 0
+
+
+def test_two_streams_at_once():
+    """Staged kernels on two streams at the same time (their only shared
+    state is the timeout counter) give what they give one after the other."""
+    R, n = 8, 40 * 2048 + 17
+    xa = [to_dev(x, 1) for x in _ranks(R, n, 1, 61)]
+    xb = [to_dev(x, 1) for x in _ranks(R, n, 1, 62)]
+    ya0 = qr.qr_allreduce_staged(4, xa)
+    yb0 = qr.qr_fc_allreduce_staged(4, 8, xb)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ya = torch.empty_like(ya0)
+    yb = torch.empty_like(yb0)
+    for _ in range(5):
+        with torch.cuda.stream(s1):
+            qr.qr_allreduce_staged(4, xa, y=ya)
+        with torch.cuda.stream(s2):
+            qr.qr_fc_allreduce_staged(4, 8, xb, y=yb)
+    torch.cuda.synchronize()
+    assert torch.equal(ya.view(torch.int16), ya0.view(torch.int16))
+    assert torch.equal(yb.view(torch.int16), yb0.view(torch.int16))
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("tiles_per_sm", [2, 60])
+def test_cuda_graph_replay(tiles_per_sm):
+    """After a first call on the device (which does the per-device setup),
+    qr_allreduce -- register-fed or staged, depending on the size -- can be
+    captured in a CUDA graph; replays give the same bytes."""
+    R = 8
+    n = (tiles_per_sm * _sms()) * 2048
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(tiles_per_sm)
+    xs = [(torch.randn(n, device="cuda", generator=gen) * (r + 1)).to(torch.bfloat16) for r in range(R)]
+    y = torch.empty_like(xs[0])
+    y_ref = qr.qr_allreduce(4, xs)  # the setup call, outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            qr.qr_allreduce(4, xs, y=y)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    assert qr.qr_wait_timeouts() == 0
