@@ -124,9 +124,17 @@ def cpu_baseline(xs, budget_s=12.0) -> dict:
     done = oracle_run(orc, xs, tiles, threads)
     dt = time.perf_counter() - t
     gbs = done * 2048 * R * 2 * len(BITS) / dt / 1e9
+    # the same oracle on one core, on a smaller sample (about 2 s)
+    one = int(max(1, min(N // 2048, 2.0 / (per_tile * threads))))
+    t = time.perf_counter()
+    done1 = oracle_run(orc, xs, one, 1)
+    dt1 = time.perf_counter() - t
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"first {done} of {N // 2048} tiles of every rank, INT4 and INT3, "
-                      f"{threads} threads, {dt:.1f} s wall"}
+                      f"{threads} threads, {dt:.1f} s wall",
+            "single_thread": {"value": round(done1 * 2048 * R * 2 * len(BITS) / dt1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"first {done1} tiles of every rank, INT4 and INT3, 1 thread, "
+                                        f"{dt1:.1f} s"}}
 
 
 def run_reference(args) -> None:
