@@ -356,6 +356,13 @@ def run_sweep(args) -> None:
                     def twoshot():
                         qr.qr_allreduce_twoshot(bits, xs, ys=ys2, workspace=ws)
 
+                    wsf = torch.empty(qr.lib().qr_twoshot_flags_workspace_bytes(bits, Rs, n), dtype=torch.uint8,
+                                      device=dev)
+                    ys3 = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
+
+                    def twoshot_flags():  # one cooperative launch, phases joined by per-tile flags
+                        qr.qr_allreduce_twoshot(bits, xs, ys=ys3, workspace=wsf, flags=True)
+
                     regs_ctas = 4 * 4 * sms  # forces the register-fed fused kernel (four waves)
 
                     def fused_regs():
@@ -363,16 +370,16 @@ def run_sweep(args) -> None:
 
                     arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
                             ("encode", encode_all), ("reduce", reduce_only), ("decode", decode_only),
-                            ("twoshot", twoshot))
-                    times = time_arms(arms, args, flush if do_flush else None, warm=(fused, fused_regs, unfused, twoshot))
+                            ("twoshot", twoshot), ("twoshot_flags", twoshot_flags))
+                    times = time_arms(arms, args, flush if do_flush else None, warm=(fused, fused_regs, unfused, twoshot, twoshot_flags))
                     same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
                         torch.equal(y.view(torch.int16), y2.view(torch.int16))) and all(
-                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in ys2)
+                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in ys2 + ys3)
                     # two-shot: R sends (2N in, W out each), R*W + W for the owners'
                     # reductions, R decodes (W in, 2N out each)
                     kernel_b = {"fused": fused_b, "fused_regs": fused_b, "unfused": unf_b, "encode": Rs * (2 * n + W),
                                 "reduce": (Rs + 1) * W, "decode": W + 2 * n,
-                                "twoshot": 4 * Rs * n + (3 * Rs + 1) * W}
+                                "twoshot": 4 * Rs * n + (3 * Rs + 1) * W, "twoshot_flags": 4 * Rs * n + (3 * Rs + 1) * W}
                     for name, alg in kernel_b.items():
                         med = statistics.median(times[name])
                         print(json.dumps({
@@ -383,7 +390,7 @@ def run_sweep(args) -> None:
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
                             "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps,
                             "burst": 1 if do_flush else args.burst}), flush=True)
-                    del wires, red, yu, ws, ys2
+                    del wires, red, yu, ws, ys2, wsf, ys3
                 del xs, y
                 torch.cuda.empty_cache()
 

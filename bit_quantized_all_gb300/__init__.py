@@ -40,7 +40,8 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_fc_allreduce", "qr_twoshot_workspace_bytes", "qr_allreduce_twoshot",
            "qr_allreduce_twoshot_static", "qr_wait_timeouts", "qr_selftest_bounded_wait",
            "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas",
-           "qr_segment_reduce_staged", "qr_fc_segment_reduce_staged")
+           "qr_segment_reduce_staged", "qr_fc_segment_reduce_staged", "qr_twoshot_flags_workspace_bytes",
+           "qr_allreduce_twoshot_flags")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
                 "qr_fc_allreduce": (i32, [i32, i32, i32, i32, vpp, sz, vp, vp]),
                 "qr_twoshot_workspace_bytes": (sz, [i32, i32, sz]),
                 "qr_allreduce_twoshot": (i32, [i32, i32, i32, vpp, sz, vpp, vp, sz, vp]),
+                "qr_twoshot_flags_workspace_bytes": (sz, [i32, i32, sz]),
+                "qr_allreduce_twoshot_flags": (i32, [i32, i32, i32, vpp, sz, vpp, vp, sz, vp]),
                 "qr_allreduce_twoshot_static": (i32, [i32, i32, i32, vpp, sz, vpp, vp]),
                 "qr_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint)]),
                 "qr_allreduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
@@ -166,6 +169,11 @@ class capi:
     def qr_allreduce_twoshot(bits, dtype, R, xs, n, ys, workspace, workspace_bytes, stream=None):
         return lib().qr_allreduce_twoshot(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), workspace,
                                           workspace_bytes, stream)
+
+    @staticmethod
+    def qr_allreduce_twoshot_flags(bits, dtype, R, xs, n, ys, workspace, workspace_bytes, stream=None):
+        return lib().qr_allreduce_twoshot_flags(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), workspace,
+                                                workspace_bytes, stream)
 
     @staticmethod
     def qr_allreduce_twoshot_static(bits, dtype, R, xs, n, ys, stream=None):
@@ -416,9 +424,13 @@ def qr_twoshot_workspace_bytes(bits: int, R: int, n: int) -> int:
     return int(lib().qr_twoshot_workspace_bytes(bits, R, n))
 
 
-def qr_allreduce_twoshot(bits: int, xs, ys=None, workspace: torch.Tensor | None = None, stream=None):
+def qr_allreduce_twoshot(bits: int, xs, ys=None, workspace: torch.Tensor | None = None, stream=None,
+                         flags: bool = False):
     """The two-shot all-reduce with its exchange laid out per rank and per
-    owner in `workspace`: returns (the R outputs, the workspace)."""
+    owner in `workspace`: returns (the R outputs, the workspace).  With
+    `flags`, the one-launch version whose phases are joined by per-tile
+    ready flags (qr_allreduce_twoshot_flags; its workspace also holds the
+    2T + 1 flag words)."""
     xs, dt, n = _check_inputs(xs)
     R = len(xs)
     dev = _same_device(xs, "qr_allreduce_twoshot")
@@ -431,16 +443,16 @@ def qr_allreduce_twoshot(bits: int, xs, ys=None, workspace: torch.Tensor | None 
         _cuda_contig(y, f"ys[{i}]")
         if y.dtype != xs[0].dtype or y.numel() != n:
             raise ValueError(f"ys[{i}] must match the inputs' dtype and size")
-    need = qr_twoshot_workspace_bytes(bits, R, n)
+    need = (lib().qr_twoshot_flags_workspace_bytes if flags else lib().qr_twoshot_workspace_bytes)(bits, R, n)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     _cuda_contig(workspace, "workspace")
     if workspace.dtype != torch.uint8:
         raise TypeError(f"workspace must be torch.uint8, got {workspace.dtype}")
     _same_device(xs + ys + [workspace], "qr_allreduce_twoshot")
-    _check(capi.qr_allreduce_twoshot(bits, dt, R, [x.data_ptr() for x in xs], n, [y.data_ptr() for y in ys],
-                                     workspace.data_ptr(), workspace.numel(), _stream(dev, stream)),
-           "qr_allreduce_twoshot")
+    call = capi.qr_allreduce_twoshot_flags if flags else capi.qr_allreduce_twoshot
+    _check(call(bits, dt, R, [x.data_ptr() for x in xs], n, [y.data_ptr() for y in ys], workspace.data_ptr(),
+                workspace.numel(), _stream(dev, stream)), "qr_allreduce_twoshot")
     return ys, workspace
 
 

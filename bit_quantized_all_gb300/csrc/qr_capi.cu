@@ -80,6 +80,54 @@ size_t twoshot_ws_bytes(int bits, int R, size_t n) {
 
 QR_EXPORT size_t qr_twoshot_workspace_bytes(int bits, int R, size_t n) { return twoshot_ws_bytes(bits, R, n); }
 
+namespace {
+
+// The two-shot workspace, then (16-byte aligned) 2T + 1 flag words.
+size_t twoshot_flags_ws_bytes(int bits, int R, size_t n, size_t *flags_offset) {
+    const size_t base = twoshot_ws_bytes(bits, R, n);
+    if (base == 0) return 0;
+    const size_t tiles = n / kTile + (n % kTile != 0);
+    const size_t off = (base + 15) / 16 * 16;
+    if (tiles > (SIZE_MAX - off) / 8 - 1) return 0;
+    if (flags_offset) *flags_offset = off;
+    return off + (2 * tiles + 1) * sizeof(uint32_t);
+}
+
+}  // namespace
+
+QR_EXPORT size_t qr_twoshot_flags_workspace_bytes(int bits, int R, size_t n) {
+    return twoshot_flags_ws_bytes(bits, R, n, nullptr);
+}
+
+QR_EXPORT qr_status_t qr_allreduce_twoshot_flags(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                                 void *const *y, void *workspace, size_t workspace_bytes,
+                                                 qr_stream_t stream) {
+    if (!x || !y || !workspace || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!x[r] || !y[r]) return QR_ERR_INVALID_ARG;
+    if (!bits_ok(bits) || !dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    size_t flags_offset = 0;
+    const size_t need = twoshot_flags_ws_bytes(bits, R, n, &flags_offset);
+    if (!value_bytes_ok(n) || need == 0 || wire_bytes(bits, n) == 0) return QR_ERR_SIZE;
+    if (workspace_bytes < need) return QR_ERR_SIZE;
+    const size_t V = 2 * n;
+    if (!aligned16(workspace)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(x[r]) || !aligned16(y[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r) {
+        if (overlaps(workspace, need, x[r], V) || overlaps(workspace, need, y[r], V)) return QR_ERR_INVALID_ARG;
+        for (int i = 0; i < R; ++i) {
+            // tile t of every input is read before tile t of any output is
+            // written: an output may be an input exactly, never partly
+            if (bad_alias(y[r], V, x[i], V)) return QR_ERR_INVALID_ARG;
+            if (i < r && overlaps(y[r], V, y[i], V)) return QR_ERR_INVALID_ARG;
+        }
+    }
+    return from_cuda(qrk::launch_twoshot_flags(bits, dtype, R, x, static_cast<long long>(n), y, workspace,
+                                               static_cast<uint8_t *>(workspace) + flags_offset,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QR_EXPORT qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
                                            void *const *y, void *workspace, size_t workspace_bytes,
                                            qr_stream_t stream) {

@@ -531,4 +531,14 @@ struct MutPtrs {
     void *p[kMaxRanks];
 };
 
+// p[i] for a run-time i without indexing the kernel-parameter array (which
+// would copy it to local memory): one select per rank.
+template <class P>
+__device__ __forceinline__ P row_pointer(const P (&p)[kMaxRanks], int i) {
+    P v = p[0];
+#pragma unroll
+    for (int r = 1; r < kMaxRanks; ++r) v = (i == r) ? p[r] : v;
+    return v;
+}
+
 }  // namespace qrk

@@ -60,6 +60,12 @@ long long twoshot_segment_tiles(long long tiles, int R);
 cudaError_t launch_twoshot(int bits, int dtype, int R, const void *const *x, long long n, void *const *y, void *ws,
                            cudaStream_t s);
 
+// The same exchange in one cooperative launch, its phases joined by per-tile
+// ready flags (qr_twoshot_flags.cu); `flags` holds 2T + 1 words that the call
+// zeroes before the launch.
+cudaError_t launch_twoshot_flags(int bits, int dtype, int R, const void *const *x, long long n, void *const *y,
+                                 void *ws, void *flags, cudaStream_t s);
+
 // The Flash Communication codec (asymmetric groups of 128): widths 4 and 8;
 // the (reduce-scatter, all-gather) width pairs (4,4), (4,8) and (8,8).
 cudaError_t launch_fc_encode(int bits, int dtype, const void *x, long long n, void *wire, cudaStream_t s);

@@ -22,16 +22,6 @@
 
 namespace qrk {
 
-// p[i] for a run-time i without indexing the kernel-parameter array (which
-// would copy it to local memory): one select per rank.
-template <class P>
-__device__ __forceinline__ P row_pointer(const P (&p)[kMaxRanks], int i) {
-    P v = p[0];
-#pragma unroll
-    for (int r = 1; r < kMaxRanks; ++r) v = (i == r) ? p[r] : v;
-    return v;
-}
-
 long long twoshot_segment_tiles(long long tiles, int R) { return (tiles + R - 1) / R; }
 
 // Phase-1: sender j = blockIdx.y quantizes its whole message straight into

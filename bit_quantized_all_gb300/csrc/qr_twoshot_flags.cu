@@ -1,0 +1,253 @@
+// qr_twoshot_flags.cu -- the two-shot all-reduce of qr_twoshot.cu in one
+// cooperative launch, its phases joined by per-tile ready flags instead of
+// launch boundaries: the protocol a multi-GPU version runs between ranks
+// (peers store wire tiles into the owner's buffer and raise a flag the owner
+// waits on), here between CTAs of one GPU ([QR] Design Highlights: Phase-1
+// sends, Phase-1B owner reduction, Phase-2 gather; [FC] key machinery).
+//
+// Work units (one 2048-value tile each, 64 threads, one 32-value block per
+// thread):
+//   phase 1: (sender j, tile t): quantize rank j's tile t into owner
+//            k = t / seg's receive buffer recv[k][j], then add one to
+//            sent[t] (a release);
+//   phase 2: tile t: wait until sent[t] == R (an acquire), reduce the R
+//            copies into the gathered wire, set reduced[t] (a release);
+//   phase 3: (rank j, tile t): wait for reduced[t], decode the gathered
+//            tile into y[j].
+// Every CTA runs all its phase-1 units, then its phase-2 units, then its
+// phase-3 units, and a cooperative launch keeps every CTA resident, so a
+// wait only ever waits for work that itself never waits (phase 1) or waits
+// only for phase 1: no cycle.  Tiles flow through the three phases as soon
+// as their inputs are ready.  Data written by other CTAs during the kernel
+// is read with L2 (.cg) loads after the acquire.
+//
+// Every wait is bounded (one second of %globaltimer).  On expiry the CTA
+// adds one to the library's timeout counter and raises the workspace's abort
+// word; every other wait sees it and returns at once, so a failed launch
+// ends promptly with incomplete outputs and the context usable.
+#include <cstdint>
+
+#include "qr_kernels32.cuh"
+#include "qr_launch.h"
+
+namespace qrk {
+
+namespace {
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void add_release(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void store_release(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Thread 0 waits (bounded) until *flag >= target, then the CTA proceeds
+// together; false if the wait ran out or another CTA gave up.
+__device__ __forceinline__ bool cta_wait(const uint32_t *flag, uint32_t target, uint32_t *abort_word,
+                                         unsigned *timeouts) {
+    __shared__ int ok;
+    if (threadIdx.x == 0) {
+        int good = 1;
+        if (ld_acquire(flag) < target) {
+            const unsigned long long t0 = global_ns();
+            while (ld_acquire(flag) < target) {
+                if (*static_cast<volatile uint32_t *>(abort_word) != 0) {
+                    good = 0;
+                    break;
+                }
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    atomicAdd(timeouts, 1u);
+                    atomicExch(abort_word, 1u);
+                    good = 0;
+                    break;
+                }
+            }
+        }
+        ok = good;
+    }
+    __syncthreads();
+    const bool r = ok != 0;
+    __syncthreads();  // `ok` is rewritten by the next wait
+    return r;
+}
+
+// One block's codes and scale from a tile written during this kernel (L2 loads).
+template <int B>
+__device__ __forceinline__ void load_block_cg(const uint8_t *tile, int g, BlockWords<B> &c, uint32_t &sb) {
+    if constexpr (B == 8) {
+        const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(tile + 32 * g));
+        const uint4 b = __ldcg(reinterpret_cast<const uint4 *>(tile + 32 * g + 16));
+        c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+        c.w[4] = b.x; c.w[5] = b.y; c.w[6] = b.z; c.w[7] = b.w;
+    } else if constexpr (B == 4) {
+        const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(tile + 16 * g));
+        c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+    } else if constexpr (B == 3) {
+        const uint2 a = __ldcg(reinterpret_cast<const uint2 *>(tile + 8 * g));
+        c.w[0] = a.x; c.w[1] = a.y;
+        c.w[2] = __ldcg(reinterpret_cast<const unsigned int *>(tile + 512 + 4 * g));
+    } else {
+        const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(tile + 16 * g));
+        const uint2 b = __ldcg(reinterpret_cast<const uint2 *>(tile + 1024 + 8 * g));
+        c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+        c.w[4] = b.x; c.w[5] = b.y;
+    }
+    sb = __ldcg(reinterpret_cast<const unsigned short *>(tile + Codec<B>::kCodeBytes + 2 * g));
+}
+
+template <int B, int DT, int R>
+__global__ void __launch_bounds__(64) twoshot_flags_kernel(ConstPtrs x, long long n, MutPtrs y, uint8_t *ws,
+                                                           long long T, long long seg, uint32_t *flags,
+                                                           unsigned *timeouts) {
+    constexpr long long kTile = Codec<B>::kTileBytes;
+    const int k = threadIdx.x;  // the block of the tile this thread works on
+    uint32_t *sent = flags, *reduced = flags + T, *abort_word = flags + 2 * T;
+    uint8_t *red = ws + static_cast<long long>(R) * R * seg * kTile;
+
+    // phase 1: sends, tile-major so that early tiles become ready early
+    for (long long u = blockIdx.x; u < R * T; u += gridDim.x) {
+        const long long t = u / R;
+        const int j = static_cast<int>(u - t * R);
+        const long long owner = t / seg;
+        uint8_t *dst = ws + ((owner * R + j) * seg + (t - owner * seg)) * kTile;
+        uint32_t raw[16];
+        load_block_values(static_cast<const uint16_t *>(row_pointer(x.p, j)), t * kTileValues + 32 * k, n, raw);
+        float2 v[16], f[16];
+        widen_block<DT>(raw, v);
+        const BlockScale2 sc = block_scale2<B>(block_absmax(v));
+        quantize_block_magic<B>(v, sc.r, sc.low_clip, f);
+        BlockWords<B> c;
+        pack_block<B>(f, c);
+        store_block_codes<B>(dst, k, c);
+        store_block_scale<B>(dst, k, sc.bits);
+        __syncthreads();
+        if (k == 0) add_release(&sent[t], 1u);
+    }
+    // phase 2: each owner's reduction of its tiles, as their copies arrive
+    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+        if (!cta_wait(&sent[t], R, abort_word, timeouts)) return;
+        const long long owner = t / seg;
+        BlockWords<B> c[R];
+        uint32_t sb[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            load_block_cg<B>(ws + ((owner * R + j) * seg + (t - owner * seg)) * kTile, k, c[j], sb[j]);
+        reduce_block<B, R>(c, sb, red + t * kTile, k);
+        __syncthreads();
+        if (k == 0) store_release(&reduced[t], 1u);
+    }
+    // phase 3: every rank decodes the gathered wire, tile by tile as it is reduced
+    for (long long u = blockIdx.x; u < R * T; u += gridDim.x) {
+        const long long t = u / R;
+        const int j = static_cast<int>(u - t * R);
+        if (!cta_wait(&reduced[t], 1u, abort_word, timeouts)) return;
+        BlockWords<B> c;
+        uint32_t sb;
+        load_block_cg<B>(red + t * kTile, k, c, sb);
+        const float s = f16_bits_to_float(sb);
+        const float2 s2 = make_float2(s, s);
+        float2 q[16];
+        unpack_block_q<B>(c, q);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 o = __fmul2_rn(q[i], s2);
+            w[i] = narrow2<DT>(o.x, o.y);
+        }
+        uint16_t *yj = static_cast<uint16_t *>(row_pointer(y.p, j));
+        const long long base = t * kTileValues + 32 * k;
+        if (base + 32 <= n) {
+            if ((reinterpret_cast<uintptr_t>(yj) & 31u) == 0) {  // whole 32-byte sectors per store
+                const uint32_t lo[8] = {w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]};
+                const uint32_t hi[8] = {w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]};
+                st_global32(yj + base, lo);
+                st_global32(yj + base + 16, hi);
+            } else {
+                uint4 *p = reinterpret_cast<uint4 *>(yj + base);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) p[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (base + 2 * i < n) yj[base + 2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+                if (base + 2 * i + 1 < n) yj[base + 2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+            }
+        }
+    }
+}
+
+template <int B, int DT, int R>
+static cudaError_t run_flags(const ConstPtrs &xp, long long n, const MutPtrs &yp, uint8_t *ws, uint32_t *flags,
+                             cudaStream_t s) {
+    const long long T = (n + kTileValues - 1) / kTileValues;
+    long long seg = twoshot_segment_tiles(T, R);
+    cudaError_t err = cudaSuccess;
+    unsigned *timeouts = wait_timeout_counter(&err);
+    if (!timeouts) return err;
+    if ((err = cudaMemsetAsync(flags, 0, static_cast<size_t>(2 * T + 1) * sizeof(uint32_t), s)) != cudaSuccess)
+        return err;
+    auto kern = twoshot_flags_kernel<B, DT, R>;
+    const int sms = sm_count(&err);
+    if (sms <= 0) return err;
+    int per_sm = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64, 0)) != cudaSuccess) return err;
+    long long grid = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
+    if (grid > R * T) grid = R * T;
+    long long nn = n, TT = T;
+    ConstPtrs xa = xp;
+    MutPtrs ya = yp;
+    void *args[] = {&xa, &nn, &ya, &ws, &TT, &seg, &flags, &timeouts};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(static_cast<unsigned>(grid)),
+                                       dim3(64), args, 0, s);
+}
+
+template <int B, int DT>
+static cudaError_t run_flags_r(int R, const ConstPtrs &xp, long long n, const MutPtrs &yp, uint8_t *ws,
+                               uint32_t *flags, cudaStream_t s) {
+    switch (R) {
+        case 1: return run_flags<B, DT, 1>(xp, n, yp, ws, flags, s);
+        case 2: return run_flags<B, DT, 2>(xp, n, yp, ws, flags, s);
+        case 3: return run_flags<B, DT, 3>(xp, n, yp, ws, flags, s);
+        case 4: return run_flags<B, DT, 4>(xp, n, yp, ws, flags, s);
+        case 5: return run_flags<B, DT, 5>(xp, n, yp, ws, flags, s);
+        case 6: return run_flags<B, DT, 6>(xp, n, yp, ws, flags, s);
+        case 7: return run_flags<B, DT, 7>(xp, n, yp, ws, flags, s);
+        case 8: return run_flags<B, DT, 8>(xp, n, yp, ws, flags, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+long long twoshot_flag_words(long long tiles) { return 2 * tiles + 1; }
+
+cudaError_t launch_twoshot_flags(int bits, int dtype, int R, const void *const *x, long long n, void *const *y,
+                                 void *ws, void *flags, cudaStream_t s) {
+    ConstPtrs xp{};
+    MutPtrs yp{};
+    for (int r = 0; r < R; ++r) {
+        xp.p[r] = x[r];
+        yp.p[r] = y[r];
+    }
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint32_t *f = static_cast<uint32_t *>(flags);
+#define QR_CASE(B)                                                                                  \
+    case B:                                                                                         \
+        return dtype ? run_flags_r<B, 1>(R, xp, n, yp, w, f, s) : run_flags_r<B, 0>(R, xp, n, yp, w, f, s);
+    switch (bits) {
+        QR_CASE(3)
+        QR_CASE(4)
+        QR_CASE(6)
+        QR_CASE(8)
+    }
+#undef QR_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qrk

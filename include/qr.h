@@ -211,6 +211,30 @@ qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R,
                                  void *workspace, size_t workspace_bytes,
                                  qr_stream_t stream);
 
+/* The same two-shot exchange in one cooperative launch, its phases joined
+ * by per-tile ready flags instead of launch boundaries -- the protocol a
+ * multi-GPU version runs between ranks (a sender stores its quantized tile
+ * into the owner's buffer and raises the owner's flag; the owner waits for
+ * R flags, reduces, and raises the tile's "reduced" flag that the decoders
+ * wait for), here between the CTAs of one GPU.  Tiles flow through the
+ * three phases as soon as their inputs are ready.  Every y[j] equals
+ * qr_allreduce's output and the workspace's exchange buffers hold the same
+ * bytes as qr_allreduce_twoshot's.
+ * `workspace` (device, 16-byte aligned, at least
+ * qr_twoshot_flags_workspace_bytes(bits, R, n) bytes) = the two-shot
+ * workspace, then, 16-byte aligned, 2T + 1 32-bit flag words that the call
+ * zeroes (on `stream`) before its launch.  Every wait on a flag is bounded
+ * (one second); if one runs out the launch counts a timeout (see
+ * qr_wait_timeouts), every other wait returns at once, and the outputs are
+ * incomplete.  Same arguments, aliasing rules and errors as
+ * qr_allreduce_twoshot; QR_ERR_CUDA if the cooperative launch is refused. */
+size_t qr_twoshot_flags_workspace_bytes(int bits, int R, size_t n); /* 0 if invalid */
+
+qr_status_t qr_allreduce_twoshot_flags(int bits, qr_dtype_t dtype, int R,
+                                       const void *const *x, size_t n, void *const *y,
+                                       void *workspace, size_t workspace_bytes,
+                                       qr_stream_t stream);
+
 /* qr_allreduce_twoshot for callers that cannot allocate device memory (no
  * counterpart on the source pages; a convenience of this library).  Some
  * callers cannot call cudaMalloc: code running inside someone else's memory

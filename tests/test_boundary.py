@@ -234,6 +234,18 @@ def test_twoshot_validation():
     assert call(4, 0, 2, xs, n, [Y, Y], WS, need) == qr.QR_ERR_INVALID_ARG
     assert call(4, 0, 2, xs, n, [A + 16, Y], WS, need) == qr.QR_ERR_INVALID_ARG      # partial in-place
     assert call(4, 0, 2, xs, n, ys, A, need) == qr.QR_ERR_INVALID_ARG              # workspace over an input
+    # the one-launch version: the same checks against its larger workspace
+    T = -(-n // 2048)
+    fneed = qr.lib().qr_twoshot_flags_workspace_bytes(4, 2, n)
+    assert fneed == -(-need // 16) * 16 + 4 * (2 * T + 1)
+    fcall = capi.qr_allreduce_twoshot_flags
+    assert fcall(4, 0, 2, xs, n, ys, WS, fneed - 1) == qr.QR_ERR_SIZE
+    assert fcall(4, 0, 2, xs, n, ys, WS, need) == qr.QR_ERR_SIZE
+    assert fcall(4, 0, 2, xs, n, ys, WS + 8, fneed) == qr.QR_ERR_MISALIGNED
+    assert fcall(4, 0, 2, xs, n, [A + 16, Y], WS, fneed) == qr.QR_ERR_INVALID_ARG
+    assert fcall(5, 0, 2, xs, n, ys, WS, fneed) == qr.QR_ERR_UNSUPPORTED
+    assert fcall(4, 0, 2, xs, n, ys, None, fneed) == qr.QR_ERR_INVALID_ARG
+    assert qr.lib().qr_twoshot_flags_workspace_bytes(4, 9, n) == 0
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):

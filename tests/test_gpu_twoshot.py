@@ -125,3 +125,74 @@ def test_large_sampled():
         red_t = oracle.segment_reduce(4, [oracle.encode(4, 1, v) for v in xt], 2048)
         got = ws[red_off + t * tb: red_off + (t + 1) * tb].cpu().numpy()
         assert_wire_equal(got, red_t, 4, f"gathered tile {t}")
+
+
+# ---------------------------------------------------------------------------
+# the one-launch version whose phases are joined by per-tile ready flags
+# ---------------------------------------------------------------------------
+def flags_check(bits, dtype, xs, what):
+    R, n = len(xs), xs[0].size
+    xs_dev = [to_dev(x, dtype) for x in xs]
+    ys, ws = qr.qr_allreduce_twoshot(bits, xs_dev, flags=True)
+    torch.cuda.synchronize()
+    y_ref = oracle.allreduce(bits, dtype, xs)
+    xmax = xmax_of(xs, dtype)
+    for j, y in enumerate(ys):
+        assert_outputs_match(to_host_u16(y), y_ref, dtype, xmax, f"{what} rank {j} output")
+    # the exchange buffers hold what the three-launch version leaves there
+    # (the parts either version writes: each owner's received tiles and the
+    # T gathered tiles; owners past the last tile own nothing)
+    ys3, ws3 = qr.qr_allreduce_twoshot(bits, xs_dev)
+    torch.cuda.synchronize()
+    base = ws3.numel()
+    T = -(-n // 2048)
+    tb = qr.qr_tile_bytes(bits)
+    seg = -(-T // R)
+    a, b = to_host_u8(ws[:base]), to_host_u8(ws3)
+    for k in range(R):
+        t0, t1 = k * seg, min(T, (k + 1) * seg)
+        for j in range(R):
+            off = (k * R + j) * seg * tb
+            if t0 < T:
+                assert_wire_equal(a[off: off + (t1 - t0) * tb], b[off: off + (t1 - t0) * tb], bits,
+                                  f"{what} owner {k} copy from rank {j}")
+    red_off = R * R * seg * tb
+    assert_wire_equal(a[red_off: red_off + T * tb], b[red_off: red_off + T * tb], bits, f"{what} gathered wire")
+    # and the protocol ran to completion: every tile saw R sends and one reduction, no abort
+    off = -(-base // 16) * 16
+    words = ws[off: off + 4 * (2 * T + 1)].cpu().numpy().view(np.uint32)
+    assert np.all(words[:T] == R) and np.all(words[T:2 * T] == 1) and words[2 * T] == 0, what
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("n", [1, 37, 2048, 2049, 2048 * 9 + 1, 2048 * 64 + 5])
+@pytest.mark.parametrize("R", [1, 2, 3, 8])
+def test_flags_segment_shapes(n, R):
+    for bits in BITS:
+        flags_check(bits, 1, _rand_ranks(R, n, 1, 30 * n + R + bits), f"flags n={n} R={R} INT{bits}")
+
+
+@pytest.mark.parametrize("cfg", [workloads.C1, workloads.C2, workloads.C3], ids=lambda c: c["name"])
+def test_flags_workloads(cfg):
+    xs = workloads.ranks(cfg)
+    for bits in cfg["bits"]:
+        flags_check(bits, cfg["dtype"], xs, f"flags {cfg['name']} INT{bits}")
+
+
+def test_flags_in_place_and_large():
+    """Every rank in place; and the benchmark's size class against the fused kernel."""
+    n, R = 2048 * 200 + 9, 4
+    xs_dev = [to_dev(x, 0) for x in _rand_ranks(R, n, 0, 8)]
+    y0 = qr.qr_allreduce(4, xs_dev)
+    xs2 = [x.clone() for x in xs_dev]
+    out, _ = qr.qr_allreduce_twoshot(4, xs2, ys=xs2, flags=True)
+    for y in out:
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    n, R = 1 << 27, 8
+    xs_dev = [x.view(torch.bfloat16) for x in workloads.device_sweep(R, n, 1, seed=12, device="cuda")]
+    for bits in (4, 3):
+        yf = qr.qr_allreduce(bits, xs_dev)
+        ys, _ = qr.qr_allreduce_twoshot(bits, xs_dev, flags=True)
+        for y in ys:
+            assert torch.equal(y.view(torch.int16), yf.view(torch.int16)), bits
+    assert qr.qr_wait_timeouts() == 0
