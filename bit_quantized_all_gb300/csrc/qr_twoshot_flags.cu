@@ -5,15 +5,16 @@
 // waits on), here between CTAs of one GPU ([QR] Design Highlights: Phase-1
 // sends, Phase-1B owner reduction, Phase-2 gather; [FC] key machinery).
 //
-// Work units (one 2048-value tile each, 64 threads, one 32-value block per
-// thread):
-//   phase 1: (sender j, tile t): quantize rank j's tile t into owner
-//            k = t / seg's receive buffer recv[k][j], then add one to
-//            sent[t] (a release);
-//   phase 2: tile t: wait until sent[t] == R (an acquire), reduce the R
-//            copies into the gathered wire, set reduced[t] (a release);
-//   phase 3: (rank j, tile t): wait for reduced[t], decode the gathered
-//            tile into y[j].
+// Work units (a chunk of C consecutive 2048-value tiles, 64 threads, one
+// 32-value block of each tile per thread):
+//   phase 1: (sender j, chunk c): quantize rank j's tiles of chunk c into
+//            their owners' receive buffers recv[k][j] (owner k = t / seg),
+//            then add one to sent[c] (a release);
+//   phase 2: chunk c: wait until sent[c] == R (an acquire), reduce the R
+//            copies of each tile into the gathered wire, set reduced[c] (a
+//            release);
+//   phase 3: (rank j, chunk c): wait for reduced[c], decode the chunk's
+//            gathered tiles into y[j].
 // Every CTA runs all its phase-1 units, then its phase-2 units, then its
 // phase-3 units, and a cooperative launch keeps every CTA resident, so a
 // wait only ever waits for work that itself never waits (phase 1) or waits
@@ -100,87 +101,120 @@ __device__ __forceinline__ void load_block_cg(const uint8_t *tile, int g, BlockW
     sb = __ldcg(reinterpret_cast<const unsigned short *>(tile + Codec<B>::kCodeBytes + 2 * g));
 }
 
-template <int B, int DT, int R>
+// Work unit = a chunk of C consecutive tiles (one block of each per thread,
+// all their loads issued before any arithmetic); flags are per chunk.
+template <int B, int DT, int R, int C>
 __global__ void __launch_bounds__(64) twoshot_flags_kernel(ConstPtrs x, long long n, MutPtrs y, uint8_t *ws,
                                                            long long T, long long seg, uint32_t *flags,
                                                            unsigned *timeouts) {
     constexpr long long kTile = Codec<B>::kTileBytes;
-    const int k = threadIdx.x;  // the block of the tile this thread works on
+    const int k = threadIdx.x;  // the block of each tile this thread works on
+    const long long chunks = (T + C - 1) / C;
     uint32_t *sent = flags, *reduced = flags + T, *abort_word = flags + 2 * T;
     uint8_t *red = ws + static_cast<long long>(R) * R * seg * kTile;
+    const auto recv_tile = [&](long long t, int j) {  // owner(t)'s copy of sender j's tile t
+        const long long owner = t / seg;
+        return ws + ((owner * R + j) * seg + (t - owner * seg)) * kTile;
+    };
 
-    // phase 1: sends, tile-major so that early tiles become ready early
-    for (long long u = blockIdx.x; u < R * T; u += gridDim.x) {
-        const long long t = u / R;
-        const int j = static_cast<int>(u - t * R);
-        const long long owner = t / seg;
-        uint8_t *dst = ws + ((owner * R + j) * seg + (t - owner * seg)) * kTile;
-        uint32_t raw[16];
-        load_block_values(static_cast<const uint16_t *>(row_pointer(x.p, j)), t * kTileValues + 32 * k, n, raw);
-        float2 v[16], f[16];
-        widen_block<DT>(raw, v);
-        const BlockScale2 sc = block_scale2<B>(block_absmax(v));
-        quantize_block_magic<B>(v, sc.r, sc.low_clip, f);
-        BlockWords<B> c;
-        pack_block<B>(f, c);
-        store_block_codes<B>(dst, k, c);
-        store_block_scale<B>(dst, k, sc.bits);
-        __syncthreads();
-        if (k == 0) add_release(&sent[t], 1u);
-    }
-    // phase 2: each owner's reduction of its tiles, as their copies arrive
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        if (!cta_wait(&sent[t], R, abort_word, timeouts)) return;
-        const long long owner = t / seg;
-        BlockWords<B> c[R];
-        uint32_t sb[R];
+    // phase 1: sends, chunk-major so that early chunks become ready early
+    for (long long u = blockIdx.x; u < R * chunks; u += gridDim.x) {
+        const long long c = u / R;
+        const int j = static_cast<int>(u - c * R);
+        const uint16_t *xj = static_cast<const uint16_t *>(row_pointer(x.p, j));
+        uint32_t raw[C][16];
 #pragma unroll
-        for (int j = 0; j < R; ++j)
-            load_block_cg<B>(ws + ((owner * R + j) * seg + (t - owner * seg)) * kTile, k, c[j], sb[j]);
-        reduce_block<B, R>(c, sb, red + t * kTile, k);
-        __syncthreads();
-        if (k == 0) store_release(&reduced[t], 1u);
-    }
-    // phase 3: every rank decodes the gathered wire, tile by tile as it is reduced
-    for (long long u = blockIdx.x; u < R * T; u += gridDim.x) {
-        const long long t = u / R;
-        const int j = static_cast<int>(u - t * R);
-        if (!cta_wait(&reduced[t], 1u, abort_word, timeouts)) return;
-        BlockWords<B> c;
-        uint32_t sb;
-        load_block_cg<B>(red + t * kTile, k, c, sb);
-        const float s = f16_bits_to_float(sb);
-        const float2 s2 = make_float2(s, s);
-        float2 q[16];
-        unpack_block_q<B>(c, q);
-        uint32_t w[16];
+        for (int i = 0; i < C; ++i)
+            if (c * C + i < T) load_block_values(xj, (c * C + i) * kTileValues + 32 * k, n, raw[i]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float2 o = __fmul2_rn(q[i], s2);
-            w[i] = narrow2<DT>(o.x, o.y);
-        }
-        uint16_t *yj = static_cast<uint16_t *>(row_pointer(y.p, j));
-        const long long base = t * kTileValues + 32 * k;
-        if (base + 32 <= n) {
-            if ((reinterpret_cast<uintptr_t>(yj) & 31u) == 0) {  // whole 32-byte sectors per store
-                const uint32_t lo[8] = {w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]};
-                const uint32_t hi[8] = {w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]};
-                st_global32(yj + base, lo);
-                st_global32(yj + base + 16, hi);
-            } else {
-                uint4 *p = reinterpret_cast<uint4 *>(yj + base);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) p[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < C; ++i) {
+            const long long t = c * C + i;
+            if (t < T) {
+                float2 v[16], f[16];
+                widen_block<DT>(raw[i], v);
+                const BlockScale2 sc = block_scale2<B>(block_absmax(v));
+                quantize_block_magic<B>(v, sc.r, sc.low_clip, f);
+                BlockWords<B> cw;
+                pack_block<B>(f, cw);
+                uint8_t *dst = recv_tile(t, j);
+                store_block_codes<B>(dst, k, cw);
+                store_block_scale<B>(dst, k, sc.bits);
             }
-        } else {
+        }
+        __syncthreads();
+        if (k == 0) add_release(&sent[c], 1u);
+    }
+    // phase 2: the owners' reductions, chunk by chunk as the copies arrive
+    for (long long c = blockIdx.x; c < chunks; c += gridDim.x) {
+        if (!cta_wait(&sent[c], R, abort_word, timeouts)) return;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                if (base + 2 * i < n) yj[base + 2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
-                if (base + 2 * i + 1 < n) yj[base + 2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+        for (int i = 0; i < C; ++i) {
+            const long long t = c * C + i;
+            if (t < T) {
+                BlockWords<B> cw[R];
+                uint32_t sb[R];
+#pragma unroll
+                for (int j = 0; j < R; ++j) load_block_cg<B>(recv_tile(t, j), k, cw[j], sb[j]);
+                reduce_block<B, R>(cw, sb, red + t * kTile, k);
+            }
+        }
+        __syncthreads();
+        if (k == 0) store_release(&reduced[c], 1u);
+    }
+    // phase 3: every rank decodes the gathered wire, chunk by chunk as it is reduced
+    for (long long u = blockIdx.x; u < R * chunks; u += gridDim.x) {
+        const long long c = u / R;
+        const int j = static_cast<int>(u - c * R);
+        if (!cta_wait(&reduced[c], 1u, abort_word, timeouts)) return;
+        uint16_t *yj = static_cast<uint16_t *>(row_pointer(y.p, j));
+        const bool y32 = (reinterpret_cast<uintptr_t>(yj) & 31u) == 0;
+        BlockWords<B> cw[C];
+        uint32_t sb[C];
+#pragma unroll
+        for (int i = 0; i < C; ++i)
+            if (c * C + i < T) load_block_cg<B>(red + (c * C + i) * kTile, k, cw[i], sb[i]);
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            const long long t = c * C + i;
+            if (t >= T) continue;
+            const float s = f16_bits_to_float(sb[i]);
+            const float2 s2 = make_float2(s, s);
+            float2 q[16];
+            unpack_block_q<B>(cw[i], q);
+            uint32_t w[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const float2 o = __fmul2_rn(q[m], s2);
+                w[m] = narrow2<DT>(o.x, o.y);
+            }
+            const long long base = t * kTileValues + 32 * k;
+            if (base + 32 <= n) {
+                if (y32) {  // whole 32-byte sectors per store
+                    const uint32_t lo[8] = {w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]};
+                    const uint32_t hi[8] = {w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]};
+                    st_global32(yj + base, lo);
+                    st_global32(yj + base + 16, hi);
+                } else {
+                    uint4 *p = reinterpret_cast<uint4 *>(yj + base);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        p[m] = make_uint4(w[4 * m], w[4 * m + 1], w[4 * m + 2], w[4 * m + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    if (base + 2 * m < n) yj[base + 2 * m] = static_cast<uint16_t>(w[m] & 0xFFFFu);
+                    if (base + 2 * m + 1 < n) yj[base + 2 * m + 1] = static_cast<uint16_t>(w[m] >> 16);
+                }
             }
         }
     }
 }
+
+#ifndef QR_FLAGS_CHUNK_TILES
+#define QR_FLAGS_CHUNK_TILES 2
+#endif
+constexpr int kFlagsChunkTiles = QR_FLAGS_CHUNK_TILES;  // tiles per work unit and per flag
 
 template <int B, int DT, int R>
 static cudaError_t run_flags(const ConstPtrs &xp, long long n, const MutPtrs &yp, uint8_t *ws, uint32_t *flags,
@@ -192,13 +226,14 @@ static cudaError_t run_flags(const ConstPtrs &xp, long long n, const MutPtrs &yp
     if (!timeouts) return err;
     if ((err = cudaMemsetAsync(flags, 0, static_cast<size_t>(2 * T + 1) * sizeof(uint32_t), s)) != cudaSuccess)
         return err;
-    auto kern = twoshot_flags_kernel<B, DT, R>;
+    auto kern = twoshot_flags_kernel<B, DT, R, kFlagsChunkTiles>;
     const int sms = sm_count(&err);
     if (sms <= 0) return err;
     int per_sm = 0;
     if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64, 0)) != cudaSuccess) return err;
     long long grid = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
-    if (grid > R * T) grid = R * T;
+    const long long units = R * ((T + kFlagsChunkTiles - 1) / kFlagsChunkTiles);
+    if (grid > units) grid = units;
     long long nn = n, TT = T;
     ConstPtrs xa = xp;
     MutPtrs ya = yp;

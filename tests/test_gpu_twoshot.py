@@ -158,10 +158,15 @@ def flags_check(bits, dtype, xs, what):
                                   f"{what} owner {k} copy from rank {j}")
     red_off = R * R * seg * tb
     assert_wire_equal(a[red_off: red_off + T * tb], b[red_off: red_off + T * tb], bits, f"{what} gathered wire")
-    # and the protocol ran to completion: every tile saw R sends and one reduction, no abort
+    # and the protocol ran to completion: the per-chunk flags in use (a
+    # prefix of each range) saw R sends and one reduction each, no abort
     off = -(-base // 16) * 16
     words = ws[off: off + 4 * (2 * T + 1)].cpu().numpy().view(np.uint32)
-    assert np.all(words[:T] == R) and np.all(words[T:2 * T] == 1) and words[2 * T] == 0, what
+    sent, reduced = words[:T], words[T:2 * T]
+    used = int(np.count_nonzero(sent))
+    assert used >= 1 and np.all(sent[:used] == R) and np.all(sent[used:] == 0), what
+    assert np.all(reduced[:used] == 1) and np.all(reduced[used:] == 0) and words[2 * T] == 0, what
+    assert used * 8 >= T, what  # chunks of at most 8 tiles cover every tile
     assert qr.qr_wait_timeouts() == 0
 
 
