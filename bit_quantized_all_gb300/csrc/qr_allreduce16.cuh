@@ -15,7 +15,7 @@ static cudaError_t run_allreduce16_r(const ConstPtrs &xp, long long n, void *y, 
     const long long T = (n + kTileValues - 1) / kTileValues;
     if (ctas == 0) {  // the library's choice of kernel
         cudaError_t err = cudaSuccess;
-        if (take_staged(R, n, &err)) return launch_staged<QrTile<B, DT>, R>(xp, n, y, 0, s);
+        if (take_staged(R, n, false, &err)) return launch_staged<QrTile<B, DT>, R>(xp, n, y, 0, s);
         if (err != cudaSuccess) return err;
     }
     auto kern = allreduce16_kernel<B, DT, R>;

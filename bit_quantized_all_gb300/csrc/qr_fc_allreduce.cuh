@@ -18,7 +18,7 @@ static cudaError_t run_fc_allreduce_r(const ConstPtrs &xp, long long n, void *y,
     if constexpr (A32) {
         if (ctas == 0) {  // the library's choice of kernel
             cudaError_t err = cudaSuccess;
-            if (take_staged(R, n, &err)) return launch_staged<FcTile<BRS, BAG, DT>, R>(xp, n, y, 0, s);
+            if (take_staged(R, n, true, &err)) return launch_staged<FcTile<BRS, BAG, DT>, R>(xp, n, y, 0, s);
             if (err != cudaSuccess) return err;
         }
     }

@@ -183,15 +183,20 @@ cudaError_t launch_staged(int R, const ConstPtrs &xp, long long n, void *y, int 
 
 // Where the library's default takes the staged kernel: full tiles per SM from
 // which it was faster than the register-fed kernel in back-to-back launches
-// on GB300 (symmetric INT4, bf16, 2^20..2^27 values per rank).  With R <= 2
-// the register-fed kernel already has enough warps and stays ahead at every
-// size; at R = 3 the staged kernel wins from ~200 tiles per SM, at R >= 4
-// from ~50 (at 2^27 values per rank: +14% at R=4 and R=6, +7% at R=8).
-inline long long staged_min_tiles_per_sm(int R) { return R <= 2 ? -1 : (R == 3 ? 128 : 48); }
+// on GB300 (bf16, 2^20..2^28 values per rank), per codec.
+//   Symmetric (INT4): with R <= 2 the register-fed kernel has warps enough
+//   and stays ahead at every size; R = 3 from ~200 tiles per SM, R >= 4 from
+//   ~50 (at 2^27 values per rank: +14% at R=4 and R=6, +7% at R=8).
+//   Asymmetric group-128: R = 2 from ~200 tiles per SM (at 2^27: 0.91 of the
+//   HBM bandwidth against 0.86, at 2^24 0.63 against 0.69), R >= 3 from ~50.
+inline long long staged_min_tiles_per_sm(int R, bool asymmetric) {
+    if (asymmetric) return R <= 1 ? -1 : (R == 2 ? 128 : 48);
+    return R <= 2 ? -1 : (R == 3 ? 128 : 48);
+}
 
-inline bool take_staged(int R, long long n, cudaError_t *err) {
+inline bool take_staged(int R, long long n, bool asymmetric, cudaError_t *err) {
     *err = cudaSuccess;
-    const long long per_sm = staged_min_tiles_per_sm(R);
+    const long long per_sm = staged_min_tiles_per_sm(R, asymmetric);
     if (per_sm < 0) return false;
     const int sms = sm_count(err);
     return sms > 0 && n / kTileValues >= per_sm * sms;

@@ -331,8 +331,9 @@ qr_status_t qr_fc_decode(int bits, qr_dtype_t dtype, const void *wire, size_t n,
 /* The fused two-shot all-reduce with this codec: reduce-scatter wires at
  * bits_rs, all-gather at bits_ag -- (4,4) INT4, (8,8) INT8, (4,8) the mixed
  * "INT6".  y may equal one of the x[r] exactly (in-place).  Kernel choice as
- * for qr_allreduce (the staged kernel for R >= 4 and at least 48 full tiles
- * per SM, R = 3: 128, with every pointer 32-byte aligned). */
+ * for qr_allreduce, with this codec's thresholds: the staged kernel for
+ * R >= 3 and at least 48 full tiles per SM (R = 2: 128), with every pointer
+ * 32-byte aligned. */
 qr_status_t qr_fc_allreduce(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
                             const void *const *x, size_t n, void *y,
                             qr_stream_t stream);
