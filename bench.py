@@ -381,6 +381,10 @@ def run_sweep(args) -> None:
                                 "reduce": (Rs + 1) * W, "decode": W + 2 * n,
                                 "twoshot": 4 * Rs * n + (3 * Rs + 1) * W, "twoshot_flags": 4 * Rs * n + (3 * Rs + 1) * W}
                     for name, alg in kernel_b.items():
+                        if not times[name]:
+                            print(json.dumps({"sweep": name, "R": Rs, "values_per_rank": n, "bits": bits,
+                                              "not_captured": True}), flush=True)
+                            continue
                         med = statistics.median(times[name])
                         print(json.dumps({
                             "sweep": name, "R": Rs, "values_per_rank": n, "storage": "fp16" if dtype == 0 else "bf16",
@@ -389,7 +393,7 @@ def run_sweep(args) -> None:
                             "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
                             "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps,
-                            "burst": 1 if do_flush else args.burst}), flush=True)
+                            "burst": 1 if do_flush else args.burst, "graph": bool(args.graph)}), flush=True)
                     del wires, red, yu, ws, ys2, wsf, ys3
                 del xs, y
                 torch.cuda.empty_cache()
@@ -409,14 +413,39 @@ def time_arms(arms, args, flush, warm=()):
             fn()
     times = {name: [] for name, _ in arms}
     burst = 1 if flush is not None else max(1, args.burst)
+    graphs = {}
+    if getattr(args, "graph", False):
+        # each arm's `burst` calls captured once and replayed: the time is the
+        # GPU's alone, without the host's per-call overhead
+        side = torch.cuda.Stream()
+        for name, fn in arms:
+            fn()  # first use of every kernel on this device happens outside the capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            try:
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g, stream=side):
+                        for _ in range(burst):
+                            fn()
+                torch.cuda.synchronize()
+                graphs[name] = g
+            except RuntimeError:
+                torch.cuda.synchronize()
+                graphs[name] = None
     for _ in range(args.reps):
         for name, fn in arms:
+            if graphs and graphs[name] is None:
+                continue
             if flush is not None:
                 flush.fill_(1)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            for _ in range(burst):
-                fn()
+            if graphs:
+                graphs[name].replay()
+            else:
+                for _ in range(burst):
+                    fn()
             e1.record()
             e1.synchronize()
             times[name].append(e0.elapsed_time(e1) / burst)
@@ -504,6 +533,8 @@ def main() -> None:
                     help="run the message-size sweep (JSON line per point) instead of the benchmark")
     ap.add_argument("--sweep-sizes", default="", help="comma-separated values per rank for --sweep")
     ap.add_argument("--reps", type=int, default=100, help="launches per sweep point")
+    ap.add_argument("--graph", action="store_true",
+                    help="sweep: capture each arm in a CUDA graph and time replays (GPU time without host overhead)")
     ap.add_argument("--burst", type=int, default=1,
                     help="sweep: back-to-back launches of one arm per timed sample where L2 is not flushed")
     ap.add_argument("--sweep-R", default="2,4,8", help="rank counts for --sweep")
