@@ -1,7 +1,8 @@
-// qr_allreduce16.cuh -- launcher of the 16-values-per-thread fused kernel
-// (allreduce16_kernel), dispatching R to a compile-time constant.  Each
-// qr_allreduce16_b<B>.cu instantiates it for one code width so that the
-// widths compile in parallel.
+// qr_allreduce16.cuh -- launchers of the 16-values-per-thread fused kernels:
+// the register-fed allreduce16_kernel and the staged kernel with QrTile
+// (qr_staged.cuh), and the choice between them; R dispatched to a
+// compile-time constant.  Each qr_allreduce16_b<B>.cu instantiates them for
+// one code width so that the widths compile in parallel.
 #pragma once
 
 #include "qr_kernels.cuh"

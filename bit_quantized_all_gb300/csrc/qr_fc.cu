@@ -1,6 +1,6 @@
 // qr_fc.cu -- launchers of the Flash Communication codec's encode, Phase-1B
-// reduce and decode kernels, and the width-pair dispatch of its fused
-// all-reduce.
+// reduce (register-fed, and the staged kernel with FcReduce) and decode
+// kernels, and the width-pair dispatch of its fused all-reduce.
 #include <cstdint>
 
 #include "qr_kernels_fc.cuh"

@@ -1,7 +1,7 @@
 // qr_fc_allreduce.cuh -- launchers of the fused Flash Communication all-reduce
 // (fc_allreduce_kernel, and the staged kernel with FcTile), R dispatched to a
-// compile-time constant.  Each
-// qr_fc_allreduce_<rs><ag>.cu instantiates one width pair.
+// compile-time constant.  Each qr_fc_allreduce_<rs><ag>.cu instantiates one
+// width pair.
 #pragma once
 
 #include <cstdint>

@@ -1,10 +1,11 @@
-// qr_kernels.cuh -- the fused two-shot kernels, templated on the code width
-// B and the storage type DT (0 = fp16, 1 = bf16).  (The standalone encode,
-// reduce and decode kernels are in qr_kernels32.cuh.)
+// qr_kernels.cuh -- the register-fed fused two-shot kernels, templated on the
+// code width B and the storage type DT (0 = fp16, 1 = bf16), and their
+// per-tile steps as the policy QrTile of the staged kernel (qr_staged.cuh).
+// (The standalone encode, reduce and decode kernels are in qr_kernels32.cuh.)
 //
-// Every kernel is a grid-stride loop over 2048-value tiles; tiles are
-// independent, so any grid size gives the same bytes.  No kernel waits on
-// another CTA, allocates, or uses global scratch memory.
+// Every kernel here is a grid-stride loop over 2048-value tiles; tiles are
+// independent, so any grid size gives the same bytes.  No kernel here waits
+// on another CTA, allocates, or uses global scratch memory.
 #pragma once
 
 #include "qr_device.cuh"

@@ -1,6 +1,8 @@
 // qr_kernels32.cuh -- the standalone encode, Phase-1B reduce and decode
 // kernels: one 32-value block per thread (encode32, reduce32) or two threads
-// per block (decode16, reduce16).
+// per block (decode16, reduce16); and the staged Phase-1B kernel
+// (staged_reduce_kernel, wire tiles brought into shared memory by bulk
+// copies) with the symmetric codec's policy QrReduce.
 //
 // A block's codes are contiguous in each section of the wire tile (slots
 // 4g..4g+3), so a thread reads or writes them with one vector access per

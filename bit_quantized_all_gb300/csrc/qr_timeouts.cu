@@ -1,7 +1,8 @@
 // qr_timeouts.cu -- the library's count of bounded waits that ran out, and a
 // self-test that makes one run out on purpose.
 //
-// Kernels that wait on shared-memory barriers (the staged fused kernel)
+// Kernels that wait (the staged fused and Phase-1B kernels on their CTA's
+// shared-memory barriers, the flag-joined two-shot on other CTAs' flags)
 // give every wait a limit of one second; when a wait runs out the kernel
 // adds one to this per-device counter, stops, and returns, so the context
 // stays usable.  The host reads (and clears) the counter with
