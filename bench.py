@@ -25,6 +25,7 @@ import concurrent.futures as cf
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -261,12 +262,20 @@ FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_pipeline.cuh", "qr_sta
                    "qr_allreduce16_b3.cu", "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_grid.cu")
 
 
-def csrc_hash(files=FUSED16_SOURCES) -> str:
+def _code_only(src: str) -> str:
+    """C/CUDA source without comments and with whitespace collapsed, so that a
+    comment edit does not make a capture of unchanged code look stale."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def csrc_hash(files=None) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "bit_quantized_all_gb300", "csrc")
-    for f in sorted(files):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+    for f in sorted(FUSED16_SOURCES if files is None else files):
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,0 +1,32 @@
+"""Host logic of the benchmark that needs no GPU: the kernel-code hash that
+ties a committed DRAM-traffic capture to the code it was taken on."""
+import json
+
+
+def test_code_only_drops_comments_and_layout():
+    import bench
+    a = "int f(int x) {  // twice x\n  return 2 * x; /* block\n comment */ }\n"
+    b = "int f(int x) {\n    return 2 * x;\n}  // reformatted, new comment\n"
+    assert bench._code_only(a) == bench._code_only(b) == "int f(int x) { return 2 * x; }"
+    assert bench._code_only("return 2 * x;") != bench._code_only("return 3 * x;")
+
+
+def test_traffic_capture_is_tied_to_the_kernel_code(tmp_path, monkeypatch):
+    import bench
+    csrc = tmp_path / "bit_quantized_all_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "k.cuh").write_text("__global__ void k() {}  // v1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "FUSED16_SOURCES", ("k.cuh",))
+    h = bench.csrc_hash(("k.cuh",))
+    rec = {"kern": {"dram_bytes_per_launch": 1234, "csrc_hash": h, "source": "capture"}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.profiled_traffic("kern") == (1234.0, "capture")
+    (csrc / "k.cuh").write_text("// a comment edit only\n__global__ void k() {}\n")
+    assert bench.profiled_traffic("kern")[0] == 1234.0
+    (csrc / "k.cuh").write_text("__global__ void k() { __syncthreads(); }\n")
+    val, why = bench.profiled_traffic("kern")
+    assert val is None and "changed" in why
+    assert bench.profiled_traffic("other")[0] is None
+
