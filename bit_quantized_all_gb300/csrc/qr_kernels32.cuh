@@ -106,21 +106,42 @@ struct BlockWords {
     uint32_t w[kWords];
 };
 
+// Four codes (each the low nibble of a magic float's bit pattern, lanes
+// 0..3) packed little-endian into the low 16 bits of the result, bits above
+// don't-care, by a chain of integer multiply-adds (which run on the FMA pipe
+// and so leave the integer pipe, the bottleneck of Phase-1B, to the rest).
+// A magic float is 0x4B40_0000 + u with u < 16, so its pattern equals u
+// modulo 2^22; the multiplier equals 16 modulo 2^16 (its high half only
+// keeps the compiler from turning it into shifts); so modulo 2^16 the chain
+// is the base-16 Horner scheme u0 + 16 (u1 + 16 (u2 + 16 u3)).
+__device__ __forceinline__ uint32_t nibbles4_lo16(float f0, float f1, float f2, float f3) {
+    constexpr uint32_t kMul = 0x5A5A0010u;
+    uint32_t t = __float_as_uint(f3) * kMul + __float_as_uint(f2);
+    t = t * kMul + __float_as_uint(f1);
+    return t * kMul + __float_as_uint(f0);
+}
+
+// The codes of slot s (lanes 0..7 = f[4s..4s+3] pairwise) as one word with
+// lane j in bits 4j..4j+3 (each code below 16).
+__device__ __forceinline__ uint32_t slot_nibbles(const float2 *f) {
+    return __byte_perm(nibbles4_lo16(f[0].x, f[0].y, f[1].x, f[1].y),
+                       nibbles4_lo16(f[2].x, f[2].y, f[3].x, f[3].y), 0x5410);
+}
+
 // The INT3 fields of slots 2h and 2h+1 from their 16 magic floats (f[4s + m]
 // = lanes 2m, 2m+1 of slot s; the code is each float's low byte): W = the two
 // slots' q2w (slot 2h in bits 0..15), X = their q1w (slot 2h in bits 0..7,
 // slot 2h+1 in 8..15).  The inverse of unpack_pair_q3: the codes go into
-// bytes (even / odd lanes, first / second half of each slot), merge into
-// nibbles, the q2 fields come out with one mask, and the q1 bits, masked to
+// nibbles (even lanes in one word, odd lanes in another) by multiply-add
+// chains, the q2 fields come out with one mask, and the q1 bits, masked to
 // every fourth bit, are gathered by three shift-and-mask steps.
 __device__ __forceinline__ void pack_pair_q3(const float2 (&f)[16], int h, uint32_t &W, uint32_t &X) {
     const int a = 8 * h, b = 8 * h + 4;  // f index of lane 0 of slot 2h, of slot 2h+1
-    const auto u = [](float v) { return __float_as_uint(v); };
-    const uint32_t el = gather_low_bytes(u(f[a].x), u(f[a + 2].x), u(f[b].x), u(f[b + 2].x));          // lanes 0, 4
-    const uint32_t eh = gather_low_bytes(u(f[a + 1].x), u(f[a + 3].x), u(f[b + 1].x), u(f[b + 3].x));  // lanes 2, 6
-    const uint32_t ol = gather_low_bytes(u(f[a].y), u(f[a + 2].y), u(f[b].y), u(f[b + 2].y));          // lanes 1, 5
-    const uint32_t oh = gather_low_bytes(u(f[a + 1].y), u(f[a + 3].y), u(f[b + 1].y), u(f[b + 3].y));  // lanes 3, 7
-    const uint32_t e = el | (eh << 4), o = ol | (oh << 4);  // nibble 4i+m: lane 2m / 2m+1 of slot 2h+i
+    // nibble 4i+m: lane 2m (e) / 2m+1 (o) of slot 2h+i
+    const uint32_t e = __byte_perm(nibbles4_lo16(f[a].x, f[a + 1].x, f[a + 2].x, f[a + 3].x),
+                                   nibbles4_lo16(f[b].x, f[b + 1].x, f[b + 2].x, f[b + 3].x), 0x5410);
+    const uint32_t o = __byte_perm(nibbles4_lo16(f[a].y, f[a + 1].y, f[a + 2].y, f[a + 3].y),
+                                   nibbles4_lo16(f[b].y, f[b + 1].y, f[b + 2].y, f[b + 3].y), 0x5410);
     W = (e & 0x33333333u) | ((o << 2) & 0xCCCCCCCCu);
     uint32_t x = ((e >> 2) & 0x11111111u) | ((o >> 1) & 0x22222222u);
     x = (x | (x >> 2)) & 0x0F0F0F0Fu;
@@ -135,6 +156,9 @@ __device__ __forceinline__ void pack_block(const float2 (&f)[16], BlockWords<B> 
         pack_pair_q3(f, 0, c.w[0], x01);
         pack_pair_q3(f, 1, c.w[1], x23);
         c.w[2] = x01 | (x23 << 16);
+    } else if constexpr (B == 4) {
+#pragma unroll
+        for (int s = 0; s < 4; ++s) c.w[s] = slot_nibbles(&f[4 * s]);
     } else {
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
@@ -143,8 +167,6 @@ __device__ __forceinline__ void pack_block(const float2 (&f)[16], BlockWords<B> 
             if constexpr (B == 8) {
                 c.w[2 * s] = __byte_perm(even, odd, 0x5140);
                 c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
-            } else if constexpr (B == 4) {
-                c.w[s] = even | (odd << 4);
             } else {
                 c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
                 const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
@@ -478,33 +500,30 @@ __global__ void __launch_bounds__(kThreads32) decode16_kernel(const uint8_t *__r
 // Codes of two slots (one half-block) from 16 magic floats f[0..7] (pairs).
 template <int B>
 __device__ __forceinline__ void pack_half(const float2 (&f)[8], HalfWords<B> &c) {
+    if constexpr (B == 4) {
+        c.w[0] = slot_nibbles(&f[0]);
+        c.w[1] = slot_nibbles(&f[4]);
+    } else if constexpr (B == 3) {
+        const uint32_t n0 = slot_nibbles(&f[0]), n1 = slot_nibbles(&f[4]);
+        c.w[0] = compress_2_of_4(n0) | (compress_2_of_4(n1) << 16);
+        c.w[1] = compress_1_of_4(n0 >> 2) | (compress_1_of_4(n1 >> 2) << 8);
+    } else {
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        const uint32_t even = gather_low_bytes(__float_as_uint(f[4 * s].x), __float_as_uint(f[4 * s + 1].x),
-                                               __float_as_uint(f[4 * s + 2].x), __float_as_uint(f[4 * s + 3].x));
-        const uint32_t odd = gather_low_bytes(__float_as_uint(f[4 * s].y), __float_as_uint(f[4 * s + 1].y),
-                                              __float_as_uint(f[4 * s + 2].y), __float_as_uint(f[4 * s + 3].y));
-        if constexpr (B == 8) {
-            c.w[2 * s] = __byte_perm(even, odd, 0x5140);
-            c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
-        } else if constexpr (B == 4) {
-            c.w[s] = even | (odd << 4);
-        } else if constexpr (B == 3) {
-            const uint32_t nib = even | (odd << 4);
-            const uint32_t q2 = compress_2_of_4(nib), q1 = compress_1_of_4(nib >> 2);
-            if (s == 0) {
-                c.w[0] = q2;
-                c.w[1] = q1;
+        for (int s = 0; s < 2; ++s) {
+            const uint32_t even = gather_low_bytes(__float_as_uint(f[4 * s].x), __float_as_uint(f[4 * s + 1].x),
+                                                   __float_as_uint(f[4 * s + 2].x), __float_as_uint(f[4 * s + 3].x));
+            const uint32_t odd = gather_low_bytes(__float_as_uint(f[4 * s].y), __float_as_uint(f[4 * s + 1].y),
+                                                  __float_as_uint(f[4 * s + 2].y), __float_as_uint(f[4 * s + 3].y));
+            if constexpr (B == 8) {
+                c.w[2 * s] = __byte_perm(even, odd, 0x5140);
+                c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
             } else {
-                c.w[0] |= q2 << 16;
-                c.w[1] |= q1 << 8;
+                c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
+                const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
+                const uint32_t q2 = compress_2_of_4(hi);
+                if (s == 0) c.w[2] = q2;
+                else c.w[2] |= q2 << 16;
             }
-        } else {
-            c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
-            const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
-            const uint32_t q2 = compress_2_of_4(hi);
-            if (s == 0) c.w[2] = q2;
-            else c.w[2] |= q2 << 16;
         }
     }
 }
