@@ -702,6 +702,7 @@ __host__ __device__ constexpr int reduce_units_per_thread() { return (R <= 2) ? 
 template <int B>
 struct QrReduce {
     static constexpr int kThreads = 64;
+    static constexpr int kCtaThreads = (B == 4) ? 640 : 512;  // see StagedReduceShape
     static constexpr uint32_t kTileIn = Codec<B>::kTileBytes, kTileOut = Codec<B>::kTileBytes;
     template <int R>
     struct Regs {
@@ -791,18 +792,21 @@ __global__ void __launch_bounds__(P::kThreads * G, 1) staged_reduce_kernel(Const
     }
 }
 
-// Launch shape of the staged Phase-1B kernel: 512 threads (eight groups of 64
-// threads for the symmetric codec),
-// each with as many stages (at most 4) as fit in 200 KiB of shared memory at
-// R * tile-bytes per stage.  Measured on GB300 at 2^27 bf16 values per rank
-// against the register-fed kernels (fraction of the measured HBM bandwidth,
-// 4 / 8 / 12 groups): INT8 R=8 0.96 -> 0.93 / 1.00 / 0.83, R=2 0.76 -> 0.69 /
-// 0.92 / 0.89; INT6 R=8 0.64 -> 0.63 / 0.76 / 0.72; INT4 R=8 0.60 -> 0.54 /
-// 0.67 / 0.69; INT3 R=8 0.34 -> 0.29 / 0.34 / 0.34 (bound by the integer
-// pipe, not by memory: it stays on reduce32_kernel).
+// Launch shape of the staged Phase-1B kernel: P::kCtaThreads threads (groups
+// of P::kThreads), each group with as many stages (at most 4) as fit in
+// 200 KiB of shared memory at R * tile-bytes per stage.  Measured on GB300 at
+// 2^27 bf16 values per rank against the register-fed kernels (fraction of the
+// measured HBM bandwidth, 4 / 8 / 12 groups of 64 threads): INT8 R=8 0.96 ->
+// 0.93 / 1.00 / 0.83, R=2 0.76 -> 0.69 / 0.92 / 0.89; INT6 R=8 0.64 -> 0.63 /
+// 0.76 / 0.72; INT4 R=8 0.60 -> 0.54 / 0.67 / 0.69; INT3 R=8 0.34 -> 0.29 /
+// 0.34 / 0.34 (bound by the integer pipe, not by memory: it stays on
+// reduce32_kernel).  Ten groups (640 threads, 20 warps at up to 96
+// registers) against eight: INT4 +2..4% at R = 2, 4, 8 (latency-bound: more
+// warps hide more), INT6 equal, INT8 -7% at R = 8 (one stage per group left
+// in 200 KiB); so ten for INT4 only.
 template <class P, int R>
 struct StagedReduceShape {
-    static constexpr int kGroups = 512 / P::kThreads;  // 16 warps
+    static constexpr int kGroups = P::kCtaThreads / P::kThreads;
     static constexpr int kFit = (200 * 1024) / (kGroups * R * P::kTileIn);
     static constexpr int kStages = kFit >= 4 ? 4 : (kFit < 1 ? 1 : kFit);
     static constexpr int kSmemBytes = kGroups * kStages * R * P::kTileIn;
