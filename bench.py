@@ -315,7 +315,7 @@ def run_sweep(args) -> None:
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     peak, peak_src = measured_hbm()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     sizes = [int(v) for v in args.sweep_sizes.split(",")] if args.sweep_sizes else SWEEP_SIZES
     dtypes = [{"fp16": workloads.FP16, "bf16": workloads.BF16}[d] for d in args.sweep_dtypes.split(",")]
     ranks = [int(r) for r in args.sweep_R.split(",")]
@@ -401,17 +401,34 @@ def run_sweep(args) -> None:
                             "input_gbs": round(Rs * n * 2 / (med / 1e3) / 1e9, 2),
                             "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
-                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps,
+                            "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None, "fused_equals_unfused": same, "reps": args.reps,
                             "burst": 1 if do_flush else args.burst, "graph": bool(args.graph)}), flush=True)
                     del wires, red, yu, ws, ys2, wsf, ys3
                 del xs, y
                 torch.cuda.empty_cache()
 
 
+class L2Flush:
+    """Evicts the L2 (129 MB) between timed samples: writes one 256 MiB buffer,
+    then reads another.  The read leaves the L2 holding clean lines, so the
+    next timed kernel does not pay for writing back the flush's dirty lines
+    (up to 129 MB, ~19 us of HBM time, which would be charged to a kernel
+    that only reads tens of MB)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self) -> None:
+        self.w.fill_(1)
+        self.r.sum()
+
+
 def time_arms(arms, args, flush, warm=()):
     """Per-arm CUDA-event times (ms per launch sequence), arms interleaved.
-    With `flush` (a buffer larger than L2) it is rewritten before every
-    timed sample and each sample is one launch sequence; without it each
+    With `flush` (an L2Flush) the L2 is evicted before every timed sample
+    and each sample is one launch sequence; without it each
     sample is `args.burst` back-to-back sequences of the same arm (their mean),
     which keeps a kernel's shared-memory configuration from being switched
     by the other arms between launches."""
@@ -447,7 +464,7 @@ def time_arms(arms, args, flush, warm=()):
             if graphs and graphs[name] is None:
                 continue
             if flush is not None:
-                flush.fill_(1)
+                flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             if graphs:
@@ -518,7 +535,7 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                             "median_ms": round(med, 5), "input_gbs": round(Rs * n * 2 / (med / 1e3) / 1e9, 2),
                             "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
-                            "l2_flushed": do_flush, "fused_equals_unfused": same, "reps": args.reps,
+                            "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None, "fused_equals_unfused": same, "reps": args.reps,
                             "burst": 1 if do_flush else args.burst}), flush=True)
                     del wires, red
                 del xs, y, yu, y2
