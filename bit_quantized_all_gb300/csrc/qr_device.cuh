@@ -58,14 +58,8 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     return r;
 }
 
-__device__ __forceinline__ uint32_t ld_u32(const void *p) {
-    return *reinterpret_cast<const uint32_t *>(p);
-}
 __device__ __forceinline__ uint32_t ld_u16(const void *p) {
     return *reinterpret_cast<const uint16_t *>(p);
-}
-__device__ __forceinline__ uint32_t ld_u8(const void *p) {
-    return *reinterpret_cast<const uint8_t *>(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -321,26 +315,6 @@ struct SlotCodes {
     uint32_t a, b;  // B=8: bytes 0-3, 4-7; B=4: word; B=6: q4w, q2w; B=3: q2w, q1w
 };
 
-template <int B>
-__device__ __forceinline__ SlotCodes load_codes(const uint8_t *tile, int k) {
-    SlotCodes c;
-    if constexpr (B == 8) {
-        const uint2 w = *reinterpret_cast<const uint2 *>(tile + 8 * k);
-        c.a = w.x;
-        c.b = w.y;
-    } else if constexpr (B == 4) {
-        c.a = ld_u32(tile + 4 * k);
-        c.b = 0;
-    } else if constexpr (B == 3) {
-        c.a = ld_u16(tile + 2 * k);
-        c.b = ld_u8(tile + 512 + k);
-    } else {
-        c.a = ld_u32(tile + 4 * k);
-        c.b = ld_u16(tile + 1024 + 2 * k);
-    }
-    return c;
-}
-
 // The codes of lanes 0,2,4,6 (`even`) and 1,3,5,7 (`odd`) of a slot, one
 // per byte.
 template <int B>
@@ -360,27 +334,6 @@ __device__ __forceinline__ void slot_even_odd_codes(const SlotCodes c, uint32_t 
         even = (c.a & 0x0F0F0F0Fu) | ((hi & 0x03030303u) << 4);
         odd = ((c.a >> 4) & 0x0F0F0F0Fu) | (((hi >> 4) & 0x03030303u) << 4);
     }
-}
-
-// The 8 signed codes q = u - bias of a slot, as exact floats.
-template <int B>
-__device__ __forceinline__ void unpack_q(const SlotCodes c, float (&q)[8]) {
-    uint32_t even, odd;
-    slot_even_odd_codes<B>(c, even, odd);
-    q[0] = magic_to_q<B>(byte_as_magic<0>(even));
-    q[2] = magic_to_q<B>(byte_as_magic<1>(even));
-    q[4] = magic_to_q<B>(byte_as_magic<2>(even));
-    q[6] = magic_to_q<B>(byte_as_magic<3>(even));
-    q[1] = magic_to_q<B>(byte_as_magic<0>(odd));
-    q[3] = magic_to_q<B>(byte_as_magic<1>(odd));
-    q[5] = magic_to_q<B>(byte_as_magic<2>(odd));
-    q[7] = magic_to_q<B>(byte_as_magic<3>(odd));
-}
-
-template <int B>
-__device__ __forceinline__ float load_scale(const uint8_t *tile, int k) {
-    return __half2float(__ushort_as_half(
-        static_cast<unsigned short>(ld_u16(tile + Codec<B>::kCodeBytes + 2 * (k >> 2)))));
 }
 
 template <int B>
