@@ -138,6 +138,72 @@ def cpu_baseline(xs, budget_s=12.0) -> dict:
                                         f"{dt1:.1f} s"}}
 
 
+def _time_oracle(orc, xs, dtype, bits_list, tiles, threads, min_s=2.0):
+    """Input GB/s and values/s of the oracle's all-reduce over the first
+    `tiles` tiles of every rank (every width in `bits_list`), on `threads`
+    threads each taking a contiguous share of the tiles, repeated until
+    `min_s` seconds have passed."""
+    R_ = len(xs)
+    n = min(tiles * 2048, xs[0].size)
+    per = -(-tiles // threads)
+    spans = [(a * 2048, min(n, (a + per) * 2048)) for a in range(0, tiles, per)]
+    spans = [sp for sp in spans if sp[0] < sp[1]]
+
+    def work(sp):
+        for b in bits_list:
+            orc.allreduce(b, dtype, [x[sp[0]:sp[1]] for x in xs])
+
+    reps, t = 0, time.perf_counter()
+    with cf.ThreadPoolExecutor(len(spans)) as ex:
+        while True:
+            list(ex.map(work, spans))
+            reps += 1
+            dt = time.perf_counter() - t
+            if dt >= min_s:
+                break
+    values = reps * n * R_ * len(bits_list)
+    return values * 2 / dt / 1e9, values / dt, reps, dt, len(spans)
+
+
+def run_cpu_sweep(args) -> None:
+    """The oracle as a CPU baseline on every workload, on one thread and on
+    all the host's cores: one JSON line per (workload, threads).  Large
+    workloads are timed on a prefix sample of their tiles (the oracle's cost
+    per tile does not depend on where the tile is); the sample is drawn with
+    the workload's own seeds, so it is the workload's first tiles."""
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    W = workloads
+    cases = [
+        ("c1: R=2, 4096 fp16 values per rank, crafted blocks", W.C1, None, None),
+        ("c2: R=4, 16x8192 bf16 decode-step activation", W.C2, None, None),
+        ("c3: R=8, 1024x5120 bf16 prefill activation, Student-t", W.C3, None, None),
+        ("c4: R=4, 32x1024x4096 fp16, N(0, 0.5)", W.C4, 4096, None),
+        ("sweep: R=8, 2^27 bf16 values per rank (256 MiB)", dict(R=8, N=1 << 27, dtype=W.BF16, bits=(4, 3)),
+         4096, 5),
+        ("sweep: R=8, 2^29 bf16 values per rank (1 GiB)", dict(R=8, N=1 << 29, dtype=W.BF16, bits=(4, 3)),
+         4096, 5),
+    ]
+    for name, cfg, sample_tiles, seed in cases:
+        T = cfg["N"] // 2048 if cfg["N"] % 2048 == 0 else cfg["N"] // 2048 + 1
+        tiles = T if sample_tiles is None else min(T, sample_tiles)
+        if seed is None and sample_tiles is None:
+            xs = W.ranks(cfg)
+        elif seed is None:  # c4: the first tiles of each rank's draw
+            xs = [W.c4_rank(r)[:tiles * 2048] for r in range(cfg["R"])]
+        else:
+            xs = [W.sweep_rank(r, tiles * 2048, cfg["dtype"], seed) for r in range(cfg["R"])]
+        for threads in (1, cores):
+            gbs, vps, reps, dt, used = _time_oracle(orc, xs, cfg["dtype"], cfg["bits"], tiles, threads)
+            print(json.dumps({"cpu_sweep": name, "R": cfg["R"], "values_per_rank": cfg["N"],
+                              "bits": list(cfg["bits"]), "threads": used, "cores": cores,
+                              "input_gbs": round(gbs, 4), "values_per_s": round(vps, 1),
+                              "sample": f"{'all' if tiles == T else 'first'} {tiles} of {T} tiles per rank, "
+                                        f"every width, {reps} passes in {dt:.1f} s",
+                              "kind": "oracle"}), flush=True)
+
+
 def run_reference(args) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -563,6 +629,8 @@ def main() -> None:
                     help="sweep: capture each arm in a CUDA graph and time replays (GPU time without host overhead)")
     ap.add_argument("--burst", type=int, default=1,
                     help="sweep: back-to-back launches of one arm per timed sample where L2 is not flushed")
+    ap.add_argument("--cpu-sweep", action="store_true",
+                    help="time the CPU oracle on every workload (1 thread and all cores); no GPU")
     ap.add_argument("--sweep-R", default="2,4,8", help="rank counts for --sweep")
     ap.add_argument("--sweep-bits", default="8,6,4,3", help="code widths for --sweep")
     ap.add_argument("--sweep-dtypes", default="fp16,bf16", help="storage types for --sweep")
@@ -571,6 +639,9 @@ def main() -> None:
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.cpu_sweep:
+        run_cpu_sweep(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -1,6 +1,9 @@
 """Host logic of the benchmark that needs no GPU: the kernel-code hash that
-ties a committed DRAM-traffic capture to the code it was taken on."""
+ties a committed DRAM-traffic capture to the code it was taken on, and the
+timing of the CPU oracle used as the CPU baseline."""
 import json
+
+import pytest
 
 
 def test_code_only_drops_comments_and_layout():
@@ -30,3 +33,17 @@ def test_traffic_capture_is_tied_to_the_kernel_code(tmp_path, monkeypatch):
     assert val is None and "changed" in why
     assert bench.profiled_traffic("other")[0] is None
 
+
+
+def test_cpu_sweep_times_the_oracle_on_a_workload():
+    import bench
+    import oracle
+    import workloads
+    oracle.build()
+    xs = workloads.ranks(workloads.C1)
+    gbs, vps, reps, dt, threads = bench._time_oracle(oracle, xs, workloads.FP16, (4, 3), tiles=2, threads=4,
+                                                     min_s=0.05)
+    assert threads == 2  # one thread per tile at most
+    assert reps >= 1 and dt >= 0.05
+    assert vps == pytest.approx(reps * 4096 * 2 * 2 / dt)
+    assert gbs == pytest.approx(vps * 2 / 1e9)
