@@ -493,6 +493,9 @@ class L2Flush:
 
 def time_arms(arms, args, flush, warm=()):
     """Per-arm CUDA-event times (ms per launch sequence), arms interleaved.
+    Before each sample the GPU is given work that outlasts the host's
+    enqueueing of the sample's first call (the L2 eviction, else a short
+    sleep kernel), so the events bracket device time only.
     With `flush` (an L2Flush) the L2 is evicted before every timed sample
     and each sample is one launch sequence; without it each
     sample is `args.burst` back-to-back sequences of the same arm (their mean),
@@ -531,6 +534,10 @@ def time_arms(arms, args, flush, warm=()):
                 continue
             if flush is not None:
                 flush()
+            else:
+                # keep the GPU busy while the host enqueues the sample's first
+                # call, so that the timed interval holds device work only
+                torch.cuda._sleep(1 << 18)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             if graphs:
