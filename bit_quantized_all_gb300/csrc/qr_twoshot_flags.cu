@@ -1,6 +1,6 @@
 // qr_twoshot_flags.cu -- the two-shot all-reduce of qr_twoshot.cu in one
-// cooperative launch, its phases joined by per-tile ready flags instead of
-// launch boundaries: the protocol a multi-GPU version runs between ranks
+// cooperative launch, its phases joined by ready flags (one pair per chunk
+// of C tiles) instead of launch boundaries: the protocol a multi-GPU version runs between ranks
 // (peers store wire tiles into the owner's buffer and raise a flag the owner
 // waits on), here between CTAs of one GPU ([QR] Design Highlights: Phase-1
 // sends, Phase-1B owner reduction, Phase-2 gather; [FC] key machinery).

@@ -212,18 +212,21 @@ qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R,
                                  qr_stream_t stream);
 
 /* The same two-shot exchange in one cooperative launch, its phases joined
- * by per-tile ready flags instead of launch boundaries -- the protocol a
- * multi-GPU version runs between ranks (a sender stores its quantized tile
- * into the owner's buffer and raises the owner's flag; the owner waits for
- * R flags, reduces, and raises the tile's "reduced" flag that the decoders
- * wait for), here between the CTAs of one GPU.  Tiles flow through the
- * three phases as soon as their inputs are ready.  Every y[j] equals
+ * by ready flags instead of launch boundaries -- the protocol a multi-GPU
+ * version runs between ranks (a sender stores its quantized tiles into the
+ * owner's buffer and raises the owner's flag; the owner waits for R
+ * raises, reduces, and raises the "reduced" flag that the decoders wait
+ * for), here between the CTAs of one GPU.  The flags are per chunk of two
+ * consecutive tiles, and chunks flow through the three phases as soon as
+ * their inputs are ready.  Every y[j] equals
  * qr_allreduce's output and the workspace's exchange buffers hold the same
  * bytes as qr_allreduce_twoshot's.
  * `workspace` (device, 16-byte aligned, at least
  * qr_twoshot_flags_workspace_bytes(bits, R, n) bytes) = the two-shot
- * workspace, then, 16-byte aligned, 2T + 1 32-bit flag words that the call
- * zeroes (on `stream`) before its launch.  Every wait on a flag is bounded
+ * workspace, then, 16-byte aligned, 2T + 1 32-bit flag words (T tiles:
+ * "sent" flags from word 0 and "reduced" flags from word T, one word per
+ * chunk used; word 2T is the abort word) that the call zeroes (on
+ * `stream`) before its launch.  Every wait on a flag is bounded
  * (one second); if one runs out the launch counts a timeout (see
  * qr_wait_timeouts), every other wait returns at once, and the outputs are
  * incomplete.  Same arguments, aliasing rules and errors as
