@@ -123,11 +123,15 @@ __global__ void __launch_bounds__(128 * G, 1) staged_allreduce_kernel(ConstPtrs 
 // Launch shape for R ranks: five groups of 128 threads (20 warps: at 96
 // registers a thread, the most that five warps in each of the SM's four
 // register quadrants allow), each with as many stages (at most 4) as fit in
-// 224 KiB of shared memory at R * 4 KiB per stage; each group sums the first
+// 192 KiB of shared memory at R * 4 KiB per stage; each group sums the first
 // R/2 ranks straight from shared memory and copies the other R/2 into
-// registers before it releases the stage.  Measured on GB300 with the
-// symmetric codec at R=8 (2^27 bf16 values per rank, INT4 and INT3,
-// back-to-back launches):
+// registers before it releases the stage.  The 192 KiB bound matters only at
+// R = 5, where two stages (200 KiB) ran at 0.93-0.94 of the copy bandwidth
+// and one stage at 1.00-1.03 (2^27 / 2^28 bf16 values per rank); one stage
+// instead of the most that fit changed R = 4 by < 0.5% and cost R = 3 2-3%,
+// and summing (R+1)/2 ranks from shared memory instead of R/2 helped at no
+// R.  Measured on GB300 with the symmetric codec at R=8 (2^27 bf16 values
+// per rank, INT4 and INT3, back-to-back launches):
 //   groups x early ranks:  5 x 0: 6.65 TB/s   5 x 2: 6.92   5 x 4: 6.99
 //                          5 x 6: 6.84        6 x 4: 6.75   6 x 6: 6.98
 //                          7 x 4: 6.50        7 x 6: 6.65   4 x 4: 6.75
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(128 * G, 1) staged_allreduce_kernel(ConstPtrs 
 template <int R>
 struct StagedShape {
     static constexpr int kGroups = 5;
-    static constexpr int kFit = (224 * 1024) / (kGroups * R * kTileValues * 2);
+    static constexpr int kFit = (192 * 1024) / (kGroups * R * kTileValues * 2);
     static constexpr int kStages = kFit >= 4 ? 4 : kFit;  // per group
     static constexpr int kSmemBytes = kGroups * kStages * R * kTileValues * 2;
     static constexpr int kEarlyRanks = R / 2;  // summed from shared memory before the stage is released
