@@ -803,7 +803,9 @@ __global__ void __launch_bounds__(P::kThreads * G, 1) staged_reduce_kernel(Const
 // reduce32_kernel).  Ten groups (640 threads, 20 warps at up to 96
 // registers) against eight: INT4 +2..4% at R = 2, 4, 8 (latency-bound: more
 // warps hide more), INT6 equal, INT8 -7% at R = 8 (one stage per group left
-// in 200 KiB); so ten for INT4 only.
+// in 200 KiB); so ten for INT4 only.  The asymmetric codec's policy runs five
+// groups of 128 threads (640), 5-10% faster than four at R = 4, 6, 8 for
+// every width pair.
 template <class P, int R>
 struct StagedReduceShape {
     static constexpr int kGroups = P::kCtaThreads / P::kThreads;

@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kThreadsFc) fc_reduce_kernel(ConstPtrs wires, 
 template <int BIN, int BOUT>
 struct FcReduce {
     static constexpr int kThreads = kThreadsFc;
-    static constexpr int kCtaThreads = 512;
+    static constexpr int kCtaThreads = 640;  // five groups: 5-10% over four at R = 4..8
     static constexpr uint32_t kTileIn = FcCodec<BIN>::kTileBytes, kTileOut = FcCodec<BOUT>::kTileBytes;
     template <int R>
     struct Regs {
