@@ -569,9 +569,11 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                     Wi, Wo = qr.qr_fc_wire_bytes(brs, n), qr.qr_fc_wire_bytes(bag, n)
                     wires = [torch.empty(Wi, dtype=torch.uint8, device=dev) for _ in range(Rs)]
                     red = torch.empty(Wo, dtype=torch.uint8, device=dev)
+                    red2 = torch.empty(Wo, dtype=torch.uint8, device=dev)
                     fused_b = 2 * Rs * n + 2 * n
                     kernel_b = {"fused": fused_b, "fused_regs": fused_b, "unfused": fused_b + 2 * Rs * Wi + 2 * Wo,
-                                "encode": Rs * (2 * n + Wi), "reduce": Rs * Wi + Wo, "decode": Wo + 2 * n}
+                                "encode": Rs * (2 * n + Wi), "reduce": Rs * Wi + Wo,
+                                "reduce_staged": Rs * Wi + Wo, "decode": Wo + 2 * n}
                     do_flush = fused_b < (512 << 20)
 
                     def fused():
@@ -587,6 +589,9 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                     def reduce_only():
                         qr.qr_fc_segment_reduce(brs, bag, wires, n, out=red)
 
+                    def reduce_staged():  # the staged Phase-1B kernel at any size
+                        qr.qr_fc_segment_reduce(brs, bag, wires, n, out=red2, staged=True)
+
                     def decode_only():
                         qr.qr_fc_decode(bag, red, n, y=yu)
 
@@ -596,10 +601,12 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                         decode_only()
 
                     arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
-                            ("encode", encode_all), ("reduce", reduce_only), ("decode", decode_only))
-                    times = time_arms(arms, args, flush if do_flush else None, warm=(fused, fused_regs, unfused))
+                            ("encode", encode_all), ("reduce", reduce_only), ("reduce_staged", reduce_staged),
+                            ("decode", decode_only))
+                    times = time_arms(arms, args, flush if do_flush else None,
+                                      warm=(fused, fused_regs, unfused, reduce_staged))
                     same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
-                        torch.equal(y.view(torch.int16), y2.view(torch.int16)))
+                        torch.equal(y.view(torch.int16), y2.view(torch.int16))) and bool(torch.equal(red, red2))
                     for name, alg in kernel_b.items():
                         med = statistics.median(times[name])
                         print(json.dumps({
@@ -610,7 +617,7 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
                             "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None, "fused_equals_unfused": same, "reps": args.reps,
                             "burst": 1 if do_flush else args.burst}), flush=True)
-                    del wires, red
+                    del wires, red, red2
                 del xs, y, yu, y2
                 torch.cuda.empty_cache()
 

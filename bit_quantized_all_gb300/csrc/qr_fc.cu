@@ -53,23 +53,34 @@ static cudaError_t run_fc_reduce_staged_t(const ConstPtrs &w, long long n, void 
     return cudaGetLastError();
 }
 
-// Where the default takes the staged Phase-1B kernel: from 48 tiles per SM,
-// for R >= 6, or R >= 4 with 8-bit input wires.  Measured on GB300 at 2^27
-// bf16 values per rank (fraction of the measured HBM bandwidth, register-fed
-// -> staged): R=8 4->4 0.38 -> 0.47, 4->8 0.45 -> 0.53, 8->8 0.72 -> 0.94;
-// R=4 4->4 0.44 -> 0.41, 4->8 0.49 -> 0.49, 8->8 0.73 -> 0.79; R=2 4->4 0.47
-// -> 0.34, 8->8 0.79 -> 0.66 (with few ranks the decode arithmetic, not the
-// memory latency, bounds the kernel, and the register-fed grid has more warps).
-constexpr long long kStagedFcReduceMinTilesPerSm = 48;
+// Where the default takes the staged Phase-1B kernel (tiles per SM from which
+// it does; 0 = never).  Measured on GB300 with bf16 messages, register-fed
+// against staged (five groups), fraction of the measured HBM bandwidth:
+//   R >= 6, and 8-bit inputs at R = 4, 5: staged from 48 (R=8 at 2^27: 4->4
+//     0.38 -> 0.53, 4->8 0.45 -> 0.58, 8->8 0.72 -> 1.00);
+//   R = 5 with 4-bit inputs, R = 4 with 4->8, R = 3 with 8->8: staged from 96
+//     (at 108 tiles per SM: 0.40 -> 0.45, 0.46 -> 0.49, 0.63 -> 0.70; at 54
+//     the register-fed kernel was 10-25% faster);
+//   otherwise (R <= 2; R = 3 with 4-bit inputs; R = 4 with 4->4) never: the
+//     decode arithmetic of few ranks, not memory latency, bounds the kernel
+//     and the register-fed grid has more warps (R=2 4->4 at 2^27: 0.50 ->
+//     0.39; R=4 4->4 within 3% either way from 2^26).
+template <int BIN, int BOUT, int R>
+__host__ __device__ constexpr long long staged_fc_reduce_min_tiles_per_sm() {
+    if (R >= 6 || (BIN == 8 && R >= 4)) return 48;
+    if ((BIN == 4 && R == 5) || (BIN == 4 && BOUT == 8 && R == 4) || (BIN == 8 && R == 3)) return 96;
+    return 0;
+}
 
 template <int BIN, int BOUT, int R>
 static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
     const long long T = (n + kTileValues - 1) / kTileValues;
-    if constexpr (R >= 6 || (BIN == 8 && R >= 4)) {
+    constexpr long long kMinTilesPerSm = staged_fc_reduce_min_tiles_per_sm<BIN, BOUT, R>();
+    if constexpr (kMinTilesPerSm > 0) {
         cudaError_t e = cudaSuccess;
         const int sms = sm_count(&e);
         if (sms <= 0) return e;
-        if (T >= kStagedFcReduceMinTilesPerSm * sms) return run_fc_reduce_staged_t<BIN, BOUT, R>(w, n, out, 0, s);
+        if (T >= kMinTilesPerSm * sms) return run_fc_reduce_staged_t<BIN, BOUT, R>(w, n, out, 0, s);
     }
     auto kern = fc_reduce_kernel<BIN, BOUT, R>;
     cudaError_t err = cudaSuccess;
