@@ -331,3 +331,47 @@ def test_cuda_graph_replay(tiles_per_sm):
         torch.cuda.synchronize()
         assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
     assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("tiles_per_sm", [2, 60])  # register-fed / staged fused kernel
+@pytest.mark.parametrize("codec", ["qr", "fc"])
+def test_dependent_calls_back_to_back(tiles_per_sm, codec):
+    """A chain of all-reduces on one stream, each reading the previous one's
+    output and the last one writing over an input the previous call read,
+    launched back to back (the fused kernels may start while the previous
+    kernel finishes): equal to the same chain with the host waiting between
+    calls."""
+    R = 4
+    n = tiles_per_sm * _sms() * 2048 + 5
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234 + tiles_per_sm)
+    xs0 = [(torch.randn(n, device="cuda", generator=gen) * (r + 1)).to(torch.bfloat16) for r in range(R)]
+
+    def call(xs, y):
+        if codec == "qr":
+            return qr.qr_allreduce(4, xs, y=y)
+        return qr.qr_fc_allreduce(4, 8, xs, y=y)
+
+    def chain(sync):
+        xs = [x.clone() for x in xs0]
+        outs = []
+        y = call(xs, None)
+        for step in range(4):
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(y)
+            xs = [y] + xs[1:]
+            # the last step writes its output over xs[1], which the step before read
+            y = call(xs, xs[1] if step == 3 else None)
+        if sync:
+            torch.cuda.synchronize()
+        outs.append(y)
+        torch.cuda.synchronize()
+        return [o.clone() for o in outs]
+
+    ref = chain(True)
+    for _ in range(3):
+        got = chain(False)
+        for a, b in zip(ref, got):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert qr.qr_wait_timeouts() == 0
