@@ -428,9 +428,9 @@ def qr_allreduce_twoshot(bits: int, xs, ys=None, workspace: torch.Tensor | None 
                          flags: bool = False):
     """The two-shot all-reduce with its exchange laid out per rank and per
     owner in `workspace`: returns (the R outputs, the workspace).  With
-    `flags`, the one-launch version whose phases are joined by per-tile
-    ready flags (qr_allreduce_twoshot_flags; its workspace also holds the
-    2T + 1 flag words)."""
+    `flags`, the one-launch version whose phases are joined by ready flags,
+    one pair per two-tile chunk (qr_allreduce_twoshot_flags; its workspace
+    also holds the 2T + 1 flag words)."""
     xs, dt, n = _check_inputs(xs)
     R = len(xs)
     dev = _same_device(xs, "qr_allreduce_twoshot")

@@ -91,6 +91,42 @@ def sweep_rank(r: int, n: int, dtype: int, seed: int = 5) -> np.ndarray:
     return to_bits(x, dtype)
 
 
+def fuzz_case(seed: int) -> dict:
+    """A random case for the fuzz tests: rank count, size, width, storage
+    type and R seeded messages mixing plain Gaussian blocks at a random
+    scale, heavy-tailed values, all-zero and constant blocks and lone
+    outliers."""
+    rng = _rng(7000 + seed)
+    R = int(rng.integers(1, 9))
+    kind = rng.integers(0, 10)
+    if kind < 5:
+        n = int(rng.integers(1, 6000))
+    elif kind < 9:
+        n = int(rng.integers(6000, 80000))
+    else:
+        n = int(rng.integers(1 << 20, (1 << 20) + 5000))
+    dtype = int(rng.integers(0, 2))
+    scale = float(10.0 ** rng.uniform(-3, 3))
+    xs = []
+    for _ in range(R):
+        if rng.random() < 0.3:
+            x = rng.standard_t(3.0, size=n).astype(np.float32) * scale
+        else:
+            x = rng.standard_normal(n, dtype=np.float32) * scale
+        blocks = (n + 31) // 32
+        for _ in range(int(rng.integers(0, 4))):
+            g = int(rng.integers(0, blocks))
+            x[32 * g: 32 * g + 32] = 0.0
+        for _ in range(int(rng.integers(0, 4))):
+            g = int(rng.integers(0, blocks))
+            x[32 * g: 32 * g + 32] = np.float32(rng.standard_normal() * scale)
+        for _ in range(int(rng.integers(0, 4))):
+            x[int(rng.integers(0, n))] = np.float32(rng.choice([-1, 1]) * scale * 10.0 ** rng.uniform(1, 3))
+        xs.append(to_bits(x, dtype))
+    return dict(R=R, n=n, dtype=dtype, bits=int(rng.choice([8, 6, 4, 3])),
+                fc=((4, 4), (4, 8), (8, 8))[int(rng.integers(0, 3))], xs=xs)
+
+
 def ranks(cfg: dict) -> list[np.ndarray]:
     gen = {"c1": c1_rank, "c2": c2_rank, "c3": c3_rank, "c4": c4_rank}[cfg["name"]]
     return [gen(r) for r in range(cfg["R"])]
