@@ -4,7 +4,8 @@ bf16, and messages that mix Gaussian and heavy-tailed values at scales from
 1e-3 to 1e3 with all-zero blocks, constant blocks and lone outliers
 (workloads.fuzz_case).  Every path: the fused kernel as the library picks
 it and forced onto the staged kernel, encode / Phase-1B / decode with their
-wires, the three-launch and the flag-joined two-shot, and the asymmetric
+wires, the three-launch and the flag-joined two-shot, random grid sizes,
+16-byte-aligned buffers, the wire-emitting variant, and the asymmetric
 codec's fused path."""
 import numpy as np
 import pytest
@@ -67,4 +68,47 @@ def test_asymmetric_codec_fused(seed):
     xs_dev = [to_dev(x, dt) for x in xs]
     y = to_host_u16(qr.qr_fc_allreduce(brs, bag, xs_dev))
     assert_outputs_match(y, y_ref, dt, xmax_of(xs, dt), what)
+    assert qr.qr_wait_timeouts() == 0
+
+
+def _offset_by_16_bytes(x: torch.Tensor) -> torch.Tensor:
+    """x's values in a buffer that starts 16 bytes past a 32-byte boundary."""
+    buf = torch.empty(x.numel() + 16, dtype=x.dtype, device=x.device)
+    v = buf[8: 8 + x.numel()]
+    assert v.data_ptr() % 32 == 16
+    v.copy_(x)
+    return v
+
+
+@pytest.mark.parametrize("seed", CASES)
+def test_symmetric_codec_launch_shapes_alignment_and_emission(seed):
+    """The same cases on random grid sizes, on 16-byte (not 32-byte) aligned
+    buffers, and through the variant that also writes the Phase-1 and
+    reduced wires."""
+    c = workloads.fuzz_case(seed)
+    R, n, dt, bits, xs = c["R"], c["n"], c["dtype"], c["bits"], c["xs"]
+    what = f"seed {seed}: R={R} n={n} dtype={dt} bits={bits}"
+    rng = np.random.Generator(np.random.PCG64(9000 + seed))
+    xmax = xmax_of(xs, dt)
+    y_ref = oracle.allreduce(bits, dt, xs)
+    xs_dev = [to_dev(x, dt) for x in xs]
+
+    ctas = int(rng.integers(1, 2000))
+    assert_outputs_match(to_host_u16(qr.qr_allreduce(bits, xs_dev, ctas=ctas)), y_ref, dt, xmax,
+                         f"{what} register-fed, {ctas} CTAs")
+    ctas = int(rng.integers(1, 200))
+    assert_outputs_match(to_host_u16(qr.qr_allreduce_staged(bits, xs_dev, ctas=ctas)), y_ref, dt, xmax,
+                         f"{what} staged, {ctas} CTAs")
+
+    xs16 = [_offset_by_16_bytes(x) for x in xs_dev]
+    y16 = _offset_by_16_bytes(torch.zeros_like(xs_dev[0]))
+    qr.qr_allreduce(bits, xs16, y=y16)
+    assert_outputs_match(to_host_u16(y16), y_ref, dt, xmax, what + " 16-byte aligned")
+
+    y, wires, red = qr.qr_allreduce_emit(bits, xs_dev)
+    assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, what + " emit")
+    w_ref = [oracle.encode(bits, dt, x) for x in xs]
+    for r in range(R):
+        assert_wire_equal(to_host_u8(wires[r]), w_ref[r], bits, f"{what} emitted wire {r}")
+    assert_wire_equal(to_host_u8(red), oracle.segment_reduce(bits, w_ref, n), bits, what + " emitted reduced wire")
     assert qr.qr_wait_timeouts() == 0
