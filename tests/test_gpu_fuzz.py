@@ -59,15 +59,35 @@ def test_symmetric_codec_every_path(seed):
 
 
 @pytest.mark.parametrize("seed", CASES)
-def test_asymmetric_codec_fused(seed):
+def test_asymmetric_codec_every_path(seed):
     c = workloads.fuzz_case(seed)
     R, n, dt, xs = c["R"], c["n"], c["dtype"], c["xs"]
     brs, bag = c["fc"]
     what = f"seed {seed}: R={R} n={n} dtype={dt} widths {brs}->{bag}"
+    rng = np.random.Generator(np.random.PCG64(11000 + seed))
+    xmax = xmax_of(xs, dt)
     y_ref = oracle.fc_allreduce(brs, bag, dt, xs)
+    w_ref = [oracle.fc_encode(brs, dt, x) for x in xs]
+    red_ref = oracle.fc_segment_reduce(brs, bag, w_ref, n)
     xs_dev = [to_dev(x, dt) for x in xs]
-    y = to_host_u16(qr.qr_fc_allreduce(brs, bag, xs_dev))
-    assert_outputs_match(y, y_ref, dt, xmax_of(xs, dt), what)
+
+    assert_outputs_match(to_host_u16(qr.qr_fc_allreduce(brs, bag, xs_dev)), y_ref, dt, xmax, what + " fused")
+    ctas = int(rng.integers(1, 2000))
+    assert_outputs_match(to_host_u16(qr.qr_fc_allreduce(brs, bag, xs_dev, ctas=ctas)), y_ref, dt, xmax,
+                         f"{what} register-fed, {ctas} CTAs")
+    ctas = int(rng.integers(0, 200))
+    assert_outputs_match(to_host_u16(qr.qr_fc_allreduce_staged(brs, bag, xs_dev, ctas=ctas)), y_ref, dt, xmax,
+                         f"{what} staged, {ctas} CTAs")
+
+    wires = [qr.qr_fc_encode(brs, x) for x in xs_dev]
+    for r in range(R):
+        assert np.array_equal(to_host_u8(wires[r]), w_ref[r]), f"{what} wire {r}"
+    red = qr.qr_fc_segment_reduce(brs, bag, wires, n)
+    assert np.array_equal(to_host_u8(red), red_ref), what + " reduced wire"
+    red_st = qr.qr_fc_segment_reduce(brs, bag, wires, n, staged=True)
+    assert np.array_equal(to_host_u8(red_st), red_ref), what + " reduced wire (staged)"
+    y_u = qr.qr_fc_decode(bag, red, n, dtype=xs_dev[0].dtype)
+    assert_outputs_match(to_host_u16(y_u), y_ref, dt, xmax, what + " unfused")
     assert qr.qr_wait_timeouts() == 0
 
 
