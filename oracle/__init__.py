@@ -84,6 +84,18 @@ def _bind(path: str) -> ctypes.CDLL:
         "orc_fc_decode": (i32, [i32, i32, u8p, sz, u16p]),
         "orc_fc_segment_reduce": (i32, [i32, i32, i32, ctypes.POINTER(u8p), sz, u8p]),
         "orc_fc_allreduce": (i32, [i32, i32, i32, i32, ctypes.POINTER(u16p), sz, u16p]),
+        "orc_fp4_value": (ctypes.c_float, [ctypes.c_uint8]),
+        "orc_fp4_round": (ctypes.c_uint8, [ctypes.c_float]),
+        "orc_fp4_round_n": (None, [f32p, sz, u8p]),
+        "orc_fp4_tile_bytes": (sz, []),
+        "orc_fp4_wire_bytes": (sz, [sz]),
+        "orc_fp4_quantize_block": (i32, [f32p, u8p, u16p]),
+        "orc_fp4_encode_f32": (i32, [f32p, sz, u8p]),
+        "orc_fp4_encode": (i32, [i32, u16p, sz, u8p]),
+        "orc_fp4_decode_f32": (i32, [u8p, sz, f32p]),
+        "orc_fp4_decode": (i32, [i32, u8p, sz, u16p]),
+        "orc_fp4_segment_reduce": (i32, [i32, ctypes.POINTER(u8p), sz, u8p]),
+        "orc_fp4_allreduce": (i32, [i32, i32, ctypes.POINTER(u16p), sz, u16p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -343,4 +355,88 @@ def fc_allreduce(bits_rs: int, bits_ag: int, dtype: int, xs) -> np.ndarray:
     y = np.empty(n, np.uint16)
     _check(lib().orc_fc_allreduce(bits_rs, bits_ag, dtype, len(xs), arr, n, _p(y, ctypes.c_uint16)),
            "fc_allreduce")
+    return y
+
+
+# ---- the FP4 (E2M1) codec: the INT4 block framework with E2M1 elements -----
+
+def fp4_value(code: int) -> float:
+    return float(lib().orc_fp4_value(code))
+
+
+def fp4_round(t: float) -> int:
+    return int(lib().orc_fp4_round(float(t)))
+
+
+def fp4_round_n(t) -> np.ndarray:
+    t = np.ascontiguousarray(t, dtype=np.float32).reshape(-1)
+    c = np.empty(t.size, np.uint8)
+    lib().orc_fp4_round_n(_p(t, ctypes.c_float), t.size, _p(c, ctypes.c_uint8))
+    return c
+
+
+def fp4_tile_bytes() -> int:
+    return int(lib().orc_fp4_tile_bytes())
+
+
+def fp4_wire_bytes(n: int) -> int:
+    return int(lib().orc_fp4_wire_bytes(n))
+
+
+def fp4_quantize_block(x):
+    """(codes, fp16 scale bits) of one 32-value block."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    assert x.size == 32
+    c = np.empty(32, np.uint8)
+    sh = np.zeros(1, np.uint16)
+    _check(lib().orc_fp4_quantize_block(_p(x, ctypes.c_float), _p(c, ctypes.c_uint8), _p(sh, ctypes.c_uint16)),
+           "fp4_quantize_block")
+    return c, int(sh[0])
+
+
+def fp4_encode_f32(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    w = np.empty(fp4_wire_bytes(x.size), np.uint8)
+    _check(lib().orc_fp4_encode_f32(_p(x, ctypes.c_float), x.size, _p(w, ctypes.c_uint8)), "fp4_encode_f32")
+    return w
+
+
+def fp4_encode(dtype: int, x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.uint16).reshape(-1)
+    w = np.empty(fp4_wire_bytes(x.size), np.uint8)
+    _check(lib().orc_fp4_encode(dtype, _p(x, ctypes.c_uint16), x.size, _p(w, ctypes.c_uint8)), "fp4_encode")
+    return w
+
+
+def fp4_decode_f32(wire, n: int) -> np.ndarray:
+    wire = np.ascontiguousarray(wire, dtype=np.uint8)
+    assert wire.size >= fp4_wire_bytes(n)
+    out = np.empty(n, np.float32)
+    _check(lib().orc_fp4_decode_f32(_p(wire, ctypes.c_uint8), n, _p(out, ctypes.c_float)), "fp4_decode_f32")
+    return out
+
+
+def fp4_decode(dtype: int, wire, n: int) -> np.ndarray:
+    wire = np.ascontiguousarray(wire, dtype=np.uint8)
+    assert wire.size >= fp4_wire_bytes(n)
+    y = np.empty(n, np.uint16)
+    _check(lib().orc_fp4_decode(dtype, _p(wire, ctypes.c_uint8), n, _p(y, ctypes.c_uint16)), "fp4_decode")
+    return y
+
+
+def fp4_segment_reduce(wires, n: int) -> np.ndarray:
+    wires = [np.ascontiguousarray(w, dtype=np.uint8) for w in wires]
+    arr = (ctypes.POINTER(ctypes.c_uint8) * len(wires))(*[_p(w, ctypes.c_uint8) for w in wires])
+    out = np.empty(fp4_wire_bytes(n), np.uint8)
+    _check(lib().orc_fp4_segment_reduce(len(wires), arr, n, _p(out, ctypes.c_uint8)), "fp4_segment_reduce")
+    return out
+
+
+def fp4_allreduce(dtype: int, xs) -> np.ndarray:
+    xs = [np.ascontiguousarray(x, dtype=np.uint16).reshape(-1) for x in xs]
+    n = xs[0].size
+    assert all(x.size == n for x in xs)
+    arr = (ctypes.POINTER(ctypes.c_uint16) * len(xs))(*[_p(x, ctypes.c_uint16) for x in xs])
+    y = np.empty(n, np.uint16)
+    _check(lib().orc_fp4_allreduce(dtype, len(xs), arr, n, _p(y, ctypes.c_uint16)), "fp4_allreduce")
     return y

@@ -678,3 +678,200 @@ done:
     free(red);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The FP4 codec [QR introduction: a hardware-accelerated FP4 quantization   */
+/* path on MI355, "FP4 and INT4 are essentially interchangeable"]: the INT4  */
+/* block framework with E2M1 elements in place of the biased integers.      */
+/* ------------------------------------------------------------------------ */
+
+/* The E2M1 magnitudes by code (bits 0..2; bit 3 is the sign): exponent bits
+ * 1..2 with bias 1, one mantissa bit, code 1 subnormal. */
+static const float FP4_GRID[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+float orc_fp4_value(uint8_t code)
+{
+    float v = FP4_GRID[code & 7u];
+    return (code & 8u) ? -v : v;
+}
+
+/* Nearest E2M1 value to t: at or beyond 6 that is 6 (saturation); below,
+ * the grid magnitude closest to |t| (the distances of a float below 6 to
+ * the grid are exact in double wherever two of them can be equal), a tie
+ * going to the even code (mantissa bit 0).  The sign bit is t's sign, so a
+ * negative t that rounds to zero gives code 8 (-0). */
+uint8_t orc_fp4_round(float t)
+{
+    double a = fabs((double)t);
+    int best = 7;
+    if (a < 6.0) {
+        double dbest = a;
+        best = 0;
+        for (int m = 1; m < 8; ++m) {
+            double dm = fabs(a - (double)FP4_GRID[m]);
+            if (dm < dbest || (dm == dbest && (m & 1) == 0 && (best & 1) != 0)) {
+                best = m;
+                dbest = dm;
+            }
+        }
+    }
+    return (uint8_t)((signbit(t) ? 8 : 0) | best);
+}
+
+void orc_fp4_round_n(const float *t, size_t n, uint8_t *code)
+{
+    for (size_t i = 0; i < n; ++i) code[i] = orc_fp4_round(t[i]);
+}
+
+/* One block of 32: A = max|x|; d = fp32_RN(A / 6) (6, the largest E2M1
+ * magnitude, plays the role of |qmin|); s = fp16_RNE(d), saturated at
+ * 65504; s == 0 stores +0 and every code is 0; r = fp32_RN(1/s);
+ * code = orc_fp4_round(fp32_RN(x * r)). */
+int orc_fp4_quantize_block(const float *x, uint8_t *code, uint16_t *scale)
+{
+    int i;
+    float A = 0.0f;
+    for (i = 0; i < BLOCK; ++i) {
+        if (!isfinite(x[i])) return -1;
+        float a = fabsf(x[i]);
+        if (a > A) A = a;
+    }
+    float d = A / 6.0f; /* IEEE fp32 division, rounded to nearest even */
+    uint16_t sh = orc_f32_to_f16(d);
+    if (sh == 0x7C00u) sh = 0x7BFFu;
+    float s = orc_f16_to_f32(sh);
+    if (s == 0.0f) {
+        *scale = 0;
+        for (i = 0; i < BLOCK; ++i) code[i] = 0;
+        return 0;
+    }
+    float r = 1.0f / s;
+    for (i = 0; i < BLOCK; ++i) {
+        float t = x[i] * r;
+        code[i] = orc_fp4_round(t);
+    }
+    *scale = sh;
+    return 0;
+}
+
+/* Tile: the INT4 layout (nibble of lane j at bits 4j of the u32 at 4k, 64
+ * fp16 scales at 1024): 1152 bytes. */
+size_t orc_fp4_tile_bytes(void) { return orc_tile_bytes(4); }
+size_t orc_fp4_wire_bytes(size_t n) { return orc_wire_bytes(4, n); }
+
+static int fp4_encode_tile(const float *x, uint8_t *tile)
+{
+    uint8_t c[TILE];
+    for (int g = 0; g < NBLOCK; ++g) {
+        uint16_t sh;
+        if (orc_fp4_quantize_block(x + BLOCK * g, c + BLOCK * g, &sh) != 0) return -1;
+        put_u16(tile + scale_offset(4) + 2 * (size_t)g, sh);
+    }
+    for (int k = 0; k < NSLOT; ++k) pack_slot(4, c + 8 * k, tile, k);
+    return 0;
+}
+
+/* value(code) * s is exact in fp32: at most 2 significant bits times an
+ * 11-bit significand. */
+static void fp4_decode_tile_f32(const uint8_t *tile, float *out)
+{
+    uint8_t c[TILE];
+    for (int k = 0; k < NSLOT; ++k) unpack_slot(4, tile, k, c + 8 * k);
+    for (int g = 0; g < NBLOCK; ++g) {
+        float s = orc_f16_to_f32((uint16_t)get_u16(tile + scale_offset(4) + 2 * (size_t)g));
+        for (int i = 0; i < BLOCK; ++i) out[BLOCK * g + i] = orc_fp4_value(c[BLOCK * g + i]) * s;
+    }
+}
+
+int orc_fp4_encode_f32(const float *x, size_t n, uint8_t *wire)
+{
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fp4_tile_bytes();
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        for (size_t i = 0; i < TILE; ++i) {
+            size_t idx = t * TILE + i;
+            buf[i] = idx < n ? x[idx] : 0.0f;
+        }
+        if (fp4_encode_tile(buf, wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+int orc_fp4_encode(int dtype, const uint16_t *x, size_t n, uint8_t *wire)
+{
+    if (dtype != ORC_FP16 && dtype != ORC_BF16) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fp4_tile_bytes();
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        for (size_t i = 0; i < TILE; ++i) {
+            size_t idx = t * TILE + i;
+            buf[i] = idx < n ? widen(dtype, x[idx]) : 0.0f;
+        }
+        if (fp4_encode_tile(buf, wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+int orc_fp4_decode_f32(const uint8_t *wire, size_t n, float *out)
+{
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fp4_tile_bytes();
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        fp4_decode_tile_f32(wire + t * tb, buf);
+        for (size_t i = 0; i < TILE && t * TILE + i < n; ++i) out[t * TILE + i] = buf[i];
+    }
+    return 0;
+}
+
+int orc_fp4_decode(int dtype, const uint8_t *wire, size_t n, uint16_t *y)
+{
+    if (dtype != ORC_FP16 && dtype != ORC_BF16) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fp4_tile_bytes();
+    float buf[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        fp4_decode_tile_f32(wire + t * tb, buf);
+        for (size_t i = 0; i < TILE && t * TILE + i < n; ++i) y[t * TILE + i] = narrow(dtype, buf[i]);
+    }
+    return 0;
+}
+
+/* Phase-1B as for the integer codes: decode the R copies, add in fp32 in rank
+ * order, re-quantize. */
+int orc_fp4_segment_reduce(int R, const uint8_t *const *wires, size_t n, uint8_t *out_wire)
+{
+    if (R < 1) return -1;
+    size_t T = (n + TILE - 1) / TILE, tb = orc_fp4_tile_bytes();
+    float acc[TILE], y[TILE];
+    for (size_t t = 0; t < T; ++t) {
+        fp4_decode_tile_f32(wires[0] + t * tb, acc);
+        for (int r = 1; r < R; ++r) {
+            fp4_decode_tile_f32(wires[r] + t * tb, y);
+            for (int i = 0; i < TILE; ++i) acc[i] = acc[i] + y[i];
+        }
+        if (fp4_encode_tile(acc, out_wire + t * tb) != 0) return -1;
+    }
+    return 0;
+}
+
+int orc_fp4_allreduce(int dtype, int R, const uint16_t *const *x, size_t n, uint16_t *y)
+{
+    if (R < 1 || (dtype != ORC_FP16 && dtype != ORC_BF16)) return -1;
+    size_t W = orc_fp4_wire_bytes(n);
+    int rc = -1;
+    uint8_t **wires = (uint8_t **)calloc((size_t)R, sizeof *wires);
+    uint8_t *red = (uint8_t *)malloc(W ? W : 1);
+    if (!wires || !red) goto done;
+    for (int r = 0; r < R; ++r) {
+        wires[r] = (uint8_t *)malloc(W ? W : 1);
+        if (!wires[r]) goto done;
+        if (orc_fp4_encode(dtype, x[r], n, wires[r]) != 0) goto done;
+    }
+    if (orc_fp4_segment_reduce(R, (const uint8_t *const *)wires, n, red) != 0) goto done;
+    rc = orc_fp4_decode(dtype, red, n, y);
+done:
+    if (wires)
+        for (int r = 0; r < R; ++r) free(wires[r]);
+    free(wires);
+    free(red);
+    return rc;
+}

@@ -136,6 +136,34 @@ int orc_fc_segment_reduce(int bits_in, int bits_out, int R, const uint8_t *const
 int orc_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, const uint16_t *const *x,
                      size_t n, uint16_t *y);
 
+/* ---- the FP4 codec --------------------------------------------------------
+ * "QuickReduce INT3 quantization and benchmarking on MI355", introduction: a
+ * hardware-accelerated FP4 quantization path on MI355, with FP4 and INT4
+ * "essentially interchangeable".  The pages give no format; the reading
+ * here keeps the INT4 block framework and tile (32 values per fp16 scale,
+ * nibble of lane j at bits 4j, 1152-byte tiles) with E2M1 elements (sign,
+ * 2 exponent bits with bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6) in place of the biased integers:
+ *   A = max|x|; d = fp32_RN(A / 6); s = fp16_RNE(d) saturated at 65504;
+ *   s == 0 stores +0 and every code is 0; r = fp32_RN(1/s);
+ *   code = nearest E2M1 value to fp32_RN(x * r), ties to the even code,
+ *   saturating at +-6, the sign bit taken from the product (-0 possible);
+ *   decode = value(code) * s (exact in fp32);
+ *   Phase-1B and Phase-2 as for the integer codes.
+ */
+float   orc_fp4_value(uint8_t code);
+uint8_t orc_fp4_round(float t);
+void    orc_fp4_round_n(const float *t, size_t n, uint8_t *code);
+size_t  orc_fp4_tile_bytes(void);              /* 1152 */
+size_t  orc_fp4_wire_bytes(size_t n);
+int orc_fp4_quantize_block(const float *x, uint8_t *code, uint16_t *scale);
+int orc_fp4_encode_f32(const float *x, size_t n, uint8_t *wire);
+int orc_fp4_encode(int dtype, const uint16_t *x, size_t n, uint8_t *wire);
+int orc_fp4_decode_f32(const uint8_t *wire, size_t n, float *out);
+int orc_fp4_decode(int dtype, const uint8_t *wire, size_t n, uint16_t *y);
+int orc_fp4_segment_reduce(int R, const uint8_t *const *wires, size_t n, uint8_t *out_wire);
+int orc_fp4_allreduce(int dtype, int R, const uint16_t *const *x, size_t n, uint16_t *y);
+
 #ifdef __cplusplus
 }
 #endif

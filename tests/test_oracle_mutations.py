@@ -17,6 +17,7 @@ import test_oracle_layout as L
 import test_oracle_quantizer as Q
 import test_oracle_fc as FC
 import test_oracle_reduce as Rd
+import test_oracle_fp4 as P4
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "qr_oracle.c")
 
@@ -72,6 +73,21 @@ MUTATIONS = [
     ("fc_zero_points_at_wrong_offset", [("meta + 64 + 4 * (size_t)g", "meta + 60 + 4 * (size_t)g")]),
     ("fc_reduce_reencodes_at_input_width", [("if (fc_encode_tile(bits_out, acc, out_wire + t * tbo) != 0) return -1;",
                                              "if (fc_encode_tile(bits_in, acc, out_wire + t * tbo) != 0) return -1;")]),
+    # the FP4 codec
+    ("fp4_ties_to_odd", [("(dm == dbest && (m & 1) == 0 && (best & 1) != 0)", "(dm == dbest && (m & 1) != 0)")]),
+    ("fp4_ties_away_from_zero", [("(dm == dbest && (m & 1) == 0 && (best & 1) != 0)", "(dm == dbest)")]),
+    ("fp4_grid_4_read_as_5", [("{0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f}",
+                               "{0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 5.0f, 6.0f}")]),
+    ("fp4_no_saturation_branch", [("    if (a < 6.0) {\n        double dbest = a;", "    if (a < 1e38) {\n        double dbest = a;")]),
+    ("fp4_sign_dropped", [("return (uint8_t)((signbit(t) ? 8 : 0) | best);", "return (uint8_t)best;")]),
+    ("fp4_scale_over_4", [("float d = A / 6.0f;", "float d = A / 4.0f;")]),
+    ("fp4_scale_not_saturated", [("    float d = A / 6.0f; /* IEEE fp32 division, rounded to nearest even */\n"
+                                  "    uint16_t sh = orc_f32_to_f16(d);\n    if (sh == 0x7C00u) sh = 0x7BFFu;",
+                                  "    float d = A / 6.0f; /* IEEE fp32 division, rounded to nearest even */\n"
+                                  "    uint16_t sh = orc_f32_to_f16(d);")]),
+    ("fp4_reduce_reverse_order",
+     [("fp4_decode_tile_f32(wires[0] + t * tb, acc);", "fp4_decode_tile_f32(wires[R - 1] + t * tb, acc);"),
+      ("fp4_decode_tile_f32(wires[r] + t * tb, y);", "fp4_decode_tile_f32(wires[R - 1 - r] + t * tb, y);")]),
 ]
 
 
@@ -115,6 +131,16 @@ def _battery(orc):
     yield lambda: FC.test_two_ranks_commute_and_rank_order(orc)
     for brs, bag in ((4, 8), (8, 8)):
         yield lambda brs=brs, bag=bag: FC.test_error_bound_against_exact_sum(orc, brs, bag, 3)
+    # the FP4 codec
+    yield lambda: P4.test_code_values_against_an_independent_decoder(orc)
+    yield lambda: P4.test_ties_go_to_the_even_code(orc)
+    yield lambda: P4.test_rounding_every_pattern_of_a_dense_range(orc)
+    yield lambda: P4.test_rounding_random_patterns_of_every_magnitude(orc)
+    yield lambda: P4.test_block_scale_against_torch(orc)
+    yield lambda: P4.test_known_answer_block_and_layout(orc)
+    yield lambda: P4.test_rank_order_is_the_order_of_the_fp32_adds(orc)
+    for R in (2, 4):
+        yield lambda R=R: P4.test_identical_ranks_on_exact_grids_scale_by_R(orc, R)
 
 
 @pytest.mark.parametrize("name,edits", MUTATIONS, ids=[m[0] for m in MUTATIONS])
