@@ -41,7 +41,8 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_allreduce_twoshot_static", "qr_wait_timeouts", "qr_selftest_bounded_wait",
            "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas",
            "qr_segment_reduce_staged", "qr_fc_segment_reduce_staged", "qr_twoshot_flags_workspace_bytes",
-           "qr_allreduce_twoshot_flags")
+           "qr_allreduce_twoshot_flags", "qr_fp4_tile_bytes", "qr_fp4_wire_bytes", "qr_fp4_encode",
+           "qr_fp4_decode", "qr_fp4_segment_reduce", "qr_fp4_allreduce")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -101,6 +102,12 @@ def lib() -> ctypes.CDLL:
                 "qr_segment_reduce_staged": (i32, [i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_fc_segment_reduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_selftest_bounded_wait": (i32, [vp]),
+                "qr_fp4_tile_bytes": (sz, []),
+                "qr_fp4_wire_bytes": (sz, [sz]),
+                "qr_fp4_encode": (i32, [i32, vp, sz, vp, vp]),
+                "qr_fp4_decode": (i32, [i32, vp, sz, vp, vp]),
+                "qr_fp4_segment_reduce": (i32, [i32, vpp, sz, vp, i32, vp]),
+                "qr_fp4_allreduce": (i32, [i32, i32, vpp, sz, vp, i32, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -193,6 +200,22 @@ class capi:
     @staticmethod
     def qr_fc_encode(bits, dtype, x, n, wire, stream=None):
         return lib().qr_fc_encode(bits, dtype, x, n, wire, stream)
+
+    @staticmethod
+    def qr_fp4_encode(dtype, x, n, wire, stream=None):
+        return lib().qr_fp4_encode(dtype, x, n, wire, stream)
+
+    @staticmethod
+    def qr_fp4_decode(dtype, wire, n, y, stream=None):
+        return lib().qr_fp4_decode(dtype, wire, n, y, stream)
+
+    @staticmethod
+    def qr_fp4_segment_reduce(R, wires, n, out, ctas, stream=None):
+        return lib().qr_fp4_segment_reduce(R, _ptr_array(wires), n, out, ctas, stream)
+
+    @staticmethod
+    def qr_fp4_allreduce(dtype, R, xs, n, y, ctas, stream=None):
+        return lib().qr_fp4_allreduce(dtype, R, _ptr_array(xs), n, y, ctas, stream)
 
     @staticmethod
     def qr_fc_decode(bits, dtype, wire, n, y, stream=None):
@@ -561,4 +584,85 @@ def qr_fc_allreduce_staged(bits_rs: int, bits_ag: int, xs, y: torch.Tensor | Non
     dev = _same_device(xs + [y], "qr_fc_allreduce_staged")
     _check(capi.qr_fc_allreduce_staged(bits_rs, bits_ag, dt, len(xs), [x.data_ptr() for x in xs], n, y.data_ptr(),
                                        ctas, _stream(dev, stream)), "qr_fc_allreduce_staged")
+    return y
+
+
+# ---------------------------------------------------------------------------
+# the FP4 codec (the INT4 block framework with E2M1 elements)
+# ---------------------------------------------------------------------------
+def qr_fp4_tile_bytes() -> int:
+    return int(lib().qr_fp4_tile_bytes())
+
+
+def qr_fp4_wire_bytes(n: int) -> int:
+    return int(lib().qr_fp4_wire_bytes(n))
+
+
+def _fp4_wire_tensor(t: torch.Tensor, n: int, what: str) -> None:
+    _cuda_contig(t, what)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{what} must be torch.uint8 (a packed wire), got {t.dtype}")
+    need = qr_fp4_wire_bytes(n)
+    if t.numel() < need:
+        raise ValueError(f"{what} holds {t.numel()} bytes; {need} are needed for {n} values at FP4")
+
+
+def qr_fp4_encode(x: torch.Tensor, wire: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Send path of the FP4 codec."""
+    _cuda_contig(x, "x")
+    dt = _dtype_code(x, "x")
+    n = x.numel()
+    if wire is None:
+        wire = torch.empty(qr_fp4_wire_bytes(n), dtype=torch.uint8, device=x.device)
+    _fp4_wire_tensor(wire, n, "wire")
+    _same_device([x, wire], "qr_fp4_encode")
+    _check(capi.qr_fp4_encode(dt, x.data_ptr(), n, wire.data_ptr(), _stream(x.device, stream)), "qr_fp4_encode")
+    return wire
+
+
+def qr_fp4_decode(wire: torch.Tensor, n: int, dtype: torch.dtype = torch.bfloat16,
+                  y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Receive path of the FP4 codec: the first n values of a wire."""
+    _fp4_wire_tensor(wire, n, "wire")
+    if y is None:
+        if dtype not in _DTYPES:
+            raise TypeError(f"dtype must be torch.float16 or torch.bfloat16, got {dtype}")
+        y = torch.empty(n, dtype=dtype, device=wire.device)
+    _cuda_contig(y, "y")
+    dt = _dtype_code(y, "y")
+    if y.numel() != n:
+        raise ValueError(f"y holds {y.numel()} values, expected {n}")
+    _same_device([wire, y], "qr_fp4_decode")
+    _check(capi.qr_fp4_decode(dt, wire.data_ptr(), n, y.data_ptr(), _stream(y.device, stream)), "qr_fp4_decode")
+    return y
+
+
+def qr_fp4_segment_reduce(wires, n: int, out: torch.Tensor | None = None, stream=None,
+                          ctas: int = 0) -> torch.Tensor:
+    """Phase-1B of the FP4 codec (the staged kernel)."""
+    wires = list(wires)
+    if not 1 <= len(wires) <= QR_MAX_RANKS:
+        raise ValueError(f"1 to {QR_MAX_RANKS} wires are supported, got {len(wires)}")
+    for i, w in enumerate(wires):
+        _fp4_wire_tensor(w, n, f"wires[{i}]")
+    if out is None:
+        out = torch.empty(qr_fp4_wire_bytes(n), dtype=torch.uint8, device=wires[0].device)
+    _fp4_wire_tensor(out, n, "out")
+    dev = _same_device(wires + [out], "qr_fp4_segment_reduce")
+    _check(capi.qr_fp4_segment_reduce(len(wires), [w.data_ptr() for w in wires], n, out.data_ptr(), ctas,
+                                      _stream(dev, stream)), "qr_fp4_segment_reduce")
+    return out
+
+
+def qr_fp4_allreduce(xs, y: torch.Tensor | None = None, stream=None, ctas: int = 0) -> torch.Tensor:
+    """The fused FP4 all-reduce (the staged kernel; every tensor 32-byte aligned)."""
+    xs, dt, n = _check_inputs(xs)
+    if y is None:
+        y = torch.empty_like(xs[0])
+    _cuda_contig(y, "y")
+    if y.dtype != xs[0].dtype or y.numel() != n:
+        raise ValueError("y must match the inputs' dtype and size")
+    dev = _same_device(xs + [y], "qr_fp4_allreduce")
+    _check(capi.qr_fp4_allreduce(dt, len(xs), [x.data_ptr() for x in xs], n, y.data_ptr(), ctas,
+                                 _stream(dev, stream)), "qr_fp4_allreduce")
     return y

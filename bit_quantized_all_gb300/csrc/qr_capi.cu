@@ -413,3 +413,68 @@ QR_EXPORT qr_status_t qr_allreduce_ctas(int bits, qr_dtype_t dtype, int R, const
                                         void *y, int ctas, qr_stream_t stream) {
     return allreduce_common(bits, dtype, R, x, n, y, nullptr, nullptr, ctas, stream);
 }
+
+// ---------------------------------------------------------------------------
+// the FP4 codec: the INT4 tile with E2M1 elements
+// ---------------------------------------------------------------------------
+
+QR_EXPORT size_t qr_fp4_tile_bytes(void) { return tile_bytes(4); }
+
+QR_EXPORT size_t qr_fp4_wire_bytes(size_t n) { return wire_bytes(4, n); }
+
+QR_EXPORT qr_status_t qr_fp4_encode(qr_dtype_t dtype, const void *x, size_t n, void *wire, qr_stream_t stream) {
+    if (!x || !wire || n == 0) return QR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return QR_ERR_UNSUPPORTED;
+    const size_t W = wire_bytes(4, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(x) || !aligned16(wire)) return QR_ERR_MISALIGNED;
+    if (overlaps(wire, W, x, 2 * n)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_fp4_encode(dtype, x, static_cast<long long>(n), wire,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_fp4_decode(qr_dtype_t dtype, const void *wire, size_t n, void *y, qr_stream_t stream) {
+    if (!wire || !y || n == 0) return QR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return QR_ERR_UNSUPPORTED;
+    const size_t W = wire_bytes(4, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(wire) || !aligned16(y)) return QR_ERR_MISALIGNED;
+    if (overlaps(y, 2 * n, wire, W)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_fp4_decode(dtype, wire, static_cast<long long>(n), y,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_fp4_segment_reduce(int R, const void *const *wires, size_t n, void *out_wire, int ctas,
+                                            qr_stream_t stream) {
+    if (!wires || !out_wire || n == 0 || R < 1 || ctas < 0) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!wires[r]) return QR_ERR_INVALID_ARG;
+    if (R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    const size_t W = wire_bytes(4, n);
+    if (!value_bytes_ok(n) || W == 0) return QR_ERR_SIZE;
+    if (!aligned16(out_wire)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(wires[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (bad_alias(out_wire, W, wires[r], W)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_fp4_reduce(R, wires, static_cast<long long>(n), out_wire, ctas,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_fp4_allreduce(qr_dtype_t dtype, int R, const void *const *x, size_t n, void *y, int ctas,
+                                       qr_stream_t stream) {
+    if (!x || !y || n == 0 || R < 1 || ctas < 0) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!x[r]) return QR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    if (!value_bytes_ok(n) || wire_bytes(4, n) == 0) return QR_ERR_SIZE;
+    const auto a32 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+    if (!a32(y)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!a32(x[r])) return QR_ERR_MISALIGNED;
+    const size_t V = 2 * n;
+    for (int r = 0; r < R; ++r)
+        if (bad_alias(y, V, x[r], V)) return QR_ERR_INVALID_ARG;
+    return from_cuda(qrk::launch_fp4_allreduce(dtype, R, x, static_cast<long long>(n), y, ctas,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}

@@ -1,0 +1,265 @@
+// qr_kernels_fp4.cuh -- the FP4 codec: the INT4 block framework and tile
+// (32 values per fp16 scale, nibble of lane j at bits 4j of the slot word,
+// 1152-byte tiles) with E2M1 elements in place of the biased integers
+// ([QR] introduction: an FP4 quantization path on MI355, "essentially
+// interchangeable" with INT4; the pages give no format, and this is the
+// library's reading of it, stated in include/qr.h):
+//   s = fp16_RNE(fp32_RN(absmax / 6)) saturated at 65504 (6 is the largest
+//   E2M1 magnitude); s == 0 stores +0 and every code is 0;
+//   r = fp32_RN(1/s); code = the E2M1 value nearest to fp32_RN(x * r), ties
+//   to the even code, saturating at +-6, sign kept (so -0 is a code);
+//   decode = value(code) * s, exact in fp32.
+// The elements go to and from E2M1 with the native conversions
+// (cvt.rn.satfinite.e2m1x2.f32 and cvt.rn.f16x2.e2m1x2, two values each).
+// Kernels: encode (one 32-value block per thread), decode (two threads per
+// block), the Phase-1B policy of the staged reduce kernel, and the per-tile
+// policy of the staged fused kernel.
+#pragma once
+
+#include "qr_kernels32.cuh"
+
+namespace qrk {
+
+struct Fp4Scale {
+    float s, r;
+    uint32_t bits;
+};
+
+__device__ __forceinline__ Fp4Scale fp4_scale(float absmax) {
+    const float d = __fdiv_rn(absmax, 6.0f);
+    uint32_t h = __half_as_ushort(__float2half_rn(d));
+    if (h == 0x7C00u) h = 0x7BFFu;  // the fp16 scale saturates at 65504
+    Fp4Scale sc;
+    sc.bits = h;
+    sc.s = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+    sc.r = (h == 0u) ? 0.0f : __frcp_rn(sc.s);
+    return sc;
+}
+
+// The E2M1 codes of eight values (lanes 0..7) as one slot word, lane j in
+// bits 4j..4j+3.  The conversion puts its first operand in the high nibble.
+__device__ __forceinline__ uint32_t e2m1_word(const float2 &a, const float2 &b, const float2 &c, const float2 &d) {
+    uint32_t w;
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(w)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+    return w;
+}
+
+// The values of a slot word's eight codes, pairwise (q[m] = lanes 2m, 2m+1):
+// the conversion yields both values of a byte as an fp16 pair, low nibble in
+// the low half, exactly.
+__device__ __forceinline__ void e2m1_word_values(uint32_t w, float2 (&q)[4]) {
+    uint32_t h[4];
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int m = 0; m < 4; ++m) q[m] = __half22float2(*reinterpret_cast<const __half2 *>(&h[m]));
+}
+
+// t = fp32_RN(v * r), or +0 for a zero scale (every code 0, not -0).
+__device__ __forceinline__ float2 fp4_scaled(const float2 &v, const Fp4Scale &sc) {
+    const float2 t = __fmul2_rn(v, make_float2(sc.r, sc.r));
+    return sc.bits == 0u ? make_float2(0.0f, 0.0f) : t;
+}
+
+// The codes of n2 = 4 * words value pairs as slot words.
+template <int kWords>
+__device__ __forceinline__ void fp4_quantize(const float2 *v, const Fp4Scale &sc, uint32_t (&w)[kWords]) {
+#pragma unroll
+    for (int k = 0; k < kWords; ++k)
+        w[k] = e2m1_word(fp4_scaled(v[4 * k], sc), fp4_scaled(v[4 * k + 1], sc), fp4_scaled(v[4 * k + 2], sc),
+                         fp4_scaled(v[4 * k + 3], sc));
+}
+
+// ---------------------------------------------------------------------------
+// send path: one 32-value block per thread
+// ---------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kThreads32) fp4_encode_kernel(const uint16_t *__restrict__ x, long long n,
+                                                                uint8_t *__restrict__ wire, long long NB) {
+    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
+    for (long long gb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb < NB; gb += S) {
+        uint32_t raw[16];
+        load_block_values(x, gb * 32, n, raw);
+        float2 v[16];
+        widen_block<DT>(raw, v);
+        const Fp4Scale sc = fp4_scale(block_absmax(v));
+        BlockWords<4> c;
+        fp4_quantize<4>(v, sc, c.w);
+        uint8_t *tile = wire + (gb >> 6) * Codec<4>::kTileBytes;
+        store_block_codes<4>(tile, static_cast<int>(gb & 63), c);
+        store_block_scale<4>(tile, static_cast<int>(gb & 63), sc.bits);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// receive path: two threads per block, 16 values and 32 output bytes each
+// ---------------------------------------------------------------------------
+template <int DT, bool Y32>  // Y32: y is 32-byte aligned (one 256-bit store per thread)
+__global__ void __launch_bounds__(kThreads32) fp4_decode_kernel(const uint8_t *__restrict__ wire, long long n,
+                                                                uint16_t *__restrict__ y, long long NH) {
+    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
+    for (long long hb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb < NH; hb += S) {
+        const long long gb = hb >> 1;
+        const uint8_t *tile = wire + (gb >> 6) * Codec<4>::kTileBytes;
+        HalfWords<4> c;
+        load_half_codes<4>(tile, static_cast<int>(gb & 63), static_cast<int>(hb & 1), c);
+        const float s = f16_bits_to_float(load_block_scale_bits<4>(tile, static_cast<int>(gb & 63)));
+        const float2 s2 = make_float2(s, s);
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            float2 q[4];
+            e2m1_word_values(c.w[k], q);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 o = __fmul2_rn(q[m], s2);
+                w[4 * k + m] = narrow2<DT>(o.x, o.y);
+            }
+        }
+        const long long base = hb * 16;
+        if (base + 16 <= n) {
+            if constexpr (Y32) {
+                st_global32(y + base, w);
+            } else {
+                uint4 *p = reinterpret_cast<uint4 *>(y + base);
+                p[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                p[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (base + 2 * i < n) y[base + 2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+                if (base + 2 * i + 1 < n) y[base + 2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Phase-1B: the policy of staged_reduce_kernel (one 32-value block per thread)
+// ---------------------------------------------------------------------------
+template <int R>
+__device__ __forceinline__ void fp4_reduce_block(const BlockWords<4> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
+                                                 int g) {
+    float2 acc[16];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float s = f16_bits_to_float(sb[r]);
+        const float2 s2 = make_float2(s, s);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float2 q[4];
+            e2m1_word_values(c[r].w[k], q);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                acc[4 * k + m] = (r == 0) ? __fmul2_rn(q[m], s2) : __ffma2_rn(q[m], s2, acc[4 * k + m]);
+        }
+    }
+    const Fp4Scale sc = fp4_scale(block_absmax(acc));
+    BlockWords<4> cw;
+    fp4_quantize<4>(acc, sc, cw.w);
+    store_block_codes<4>(tile, g, cw);
+    store_block_scale<4>(tile, g, sc.bits);
+}
+
+struct Fp4Reduce {
+    static constexpr int kThreads = 64;
+    static constexpr int kCtaThreads = 640;
+    static constexpr uint32_t kTileIn = Codec<4>::kTileBytes, kTileOut = Codec<4>::kTileBytes;
+    template <int R>
+    struct Regs {
+        BlockWords<4> c[R];
+        uint32_t sb[R];
+    };
+    template <int R>
+    static __device__ __forceinline__ void load(const uint8_t *stage, int k, Regs<R> &g) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            load_block_codes<4>(stage + r * kTileIn, k, g.c[r]);
+            g.sb[r] = load_block_scale_bits<4>(stage + r * kTileIn, k);
+        }
+    }
+    template <int R>
+    static __device__ __forceinline__ void reduce(const Regs<R> &g, uint8_t *tile_out, int k, long long, long long) {
+        fp4_reduce_block<R>(g.c, g.sb, tile_out, k);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// the fused all-reduce: the per-tile policy of staged_allreduce_kernel
+// (16 values per thread, two threads per block sharing the absmax)
+// ---------------------------------------------------------------------------
+
+// Quantize 16 values and return their decoded values (without the scale).
+__device__ __forceinline__ void fp4_roundtrip16(const float2 (&v)[8], const Fp4Scale &sc, float2 (&q)[8]) {
+    uint32_t w[2];
+    fp4_quantize<2>(v, sc, w);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float2 qk[4];
+        e2m1_word_values(w[k], qk);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) q[4 * k + m] = qk[m];
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void fp4_accumulate_rank(const uint32_t (&w)[8], float2 (&acc)[8], bool first) {
+    float2 v[8], q[8];
+    widen16<DT>(w, v);
+    const Fp4Scale sc = fp4_scale(pair_absmax(v));
+    fp4_roundtrip16(v, sc, q);
+    const float2 s2 = make_float2(sc.s, sc.s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = first ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[i]);
+}
+
+template <int DT>
+__device__ __forceinline__ void fp4_finish_tile(const float2 (&acc)[8], uint16_t *y, long long base, long long n,
+                                                bool full, bool swapped) {
+    const Fp4Scale sc = fp4_scale(pair_absmax(acc));
+    float2 q[8], o[8];
+    fp4_roundtrip16(acc, sc, q);
+    const float2 s2 = make_float2(sc.s, sc.s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __fmul2_rn(q[i], s2);
+    store16<DT>(y, base, n, full, o, swapped);
+}
+
+template <int DT>
+struct Fp4Tile {
+    static __device__ __forceinline__ void accumulate(const uint32_t (&w)[8], float2 (&acc)[8], bool first) {
+        fp4_accumulate_rank<DT>(w, acc, first);
+    }
+    static __device__ __forceinline__ void finish(const float2 (&acc)[8], uint16_t *y, long long base, long long n,
+                                                  bool swapped) {
+        fp4_finish_tile<DT>(acc, y, base, n, true, swapped);
+    }
+    // Bounds-checked loads of the last, partial tile (not inlined, as for
+    // the symmetric codec's tile).
+    template <int R>
+    static __device__ __noinline__ void ragged(const ConstPtrs &x, long long n, uint16_t *y, long long base) {
+        uint32_t raw[R][8];
+#pragma unroll
+        for (int r = 0; r < R; ++r) load16(static_cast<const uint16_t *>(x.p[r]), base, n, false, raw[r]);
+        float2 acc[8];
+#pragma unroll
+        for (int r = 0; r < R; ++r) fp4_accumulate_rank<DT>(raw[r], acc, r == 0);
+        fp4_finish_tile<DT>(acc, y, base, n, false, false);
+    }
+};
+
+}  // namespace qrk

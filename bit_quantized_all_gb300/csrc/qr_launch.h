@@ -37,6 +37,16 @@ cudaError_t launch_allreduce(int bits, int dtype, int R, const void *const *x, l
                              void *y, void *const *wire_out, void *red_out, int ctas,
                              cudaStream_t s);
 
+// The FP4 codec (qr_fp4.cu): encode, decode, Phase-1B on the staged reduce
+// kernel and the fused all-reduce on the staged fused kernel (every x[r]
+// and y 32-byte aligned), each staged launch with min(ctas or #SMs, #SMs,
+// tiles) persistent CTAs.
+cudaError_t launch_fp4_encode(int dtype, const void *x, long long n, void *wire, cudaStream_t s);
+cudaError_t launch_fp4_decode(int dtype, const void *wire, long long n, void *y, cudaStream_t s);
+cudaError_t launch_fp4_reduce(int R, const void *const *wires, long long n, void *out, int ctas, cudaStream_t s);
+cudaError_t launch_fp4_allreduce(int dtype, int R, const void *const *x, long long n, void *y, int ctas,
+                                 cudaStream_t s);
+
 struct ConstPtrs;
 
 // The 16-values-per-thread fused kernel (every pointer 32-byte aligned, no

@@ -358,6 +358,48 @@ qr_status_t qr_fc_allreduce_staged(int bits_rs, int bits_ag, qr_dtype_t dtype, i
                                    const void *const *x, size_t n, void *y,
                                    int ctas, qr_stream_t stream);
 
+/* ---- the FP4 codec -------------------------------------------------------
+ * "QuickReduce INT3 quantization and benchmarking on MI355", introduction: a
+ * hardware-accelerated FP4 quantization path on MI355, "essentially
+ * interchangeable" with INT4.  The page gives no format; this library reads
+ * it as the INT4 block framework and tile with E2M1 elements (sign, two
+ * exponent bits with bias 1, one mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6) in place of the biased integers:
+ *   per block of 32 values: A = max|x|; d = fp32_RN(A / 6);
+ *   s = fp16_RNE(d), saturated at 65504; s == 0 stores +0 and every code is
+ *   0; r = fp32_RN(1/s); code = the E2M1 value nearest to fp32_RN(x * r),
+ *   ties to the even code, saturating at +-6, the sign kept (-0 is code 8);
+ *   decode = value(code) * s (exact in fp32);
+ *   Phase-1B sums the R decoded copies in fp32 in rank order and
+ *   re-quantizes; Phase-2 decodes and rounds to fp16/bf16 (half to even).
+ * Wire: the INT4 layout -- tile t at byte t*1152; the code of value 8k+j of
+ * the tile in bits 4j..4j+3 of the little-endian uint32 at byte 4k; the fp16
+ * scale of block g (values 32g..32g+31) at byte 1024 + 2g.  Conversions to
+ * and from E2M1 run on the native instructions.  Arguments, aliasing and
+ * errors as for the symmetric codec's calls of the same name, except where
+ * stated. */
+size_t qr_fp4_tile_bytes(void);          /* 1152 */
+size_t qr_fp4_wire_bytes(size_t n);      /* ceil(n/2048) * 1152, 0 on overflow */
+
+qr_status_t qr_fp4_encode(qr_dtype_t dtype, const void *x, size_t n, void *wire,
+                          qr_stream_t stream);
+
+qr_status_t qr_fp4_decode(qr_dtype_t dtype, const void *wire, size_t n, void *y,
+                          qr_stream_t stream);
+
+/* Phase-1B of the FP4 codec on the staged kernel (the R wire tiles brought
+ * into shared memory by bulk copies), `ctas` = 0 for one CTA per SM, else
+ * min(ctas, #SMs); the result does not depend on it; ctas < 0 is
+ * QR_ERR_INVALID_ARG.  out_wire may equal one of the wires exactly. */
+qr_status_t qr_fp4_segment_reduce(int R, const void *const *wires, size_t n,
+                                  void *out_wire, int ctas, qr_stream_t stream);
+
+/* The fused FP4 all-reduce D(E(sum_r D(E(x_r)))) on the staged kernel;
+ * every x[r] and y 32-byte aligned (QR_ERR_MISALIGNED otherwise); `ctas` as
+ * above; y may equal one of the x[r] exactly (in place). */
+qr_status_t qr_fp4_allreduce(qr_dtype_t dtype, int R, const void *const *x,
+                             size_t n, void *y, int ctas, qr_stream_t stream);
+
 /* A static string naming a status code (never NULL). */
 const char *qr_status_string(qr_status_t status);
 

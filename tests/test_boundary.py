@@ -200,6 +200,40 @@ def test_fc_validation():
     assert capi.qr_fc_allreduce(4, 8, 0, 2, [A, B], 2**63, Y) == qr.QR_ERR_SIZE
 
 
+def test_fp4_sizes():
+    assert qr.qr_fp4_tile_bytes() == qr.qr_tile_bytes(4) == 1152
+    assert qr.qr_fp4_wire_bytes(2049) == 2 * 1152 and qr.qr_fp4_wire_bytes(1) == 1152
+
+
+@no_gpu_only
+def test_fp4_validation():
+    n = 2048 + 5
+    assert capi.qr_fp4_encode(0, A, 0, B) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_encode(0, None, n, B) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_encode(2, A, n, B) == qr.QR_ERR_UNSUPPORTED       # dtype
+    assert capi.qr_fp4_encode(0, A + 2, n, B) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_fp4_encode(1, A, n, A + 32) == qr.QR_ERR_INVALID_ARG   # wire overlaps x
+    assert capi.qr_fp4_decode(1, None, n, Y) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_decode(3, A, n, Y) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_fp4_decode(1, A, n, A + 16) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_decode(1, A, n, Y + 8) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_fp4_segment_reduce(0, [A], n, Y, 0) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_segment_reduce(2, [A, None], n, Y, 0) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_segment_reduce(2, [A, B], n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_segment_reduce(9, [A + 4096 * i for i in range(9)], n, Y, 0) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_fp4_segment_reduce(2, [A, B + 8], n, Y, 0) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_fp4_segment_reduce(2, [A, B], n, A + 16, 0) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_segment_reduce(2, [A, B], 2**63, Y, 0) == qr.QR_ERR_SIZE
+    assert capi.qr_fp4_allreduce(0, 2, [A, None], n, Y, 0) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_allreduce(0, 2, [A, B], n, Y, -1) == qr.QR_ERR_INVALID_ARG
+    assert capi.qr_fp4_allreduce(2, 2, [A, B], n, Y, 0) == qr.QR_ERR_UNSUPPORTED    # dtype
+    assert capi.qr_fp4_allreduce(0, 9, [A + 4096 * i for i in range(9)], n, Y, 0) == qr.QR_ERR_UNSUPPORTED
+    assert capi.qr_fp4_allreduce(0, 2, [A, B + 16], n, Y, 0) == qr.QR_ERR_MISALIGNED  # 32-byte alignment
+    assert capi.qr_fp4_allreduce(0, 2, [A, B], n, Y + 16, 0) == qr.QR_ERR_MISALIGNED
+    assert capi.qr_fp4_allreduce(0, 2, [A, B], n, A + 32, 0) == qr.QR_ERR_INVALID_ARG  # partial overlap
+    assert capi.qr_fp4_allreduce(0, 2, [A, B], 2**63, Y, 0) == qr.QR_ERR_SIZE
+
+
 def test_twoshot_workspace_bytes():
     for bits in (3, 4, 6, 8):
         tb = qr.qr_tile_bytes(bits)
