@@ -389,6 +389,9 @@ def run_sweep(args) -> None:
     if args.sweep_codec == "fc":
         run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks)
         return
+    if args.sweep_codec == "fp4":
+        run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks)
+        return
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for dtype in dtypes:
         tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
@@ -622,6 +625,64 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                 torch.cuda.empty_cache()
 
 
+def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
+    """The sweep for the FP4 codec (the INT4 tile with E2M1 elements): the
+    fused kernel and the three unfused steps, interleaved."""
+    import torch
+
+    for dtype in dtypes:
+        tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
+        for Rs in ranks:
+            for n in sizes:
+                xs = [x.view(tdt) for x in workloads.device_sweep(Rs, n, dtype, seed=SEED, device=dev)]
+                y = torch.empty(n, dtype=tdt, device=dev)
+                yu = torch.empty(n, dtype=tdt, device=dev)
+                W = qr.qr_fp4_wire_bytes(n)
+                wires = [torch.empty(W, dtype=torch.uint8, device=dev) for _ in range(Rs)]
+                red = torch.empty(W, dtype=torch.uint8, device=dev)
+                fused_b = 2 * Rs * n + 2 * n
+                kernel_b = {"fused": fused_b, "unfused": fused_b + 2 * Rs * W + 2 * W,
+                            "encode": Rs * (2 * n + W), "reduce": (Rs + 1) * W, "decode": W + 2 * n}
+                do_flush = fused_b < (512 << 20)
+
+                def fused():
+                    qr.qr_fp4_allreduce(xs, y=y)
+
+                def encode_all():
+                    for r in range(Rs):
+                        qr.qr_fp4_encode(xs[r], wire=wires[r])
+
+                def reduce_only():
+                    qr.qr_fp4_segment_reduce(wires, n, out=red)
+
+                def decode_only():
+                    qr.qr_fp4_decode(red, n, y=yu)
+
+                def unfused():
+                    encode_all()
+                    reduce_only()
+                    decode_only()
+
+                arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all), ("reduce", reduce_only),
+                        ("decode", decode_only))
+                times = time_arms(arms, args, flush if do_flush else None, warm=(fused, unfused))
+                same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
+                for name, alg in kernel_b.items():
+                    med = statistics.median(times[name])
+                    print(json.dumps({
+                        "sweep": name, "codec": "fp4", "R": Rs, "values_per_rank": n,
+                        "storage": "fp16" if dtype == 0 else "bf16",
+                        "median_ms": round(med, 5), "input_gbs": round(Rs * n * 2 / (med / 1e3) / 1e9, 2),
+                        "alg_gbs": round(alg / (med / 1e3) / 1e9, 2),
+                        "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
+                        "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None,
+                        "fused_equals_unfused": same, "reps": args.reps,
+                        "burst": 1 if do_flush else args.burst}), flush=True)
+                del wires, red
+                del xs, y, yu
+                torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -648,8 +709,8 @@ def main() -> None:
     ap.add_argument("--sweep-R", default="2,4,8", help="rank counts for --sweep")
     ap.add_argument("--sweep-bits", default="8,6,4,3", help="code widths for --sweep")
     ap.add_argument("--sweep-dtypes", default="fp16,bf16", help="storage types for --sweep")
-    ap.add_argument("--sweep-codec", choices=["qr", "fc"], default="qr",
-                    help="qr: symmetric 32-value blocks; fc: asymmetric groups of 128")
+    ap.add_argument("--sweep-codec", choices=["qr", "fc", "fp4"], default="qr",
+                    help="qr: symmetric 32-value blocks; fc: asymmetric groups of 128; fp4: E2M1 blocks")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

@@ -203,17 +203,22 @@ struct Fp4Reduce {
 // (16 values per thread, two threads per block sharing the absmax)
 // ---------------------------------------------------------------------------
 
+// The E2M1 values nearest to a pair (the codes never leave the register the
+// conversion writes: no packing into slot words on the way back).
+__device__ __forceinline__ float2 e2m1_nearest(const float2 &t) {
+    uint32_t h;
+    asm("{ .reg .b8 b;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b; }"
+        : "=r"(h)
+        : "f"(t.x), "f"(t.y));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
 // Quantize 16 values and return their decoded values (without the scale).
 __device__ __forceinline__ void fp4_roundtrip16(const float2 (&v)[8], const Fp4Scale &sc, float2 (&q)[8]) {
-    uint32_t w[2];
-    fp4_quantize<2>(v, sc, w);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        float2 qk[4];
-        e2m1_word_values(w[k], qk);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) q[4 * k + m] = qk[m];
-    }
+    for (int i = 0; i < 8; ++i) q[i] = e2m1_nearest(fp4_scaled(v[i], sc));
 }
 
 template <int DT>

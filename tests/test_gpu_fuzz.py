@@ -5,8 +5,8 @@ bf16, and messages that mix Gaussian and heavy-tailed values at scales from
 (workloads.fuzz_case).  Every path: the fused kernel as the library picks
 it and forced onto the staged kernel, encode / Phase-1B / decode with their
 wires, the three-launch and the flag-joined two-shot, random grid sizes,
-16-byte-aligned buffers, the wire-emitting variant, and the asymmetric
-codec's fused path."""
+16-byte-aligned buffers, the wire-emitting variant, the asymmetric codec's
+paths and the FP4 codec's."""
 import numpy as np
 import pytest
 import torch
@@ -131,4 +131,27 @@ def test_symmetric_codec_launch_shapes_alignment_and_emission(seed):
     for r in range(R):
         assert_wire_equal(to_host_u8(wires[r]), w_ref[r], bits, f"{what} emitted wire {r}")
     assert_wire_equal(to_host_u8(red), oracle.segment_reduce(bits, w_ref, n), bits, what + " emitted reduced wire")
+    assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("seed", CASES)
+def test_fp4_codec_every_path(seed):
+    c = workloads.fuzz_case(seed)
+    R, n, dt, xs = c["R"], c["n"], c["dtype"], c["xs"]
+    what = f"seed {seed}: R={R} n={n} dtype={dt} FP4"
+    rng = np.random.Generator(np.random.PCG64(13000 + seed))
+    xmax = xmax_of(xs, dt)
+    y_ref = oracle.fp4_allreduce(dt, xs)
+    w_ref = [oracle.fp4_encode(dt, x) for x in xs]
+    xs_dev = [to_dev(x, dt) for x in xs]
+    ctas = int(rng.integers(0, 200))
+    assert_outputs_match(to_host_u16(qr.qr_fp4_allreduce(xs_dev, ctas=ctas)), y_ref, dt, xmax,
+                         f"{what} fused, {ctas} CTAs")
+    wires = [qr.qr_fp4_encode(x) for x in xs_dev]
+    for r in range(R):
+        assert np.array_equal(to_host_u8(wires[r]), w_ref[r]), f"{what} wire {r}"
+    red = qr.qr_fp4_segment_reduce(wires, n, ctas=int(rng.integers(0, 200)))
+    assert np.array_equal(to_host_u8(red), oracle.fp4_segment_reduce(w_ref, n)), what + " reduced wire"
+    y_u = qr.qr_fp4_decode(red, n, dtype=xs_dev[0].dtype)
+    assert_outputs_match(to_host_u16(y_u), y_ref, dt, xmax, what + " unfused")
     assert qr.qr_wait_timeouts() == 0
