@@ -150,6 +150,9 @@ int orc_fc_allreduce(int bits_rs, int bits_ag, int dtype, int R, const uint16_t 
  *   saturating at +-6, the sign bit taken from the product (-0 possible);
  *   decode = value(code) * s (exact in fp32);
  *   Phase-1B and Phase-2 as for the integer codes.
+ * The pins check this reading (element rounding against an independent
+ * E2M1 implementation, the scale against torch, closed forms); parity with
+ * the pages' own FP4 path is unpinned, since the pages give no format.
  */
 float   orc_fp4_value(uint8_t code);
 uint8_t orc_fp4_round(float t);
