@@ -7,6 +7,8 @@ it and forced onto the staged kernel, encode / Phase-1B / decode with their
 wires, the three-launch and the flag-joined two-shot, random grid sizes,
 16-byte-aligned buffers, the wire-emitting variant, the asymmetric codec's
 paths and the FP4 codec's."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,8 @@ from qr_testlib import assert_outputs_match, assert_wire_equal, to_dev, to_host_
 
 pytestmark = pytest.mark.gpu
 
-CASES = range(150)
+# seeds a:b from QR_FUZZ_SEEDS (default 0:150)
+CASES = range(*(int(v) for v in os.environ.get("QR_FUZZ_SEEDS", "0:150").split(":")))
 
 
 @pytest.fixture(scope="module", autouse=True)
