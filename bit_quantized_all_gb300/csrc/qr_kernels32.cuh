@@ -720,11 +720,10 @@ __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const 
     float2 acc[16];
     if constexpr (B == 3) {
         // codes decoded to fp16 through E2M1, scaled and summed by fp16-operand
-        // fmas into fp32 (acc starts at +0: only the sign of a zero sum can
-        // differ from starting at the first rank's product, and the
-        // re-quantized codes do not see it)
+        // fmas into fp32 (acc starts at -0, so the first fma returns the first
+        // rank's product exactly, signed zeros included)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 16; ++i) acc[i] = make_float2(-0.0f, -0.0f);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             uint32_t h[16];
@@ -746,8 +745,9 @@ __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const 
         // Measured against the float path at 2^27 / 2^28 values per rank: R = 8
         // 0.70 / 0.71 -> 0.75 / 0.77 of HBM, R = 4 0.63 / 0.66 -> 0.65 / 0.68,
         // R = 2 0.55 / 0.58 -> 0.54 / 0.56 (so R <= 3 keeps the float path).
+        // acc starts at -0: the first fma returns the first rank's product.
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 16; ++i) acc[i] = make_float2(-0.0f, -0.0f);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const unsigned short sh = static_cast<unsigned short>(sb[r]);

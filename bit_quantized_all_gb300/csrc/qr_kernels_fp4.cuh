@@ -56,14 +56,7 @@ __device__ __forceinline__ uint32_t e2m1_word(const float2 &a, const float2 &b, 
 // the low half, exactly.
 __device__ __forceinline__ void e2m1_word_values(uint32_t w, float2 (&q)[4]) {
     uint32_t h[4];
-    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(w));
+    e2m1_pairs_to_f16x2(w, h);
 #pragma unroll
     for (int m = 0; m < 4; ++m) q[m] = __half22float2(*reinterpret_cast<const __half2 *>(&h[m]));
 }
@@ -151,21 +144,26 @@ __global__ void __launch_bounds__(kThreads32) fp4_decode_kernel(const uint8_t *_
 // ---------------------------------------------------------------------------
 // Phase-1B: the policy of staged_reduce_kernel (one 32-value block per thread)
 // ---------------------------------------------------------------------------
+// The codes' fp16 values (from the native conversion) are scaled and summed
+// by fp16-operand fmas into fp32 -- exact products, one rounding per add, the
+// same as fp32 fmas of the widened operands; acc starts at -0, so the first
+// fma returns the first rank's product exactly, signed zeros included (they
+// decide E2M1 codes 0 and 8 on re-quantization).
 template <int R>
 __device__ __forceinline__ void fp4_reduce_block(const BlockWords<4> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
                                                  int g) {
     float2 acc[16];
 #pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = make_float2(-0.0f, -0.0f);
+#pragma unroll
     for (int r = 0; r < R; ++r) {
-        const float s = f16_bits_to_float(sb[r]);
-        const float2 s2 = make_float2(s, s);
+        const unsigned short sh = static_cast<unsigned short>(sb[r]);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            float2 q[4];
-            e2m1_word_values(c[r].w[k], q);
+            uint32_t h[4];
+            e2m1_pairs_to_f16x2(c[r].w[k], h);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-                acc[4 * k + m] = (r == 0) ? __fmul2_rn(q[m], s2) : __ffma2_rn(q[m], s2, acc[4 * k + m]);
+            for (int m = 0; m < 4; ++m) fma_f16x2_f16_f32(h[m], sh, acc[4 * k + m]);
         }
     }
     const Fp4Scale sc = fp4_scale(block_absmax(acc));
