@@ -363,6 +363,25 @@ __device__ __forceinline__ void unpack_pair_q3_f16(uint32_t W, uint32_t X, uint3
     }
 }
 
+// The 8 signed INT6 codes of a slot as exact fp16 pairs h[0..3] = lanes
+// (0, 2), (4, 6), (1, 3), (5, 7): the 6-bit codes, one per byte (even and
+// odd lanes apart), become the low bytes of two fp16 patterns 0x64xx
+// (1024 + code) by one byte permute, and one packed fp16 fma per pair removes
+// the offset and the bias -- half the byte permutes of the float path.
+__device__ __forceinline__ void unpack_slot_q6_f16(const SlotCodes c, uint32_t (&h)[4]) {
+    uint32_t even, odd;
+    slot_even_odd_codes<6>(c, even, odd);
+    const __half2 one = __float2half2_rn(1.0f), off = __float2half2_rn(-1056.0f);
+    const auto fix = [&](uint32_t t) {
+        const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&t), one, off);
+        return *reinterpret_cast<const uint32_t *>(&r);
+    };
+    h[0] = fix(__byte_perm(even, 0x64646464u, 0x4140));
+    h[1] = fix(__byte_perm(even, 0x64646464u, 0x4342));
+    h[2] = fix(__byte_perm(odd, 0x64646464u, 0x4140));
+    h[3] = fix(__byte_perm(odd, 0x64646464u, 0x4342));
+}
+
 // The 32 signed codes of a block as exact floats, pairwise.
 template <int B>
 __device__ __forceinline__ void unpack_block_q(const BlockWords<B> &c, float2 (&q)[16]) {
@@ -721,7 +740,9 @@ __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const 
     if constexpr (B == 3) {
         // codes decoded to fp16 through E2M1, scaled and summed by fp16-operand
         // fmas into fp32 (acc starts at -0, so the first fma returns the first
-        // rank's product exactly, signed zeros included)
+        // rank's product exactly, signed zeros included).  Decoding through the
+        // fp16 1024 instead (logic operations and packed fp16 fmas, as INT4
+        // does) measured 10% slower at R = 8 and equal at R = 2, 4.
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = make_float2(-0.0f, -0.0f);
 #pragma unroll
@@ -759,6 +780,25 @@ __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const 
                 for (int m = 0; m < 4; ++m) fma_f16x2_f16_f32(q[m], sh, acc[4 * k + m]);
             }
         }
+    } else if constexpr (B == 6) {
+        // codes decoded to fp16 by byte permutes, summed by fp16-operand fmas;
+        // here acc[4s + i] holds lanes (0, 2), (4, 6), (1, 3), (5, 7) of slot s.
+        // Measured against the float path at 2^27 / 2^28 bf16 values per rank:
+        // R = 8 0.76 / 0.78 -> 0.82 / 0.84 of HBM, R = 2 0.57 / 0.60 -> 0.60 /
+        // 0.62, R = 4 equal (0.67 / 0.69).  acc starts at -0 as above.
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = make_float2(-0.0f, -0.0f);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const unsigned short sh = static_cast<unsigned short>(sb[r]);
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+                uint32_t h[4];
+                unpack_slot_q6_f16(slot_codes<6>(c[r], sl), h);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) fma_f16x2_f16_f32(h[i], sh, acc[4 * sl + i]);
+            }
+        }
     } else {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -777,6 +817,17 @@ __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const 
     if constexpr (B == 4 && R >= 4) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) cw.w[k] = slot_nibbles_m4(&f[4 * k]);
+    } else if constexpr (B == 6) {
+        float2 fs[16];
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+            const float2 *g = &f[4 * sl];
+            fs[4 * sl] = make_float2(g[0].x, g[2].x);      // lanes 0, 1
+            fs[4 * sl + 1] = make_float2(g[0].y, g[2].y);  // lanes 2, 3
+            fs[4 * sl + 2] = make_float2(g[1].x, g[3].x);  // lanes 4, 5
+            fs[4 * sl + 3] = make_float2(g[1].y, g[3].y);  // lanes 6, 7
+        }
+        pack_block<B>(fs, cw);
     } else {
         pack_block<B>(f, cw);
     }
@@ -831,7 +882,7 @@ __host__ __device__ constexpr int reduce_units_per_thread() { return (R <= 2) ? 
 template <int B>
 struct QrReduce {
     static constexpr int kThreads = 64;
-    static constexpr int kCtaThreads = (B == 4) ? 640 : 512;  // see StagedReduceShape
+    static constexpr int kCtaThreads = (B == 4 || B == 6) ? 640 : 512;  // see StagedReduceShape
     static constexpr uint32_t kTileIn = Codec<B>::kTileBytes, kTileOut = Codec<B>::kTileBytes;
     template <int R>
     struct Regs {
@@ -931,8 +982,9 @@ __global__ void __launch_bounds__(P::kThreads * G, 1) staged_reduce_kernel(Const
 // 0.34 / 0.34 (bound by the integer pipe, not by memory: it stays on
 // reduce32_kernel).  Ten groups (640 threads, 20 warps at up to 96
 // registers) against eight: INT4 +2..4% at R = 2, 4, 8 (latency-bound: more
-// warps hide more), INT6 equal, INT8 -7% at R = 8 (one stage per group left
-// in 200 KiB); so ten for INT4 only.  The asymmetric codec's policy runs five
+// warps hide more); INT6, once its Phase-1B decoded through fp16, +3% at
+// R = 2, +9% at R = 6 (0.73 -> 0.80 at 2^28), equal at R = 4, 8; INT8 -7% at
+// R = 8 (one stage per group left in 200 KiB); so ten for INT4 and INT6.  The asymmetric codec's policy runs five
 // groups of 128 threads (640), 5-10% faster than four at R = 4, 6, 8 for
 // every width pair.
 template <class P, int R>

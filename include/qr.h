@@ -116,9 +116,10 @@ qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires,
                               size_t n, void *out_wire, qr_stream_t stream);
 
 /* qr_segment_reduce on the staged kernel, whatever the size: a persistent
- * kernel (one CTA per SM of groups of 64 threads, ten for INT4, else eight)
- * whose groups bring the R ranks' wire tiles into shared memory with bulk
- * asynchronous copies, a few tiles ahead, and reduce from there.  `ctas` = 0 for one CTA per SM,
+ * kernel (one CTA per SM of groups of 64 threads, ten for INT4 and INT6,
+ * else eight) whose groups bring the R ranks' wire tiles into shared memory
+ * with bulk asynchronous copies, a few tiles ahead, and reduce from there.
+ * `ctas` = 0 for one CTA per SM,
  * else min(ctas, #SMs) (at most one per tile); the result does not depend on
  * it; ctas < 0 is QR_ERR_INVALID_ARG.  qr_segment_reduce itself takes this
  * kernel for INT4, INT6 and INT8 from 48 tiles per SM.  Its waits on its
