@@ -253,22 +253,31 @@ __device__ __forceinline__ void unpack_slot_q2(const SlotCodes c, float2 (&q)[4]
     q[3] = __fadd2_rn(make_float2(byte_as_magic<3>(even), byte_as_magic<3>(odd)), nm);
 }
 
+// The 3-bit codes of two consecutive INT3 slots in nibbles, from the slots'
+// q2w (W: slot 0 in bits 0..15) and q1w (X: slot 0 in bits 0..7, slot 1 in
+// 8..15; bits above 15 are ignored): e nibble 4i+m = lane 2m of slot i, o
+// nibble 4i+m = lane 2m+1, each nibble q2 | q1 << 2.  The q1 bits are placed
+// by two byte-permute lookups: a selector nibble of three q1 bits (lanes j,
+// j+1, j+2) picks the table byte that holds lane j's bit at bit 2 and lane
+// j+2's at bit 6 -- 8 integer operations where spreading the q1 byte by
+// shifts and masks took 11.
+__device__ __forceinline__ void q3_nibbles(uint32_t W, uint32_t X, uint32_t &e, uint32_t &o) {
+    constexpr uint32_t kQ1Lo = 0x04000400u, kQ1Hi = 0x44404440u;  // byte k = (k & 1) << 2 | (k & 4) << 4
+    e = (W & 0x33333333u) | __byte_perm(kQ1Lo, kQ1Hi, X & 0x7777u);
+    o = ((W >> 2) & 0x33333333u) | __byte_perm(kQ1Lo, kQ1Hi, (X >> 1) & 0x7777u);
+}
+
 // The 16 signed INT3 codes of two consecutive slots as exact floats,
 // pairwise (q[4i + m] = lanes 2m, 2m+1 of slot i).  W: the two slots' q2w
 // (slot 0 in bits 0..15); X: their q1w (slot 0 in bits 0..7, slot 1 in
-// 8..15; bits above 15 are ignored).  The q1 bits are spread to every fourth
-// bit (three shift-and-mask steps) and merged with the q2 fields into
-// 3-bit codes in nibbles, even lanes in one word and odd lanes in another;
-// each code's byte then goes into a magic float by one byte permute (which
-// can take any byte, so the codes need no further ordering).  18 integer
-// operations per 16 values where spreading each slot's fields apart takes
-// about twice as many.
+// 8..15; bits above 15 are ignored).  The q1 bits are merged with the q2
+// fields into 3-bit codes in nibbles, even lanes in one word and odd lanes
+// in another (q3_nibbles); each code's byte then goes into a magic float by
+// one byte permute (which can take any byte, so the codes need no further
+// ordering).
 __device__ __forceinline__ void unpack_pair_q3(uint32_t W, uint32_t X, float2 (&q)[8]) {
-    uint32_t x = (X & 0xFFu) | ((X << 8) & 0x00FF0000u);  // slot i's q1 byte at bits 16i
-    x = (x | (x << 4)) & 0x0F0F0F0Fu;
-    x = (x | (x << 2)) & 0x33333333u;  // lane j = 4a+2b+c of slot i at bit 16i + 8a + 4b + c
-    const uint32_t e = (W & 0x33333333u) | ((x << 2) & 0x44444444u);           // nibble 4i+m: lane 2m
-    const uint32_t o = ((W >> 2) & 0x33333333u) | ((x << 1) & 0x44444444u);    // nibble 4i+m: lane 2m+1
+    uint32_t e, o;  // nibble 4i+m: lane 2m / 2m+1 of slot i
+    q3_nibbles(W, X, e, o);
     const uint32_t el = e & 0x0F0F0F0Fu, eh = (e >> 4) & 0x0F0F0F0Fu;          // byte t: nibble 2t / 2t+1
     const uint32_t ol = o & 0x0F0F0F0Fu, oh = (o >> 4) & 0x0F0F0F0Fu;
     const float2 nm = make_float2(-Codec<3>::kMagic, -Codec<3>::kMagic);
@@ -341,17 +350,14 @@ __device__ __forceinline__ uint32_t slot_nibbles_m4(const float2 *f) {
 // byte permute per four codes looks each code's E2M1 code up in an 8-entry
 // byte table (the low-nibble table for the even lanes, the same codes shifted
 // into the high nibble for the odd lanes), an OR pairs them, and the native
-// E2M1 conversion yields two fp16 values per byte.  11 integer operations
-// per 8 values where the float path takes 17.
+// E2M1 conversion yields two fp16 values per byte.  8 integer operations
+// per 8 values where the float path takes 14.
 __device__ __forceinline__ void unpack_pair_q3_f16(uint32_t W, uint32_t X, uint32_t (&h)[8]) {
     // E2M1 codes of u - 4 for u = 0..7: -4, -3, -2, -1, 0, 1, 2, 3
     constexpr uint32_t kLo0 = 0x0A0C0D0Eu, kLo1 = 0x05040200u;  // bytes 0-3, 4-7
     constexpr uint32_t kHi0 = 0xA0C0D0E0u, kHi1 = 0x50402000u;
-    uint32_t x = (X & 0xFFu) | ((X << 8) & 0x00FF0000u);
-    x = (x | (x << 4)) & 0x0F0F0F0Fu;
-    x = (x | (x << 2)) & 0x33333333u;
-    const uint32_t e = (W & 0x33333333u) | ((x << 2) & 0x44444444u);         // nibble 4i+m: lane 2m
-    const uint32_t o = ((W >> 2) & 0x33333333u) | ((x << 1) & 0x44444444u);  // nibble 4i+m: lane 2m+1
+    uint32_t e, o;  // nibble 4i+m: lane 2m / 2m+1 of slot i
+    q3_nibbles(W, X, e, o);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const uint32_t ei = e >> (16 * i), oi = o >> (16 * i);  // the byte permute reads 4 selector nibbles
