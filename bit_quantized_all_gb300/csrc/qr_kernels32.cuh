@@ -990,7 +990,10 @@ __global__ void __launch_bounds__(P::kThreads * G, 1) staged_reduce_kernel(Const
 // registers) against eight: INT4 +2..4% at R = 2, 4, 8 (latency-bound: more
 // warps hide more); INT6, once its Phase-1B decoded through fp16, +3% at
 // R = 2, +9% at R = 6 (0.73 -> 0.80 at 2^28), equal at R = 4, 8; INT8 -7% at
-// R = 8 (one stage per group left in 200 KiB); so ten for INT4 and INT6.  The asymmetric codec's policy runs five
+// R = 8 (one stage per group left in 200 KiB); so ten for INT4 and INT6.
+// Deeper rings do not pay: a 224 KiB budget (one more stage for INT8 at
+// R = 3, 4, 6, INT4 / FP4 at R = 6, FC 8->8 at R = 5, 7) measured INT8
+// -3 / -6 / -11%, FP4 -3.5%, FC 8->8 R = 7 -2.5%, INT4 equal.  The asymmetric codec's policy runs five
 // groups of 128 threads (640), 5-10% faster than four at R = 4, 6, 8 for
 // every width pair.
 template <class P, int R>
