@@ -978,6 +978,19 @@ __global__ void __launch_bounds__(P::kThreads * G, 1) staged_reduce_kernel(Const
     }
 }
 
+// Most ring stages per group: four, but one for INT8 from four ranks (the
+// memory-bound case, where a deeper ring measured slower): at 2^27 / 2^28
+// bf16 values per rank, R = 5 0.92 / 0.93 -> 1.00 / 1.02 of HBM (was two
+// stages), R = 4 0.96 / 0.97 -> 0.97 / 1.00 (was two).
+template <class P, int R>
+struct StagedReduceStageCap {
+    static constexpr int value = 4;
+};
+template <int R>
+struct StagedReduceStageCap<QrReduce<8>, R> {
+    static constexpr int value = (R >= 4) ? 1 : 4;
+};
+
 // Launch shape of the staged Phase-1B kernel: P::kCtaThreads threads (groups
 // of P::kThreads), each group with as many stages (at most 4) as fit in
 // 200 KiB of shared memory at R * tile-bytes per stage.  Measured on GB300 at
@@ -1000,7 +1013,8 @@ template <class P, int R>
 struct StagedReduceShape {
     static constexpr int kGroups = P::kCtaThreads / P::kThreads;
     static constexpr int kFit = (200 * 1024) / (kGroups * R * P::kTileIn);
-    static constexpr int kStages = kFit >= 4 ? 4 : (kFit < 1 ? 1 : kFit);
+    static constexpr int kCap = StagedReduceStageCap<P, R>::value;
+    static constexpr int kStages = kFit >= kCap ? kCap : (kFit < 1 ? 1 : kFit);
     static constexpr int kSmemBytes = kGroups * kStages * R * P::kTileIn;
 };
 
