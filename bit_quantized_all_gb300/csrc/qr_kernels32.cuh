@@ -1016,6 +1016,8 @@ struct StagedReduceShape {
     static constexpr int kCap = StagedReduceStageCap<P, R>::value;
     static constexpr int kStages = kFit >= kCap ? kCap : (kFit < 1 ? 1 : kFit);
     static constexpr int kSmemBytes = kGroups * kStages * R * P::kTileIn;
+    // the ring plus the kernel's static barriers and pointers within one CTA's 227 KB
+    static_assert(kSmemBytes + 1024 <= 227 * 1024, "staged Phase-1B ring exceeds the shared memory of a CTA");
 };
 
 }  // namespace qrk
