@@ -2,6 +2,7 @@
 ties a committed DRAM-traffic capture to the code it was taken on, and the
 timing of the CPU oracle used as the CPU baseline."""
 import json
+import time
 
 import pytest
 
@@ -47,3 +48,35 @@ def test_cpu_sweep_times_the_oracle_on_a_workload():
     assert reps >= 1 and dt >= 0.05
     assert vps == pytest.approx(reps * 4096 * 2 * 2 / dt)
     assert gbs == pytest.approx(vps * 2 / 1e9)
+
+
+def test_reference_arm_line_carries_the_contract_keys(monkeypatch, capsys):
+    """The reference arm's JSON line: every key the benchmark contract names,
+    with its own value repeated as the CPU baseline and the end-to-end figure
+    (the inputs and the timed oracle work are stubbed: this checks the line,
+    not the oracle)."""
+    import argparse
+
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setattr(bench, "host_inputs", lambda *a, **k: [])
+    monkeypatch.setattr(bench, "oracle_calibrate", lambda orc, xs, threads: 1e9)  # one tile per step
+    def fake_run(orc, xs, tiles, threads, start=0):
+        time.sleep(0.002)  # a measurable step
+        return tiles
+
+    monkeypatch.setattr(bench, "oracle_run", fake_run)
+    bench.run_reference(argparse.Namespace(steps=3, warmup=3, gpus=1))
+    line = json.loads(capsys.readouterr().out)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert (line["n_gpus"], line["steps"], line["warmup"]) == (1, 3, 3)
+    assert line["higher_is_better"] is True and line["vs_baseline"] is None
+    assert "workload" in line["config"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
