@@ -1,6 +1,7 @@
 """Host logic of the benchmark that needs no GPU: the kernel-code hash that
-ties a committed DRAM-traffic capture to the code it was taken on, and the
-timing of the CPU oracle used as the CPU baseline."""
+ties a committed DRAM-traffic capture to the code it was taken on, the
+timing of the CPU oracle used as the CPU baseline, and the keys of the
+reference arm's JSON line."""
 import json
 import time
 
