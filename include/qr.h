@@ -118,7 +118,7 @@ qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires,
 /* qr_segment_reduce on the staged kernel, whatever the size: a persistent
  * kernel (one CTA per SM of groups of 64 threads, ten for INT4 and INT6,
  * else eight) whose groups bring the R ranks' wire tiles into shared memory
- * with bulk asynchronous copies, a few tiles ahead, and reduce from there.
+ * with bulk asynchronous copies, one to four tiles ahead, and reduce from there.
  * `ctas` = 0 for one CTA per SM,
  * else min(ctas, #SMs) (at most one per tile); the result does not depend on
  * it; ctas < 0 is QR_ERR_INVALID_ARG.  qr_segment_reduce itself takes this
@@ -162,7 +162,7 @@ qr_status_t qr_allreduce_emit(int bits, qr_dtype_t dtype, int R,
 
 /* qr_allreduce on the staged kernel, whatever the size: a persistent kernel
  * (one CTA per SM) whose CTAs bring every rank's slice of a tile into shared
- * memory with bulk asynchronous copies, several tiles ahead, and run the
+ * memory with bulk asynchronous copies, one to four tiles ahead, and run the
  * arithmetic from there.  `ctas` = 0 for one CTA per SM, else min(ctas,
  * #SMs) CTAs (at least one, at most one per full tile); the result does not
  * depend on it.  Every x[r] and y must be 32-byte aligned
