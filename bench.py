@@ -288,7 +288,7 @@ def _gpu_uuid(torch, dev) -> str | None:
         u = torch.cuda.get_device_properties(dev).uuid
         s = str(u)
         return s if s.startswith("GPU-") else "GPU-" + s
-    except (AttributeError, RuntimeError):  # no uuid property in this torch, or no device
+    except (AttributeError, AssertionError, RuntimeError):  # no uuid property, or no such device
         return None
 
 
