@@ -81,3 +81,31 @@ def test_reference_arm_line_carries_the_contract_keys(monkeypatch, capsys):
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("tiles, threads, start", [(7, 3, 0), (10, 4, 5), (1, 8, 9), (10, 1, 0), (25, 6, 3)])
+def test_oracle_run_counts_the_tiles_it_reduces(monkeypatch, tiles, threads, start):
+    """The CPU baseline's work accounting: every tile reported as done was
+    reduced once per code width, chunks start where the step left off (modulo
+    the message) and none runs past its end."""
+    import threading
+
+    import bench
+    T = 10
+    monkeypatch.setattr(bench, "N", T * 2048)
+    seen, lock = [], threading.Lock()
+
+    def fake_tiles(orc, xs, bits, t0, t1):
+        assert 0 <= t0 < t1 <= T
+        with lock:
+            seen.extend((bits, t) for t in range(t0, t1))
+
+    monkeypatch.setattr(bench, "_oracle_tiles", fake_tiles)
+    done = bench.oracle_run(None, [], tiles, threads, start=start)
+    assert 1 <= done <= tiles
+    for bits in bench.BITS:
+        got = [t for b, t in seen if b == bits]
+        assert len(got) == done  # one reduction per counted tile and width
+        if tiles <= T:  # the benchmark never asks for more than the message
+            assert len(set(got)) == done
+    assert (start % T) in {t for _, t in seen}
