@@ -42,7 +42,7 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas",
            "qr_segment_reduce_staged", "qr_fc_segment_reduce_staged", "qr_twoshot_flags_workspace_bytes",
            "qr_allreduce_twoshot_flags", "qr_fp4_tile_bytes", "qr_fp4_wire_bytes", "qr_fp4_encode",
-           "qr_fp4_decode", "qr_fp4_segment_reduce", "qr_fp4_allreduce")
+           "qr_fp4_decode", "qr_fp4_segment_reduce", "qr_fp4_allreduce", "qr_selftest_twoshot_flags_drop")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
                 "qr_twoshot_flags_workspace_bytes": (sz, [i32, i32, sz]),
                 "qr_allreduce_twoshot_flags": (i32, [i32, i32, i32, vpp, sz, vpp, vp, sz, vp]),
                 "qr_allreduce_twoshot_static": (i32, [i32, i32, i32, vpp, sz, vpp, vp]),
+                "qr_selftest_twoshot_flags_drop": (i32, [i32, i32, i32, vpp, sz, vpp, vp, sz, i32, vp]),
                 "qr_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint)]),
                 "qr_allreduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_fc_allreduce_staged": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
@@ -185,6 +186,12 @@ class capi:
     @staticmethod
     def qr_allreduce_twoshot_static(bits, dtype, R, xs, n, ys, stream=None):
         return lib().qr_allreduce_twoshot_static(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), stream)
+
+    @staticmethod
+    def qr_selftest_twoshot_flags_drop(bits, dtype, R, xs, n, ys, workspace, workspace_bytes, drop_sender,
+                                       stream=None):
+        return lib().qr_selftest_twoshot_flags_drop(bits, dtype, R, _ptr_array(xs), n, _ptr_array(ys), workspace,
+                                                    workspace_bytes, drop_sender, stream)
 
     @staticmethod
     def qr_wait_timeouts():
@@ -437,7 +444,8 @@ def qr_allreduce_emit(bits: int, xs, y: torch.Tensor | None = None, wire_out=Non
 
 def qr_wait_timeouts() -> int:
     """Device-side waits that ran out on the current device since the last
-    call (0 in a correct run); resets the count.  Synchronizes the device."""
+    call (0 in a correct run); reads and resets the count in one atomic step
+    after waiting for all work enqueued on the device."""
     st, count = capi.qr_wait_timeouts()
     _check(st, "qr_wait_timeouts")
     return count

@@ -99,9 +99,10 @@ QR_EXPORT size_t qr_twoshot_flags_workspace_bytes(int bits, int R, size_t n) {
     return twoshot_flags_ws_bytes(bits, R, n, nullptr);
 }
 
-QR_EXPORT qr_status_t qr_allreduce_twoshot_flags(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
-                                                 void *const *y, void *workspace, size_t workspace_bytes,
-                                                 qr_stream_t stream) {
+// qr_allreduce_twoshot_flags and its self-test share the checks and the launch.
+static qr_status_t twoshot_flags_call(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                      void *const *y, void *workspace, size_t workspace_bytes, int drop_sender,
+                                      qr_stream_t stream) {
     if (!x || !y || !workspace || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
     for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
         if (!x[r] || !y[r]) return QR_ERR_INVALID_ARG;
@@ -124,8 +125,21 @@ QR_EXPORT qr_status_t qr_allreduce_twoshot_flags(int bits, qr_dtype_t dtype, int
         }
     }
     return from_cuda(qrk::launch_twoshot_flags(bits, dtype, R, x, static_cast<long long>(n), y, workspace,
-                                               static_cast<uint8_t *>(workspace) + flags_offset,
+                                               static_cast<uint8_t *>(workspace) + flags_offset, drop_sender,
                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QR_EXPORT qr_status_t qr_allreduce_twoshot_flags(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                                 void *const *y, void *workspace, size_t workspace_bytes,
+                                                 qr_stream_t stream) {
+    return twoshot_flags_call(bits, dtype, R, x, n, y, workspace, workspace_bytes, -1, stream);
+}
+
+QR_EXPORT qr_status_t qr_selftest_twoshot_flags_drop(int bits, qr_dtype_t dtype, int R, const void *const *x,
+                                                     size_t n, void *const *y, void *workspace,
+                                                     size_t workspace_bytes, int drop_sender, qr_stream_t stream) {
+    if (drop_sender < 0 || drop_sender >= R) return QR_ERR_INVALID_ARG;
+    return twoshot_flags_call(bits, dtype, R, x, n, y, workspace, workspace_bytes, drop_sender, stream);
 }
 
 QR_EXPORT qr_status_t qr_allreduce_twoshot(int bits, qr_dtype_t dtype, int R, const void *const *x, size_t n,

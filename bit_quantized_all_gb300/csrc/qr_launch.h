@@ -15,12 +15,24 @@ int grid_for(const void *kernel, int threads, long long tiles, int ctas, int wav
 // Streaming multiprocessors of the current device (cached); 0 on error.
 int sm_count(cudaError_t *err);
 
-// Raises the dynamic shared-memory limit of `kernel` to `bytes` on the
-// current device (once per device and kernel).
+// A number that identifies the calling thread's current CUDA context for the
+// life of the process (cuCtxGetId + 1; never reused, unlike a device ordinal
+// or a context handle after cudaDeviceReset); 0 with *err set on failure.
+// If no context is current yet, the current device's primary context is
+// initialized first.
+unsigned long long context_id(cudaError_t *err);
+
+// The device address of a __device__ symbol of this library in the current
+// context (cudaGetSymbolAddress, cached per context and symbol, so that an
+// address from a context that was torn down is never reused).
+cudaError_t context_symbol_address(const void *symbol, void **ptr);
+
+// Raises the dynamic shared-memory limit of `kernel` to `bytes` in the
+// current context (once per context and kernel).
 cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
 
-// Device address of the library's wait-timeout counter on the current
-// device (qr_timeouts.cu); nullptr with *err set on failure.
+// Device address of the library's wait-timeout counter in the current
+// context (qr_timeouts.cu); nullptr with *err set on failure.
 unsigned *wait_timeout_counter(cudaError_t *err);
 
 cudaError_t launch_encode(int bits, int dtype, const void *x, long long n, void *wire,
@@ -70,11 +82,13 @@ long long twoshot_segment_tiles(long long tiles, int R);
 cudaError_t launch_twoshot(int bits, int dtype, int R, const void *const *x, long long n, void *const *y, void *ws,
                            cudaStream_t s);
 
-// The same exchange in one cooperative launch, its phases joined by per-tile
+// The same exchange in one cooperative launch, its phases joined by per-chunk
 // ready flags (qr_twoshot_flags.cu); `flags` holds 2T + 1 words that the call
-// zeroes before the launch.
+// zeroes before the launch.  `drop_sender` is -1, or (self-test only) a rank
+// whose sends are written but never announced, so that the owners' waits
+// run out.
 cudaError_t launch_twoshot_flags(int bits, int dtype, int R, const void *const *x, long long n, void *const *y,
-                                 void *ws, void *flags, cudaStream_t s);
+                                 void *ws, void *flags, int drop_sender, cudaStream_t s);
 
 // The Flash Communication codec (asymmetric groups of 128): widths 4 and 8;
 // the (reduce-scatter, all-gather) width pairs (4,4), (4,8) and (8,8).

@@ -4,12 +4,10 @@
 // Kernels that wait (the staged fused and Phase-1B kernels on their CTA's
 // shared-memory barriers, the flag-joined two-shot on other CTAs' flags)
 // give every wait a limit of one second; when a wait runs out the kernel
-// adds one to this per-device counter, stops, and returns, so the context
-// stays usable.  The host reads (and clears) the counter with
+// adds one to this counter (one per device, held in each CUDA context that
+// loads the library), stops, and returns, so the context stays usable.  The
+// host reads and clears the counter in one atomic step with
 // qr_wait_timeouts.  In a correct launch it never moves.
-#include <map>
-#include <mutex>
-
 #include <cuda_runtime.h>
 
 #include "../../include/qr.h"
@@ -21,6 +19,7 @@
 namespace {
 
 __device__ unsigned g_wait_timeouts;
+__device__ unsigned g_wait_timeouts_taken;  // what the last read-and-clear found
 
 // One thread waits on a barrier that nothing will ever complete.
 __global__ void bounded_wait_selftest_kernel(unsigned *timeouts) {
@@ -30,21 +29,19 @@ __global__ void bounded_wait_selftest_kernel(unsigned *timeouts) {
     if (!qrk::mbar_wait(&bar, 0)) atomicAdd(timeouts, 1u);
 }
 
+// Reads the counter and sets it to zero in one atomic step, so that an
+// increment from a kernel still running elsewhere is either counted now or
+// left for the next read, never lost.
+__global__ void take_timeouts_kernel() { g_wait_timeouts_taken = atomicExch(&g_wait_timeouts, 0u); }
+
 }  // namespace
 
 namespace qrk {
 
 unsigned *wait_timeout_counter(cudaError_t *err) {
-    int dev = 0;
-    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return nullptr;
-    static std::mutex mu;
-    static std::map<int, unsigned *> addr;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = addr.find(dev);
-    if (it != addr.end()) return it->second;
     void *p = nullptr;
-    if ((*err = cudaGetSymbolAddress(&p, g_wait_timeouts)) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<unsigned *>(p);
+    if ((*err = context_symbol_address(reinterpret_cast<const void *>(&g_wait_timeouts), &p)) != cudaSuccess)
+        return nullptr;
     return static_cast<unsigned *>(p);
 }
 
@@ -52,10 +49,13 @@ unsigned *wait_timeout_counter(cudaError_t *err) {
 
 QR_EXPORT qr_status_t qr_wait_timeouts(unsigned *count) {
     if (!count) return QR_ERR_INVALID_ARG;
+    // every kernel this process has enqueued on the current device, on any
+    // stream, finishes first, so its timeouts are in the count
+    if (cudaDeviceSynchronize() != cudaSuccess) return QR_ERR_CUDA;
+    take_timeouts_kernel<<<1, 1, 0, 0>>>();
+    if (cudaGetLastError() != cudaSuccess) return QR_ERR_CUDA;
     unsigned v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof v) != cudaSuccess) return QR_ERR_CUDA;
-    const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof zero) != cudaSuccess) return QR_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_wait_timeouts_taken, sizeof v) != cudaSuccess) return QR_ERR_CUDA;
     *count = v;
     return QR_OK;
 }

@@ -23,9 +23,12 @@
 // is read with L2 (.cg) loads after the acquire.
 //
 // Every wait is bounded (one second of %globaltimer).  On expiry the CTA
-// adds one to the library's timeout counter and raises the workspace's abort
-// word; every other wait sees it and returns at once, so a failed launch
-// ends promptly with incomplete outputs and the context usable.
+// raises the workspace's abort word, and the CTA that raised it first adds
+// one to the library's timeout counter (so a failed launch counts exactly
+// one timeout); every other wait sees the word and returns at once, so a
+// failed launch ends promptly with incomplete outputs and the context usable.
+// For a self-test, one sender's announcements can be left out (its tiles are
+// still written), which makes the owners' waits run out.
 #include <cstdint>
 
 #include "qr_kernels32.cuh"
@@ -62,8 +65,7 @@ __device__ __forceinline__ bool cta_wait(const uint32_t *flag, uint32_t target, 
                     break;
                 }
                 if (global_ns() - t0 > kWaitLimitNs) {
-                    atomicAdd(timeouts, 1u);
-                    atomicExch(abort_word, 1u);
+                    if (atomicExch(abort_word, 1u) == 0u) atomicAdd(timeouts, 1u);
                     good = 0;
                     break;
                 }
@@ -106,7 +108,7 @@ __device__ __forceinline__ void load_block_cg(const uint8_t *tile, int g, BlockW
 template <int B, int DT, int R, int C>
 __global__ void __launch_bounds__(64) twoshot_flags_kernel(ConstPtrs x, long long n, MutPtrs y, uint8_t *ws,
                                                            long long T, long long seg, uint32_t *flags,
-                                                           unsigned *timeouts) {
+                                                           unsigned *timeouts, int drop_sender) {
     constexpr long long kTile = Codec<B>::kTileBytes;
     const int k = threadIdx.x;  // the block of each tile this thread works on
     const long long chunks = (T + C - 1) / C;
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(64) twoshot_flags_kernel(ConstPtrs x, long lon
             }
         }
         __syncthreads();
-        if (k == 0) add_release(&sent[c], 1u);
+        if (k == 0 && j != drop_sender) add_release(&sent[c], 1u);
     }
     // phase 2: the owners' reductions, chunk by chunk as the copies arrive
     for (long long c = blockIdx.x; c < chunks; c += gridDim.x) {
@@ -218,7 +220,7 @@ constexpr int kFlagsChunkTiles = QR_FLAGS_CHUNK_TILES;  // tiles per work unit a
 
 template <int B, int DT, int R>
 static cudaError_t run_flags(const ConstPtrs &xp, long long n, const MutPtrs &yp, uint8_t *ws, uint32_t *flags,
-                             cudaStream_t s) {
+                             int drop_sender, cudaStream_t s) {
     const long long T = (n + kTileValues - 1) / kTileValues;
     long long seg = twoshot_segment_tiles(T, R);
     cudaError_t err = cudaSuccess;
@@ -237,23 +239,24 @@ static cudaError_t run_flags(const ConstPtrs &xp, long long n, const MutPtrs &yp
     long long nn = n, TT = T;
     ConstPtrs xa = xp;
     MutPtrs ya = yp;
-    void *args[] = {&xa, &nn, &ya, &ws, &TT, &seg, &flags, &timeouts};
+    int drop = drop_sender;
+    void *args[] = {&xa, &nn, &ya, &ws, &TT, &seg, &flags, &timeouts, &drop};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(static_cast<unsigned>(grid)),
                                        dim3(64), args, 0, s);
 }
 
 template <int B, int DT>
 static cudaError_t run_flags_r(int R, const ConstPtrs &xp, long long n, const MutPtrs &yp, uint8_t *ws,
-                               uint32_t *flags, cudaStream_t s) {
+                               uint32_t *flags, int drop, cudaStream_t s) {
     switch (R) {
-        case 1: return run_flags<B, DT, 1>(xp, n, yp, ws, flags, s);
-        case 2: return run_flags<B, DT, 2>(xp, n, yp, ws, flags, s);
-        case 3: return run_flags<B, DT, 3>(xp, n, yp, ws, flags, s);
-        case 4: return run_flags<B, DT, 4>(xp, n, yp, ws, flags, s);
-        case 5: return run_flags<B, DT, 5>(xp, n, yp, ws, flags, s);
-        case 6: return run_flags<B, DT, 6>(xp, n, yp, ws, flags, s);
-        case 7: return run_flags<B, DT, 7>(xp, n, yp, ws, flags, s);
-        case 8: return run_flags<B, DT, 8>(xp, n, yp, ws, flags, s);
+        case 1: return run_flags<B, DT, 1>(xp, n, yp, ws, flags, drop, s);
+        case 2: return run_flags<B, DT, 2>(xp, n, yp, ws, flags, drop, s);
+        case 3: return run_flags<B, DT, 3>(xp, n, yp, ws, flags, drop, s);
+        case 4: return run_flags<B, DT, 4>(xp, n, yp, ws, flags, drop, s);
+        case 5: return run_flags<B, DT, 5>(xp, n, yp, ws, flags, drop, s);
+        case 6: return run_flags<B, DT, 6>(xp, n, yp, ws, flags, drop, s);
+        case 7: return run_flags<B, DT, 7>(xp, n, yp, ws, flags, drop, s);
+        case 8: return run_flags<B, DT, 8>(xp, n, yp, ws, flags, drop, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -263,7 +266,7 @@ static cudaError_t run_flags_r(int R, const ConstPtrs &xp, long long n, const Mu
 long long twoshot_flag_words(long long tiles) { return 2 * tiles + 1; }
 
 cudaError_t launch_twoshot_flags(int bits, int dtype, int R, const void *const *x, long long n, void *const *y,
-                                 void *ws, void *flags, cudaStream_t s) {
+                                 void *ws, void *flags, int drop_sender, cudaStream_t s) {
     ConstPtrs xp{};
     MutPtrs yp{};
     for (int r = 0; r < R; ++r) {
@@ -274,7 +277,8 @@ cudaError_t launch_twoshot_flags(int bits, int dtype, int R, const void *const *
     uint32_t *f = static_cast<uint32_t *>(flags);
 #define QR_CASE(B)                                                                                  \
     case B:                                                                                         \
-        return dtype ? run_flags_r<B, 1>(R, xp, n, yp, w, f, s) : run_flags_r<B, 0>(R, xp, n, yp, w, f, s);
+        return dtype ? run_flags_r<B, 1>(R, xp, n, yp, w, f, drop_sender, s)                       \
+                     : run_flags_r<B, 0>(R, xp, n, yp, w, f, drop_sender, s);
     switch (bits) {
         QR_CASE(3)
         QR_CASE(4)

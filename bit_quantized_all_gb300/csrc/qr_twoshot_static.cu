@@ -14,15 +14,14 @@
 // In host code `g_twoshot_workspace` names a host-side stand-in, not a device
 // address; a kernel given it would fault (or, where the GPU can reach host
 // memory, silently use the wrong memory).  The device address is obtained
-// with cudaGetSymbolAddress once per device, with that device current, on
-// the first call made while it is current, and cached.
+// with cudaGetSymbolAddress once per CUDA context, with that context's
+// device current, on the first call made in it, and cached per context.
 #include <cstdint>
-#include <map>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "../../include/qr.h"
+#include "qr_launch.h"
 
 #define QR_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -30,25 +29,12 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_twoshot_workspace[QR_TWOSHOT_STATIC_WORKSPACE_BYTES];
 
-// the workspace's device address for the current device (set up on first use)
+// The workspace's device address in the current context.  It is looked up
+// with cudaGetSymbolAddress once per CUDA context (with that context's
+// device current) and cached under the context's id, so that after a
+// cudaDeviceReset the address from the torn-down context is never reused.
 cudaError_t workspace_address(void **ptr) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    static std::mutex mu;
-    static std::map<int, void *> addr;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = addr.find(dev);
-    if (it != addr.end()) {
-        *ptr = it->second;
-        return cudaSuccess;
-    }
-    void *p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_twoshot_workspace);
-    if (err != cudaSuccess) return err;
-    addr[dev] = p;
-    *ptr = p;
-    return cudaSuccess;
+    return qrk::context_symbol_address(reinterpret_cast<const void *>(&g_twoshot_workspace), ptr);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -54,11 +54,24 @@
  *   - An output may alias an input of the same call exactly (same pointer,
  *     in-place) where noted; partial overlap is rejected.
  *   - Calls are thread-safe.  The library keeps only a per-device cache of
- *     launch limits (SM count, occupancy, the staged kernels' shared-memory
- *     limits), filled on first use, and a per-device counter of device-side
- *     waits that ran out (qr_wait_timeouts).  The first launch of each
- *     staged kernel on a device does this setup (a function attribute and a
- *     symbol address); make it before any stream capture.
+ *     launch limits (SM count, occupancy), a per-context cache of what lives
+ *     in a CUDA context (the staged kernels' shared-memory limits, the
+ *     device addresses of the library's own device variables), filled on
+ *     first use, and a counter of device-side waits that ran out
+ *     (qr_wait_timeouts).  The first launch of each staged kernel in a
+ *     context does this setup (a function attribute and a symbol address);
+ *     make it before any stream capture.  The per-context entries are keyed
+ *     by the context's id, so after cudaDeviceReset (or any other teardown
+ *     and re-creation of the context) the first call in the new context
+ *     repeats the setup instead of reusing addresses of the old one.
+ *   - Failure of a device-side wait: the staged kernels and the flag-joined
+ *     two-shot bound every wait (one second).  A wait that runs out (which
+ *     a correct launch never does) makes the kernel stop early and count
+ *     one timeout; the call has already returned QR_OK, because it returns
+ *     when the work is enqueued, and its outputs are then incomplete.  To
+ *     detect this, call qr_wait_timeouts after the work has been enqueued:
+ *     it waits for the device and returns the number of such timeouts since
+ *     the last call (0 when every launch completed).
  */
 #ifndef QR_H
 #define QR_H
@@ -253,10 +266,12 @@ qr_status_t qr_allreduce_twoshot_flags(int bits, qr_dtype_t dtype, int R,
  *     QR_TWOSHOT_STATIC_WORKSPACE_BYTES returns QR_ERR_SIZE and does nothing
  *     (32 MiB holds, for example, R=8 at INT4 up to 6.6 M values per rank, at
  *     INT8 up to 3.5 M).
- *   - The first call made while a device is current looks up the buffer's
- *     device address on that device (cudaGetSymbolAddress); make that first
- *     call before any stream capture.  It allocates nothing, and neither does
- *     any later call.
+ *   - The first call made in a CUDA context looks up the buffer's device
+ *     address in that context (cudaGetSymbolAddress, with the context's
+ *     device current); make that first call before any stream capture.  The
+ *     address is cached per context, so a context re-created after
+ *     cudaDeviceReset gets its own lookup.  It allocates nothing, and neither
+ *     does any later call.
  *   - All calls share the one buffer, and it keeps the last call's contents.
  *     Nothing in it needs to start at zero (every byte a call reads is
  *     written by that call first), but calls that overlap on the GPU (on two
@@ -271,20 +286,40 @@ qr_status_t qr_allreduce_twoshot_static(int bits, qr_dtype_t dtype, int R,
 
 /* Device-side waits that ran out (no counterpart on the source pages; a
  * safety property of this library).  A kernel that waits on a shared-memory
- * barrier gives each wait one second; if a wait runs out (which a correct
- * launch never does) the kernel adds one to a per-device counter, stops
- * issuing work, waits (again bounded) for its own copies in flight and
- * returns, leaving the context usable; its outputs are then incomplete.
- * qr_wait_timeouts stores the current device's count in *count and resets
- * it to zero; it synchronizes with the device (a blocking copy), so call it
- * between steps, not inside a stream capture.  QR_ERR_INVALID_ARG for a
- * null `count`, QR_ERR_CUDA if the copy fails. */
+ * barrier or on another CTA's flag gives each wait one second; if a wait
+ * runs out (which a correct launch never does) the kernel adds one to a
+ * counter (one per device in the current context), stops issuing work,
+ * waits (again bounded) for its own copies in flight and returns, leaving
+ * the context usable; its outputs are then incomplete, although the call
+ * that enqueued it returned QR_OK.  A flag-joined two-shot launch that
+ * fails counts exactly one timeout, however many of its waits give up.
+ * qr_wait_timeouts first waits for all work this process has enqueued on
+ * the current device (cudaDeviceSynchronize), then reads the counter and
+ * resets it to zero in one atomic step (an increment is never lost between
+ * the read and the reset), and stores the count in *count.  Call it between
+ * steps, never inside a stream capture.  QR_ERR_INVALID_ARG for a null
+ * `count`, QR_ERR_CUDA if a CUDA call fails. */
 qr_status_t qr_wait_timeouts(unsigned *count);
 
 /* Self-test of the bounded wait: enqueues one single-thread kernel on
  * `stream` that waits on a barrier nothing completes; after one second it
  * gives up and adds one to the qr_wait_timeouts counter.  Only for tests. */
 qr_status_t qr_selftest_bounded_wait(qr_stream_t stream);
+
+/* Self-test of the flag-joined two-shot's failure path (no counterpart on
+ * the source pages; only for tests): qr_allreduce_twoshot_flags with the
+ * same arguments, except that sender `drop_sender` (0 <= drop_sender < R,
+ * else QR_ERR_INVALID_ARG) writes its quantized tiles into the owners'
+ * buffers but never raises their "sent" flags, as a peer that stopped
+ * would.  Every owner's wait then runs out after one second, the launch
+ * raises the workspace's abort word (flag word 2T), counts exactly one
+ * timeout (qr_wait_timeouts) and returns; the outputs are incomplete.  The
+ * next normal call over the same workspace is unaffected (each call clears
+ * the flag words before its launch). */
+qr_status_t qr_selftest_twoshot_flags_drop(int bits, qr_dtype_t dtype, int R,
+                                           const void *const *x, size_t n, void *const *y,
+                                           void *workspace, size_t workspace_bytes,
+                                           int drop_sender, qr_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * The Flash Communication codec ([FC] key machinery "asymmetric group-128

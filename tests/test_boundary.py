@@ -280,6 +280,12 @@ def test_twoshot_validation():
     assert fcall(5, 0, 2, xs, n, ys, WS, fneed) == qr.QR_ERR_UNSUPPORTED
     assert fcall(4, 0, 2, xs, n, ys, None, fneed) == qr.QR_ERR_INVALID_ARG
     assert qr.lib().qr_twoshot_flags_workspace_bytes(4, 9, n) == 0
+    # the failure-path self-test: the same checks, and the dropped sender must be a rank
+    dcall = capi.qr_selftest_twoshot_flags_drop
+    for drop in (-1, 2, 8):
+        assert dcall(4, 0, 2, xs, n, ys, WS, fneed, drop) == qr.QR_ERR_INVALID_ARG
+    assert dcall(4, 0, 2, xs, n, ys, WS, fneed - 1, 0) == qr.QR_ERR_SIZE
+    assert dcall(4, 0, 2, xs, n, ys, WS + 8, fneed, 1) == qr.QR_ERR_MISALIGNED
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):

@@ -201,3 +201,40 @@ def test_flags_in_place_and_large():
         for y in ys:
             assert torch.equal(y.view(torch.int16), yf.view(torch.int16)), bits
     assert qr.qr_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("R,drop", [(2, 1), (8, 0), (8, 5)])
+def test_flags_wait_runs_out_when_a_sender_never_announces(R, drop):
+    """The failure path of the flag-joined protocol: sender `drop` writes its
+    tiles into the owners' buffers but never raises their flags (as a peer
+    that stopped would).  The owners' waits give up after one second; the
+    launch returns, raises the abort word, counts exactly one timeout, and
+    leaves the context usable: the next normal call over the same workspace
+    matches the oracle bit for bit."""
+    n, bits, dtype = 2048 * 40 + 11, 4, 1
+    xs = _rand_ranks(R, n, dtype, 900 + 10 * R + drop)
+    xs_dev = [to_dev(x, dtype) for x in xs]
+    ws = torch.empty(qr.lib().qr_twoshot_flags_workspace_bytes(bits, R, n), dtype=torch.uint8, device="cuda")
+    ys = [torch.zeros_like(xs_dev[0]) for _ in range(R)]
+    assert qr.qr_wait_timeouts() == 0
+    from bit_quantized_all_gb300 import capi
+    st = torch.cuda.current_stream().cuda_stream
+    status = capi.qr_selftest_twoshot_flags_drop(bits, dtype, R, [x.data_ptr() for x in xs_dev], n,
+                                                 [y.data_ptr() for y in ys], ws.data_ptr(), ws.numel(), drop, st)
+    assert status == qr.QR_OK  # enqueued; the failure shows only on the device
+    torch.cuda.synchronize()
+    assert qr.qr_wait_timeouts() == 1
+    T = -(-n // 2048)
+    off = -(-qr.qr_twoshot_workspace_bytes(bits, R, n) // 16) * 16
+    words = ws[off: off + 4 * (2 * T + 1)].cpu().numpy().view(np.uint32)
+    assert words[2 * T] == 1  # the abort word
+    sent = words[:T]
+    assert np.all(sent <= R - 1)  # no chunk ever saw all R announcements
+    assert np.all(words[T:2 * T] == 0)  # nothing was reduced
+    # a normal call over the same workspace
+    ys2, _ = qr.qr_allreduce_twoshot(bits, xs_dev, workspace=ws, flags=True)
+    torch.cuda.synchronize()
+    y_ref = oracle.allreduce(bits, dtype, xs)
+    for j, y in enumerate(ys2):
+        assert_outputs_match(to_host_u16(y), y_ref, dtype, xmax_of(xs, dtype), f"after the drop, rank {j}")
+    assert qr.qr_wait_timeouts() == 0
