@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Benchmark of the fused quantize -> reduce -> dequantize all-reduce codec.
 
-Workload: R = 8 ranks, 2^27 bf16 values per rank (32 x 1024 x 4096, 256 MiB
-per rank, 2 GiB of input per call), N(0,1) with 8 seeded outlier channels x20.
+Workload: the message-size sweep's point R = 8 ranks, 2^27 bf16 values per
+rank (256 MiB per rank, 2 GiB of input per call), N(0,1) viewed as rows of
+4096 channels with 8 seeded outlier channels x20.
 One step = one fused qr_allreduce at INT4 and one at INT3 over the same
 inputs (the whole hot path: send-path quantize, Phase-1B decode + fp32 sum +
 re-quantize, Phase-2 decode), two kernel launches.  The inputs (2 GiB) exceed
@@ -44,7 +45,8 @@ N = 1 << 27
 DTYPE = workloads.BF16
 BITS = (4, 3)
 SEED = 5
-WORKLOAD = "allreduce R=8 x 32x1024x4096 bf16 per rank (256 MiB/rank), fused INT4 + INT3 per step"
+WORKLOAD = ("sweep point R=8, 2^27 bf16 values per rank (256 MiB/rank, N(0,1) + 8 outlier channels x20), "
+            "fused INT4 + INT3 all-reduce per step")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -54,7 +56,7 @@ def set_values_per_rank(n: int) -> None:
         if n <= 0 or n % 2048:
             raise SystemExit("--values-per-rank must be a positive multiple of 2048")
         N = n
-        WORKLOAD = f"allreduce R=8 x {n} bf16 values per rank (profiling case), fused INT4 + INT3 per step"
+        WORKLOAD = f"sweep point R=8, {n} bf16 values per rank (profiling case), fused INT4 + INT3 per step"
 
 
 def tile_bytes(bits: int) -> int:
@@ -231,10 +233,10 @@ def run_reference(args) -> None:
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config({"reference_step": f"{step_tiles} tiles of every rank, INT4 and INT3"}),
+        "config": config(),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{step_tiles} consecutive tiles per step (of {N // 2048}), "
-                                   f"{threads} threads"},
+                         "sample": f"{step_tiles} consecutive tiles of every rank per step (of {N // 2048}), "
+                                   f"INT4 and INT3, {threads} threads"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -683,6 +685,118 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                 torch.cuda.empty_cache()
 
 
+def _graph_times(fn, reps, burst, flush, torch):
+    """CUDA-event times (ms per call) of `burst` calls of `fn` captured in one
+    CUDA graph and replayed `reps` times; with `flush` the L2 is evicted
+    before each replay (each sample then starts on cold data)."""
+    fn()  # the first use of each kernel (per-context setup) outside the capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(burst):
+                fn()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        else:
+            torch.cuda._sleep(1 << 16)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1) / burst)
+    return out
+
+
+def run_configs(args) -> None:
+    """GPU throughput on the four named workloads (c1..c4 of workloads.py),
+    every width each one lists, fused and unfused arms, with the L2 evicted
+    before every call (cold: inputs come from HBM) and back to back (warm:
+    inputs that fit the 129 MB L2 stay there); GPU time per call from CUDA
+    graph replays, so the host's per-call overhead is not in it.  Beside each
+    workload, the oracle on the host cores (one thread and all)."""
+    import torch
+
+    from bit_quantized_all_gb300 import build
+    build.build()
+    import bit_quantized_all_gb300 as qr
+    import oracle as orc
+    orc.build()
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    peak, peak_src = measured_hbm()
+    flush = L2Flush(dev)
+    cores = os.cpu_count() or 1
+    W = workloads
+    for cfg in (W.C1, W.C2, W.C3, W.C4):
+        Rs, n, dtype = cfg["R"], cfg["N"], cfg["dtype"]
+        tdt = torch.float16 if dtype == W.FP16 else torch.bfloat16
+        xs_host = W.ranks(cfg)
+        xs = [torch.from_numpy(x.view(np.int16)).to(dev).view(tdt) for x in xs_host]
+        y = torch.empty(n, dtype=tdt, device=dev)
+        yu = torch.empty(n, dtype=tdt, device=dev)
+        in_bytes = Rs * n * 2
+        for bits in cfg["bits"]:
+            Wb = qr.qr_wire_bytes(bits, n)
+            wires = [torch.empty(Wb, dtype=torch.uint8, device=dev) for _ in range(Rs)]
+            red = torch.empty(Wb, dtype=torch.uint8, device=dev)
+
+            def fused():
+                qr.qr_allreduce(bits, xs, y=y)
+
+            def unfused():
+                for r in range(Rs):
+                    qr.qr_encode(bits, xs[r], wire=wires[r])
+                qr.qr_segment_reduce(bits, wires, n, out=red)
+                qr.qr_decode(bits, red, n, y=yu)
+
+            alg = {"fused": 2 * Rs * n + 2 * n, "unfused": 2 * Rs * n + 2 * n + 2 * (Rs + 1) * Wb}
+            launches = {"fused": 1, "unfused": Rs + 2}
+            fused()
+            unfused()
+            torch.cuda.synchronize()
+            same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
+            for name, fn in (("fused", fused), ("unfused", unfused)):
+                for l2 in ("cold", "warm"):
+                    t = _graph_times(fn, args.reps, 1 if l2 == "cold" else args.burst,
+                                     flush if l2 == "cold" else None, torch)
+                    med = statistics.median(t)
+                    fits = alg[name] <= 129e6
+                    print(json.dumps({
+                        "config": cfg["name"], "R": Rs, "values_per_rank": n,
+                        "storage": "fp16" if dtype == W.FP16 else "bf16", "bits": bits, "arm": name,
+                        "launches_per_call": launches[name], "l2": l2,
+                        "l2_note": ("evicted before each call (write then read 256 MiB)" if l2 == "cold" else
+                                    (f"{args.burst} calls back to back; the call's bytes fit the 129 MB L2"
+                                     if fits else f"{args.burst} calls back to back; larger than the L2")),
+                        "gpu_us_per_call": round(med * 1e3, 3),
+                        "input_gbs": round(in_bytes / (med / 1e3) / 1e9, 2),
+                        "alg_bytes": alg[name], "alg_gbs": round(alg[name] / (med / 1e3) / 1e9, 2),
+                        "frac_of_hbm": round(alg[name] / (med / 1e3) / 1e9 / peak, 4), "peak_gbs": peak,
+                        "peak_source": peak_src, "fused_equals_unfused": same, "reps": args.reps,
+                        "timing": "CUDA graph replays, median"}), flush=True)
+            del wires, red
+        # the oracle on the host cores: the whole workload (c4: its first 2048 tiles)
+        T = -(-n // 2048)
+        tiles = T if cfg["name"] != "c4" else min(T, 2048)
+        for threads in (1, cores):
+            gbs, vps, reps, dt, used = _time_oracle(orc, xs_host, dtype, cfg["bits"], tiles, threads, min_s=1.0)
+            print(json.dumps({"config": cfg["name"], "arm": "cpu_oracle", "R": Rs, "values_per_rank": n,
+                              "bits": list(cfg["bits"]), "threads": used, "cores": cores,
+                              "input_gbs": round(gbs, 4), "values_per_s": round(vps, 1),
+                              "sample": f"{'all' if tiles == T else 'first'} {tiles} of {T} tiles per rank, "
+                                        f"every width, {reps} passes in {dt:.1f} s"}), flush=True)
+        del xs, y, yu, xs_host
+        torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -706,6 +820,9 @@ def main() -> None:
                     help="sweep: back-to-back launches of one arm per timed sample where L2 is not flushed")
     ap.add_argument("--cpu-sweep", action="store_true",
                     help="time the CPU oracle on every workload (1 thread and all cores); no GPU")
+    ap.add_argument("--configs", action="store_true",
+                    help="GPU throughput on the named workloads c1..c4 (every width, fused and unfused, "
+                         "cold and warm L2), with the oracle on the host cores beside each")
     ap.add_argument("--sweep-R", default="2,4,8", help="rank counts for --sweep")
     ap.add_argument("--sweep-bits", default="8,6,4,3", help="code widths for --sweep")
     ap.add_argument("--sweep-dtypes", default="fp16,bf16", help="storage types for --sweep")
@@ -717,6 +834,9 @@ def main() -> None:
         return
     if args.cpu_sweep:
         run_cpu_sweep(args)
+        return
+    if args.configs:
+        run_configs(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -66,11 +66,28 @@ __device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
 
 // f = clip(RN(v*r), qmin, qmax) + 1.5*2^23 + bias (the code in the low byte),
 // with the clip at qmin only where block_scale2 says it can matter.
+//
+// INT3 without the lower clip leaves the upper one to the packing: for a
+// normal scale every t = RN(v*r) is at most |qmin|*(1 + 2^-10.9), so its code
+// is at most |qmin| + bias = 8, which still fits the nibble that pack_pair_q3
+// builds and where one subtraction per eight codes turns 8 into 7 -- the same
+// code as clipping t at qmax first (t <= 3 is unchanged by the clip; for
+// t > 3, RNE(t) + 4 is 7 or 8 and becomes 7, as RNE(3) + 4 is).  That
+// removes one float minimum (integer-pipe work) per value.  The products are then scalar multiplies: a packed multiply whose
+// only use is a packed add is contracted into one rounding by the compiler,
+// which would change the codes.
 template <int B>
 __device__ __forceinline__ void quantize_block_magic(const float2 (&v)[16], float r, bool low_clip,
                                                      float2 (&f)[16]) {
     const float2 r2 = make_float2(r, r);
     const float2 m2 = make_float2(Codec<B>::kMagic, Codec<B>::kMagic);
+    if constexpr (B == 3) {
+        if (!low_clip) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = __fadd2_rn(make_float2(__fmul_rn(v[i].x, r), __fmul_rn(v[i].y, r)), m2);
+            return;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         float2 t = __fmul2_rn(v[i], r2);
@@ -133,15 +150,19 @@ __device__ __forceinline__ uint32_t slot_nibbles(const float2 *f) {
 // slots' q2w (slot 2h in bits 0..15), X = their q1w (slot 2h in bits 0..7,
 // slot 2h+1 in 8..15).  The inverse of unpack_pair_q3: the codes go into
 // nibbles (even lanes in one word, odd lanes in another) by multiply-add
-// chains, the q2 fields come out with one mask, and the q1 bits, masked to
-// every fourth bit, are gathered by three shift-and-mask steps.
+// chains, a code of 8 (a value quantize_block_magic left unclipped at qmax)
+// becomes 7 by one subtraction per eight nibbles, the q2 fields come out with
+// one mask, and the q1 bits, masked to every fourth bit, are gathered by
+// three shift-and-mask steps.
 __device__ __forceinline__ void pack_pair_q3(const float2 (&f)[16], int h, uint32_t &W, uint32_t &X) {
     const int a = 8 * h, b = 8 * h + 4;  // f index of lane 0 of slot 2h, of slot 2h+1
-    // nibble 4i+m: lane 2m (e) / 2m+1 (o) of slot 2h+i
-    const uint32_t e = __byte_perm(nibbles4_lo16(f[a].x, f[a + 1].x, f[a + 2].x, f[a + 3].x),
-                                   nibbles4_lo16(f[b].x, f[b + 1].x, f[b + 2].x, f[b + 3].x), 0x5410);
-    const uint32_t o = __byte_perm(nibbles4_lo16(f[a].y, f[a + 1].y, f[a + 2].y, f[a + 3].y),
-                                   nibbles4_lo16(f[b].y, f[b + 1].y, f[b + 2].y, f[b + 3].y), 0x5410);
+    // nibble 4i+m: lane 2m (e) / 2m+1 (o) of slot 2h+i; every nibble is a code 0..8
+    uint32_t e = __byte_perm(nibbles4_lo16(f[a].x, f[a + 1].x, f[a + 2].x, f[a + 3].x),
+                             nibbles4_lo16(f[b].x, f[b + 1].x, f[b + 2].x, f[b + 3].x), 0x5410);
+    uint32_t o = __byte_perm(nibbles4_lo16(f[a].y, f[a + 1].y, f[a + 2].y, f[a + 3].y),
+                             nibbles4_lo16(f[b].y, f[b + 1].y, f[b + 2].y, f[b + 3].y), 0x5410);
+    e -= (e >> 3) & 0x11111111u;  // 8 -> 7 (bit 3 of a nibble is set only by 8)
+    o -= (o >> 3) & 0x11111111u;
     W = (e & 0x33333333u) | ((o << 2) & 0xCCCCCCCCu);
     uint32_t x = ((e >> 2) & 0x11111111u) | ((o >> 1) & 0x22222222u);
     x = (x | (x >> 2)) & 0x0F0F0F0Fu;
