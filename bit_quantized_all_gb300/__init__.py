@@ -42,7 +42,10 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_allreduce_staged", "qr_fc_allreduce_staged", "qr_fc_allreduce_ctas",
            "qr_segment_reduce_staged", "qr_fc_segment_reduce_staged", "qr_twoshot_flags_workspace_bytes",
            "qr_allreduce_twoshot_flags", "qr_fp4_tile_bytes", "qr_fp4_wire_bytes", "qr_fp4_encode",
-           "qr_fp4_decode", "qr_fp4_segment_reduce", "qr_fp4_allreduce", "qr_selftest_twoshot_flags_drop")
+           "qr_fp4_decode", "qr_fp4_segment_reduce", "qr_fp4_allreduce", "qr_selftest_twoshot_flags_drop",
+           "qr_twoshot_peer_workspace_bytes", "qr_twoshot_peer_send", "qr_twoshot_peer_reduce",
+           "qr_twoshot_peer_decode", "qr_ipc_handle_bytes", "qr_ipc_get_handle", "qr_ipc_open_handle",
+           "qr_ipc_close_handle")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"

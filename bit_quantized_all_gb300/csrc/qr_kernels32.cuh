@@ -758,11 +758,11 @@ __global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, u
 // exact), re-quantize.
 // Phase-1B of one 32-value block from its R ranks' codes c[r] and fp16 scale
 // bits sb[r]: decode, add in fp32 in rank order (fma(q, s, acc) =
-// RN(acc + q*s): q*s is exact), re-quantize, and write the block's codes
-// and scale into `tile` (block g).
+// RN(acc + q*s): q*s is exact), re-quantize; the block's codes go to cw and
+// its fp16 scale bits to scale_bits.
 template <int B, int R>
-__device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
-                                             int g) {
+__device__ __forceinline__ void reduce_block_words(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
+                                                   BlockWords<B> &cw, uint32_t &scale_bits) {
     float2 acc[16];
     if constexpr (B == 3) {
         // codes decoded to fp16 through E2M1, scaled and summed by fp16-operand
@@ -840,7 +840,6 @@ __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const 
     const BlockScale2 sc = block_scale2<B>(block_absmax(acc));
     float2 f[16];
     quantize_block_magic<B>(acc, sc.r, sc.low_clip, f);
-    BlockWords<B> cw;
     if constexpr (B == 4 && R >= 4) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) cw.w[k] = slot_nibbles_m4(&f[4 * k]);
@@ -858,8 +857,18 @@ __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const 
     } else {
         pack_block<B>(f, cw);
     }
+    scale_bits = sc.bits;
+}
+
+// reduce_block_words, written into `tile` as its block g.
+template <int B, int R>
+__device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
+                                             int g) {
+    BlockWords<B> cw;
+    uint32_t bits;
+    reduce_block_words<B, R>(c, sb, cw, bits);
     store_block_codes<B>(tile, g, cw);
-    store_block_scale<B>(tile, g, sc.bits);
+    store_block_scale<B>(tile, g, bits);
 }
 
 template <int B, int R, int U>

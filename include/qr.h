@@ -284,6 +284,72 @@ qr_status_t qr_allreduce_twoshot_static(int bits, qr_dtype_t dtype, int R,
                                         const void *const *x, size_t n,
                                         void *const *y, qr_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * The two-shot all-reduce run by R separate ranks, each in its own process
+ * (or on its own GPU), storing into the other ranks' workspaces ([QR]
+ * Design Highlights: Phase-1 sends segment k of every rank's quantized
+ * message to owner k, Phase-1B the owner reduces its segment, Phase-2 every
+ * rank gathers all segments; [FC] key machinery: all-to-all, local sum and
+ * re-quantization, all-gather, over peer-to-peer GPU memory access).
+ * Every rank owns a workspace of qr_twoshot_peer_workspace_bytes(bits, R, n)
+ * bytes (device, 16-byte aligned) in its own memory; with seg = ceil(T/R)
+ * tiles of the T-tile wire it holds
+ *   recv[s]  at byte (s*seg) * qr_tile_bytes(bits), s = 0..R-1: sender s's
+ *            quantized copy of the segment this rank owns (segment j of rank
+ *            j: tiles [j*seg, (j+1)*seg));
+ *   gathered at byte (R*seg) * qr_tile_bytes(bits): the reduced wire in tile
+ *            order, byte-identical to qr_segment_reduce's output.
+ * One step is three calls on every rank, in this order: qr_twoshot_peer_send,
+ * qr_twoshot_peer_reduce, qr_twoshot_peer_decode.  Before a rank starts a
+ * call, the previous call of EVERY rank must have finished on the GPU (the
+ * caller joins the ranks, for example by synchronizing its stream and
+ * meeting the others at a host barrier): no kernel of these calls waits on
+ * another rank, and a call of one rank reads what the previous call of the
+ * other ranks wrote.  `workspaces` is a host array of R device pointers, as
+ * mapped in the calling process: entry r is rank r's workspace (the caller's
+ * own at entry `rank`; the others opened with qr_ipc_open_handle, or
+ * reached by peer access between GPUs of one process); workspaces must not
+ * overlap.  Every rank's decoded output equals qr_allreduce's output over
+ * the R messages.  Loads and stores only: no bulk copy or multicast touches
+ * another rank's memory.  Errors as for qr_allreduce_twoshot; `rank` outside
+ * [0, R) is QR_ERR_INVALID_ARG.  0 from the size call means unsupported
+ * bits or R, n == 0, or overflow. */
+size_t qr_twoshot_peer_workspace_bytes(int bits, int R, size_t n); /* 2*R*seg tiles */
+
+/* Phase-1 of rank `rank`: quantize its n values `x` and store segment k of
+ * the wire into recv[rank] of workspaces[k], for every k. */
+qr_status_t qr_twoshot_peer_send(int bits, qr_dtype_t dtype, int R, int rank,
+                                 const void *x, size_t n, void *const *workspaces,
+                                 qr_stream_t stream);
+
+/* Phase-1B of owner `rank`: decode the R copies recv[0..R-1] of its segment
+ * from workspaces[rank], sum them in fp32 in sender order, re-quantize, and
+ * store the reduced tiles into the gathered wire of every workspace (the
+ * all-gather).  An owner past the last tile (R > T) does nothing. */
+qr_status_t qr_twoshot_peer_reduce(int bits, int R, int rank, size_t n,
+                                   void *const *workspaces, qr_stream_t stream);
+
+/* Phase-2 of a rank: decode the gathered wire of its own `workspace` into
+ * its n-value output `y` (which must not overlap the workspace). */
+qr_status_t qr_twoshot_peer_decode(int bits, qr_dtype_t dtype, int R, size_t n,
+                                   const void *workspace, void *y, qr_stream_t stream);
+
+/* Sharing a device buffer with another process (no counterpart on the source
+ * pages; the plumbing of the per-rank two-shot).  A handle is
+ * QR_IPC_HANDLE_BYTES bytes of host memory: the CUDA IPC handle of the
+ * allocation that holds `dev_ptr`, followed by the offset of `dev_ptr` in
+ * it (so buffers carved out of a larger allocation can be shared).
+ * qr_ipc_get_handle fills `handle`; qr_ipc_open_handle, in another process
+ * on the same node, maps it and stores the buffer's address in *dev_ptr;
+ * qr_ipc_close_handle unmaps a pointer qr_ipc_open_handle returned.  A
+ * process cannot open its own handles.  QR_ERR_INVALID_ARG for null
+ * arguments or an unknown pointer, QR_ERR_CUDA if CUDA refuses. */
+#define QR_IPC_HANDLE_BYTES 72
+size_t qr_ipc_handle_bytes(void); /* QR_IPC_HANDLE_BYTES */
+qr_status_t qr_ipc_get_handle(const void *dev_ptr, void *handle);
+qr_status_t qr_ipc_open_handle(const void *handle, void **dev_ptr);
+qr_status_t qr_ipc_close_handle(void *dev_ptr);
+
 /* Device-side waits that ran out (no counterpart on the source pages; a
  * safety property of this library).  A kernel that waits on a shared-memory
  * barrier or on another CTA's flag gives each wait one second; if a wait

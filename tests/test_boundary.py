@@ -288,6 +288,61 @@ def test_twoshot_validation():
     assert dcall(4, 0, 2, xs, n, ys, WS + 8, fneed, 1) == qr.QR_ERR_MISALIGNED
 
 
+def test_peer_workspace_bytes():
+    from bit_quantized_all_gb300 import peer
+    L = peer._lib()
+    for bits in (3, 4, 6, 8):
+        tb = qr.qr_tile_bytes(bits)
+        for R in (1, 2, 3, 8):
+            for n in (1, 2048, 2049, 2048 * 17 + 5, 2**27):
+                T = -(-n // 2048)
+                seg = -(-T // R)
+                assert L.qr_twoshot_peer_workspace_bytes(bits, R, n) == 2 * R * seg * tb
+    assert L.qr_twoshot_peer_workspace_bytes(5, 2, 100) == 0
+    assert L.qr_twoshot_peer_workspace_bytes(4, 0, 100) == 0
+    assert L.qr_twoshot_peer_workspace_bytes(4, 9, 100) == 0
+    assert L.qr_twoshot_peer_workspace_bytes(4, 2, 0) == 0
+    assert L.qr_twoshot_peer_workspace_bytes(8, 8, 2**64 - 1) == 0
+    assert L.qr_ipc_handle_bytes() == peer.QR_IPC_HANDLE_BYTES == 72
+
+
+@no_gpu_only
+def test_peer_validation():
+    from bit_quantized_all_gb300 import peer
+    L = peer._lib()
+    n = 2048 * 5 + 3
+    need = L.qr_twoshot_peer_workspace_bytes(4, 2, n)
+    W0, W1 = 0x7F3000000000, 0x7F4000000000
+    ws = peer._ptrs([W0, W1])
+    send, red, dec = L.qr_twoshot_peer_send, L.qr_twoshot_peer_reduce, L.qr_twoshot_peer_decode
+    assert send(4, 0, 2, 0, None, n, ws, None) == qr.QR_ERR_INVALID_ARG           # no input
+    assert send(4, 0, 2, 0, A, n, None, None) == qr.QR_ERR_INVALID_ARG            # no workspaces
+    assert send(4, 0, 2, 0, A, n, peer._ptrs([W0, None]), None) == qr.QR_ERR_INVALID_ARG
+    assert send(4, 0, 2, 2, A, n, ws, None) == qr.QR_ERR_INVALID_ARG              # rank out of range
+    assert send(4, 0, 2, -1, A, n, ws, None) == qr.QR_ERR_INVALID_ARG
+    assert send(4, 0, 2, 0, A, 0, ws, None) == qr.QR_ERR_INVALID_ARG
+    assert send(5, 0, 2, 0, A, n, ws, None) == qr.QR_ERR_UNSUPPORTED
+    assert send(4, 2, 2, 0, A, n, ws, None) == qr.QR_ERR_UNSUPPORTED              # dtype
+    assert send(4, 0, 9, 0, A, n, peer._ptrs([W0 + 2**30 * i for i in range(9)]), None) == qr.QR_ERR_UNSUPPORTED
+    assert send(4, 0, 2, 0, A + 8, n, ws, None) == qr.QR_ERR_MISALIGNED
+    assert send(4, 0, 2, 0, A, n, peer._ptrs([W0, W1 + 8]), None) == qr.QR_ERR_MISALIGNED
+    assert send(4, 0, 2, 0, A, n, peer._ptrs([W0, W0 + 64]), None) == qr.QR_ERR_INVALID_ARG   # overlapping
+    assert send(4, 0, 2, 0, W0 + 16, n, ws, None) == qr.QR_ERR_INVALID_ARG                   # input in a workspace
+    assert red(4, 2, 2, n, ws, None) == qr.QR_ERR_INVALID_ARG
+    assert red(4, 2, 0, n, None, None) == qr.QR_ERR_INVALID_ARG
+    assert red(4, 2, 0, n, peer._ptrs([W0, W0 + need - 16]), None) == qr.QR_ERR_INVALID_ARG
+    assert red(7, 2, 0, n, ws, None) == qr.QR_ERR_UNSUPPORTED
+    assert dec(4, 0, 2, n, None, Y, None) == qr.QR_ERR_INVALID_ARG
+    assert dec(4, 0, 2, n, W0, None, None) == qr.QR_ERR_INVALID_ARG
+    assert dec(4, 0, 2, n, W0 + 8, Y, None) == qr.QR_ERR_MISALIGNED
+    assert dec(4, 0, 2, n, W0, W0 + 32, None) == qr.QR_ERR_INVALID_ARG              # output in the workspace
+    assert dec(4, 3, 2, n, W0, Y, None) == qr.QR_ERR_UNSUPPORTED
+    assert L.qr_ipc_get_handle(None, None) == qr.QR_ERR_INVALID_ARG
+    assert L.qr_ipc_open_handle(None, None) == qr.QR_ERR_INVALID_ARG
+    assert L.qr_ipc_close_handle(None) == qr.QR_ERR_INVALID_ARG
+    assert L.qr_ipc_close_handle(W0) == qr.QR_ERR_INVALID_ARG                       # never opened
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qr, "LIB_PATH", str(tmp_path / "missing" / "libqr.so"))
     monkeypatch.setattr(qr, "_lib", None)

@@ -1,0 +1,130 @@
+"""The per-rank two-shot all-reduce with the library's kernels: R processes
+on the one GPU, each with its own CUDA context, its own workspace and its own
+message, the peers' workspaces mapped through CUDA IPC (qr_ipc_*), the
+phases joined by host barriers (no kernel waits on another process).
+
+Every rank's output equals the oracle's all-reduce of the R messages bit for
+bit, and the fused kernel's output in that process; the gathered wire in
+every rank's workspace equals the oracle's Phase-1B output byte for byte; two
+steps run in a row over the same workspaces with different data; ragged
+tails and fewer tiles than ranks are covered.  The same calls on a multi-GPU
+node would store across NVLink; that is not measured here."""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from bit_quantized_all_gb300 import build
+    build.build()
+    import oracle
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _inputs(R, n, dtype, seed):
+    import oracle
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for r in range(R):
+        v = rng.standard_normal(n).astype(np.float32) * np.float32(1 + r)
+        v[rng.integers(0, n, size=max(1, n // 100))] *= 40.0
+        out.append(oracle.narrow(dtype, v))
+    return out
+
+
+def _worker(rank, world, port, cases, q):
+    sys.path.insert(0, ROOT)
+    os.environ["PYTORCH_CUDA_ALLOC_CONF"] = "expandable_segments:False"  # IPC needs plain allocations
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(0)
+    import bit_quantized_all_gb300 as qr
+    import oracle
+    from bit_quantized_all_gb300.peer import PeerTwoShot, init_group
+    tdt = {0: torch.float16, 1: torch.bfloat16}
+    group = init_group(rank, world, port, timeout_s=120.0)
+    try:
+        for ci, (bits, n, dtype) in enumerate(cases):
+            peer = PeerTwoShot(bits, n, dtype, group=group)
+            T = -(-n // 2048)
+            seg = -(-T // world)
+            tb = qr.qr_tile_bytes(bits)
+            for step in range(2):
+                xs = _inputs(world, n, dtype, 1000 * ci + 10 * step + 3)
+                dev = [torch.from_numpy(x.view(np.int16)).cuda().view(tdt[dtype]) for x in xs]
+                y = peer.allreduce_tensor(dev[rank])
+                torch.cuda.synchronize()
+                got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+                ref = oracle.allreduce(bits, dtype, xs)
+                fused = qr.qr_allreduce(bits, dev).view(torch.int16).cpu().numpy().view(np.uint16)
+                red_ref = oracle.segment_reduce(bits, [oracle.encode(bits, dtype, x) for x in xs], n)
+                g = world * seg * tb
+                red = peer.workspace[g: g + T * tb].cpu().numpy()
+                status = []
+                if not np.array_equal(got, ref):
+                    status.append(f"output differs from the oracle at {np.flatnonzero(got != ref)[:5]}")
+                if not np.array_equal(got, fused):
+                    status.append("output differs from the fused kernel")
+                if not np.array_equal(red, red_ref):
+                    status.append(f"gathered wire differs at byte {np.flatnonzero(red != red_ref)[:3]}")
+                q.put((rank, ci, step, "ok" if not status else "; ".join(status)))
+            peer.close()
+        q.put((rank, -1, -1, f"timeouts={qr.qr_wait_timeouts()}"))
+    except Exception as e:  # noqa: BLE001  (reported to the parent)
+        q.put((rank, -2, -2, f"exception: {type(e).__name__}: {e}"))
+    finally:
+        try:
+            dist.destroy_process_group()
+        except Exception:  # noqa: BLE001
+            pass
+
+
+def _run(world, cases):
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, cases, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=600)
+    alive = [p for p in procs if p.is_alive()]
+    for p in alive:
+        p.kill()
+    out = []
+    while not q.empty():
+        out.append(q.get())
+    assert not alive, f"{len(alive)} rank processes did not finish: {out}"
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    return out
+
+
+@pytest.mark.parametrize("world,cases", [
+    (2, [(4, 2048 * 40 + 37, 1), (3, 2048 * 9, 0), (8, 2048 * 3 + 1, 1), (6, 100, 0)]),
+    (4, [(4, 2048 * 40 + 37, 1), (3, 2048 * 9 + 5, 1), (6, 2048 * 2, 0), (8, 700, 1)]),
+    (8, [(4, 2048 * 64 + 11, 1), (3, 2048 * 5, 1)]),
+], ids=["R2", "R4", "R8"])
+def test_every_rank_matches_the_oracle(world, cases):
+    res = _run(world, cases)
+    steps = [r for r in res if r[1] >= 0]
+    assert len(steps) == world * len(cases) * 2, res
+    assert all(r[3] == "ok" for r in steps), [r for r in steps if r[3] != "ok"]
+    assert sorted(r[3] for r in res if r[1] == -1) == ["timeouts=0"] * world, res
+    assert not [r for r in res if r[1] == -2], res
