@@ -797,6 +797,83 @@ def run_configs(args) -> None:
         torch.cuda.empty_cache()
 
 
+def run_medium(args) -> None:
+    """Medium messages, R = 8, INT4, bf16.  (1) Back to back with every call
+    reading HBM: K sets of the inputs (and K outputs) spanning at least
+    640 MiB, one CUDA graph of K calls, set k by call k; beside it K device
+    copies of 9N bytes (the 18N bytes a fused call moves), the size-matched
+    bandwidth.  (2) One call after an L2 eviction, for the default launch,
+    the register-fed kernel at several CTA counts and the staged kernel at
+    several CTA counts."""
+    import torch
+
+    from bit_quantized_all_gb300 import build
+    build.build()
+    import bit_quantized_all_gb300 as qr
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    peak, peak_src = measured_hbm()
+    Rm = 8
+    sizes = [int(v) for v in args.sweep_sizes.split(",")] if args.sweep_sizes else \
+        [1 << 20, 1 << 21, 1 << 22, 5242880, 1 << 23, 1 << 24, 1 << 25]
+
+    def graph_per_call(fns, reps):
+        for f in fns:
+            f()
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for f in fns:
+                    f()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            torch.cuda._sleep(1 << 16)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts) / len(fns)
+
+    flush = L2Flush(dev)
+    for n in sizes:
+        K = max(2, -(-(640 << 20) // (2 * Rm * n)))
+        base = [x.view(torch.bfloat16) for x in workloads.device_sweep(Rm, n, workloads.BF16, seed=SEED, device=dev)]
+        sets = [[b.clone() for b in base] for _ in range(K)]
+        ys = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        t_f = graph_per_call([(lambda k=k: qr.qr_allreduce(4, sets[k], y=ys[k])) for k in range(K)], args.reps)
+        alg = 2 * Rm * n + 2 * n
+        src = [torch.empty(alg // 2, dtype=torch.uint8, device=dev) for _ in range(K)]
+        dst = [torch.empty(alg // 2, dtype=torch.uint8, device=dev) for _ in range(K)]
+        t_c = graph_per_call([(lambda k=k: dst[k].copy_(src[k])) for k in range(K)], args.reps)
+        print(json.dumps({"medium": "back_to_back", "R": Rm, "bits": 4, "values_per_rank": n, "rotated_sets": K,
+                          "fused_us": round(t_f * 1e3, 2), "fused_frac": round(alg / (t_f / 1e3) / 1e9 / peak, 3),
+                          "copy_of_same_bytes_us": round(t_c * 1e3, 2),
+                          "copy_frac": round(alg / (t_c / 1e3) / 1e9 / peak, 3),
+                          "fused_over_copy": round(t_c / t_f, 3), "peak_gbs": peak}), flush=True)
+        del src, dst, sets
+        y = ys[0]
+        arms = [("default", lambda: qr.qr_allreduce(4, base, y=y))]
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        for c in (sms // 2, sms, 2 * sms, 3 * sms, 4 * sms):
+            arms.append((f"register_fed_{c}", (lambda c=c: qr.qr_allreduce(4, base, y=y, ctas=c))))
+        for c in (sms // 2, 3 * sms // 4, sms):
+            arms.append((f"staged_{c}", (lambda c=c: qr.qr_allreduce_staged(4, base, y=y, ctas=c))))
+        for name, fn in arms:
+            med = statistics.median(_graph_times(fn, args.reps, 1, flush, torch))
+            print(json.dumps({"medium": "cold_single_call", "R": Rm, "bits": 4, "values_per_rank": n, "arm": name,
+                              "us": round(med * 1e3, 2), "frac": round(alg / (med / 1e3) / 1e9 / peak, 3)}),
+                  flush=True)
+        del base, ys, y
+        torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -820,6 +897,9 @@ def main() -> None:
                     help="sweep: back-to-back launches of one arm per timed sample where L2 is not flushed")
     ap.add_argument("--cpu-sweep", action="store_true",
                     help="time the CPU oracle on every workload (1 thread and all cores); no GPU")
+    ap.add_argument("--medium", action="store_true",
+                    help="medium messages (R=8 INT4): back-to-back calls against a copy of the same bytes, "
+                         "and single cold calls at several launch shapes")
     ap.add_argument("--configs", action="store_true",
                     help="GPU throughput on the named workloads c1..c4 (every width, fused and unfused, "
                          "cold and warm L2), with the oracle on the host cores beside each")
@@ -837,6 +917,9 @@ def main() -> None:
         return
     if args.configs:
         run_configs(args)
+        return
+    if args.medium:
+        run_medium(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
