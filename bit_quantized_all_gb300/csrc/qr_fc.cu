@@ -54,23 +54,24 @@ static cudaError_t run_fc_reduce_staged_t(const ConstPtrs &w, long long n, void 
 }
 
 // Where the default takes the staged Phase-1B kernel (tiles per SM from which
-// it does; 0 = never).  Measured on GB300 with bf16 messages, register-fed
-// against staged (five groups), fraction of the measured HBM bandwidth:
-//   R >= 6, and 8-bit inputs at R = 4, 5: staged from 48 (R=8 at 2^27: 4->4
-//     0.38 -> 0.53, 4->8 0.45 -> 0.58, 8->8 0.72 -> 1.00);
-//   R = 5 with 4-bit inputs, R = 4 with 4->8, R = 3 with 8->8: staged from 96
-//     (at 108 tiles per SM: 0.40 -> 0.45, 0.46 -> 0.49, 0.63 -> 0.70; at 54
-//     the register-fed kernel was 10-25% faster);
-//   otherwise (R <= 2; R = 3 with 4-bit inputs; R = 4 with 4->4) never: the
-//     decode arithmetic of few ranks, not memory latency, bounds the kernel
-//     and the register-fed grid has more warps (R=2 4->4 at 2^27: 0.50 ->
-//     0.39; R=4 4->4 within 3% either way from 2^26).
+// it does; 0 = never), else the register-fed kernel with two tiles in flight
+// per thread.  Measured on GB300 at 2^27 bf16 values per rank, fraction of the
+// measured HBM bandwidth, register-fed with one tile in flight / with two /
+// staged (five groups):
+//   4 -> 4: R=2 0.51 / 0.52 / 0.39, R=4 0.46 / 0.56 / 0.47, R=6 0.39 / 0.57 /
+//     0.51, R=8 0.39 / 0.58 / 0.53;
+//   4 -> 8: R=2 0.59 / 0.64 / 0.50, R=4 0.51 / 0.64 / 0.54, R=8 0.47 / 0.62 /
+//     0.58;
+//   8 -> 8: R=2 0.82 / 0.85 / 0.73, R=3 0.74 / 0.86 / 0.83, R=4 0.75 / 0.87 /
+//     0.88, R=6 0.61 / 0.90 / 0.95, R=8 0.74 / 0.93 / 1.01;
+// so the staged kernel only for 8-bit inputs from R = 4 (memory-bound there),
+// from 48 tiles per SM (below that the register-fed grid has more warps).
 template <int BIN, int BOUT, int R>
 __host__ __device__ constexpr long long staged_fc_reduce_min_tiles_per_sm() {
-    if (R >= 6 || (BIN == 8 && R >= 4)) return 48;
-    if ((BIN == 4 && R == 5) || (BIN == 4 && BOUT == 8 && R == 4) || (BIN == 8 && R == 3)) return 96;
-    return 0;
+    return (BIN == 8 && R >= 4) ? 48 : 0;
 }
+
+constexpr int kFcReduceUnroll = 2;  // tiles per thread in flight in the register-fed kernel
 
 template <int BIN, int BOUT, int R>
 static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
@@ -82,9 +83,10 @@ static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, c
         if (sms <= 0) return e;
         if (T >= kMinTilesPerSm * sms) return run_fc_reduce_staged_t<BIN, BOUT, R>(w, n, out, 0, s);
     }
-    auto kern = fc_reduce_kernel<BIN, BOUT, R>;
+    auto kern = fc_reduce_kernel<BIN, BOUT, R, kFcReduceUnroll>;
     cudaError_t err = cudaSuccess;
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, 4, &err);
+    const long long units = (T + kFcReduceUnroll - 1) / kFcReduceUnroll;
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, units, 0, 4, &err);
     if (grid <= 0) return err;
     kern<<<grid, kThreadsFc, 0, s>>>(w, n, static_cast<uint8_t *>(out), T);
     return cudaGetLastError();

@@ -145,22 +145,14 @@ __device__ __forceinline__ uint32_t slot_nibbles(const float2 *f) {
                        nibbles4_lo16(f[2].x, f[2].y, f[3].x, f[3].y), 0x5410);
 }
 
-// The INT3 fields of slots 2h and 2h+1 from their 16 magic floats (f[4s + m]
-// = lanes 2m, 2m+1 of slot s; the code is each float's low byte): W = the two
-// slots' q2w (slot 2h in bits 0..15), X = their q1w (slot 2h in bits 0..7,
-// slot 2h+1 in 8..15).  The inverse of unpack_pair_q3: the codes go into
-// nibbles (even lanes in one word, odd lanes in another) by multiply-add
-// chains, a code of 8 (a value quantize_block_magic left unclipped at qmax)
-// becomes 7 by one subtraction per eight nibbles, the q2 fields come out with
-// one mask, and the q1 bits, masked to every fourth bit, are gathered by
-// three shift-and-mask steps.
-__device__ __forceinline__ void pack_pair_q3(const float2 (&f)[16], int h, uint32_t &W, uint32_t &X) {
-    const int a = 8 * h, b = 8 * h + 4;  // f index of lane 0 of slot 2h, of slot 2h+1
-    // nibble 4i+m: lane 2m (e) / 2m+1 (o) of slot 2h+i; every nibble is a code 0..8
-    uint32_t e = __byte_perm(nibbles4_lo16(f[a].x, f[a + 1].x, f[a + 2].x, f[a + 3].x),
-                             nibbles4_lo16(f[b].x, f[b + 1].x, f[b + 2].x, f[b + 3].x), 0x5410);
-    uint32_t o = __byte_perm(nibbles4_lo16(f[a].y, f[a + 1].y, f[a + 2].y, f[a + 3].y),
-                             nibbles4_lo16(f[b].y, f[b + 1].y, f[b + 2].y, f[b + 3].y), 0x5410);
+// The q2w / q1w fields of two slots from their codes in nibbles (nibble
+// 4i+m of e / o: lane 2m / 2m+1 of slot i, every nibble a code 0..8): W = the
+// two slots' q2w (slot 0 in bits 0..15), X = their q1w (slot 0 in bits 0..7,
+// slot 1 in 8..15).  A code of 8 (a value quantize_block_magic left
+// unclipped at qmax) becomes 7 by one subtraction per eight nibbles, the q2
+// fields come out with one mask, and the q1 bits, masked to every fourth bit,
+// are gathered by three shift-and-mask steps.
+__device__ __forceinline__ void q3_fields_from_nibbles(uint32_t e, uint32_t o, uint32_t &W, uint32_t &X) {
     e -= (e >> 3) & 0x11111111u;  // 8 -> 7 (bit 3 of a nibble is set only by 8)
     o -= (o >> 3) & 0x11111111u;
     W = (e & 0x33333333u) | ((o << 2) & 0xCCCCCCCCu);
@@ -168,6 +160,29 @@ __device__ __forceinline__ void pack_pair_q3(const float2 (&f)[16], int h, uint3
     x = (x | (x >> 2)) & 0x0F0F0F0Fu;
     x = (x | (x >> 4)) & 0x00FF00FFu;
     X = (x & 0xFFu) | ((x >> 8) & 0xFF00u);
+}
+
+// The INT3 fields of slots 2h and 2h+1 from their 16 magic floats (f[4s + m]
+// = lanes 2m, 2m+1 of slot s; the code is each float's low byte), W and X as
+// above.  The inverse of unpack_pair_q3: the codes go into nibbles (even
+// lanes in one word, odd lanes in another) by multiply-add chains.
+__device__ __forceinline__ void pack_pair_q3(const float2 (&f)[16], int h, uint32_t &W, uint32_t &X) {
+    const int a = 8 * h, b = 8 * h + 4;  // f index of lane 0 of slot 2h, of slot 2h+1
+    q3_fields_from_nibbles(__byte_perm(nibbles4_lo16(f[a].x, f[a + 1].x, f[a + 2].x, f[a + 3].x),
+                                       nibbles4_lo16(f[b].x, f[b + 1].x, f[b + 2].x, f[b + 3].x), 0x5410),
+                           __byte_perm(nibbles4_lo16(f[a].y, f[a + 1].y, f[a + 2].y, f[a + 3].y),
+                                       nibbles4_lo16(f[b].y, f[b + 1].y, f[b + 2].y, f[b + 3].y), 0x5410),
+                           W, X);
+}
+
+// pack_pair_q3 for magic floats paired by lane: F[L] = (lane L of slot 2h,
+// lane L of slot 2h+1).
+__device__ __forceinline__ void pack_pair_q3_lanes(const float2 (&F)[8], uint32_t &W, uint32_t &X) {
+    q3_fields_from_nibbles(__byte_perm(nibbles4_lo16(F[0].x, F[2].x, F[4].x, F[6].x),
+                                       nibbles4_lo16(F[0].y, F[2].y, F[4].y, F[6].y), 0x5410),
+                           __byte_perm(nibbles4_lo16(F[1].x, F[3].x, F[5].x, F[7].x),
+                                       nibbles4_lo16(F[1].y, F[3].y, F[5].y, F[7].y), 0x5410),
+                           W, X);
 }
 
 template <int B>
@@ -388,6 +403,32 @@ __device__ __forceinline__ void unpack_pair_q3_f16(uint32_t W, uint32_t X, uint3
 #pragma unroll
         for (int m = 0; m < 4; ++m) h[4 * i + m] = hi[m];
     }
+}
+
+// The 16 signed INT3 codes of two consecutive slots (W, X as for
+// unpack_pair_q3) as exact fp16 pairs by lane, h[L] = (lane L of slot 0,
+// lane L of slot 1): after the q1 bits are merged into nibbles (q3_nibbles),
+// one logic operation puts two codes 16 bits apart into the mantissas of the
+// fp16 pair (1024, 1024) and one packed fp16 fma removes the offset and the
+// bias (and the factor 16 of a code in bits 4..7): exact at every step.
+__device__ __forceinline__ void unpack_pair_q3_f16_lanes(uint32_t W, uint32_t X, uint32_t (&h)[8]) {
+    uint32_t e, o;
+    q3_nibbles(W, X, e, o);
+    const __half2 one = __float2half2_rn(1.0f), sixteenth = __float2half2_rn(0.0625f);
+    const __half2 off0 = __float2half2_rn(-1028.0f), off4 = __float2half2_rn(-68.0f);
+    const auto fix = [](uint32_t t, __half2 m, __half2 a) {
+        const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&t), m, a);
+        return *reinterpret_cast<const uint32_t *>(&r);
+    };
+    const uint32_t e8 = e >> 8, o8 = o >> 8;
+    h[0] = fix((e & 0x000F000Fu) | 0x64006400u, one, off0);         // lane 0: nibbles 0 and 4 of e
+    h[2] = fix((e & 0x00F000F0u) | 0x64006400u, sixteenth, off4);   // lane 2: nibbles 1 and 5
+    h[4] = fix((e8 & 0x000F000Fu) | 0x64006400u, one, off0);        // lane 4: nibbles 2 and 6
+    h[6] = fix((e8 & 0x00F000F0u) | 0x64006400u, sixteenth, off4);  // lane 6: nibbles 3 and 7
+    h[1] = fix((o & 0x000F000Fu) | 0x64006400u, one, off0);
+    h[3] = fix((o & 0x00F000F0u) | 0x64006400u, sixteenth, off4);
+    h[5] = fix((o8 & 0x000F000Fu) | 0x64006400u, one, off0);
+    h[7] = fix((o8 & 0x00F000F0u) | 0x64006400u, sixteenth, off4);
 }
 
 // The 8 signed INT6 codes of a slot as exact fp16 pairs h[0..3] = lanes
@@ -764,12 +805,44 @@ template <int B, int R>
 __device__ __forceinline__ void reduce_block_words(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
                                                    BlockWords<B> &cw, uint32_t &scale_bits) {
     float2 acc[16];
-    if constexpr (B == 3) {
+    if constexpr (B == 3 && R <= 4) {
+        // codes decoded to fp16 through the fp16 1024 (logic operations and
+        // packed fp16 fmas), paired by lane across two slots (A[h][L] = lane L
+        // of slots 2h and 2h+1), scaled and summed by fp16-operand fmas into
+        // fp32; acc starts at -0, so the first fma returns the first rank's
+        // product exactly.  Measured against the E2M1 decode below at 2^27
+        // values per rank: 6% faster at R = 2, 1% at R = 4, 9% slower at R = 8.
+        float2 A[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int L = 0; L < 8; ++L) A[h][L] = make_float2(-0.0f, -0.0f);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const unsigned short sh = static_cast<unsigned short>(sb[r]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t hp[8];
+                unpack_pair_q3_f16_lanes(c[r].w[h], h ? (c[r].w[2] >> 16) : c[r].w[2], hp);
+#pragma unroll
+                for (int L = 0; L < 8; ++L) fma_f16x2_f16_f32(hp[L], sh, A[h][L]);
+            }
+        }
+        const BlockScale2 sc = block_scale2<B>(absmax_n<32>(reinterpret_cast<const float *>(A)));
+        float2 F[2][8];
+        quantize_block_magic<B>(reinterpret_cast<const float2(&)[16]>(A), sc.r, sc.low_clip,
+                                reinterpret_cast<float2(&)[16]>(F));
+        uint32_t x01, x23;
+        pack_pair_q3_lanes(F[0], cw.w[0], x01);
+        pack_pair_q3_lanes(F[1], cw.w[1], x23);
+        cw.w[2] = x01 | (x23 << 16);
+        scale_bits = sc.bits;
+        return;
+    } else if constexpr (B == 3) {
         // codes decoded to fp16 through E2M1, scaled and summed by fp16-operand
         // fmas into fp32 (acc starts at -0, so the first fma returns the first
-        // rank's product exactly, signed zeros included).  Decoding through the
-        // fp16 1024 instead (logic operations and packed fp16 fmas, as INT4
-        // does) measured 10% slower at R = 8 and equal at R = 2, 4.
+        // rank's product exactly, signed zeros included).  (R <= 4 takes the
+        // fp16-1024 decode above.)
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = make_float2(-0.0f, -0.0f);
 #pragma unroll

@@ -335,18 +335,36 @@ __device__ __forceinline__ void fc_reduce_tile(const HalfWords<BIN> (&c)[R], con
     fc_store16<BOUT>(tile_out, i, f, p);
 }
 
-template <int BIN, int BOUT, int R>
-__global__ void __launch_bounds__(kThreadsFc) fc_reduce_kernel(ConstPtrs wires, long long n, uint8_t *out,
-                                                               long long T) {
+// U tiles a grid stride apart per iteration, the loads of all U issued
+// before any arithmetic (the kernel is bound by latency, not by a pipe: with
+// one tile in flight its issue rate stayed near 0.63 of the peak).  The
+// branch on t < T is uniform across the CTA, so whole warps reach the group
+// shuffles.
+template <int BIN, int BOUT, int R, int U>
+__global__ void __launch_bounds__(kThreadsFc, 4) fc_reduce_kernel(ConstPtrs wires, long long n, uint8_t *out,
+                                                                  long long T) {
     const int i = threadIdx.x;
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        HalfWords<BIN> c[R];
-        float s[R], z[R];
+    const long long S = gridDim.x;
+    for (long long t0 = blockIdx.x; t0 < T; t0 += U * S) {
+        HalfWords<BIN> c[U][R];
+        float s[U][R], z[U][R];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-            fc_load16<BIN>(static_cast<const uint8_t *>(wires.p[r]) + t * FcCodec<BIN>::kTileBytes, i, c[r], s[r],
-                           z[r]);
-        fc_reduce_tile<BIN, BOUT, R>(c, s, z, out + t * FcCodec<BOUT>::kTileBytes, i, t * kTileValues + 16 * i, n);
+        for (int u = 0; u < U; ++u) {
+            const long long t = t0 + u * S;
+            if (t < T) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    fc_load16<BIN>(static_cast<const uint8_t *>(wires.p[r]) + t * FcCodec<BIN>::kTileBytes, i,
+                                   c[u][r], s[u][r], z[u][r]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long t = t0 + u * S;
+            if (t < T)
+                fc_reduce_tile<BIN, BOUT, R>(c[u], s[u], z[u], out + t * FcCodec<BOUT>::kTileBytes, i,
+                                             t * kTileValues + 16 * i, n);
+        }
     }
 }
 

@@ -424,9 +424,9 @@ qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R,
 /* qr_fc_segment_reduce on the staged Phase-1B kernel at any size, as
  * qr_segment_reduce_staged (`ctas` = 0 for one CTA per SM, else min(ctas,
  * #SMs); ctas < 0 is QR_ERR_INVALID_ARG).  qr_fc_segment_reduce itself
- * takes it from 48 tiles per SM when R >= 6, or R >= 4 with bits_in = 8;
- * from 96 tiles per SM when R = 5, R = 4 with bits 4 -> 8, or R = 3 with
- * bits_in = 8; never otherwise. */
+ * takes it from 48 tiles per SM when bits_in = 8 and R >= 4, and otherwise
+ * runs a grid-stride kernel that keeps two tiles' loads in flight per
+ * thread. */
 qr_status_t qr_fc_segment_reduce_staged(int bits_in, int bits_out, int R,
                                         const void *const *wires, size_t n,
                                         void *out_wire, int ctas, qr_stream_t stream);
