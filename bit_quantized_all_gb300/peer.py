@@ -130,6 +130,12 @@ class PeerTwoShot:
         self.bits, self.n, self.dtype = bits, n, dtype
         self.ops = CudaPeerOps() if ops is None else ops
         need = self.ops.workspace_bytes(bits, self.R, n)
+        # every rank must agree on the shape: a peer's kernels store into this
+        # rank's workspace at offsets computed from their own (bits, n)
+        shapes = [None] * self.R
+        dist.all_gather_object(shapes, (bits, n, dtype, need), group=group)
+        if any(sh != shapes[0] for sh in shapes):
+            raise ValueError(f"rank {self.rank}: the ranks disagree on (bits, n, dtype, workspace bytes): {shapes}")
         if need == 0:
             raise ValueError(f"unsupported two-shot shape: bits={bits} R={self.R} n={n}")
         self.workspace, self.ws_ptr = self.ops.alloc(need)

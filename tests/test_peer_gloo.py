@@ -165,6 +165,43 @@ def _worker(rank, world, port, cases, leave_after, q):
             pass
 
 
+def _mismatch_worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import oracle
+    from bit_quantized_all_gb300.peer import PeerTwoShot, init_group
+    oracle.build()
+    group = init_group(rank, world, port, timeout_s=20.0)
+    try:
+        ops = ShmOps({}, {})
+        try:
+            PeerTwoShot(4, 2048 * (3 + rank), 1, group=group, ops=ops)  # every rank a different n
+            q.put((rank, "constructed"))
+        except ValueError as e:
+            q.put((rank, f"refused: {e}"))
+        q.put((rank, f"allocated={hasattr(ops, 'owned')}"))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_ranks_that_disagree_on_the_shape_are_refused_before_any_mapping():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_mismatch_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    out = []
+    while not q.empty():
+        out.append(q.get())
+    assert len(out) == 2 * world, out
+    assert all(m.startswith("refused") or m == "allocated=False" for _, m in out), out
+
+
 def _run(world, cases, leave_after=None):
     port = _free_port()
     ctx = mp.get_context("spawn")
