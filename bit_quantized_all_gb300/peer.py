@@ -189,6 +189,36 @@ class PeerTwoShot:
         self._opened = []
 
 
+def twoshot_peer_local(bits: int, xs, ys=None, stream=None):
+    """All R ranks' per-rank calls from one process, on one device and one
+    stream: R workspaces in this process, every rank's send, then every
+    owner's reduce, then every rank's decode (the stream order is the join).
+    Returns (the R outputs, the R workspaces).  Each output equals
+    qr_allreduce's."""
+    from . import _check_inputs, _same_device
+    xs, dt, n = _check_inputs(xs)
+    R = len(xs)
+    dev = _same_device(xs, "twoshot_peer_local")
+    ops = CudaPeerOps(dev)
+    need = ops.workspace_bytes(bits, R, n)
+    if need == 0:
+        raise ValueError(f"unsupported two-shot shape: bits={bits} R={R} n={n}")
+    ws = [torch.empty(need, dtype=torch.uint8, device=dev) for _ in range(R)]
+    ys = [torch.empty_like(xs[0]) for _ in range(R)] if ys is None else list(ys)
+    for y in ys:
+        if y.dtype != xs[0].dtype or y.numel() != n or not y.is_contiguous() or y.device != dev:
+            raise ValueError("every output must match the inputs")
+    peers = [w.data_ptr() for w in ws]
+    s = ops.stream(stream)
+    for j in range(R):
+        ops.send(bits, dt, R, j, xs[j].data_ptr(), n, peers, s)
+    for j in range(R):
+        ops.reduce(bits, R, j, n, peers, s)
+    for j in range(R):
+        ops.decode(bits, dt, R, n, peers[j], ys[j].data_ptr(), s)
+    return ys, ws
+
+
 def init_group(rank: int, world: int, port: int, timeout_s: float = 60.0):
     """A gloo process group on 127.0.0.1 for the host joins."""
     import torch.distributed as dist
@@ -197,4 +227,4 @@ def init_group(rank: int, world: int, port: int, timeout_s: float = 60.0):
     return dist.group.WORLD
 
 
-__all__ = ["PeerTwoShot", "PeerError", "CudaPeerOps", "init_group", "QR_IPC_HANDLE_BYTES"]
+__all__ = ["PeerTwoShot", "PeerError", "CudaPeerOps", "twoshot_peer_local", "init_group", "QR_IPC_HANDLE_BYTES"]

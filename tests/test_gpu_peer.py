@@ -116,6 +116,36 @@ def _run(world, cases):
     return out
 
 
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("bits", [3, 4, 6, 8])
+def test_one_process_driving_every_rank(bits, R):
+    """The per-rank calls issued for all R ranks from one process on one
+    stream (every send, then every reduce, then every decode): every output
+    and every gathered wire equals the oracle's, ragged tail included, and
+    fewer tiles than ranks at the small size."""
+    import oracle
+    import bit_quantized_all_gb300 as qr
+    from bit_quantized_all_gb300.peer import twoshot_peer_local
+    for n in (2048 * 13 + 77, 1500):
+        dtype = 1 if bits in (3, 4) else 0
+        xs = _inputs(R, n, dtype, 50 * bits + R + n)
+        tdt = {0: torch.float16, 1: torch.bfloat16}[dtype]
+        dev = [torch.from_numpy(x.view(np.int16)).cuda().view(tdt) for x in xs]
+        ys, ws = twoshot_peer_local(bits, dev)
+        torch.cuda.synchronize()
+        ref = oracle.allreduce(bits, dtype, xs)
+        red_ref = oracle.segment_reduce(bits, [oracle.encode(bits, dtype, x) for x in xs], n)
+        T = -(-n // 2048)
+        seg = -(-T // R)
+        tb = qr.qr_tile_bytes(bits)
+        for j in range(R):
+            got = ys[j].view(torch.int16).cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, ref), (bits, R, n, j)
+            g = R * seg * tb
+            assert np.array_equal(ws[j][g: g + T * tb].cpu().numpy(), red_ref), (bits, R, n, j)
+    assert qr.qr_wait_timeouts() == 0
+
+
 @pytest.mark.parametrize("world,cases", [
     (2, [(4, 2048 * 40 + 37, 1), (3, 2048 * 9, 0), (8, 2048 * 3 + 1, 1), (6, 100, 0)]),
     (4, [(4, 2048 * 40 + 37, 1), (3, 2048 * 9 + 5, 1), (6, 2048 * 2, 0), (8, 700, 1)]),
