@@ -388,6 +388,7 @@ def run_sweep(args) -> None:
     dtypes = [{"fp16": workloads.FP16, "bf16": workloads.BF16}[d] for d in args.sweep_dtypes.split(",")]
     ranks = [int(r) for r in args.sweep_R.split(",")]
     widths = [int(b) for b in args.sweep_bits.split(",")]
+    from bit_quantized_all_gb300.peer import CudaPeerOps, twoshot_peer_local
     if args.sweep_codec == "fc":
         run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks)
         return
@@ -443,6 +444,15 @@ def run_sweep(args) -> None:
                     def twoshot_flags():  # one cooperative launch, phases joined by per-tile flags
                         qr.qr_allreduce_twoshot(bits, xs, ys=ys3, workspace=wsf, flags=True)
 
+                    # the per-rank two-shot (qr_twoshot_peer_*), every rank's calls
+                    # issued from this process: R sends, R owner reductions, R decodes
+                    wsp = [torch.empty(CudaPeerOps(dev).workspace_bytes(bits, Rs, n), dtype=torch.uint8, device=dev)
+                           for _ in range(Rs)]
+                    ys4 = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
+
+                    def twoshot_peer():
+                        twoshot_peer_local(bits, xs, ys=ys4, workspaces=wsp)
+
                     regs_ctas = 4 * 4 * sms  # forces the register-fed fused kernel (four waves)
 
                     def fused_regs():
@@ -450,16 +460,20 @@ def run_sweep(args) -> None:
 
                     arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
                             ("encode", encode_all), ("reduce", reduce_only), ("decode", decode_only),
-                            ("twoshot", twoshot), ("twoshot_flags", twoshot_flags))
-                    times = time_arms(arms, args, flush if do_flush else None, warm=(fused, fused_regs, unfused, twoshot, twoshot_flags))
+                            ("twoshot", twoshot), ("twoshot_flags", twoshot_flags), ("twoshot_peer", twoshot_peer))
+                    times = time_arms(arms, args, flush if do_flush else None,
+                                      warm=(fused, fused_regs, unfused, twoshot, twoshot_flags, twoshot_peer))
                     same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
                         torch.equal(y.view(torch.int16), y2.view(torch.int16))) and all(
-                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in ys2 + ys3)
+                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in ys2 + ys3 + ys4)
                     # two-shot: R sends (2N in, W out each), R*W + W for the owners'
-                    # reductions, R decodes (W in, 2N out each)
+                    # reductions, R decodes (W in, 2N out each); the per-rank
+                    # two-shot's owners store their reduced segment into all R
+                    # workspaces (R*W + R*W) and every rank decodes its own copy
                     kernel_b = {"fused": fused_b, "fused_regs": fused_b, "unfused": unf_b, "encode": Rs * (2 * n + W),
                                 "reduce": (Rs + 1) * W, "decode": W + 2 * n,
-                                "twoshot": 4 * Rs * n + (3 * Rs + 1) * W, "twoshot_flags": 4 * Rs * n + (3 * Rs + 1) * W}
+                                "twoshot": 4 * Rs * n + (3 * Rs + 1) * W, "twoshot_flags": 4 * Rs * n + (3 * Rs + 1) * W,
+                                "twoshot_peer": 4 * Rs * n + 4 * Rs * W}
                     for name, alg in kernel_b.items():
                         if not times[name]:
                             print(json.dumps({"sweep": name, "R": Rs, "values_per_rank": n, "bits": bits,
@@ -474,7 +488,7 @@ def run_sweep(args) -> None:
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
                             "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None, "fused_equals_unfused": same, "reps": args.reps,
                             "burst": 1 if do_flush else args.burst, "graph": bool(args.graph)}), flush=True)
-                    del wires, red, yu, ws, ys2, wsf, ys3
+                    del wires, red, yu, ws, ys2, wsf, ys3, wsp, ys4
                 del xs, y
                 torch.cuda.empty_cache()
 

@@ -54,10 +54,9 @@ static cudaError_t run_fc_reduce_staged_t(const ConstPtrs &w, long long n, void 
 }
 
 // Where the default takes the staged Phase-1B kernel (tiles per SM from which
-// it does; 0 = never), else the register-fed kernel with two tiles in flight
-// per thread.  Measured on GB300 at 2^27 bf16 values per rank, fraction of the
-// measured HBM bandwidth, register-fed with one tile in flight / with two /
-// staged (five groups):
+// it does; 0 = never), else a register-fed kernel.  Measured on GB300 at 2^27
+// bf16 values per rank, fraction of the measured HBM bandwidth, register-fed
+// with one tile in flight / with two / staged (five groups):
 //   4 -> 4: R=2 0.51 / 0.52 / 0.39, R=4 0.46 / 0.56 / 0.47, R=6 0.39 / 0.57 /
 //     0.51, R=8 0.39 / 0.58 / 0.53;
 //   4 -> 8: R=2 0.59 / 0.64 / 0.50, R=4 0.51 / 0.64 / 0.54, R=8 0.47 / 0.62 /
@@ -73,6 +72,17 @@ __host__ __device__ constexpr long long staged_fc_reduce_min_tiles_per_sm() {
 
 constexpr int kFcReduceUnroll = 2;  // tiles per thread in flight in the register-fed kernel
 
+// Where the register-fed Phase-1B loads one tile ahead (fc_reduce_ahead_kernel)
+// instead of two tiles at once, and with how many CTAs per SM (0 = not).  At
+// 2^27 values per rank, two at once / one ahead: 4-bit inputs R=4 0.56 / 0.58,
+// R=6 0.57 / 0.59, R=8 0.58 / 0.62 (4 -> 4) and 0.62 / 0.67 (4 -> 8), with
+// five CTAs per SM and four waves (at R = 2 one ahead was slower); 8 -> 8 at
+// R=3 0.86 / 0.93 (0.89 / 0.96 at 2^28) with eight CTAs per SM and two waves.
+template <int BIN, int BOUT, int R>
+__host__ __device__ constexpr int fc_reduce_ahead_min_blocks() {
+    return (BIN == 4 && R >= 4) ? 5 : (BIN == 8 && R == 3) ? 8 : 0;
+}
+
 template <int BIN, int BOUT, int R>
 static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
     const long long T = (n + kTileValues - 1) / kTileValues;
@@ -83,8 +93,16 @@ static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, c
         if (sms <= 0) return e;
         if (T >= kMinTilesPerSm * sms) return run_fc_reduce_staged_t<BIN, BOUT, R>(w, n, out, 0, s);
     }
-    auto kern = fc_reduce_kernel<BIN, BOUT, R, kFcReduceUnroll>;
     cudaError_t err = cudaSuccess;
+    constexpr int kAhead = fc_reduce_ahead_min_blocks<BIN, BOUT, R>();
+    if constexpr (kAhead > 0) {
+        auto kern = fc_reduce_ahead_kernel<BIN, BOUT, R, kAhead>;
+        const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, BIN == 4 ? 4 : 2, &err);
+        if (grid <= 0) return err;
+        kern<<<grid, kThreadsFc, 0, s>>>(w, n, static_cast<uint8_t *>(out), T);
+        return cudaGetLastError();
+    }
+    auto kern = fc_reduce_kernel<BIN, BOUT, R, kFcReduceUnroll>;
     const long long units = (T + kFcReduceUnroll - 1) / kFcReduceUnroll;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, units, 0, 4, &err);
     if (grid <= 0) return err;

@@ -368,6 +368,48 @@ __global__ void __launch_bounds__(kThreadsFc, 4) fc_reduce_kernel(ConstPtrs wire
     }
 }
 
+// One tile's R code words, scales and zero points, as one thread holds them.
+template <int BIN, int R>
+struct FcReduceSet {
+    HalfWords<BIN> c[R];
+    float s[R], z[R];
+};
+
+template <int BIN, int R>
+__device__ __forceinline__ void fc_load_set(const ConstPtrs &wires, long long t, int i, FcReduceSet<BIN, R> &g) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        fc_load16<BIN>(static_cast<const uint8_t *>(wires.p[r]) + t * FcCodec<BIN>::kTileBytes, i, g.c[r], g.s[r],
+                       g.z[r]);
+}
+
+// Phase-1B one tile ahead: the loads of the CTA's next tile (a grid stride
+// on) are issued before this tile is reduced, so every thread has loads in
+// flight while it computes; two register sets take turns.  MINB caps the
+// registers (CTAs per SM).  Same results as fc_reduce_kernel.
+template <int BIN, int BOUT, int R, int MINB>
+__global__ void __launch_bounds__(kThreadsFc, MINB) fc_reduce_ahead_kernel(ConstPtrs wires, long long n,
+                                                                           uint8_t *out, long long T) {
+    const int i = threadIdx.x;
+    const long long S = gridDim.x;
+    long long t = blockIdx.x;
+    if (t >= T) return;
+    FcReduceSet<BIN, R> a, b;
+    fc_load_set<BIN, R>(wires, t, i, a);
+    while (true) {
+        if (t + S < T) fc_load_set<BIN, R>(wires, t + S, i, b);
+        fc_reduce_tile<BIN, BOUT, R>(a.c, a.s, a.z, out + t * FcCodec<BOUT>::kTileBytes, i, t * kTileValues + 16 * i,
+                                     n);
+        t += S;
+        if (t >= T) break;
+        if (t + S < T) fc_load_set<BIN, R>(wires, t + S, i, a);
+        fc_reduce_tile<BIN, BOUT, R>(b.c, b.s, b.z, out + t * FcCodec<BOUT>::kTileBytes, i, t * kTileValues + 16 * i,
+                                     n);
+        t += S;
+        if (t >= T) break;
+    }
+}
+
 // The Flash Communication Phase-1B as a policy for staged_reduce_kernel
 // (qr_kernels32.cuh): 16 values per thread, 128 threads per tile.
 template <int BIN, int BOUT>

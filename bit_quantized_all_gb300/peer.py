@@ -189,12 +189,14 @@ class PeerTwoShot:
         self._opened = []
 
 
-def twoshot_peer_local(bits: int, xs, ys=None, stream=None):
+def twoshot_peer_local(bits: int, xs, ys=None, workspaces=None, stream=None):
     """All R ranks' per-rank calls from one process, on one device and one
     stream: R workspaces in this process, every rank's send, then every
     owner's reduce, then every rank's decode (the stream order is the join).
     Returns (the R outputs, the R workspaces).  Each output equals
-    qr_allreduce's."""
+    qr_allreduce's.  `workspaces` (R uint8 tensors of
+    qr_twoshot_peer_workspace_bytes each) and `ys` may be passed in to reuse
+    them."""
     from . import _check_inputs, _same_device
     xs, dt, n = _check_inputs(xs)
     R = len(xs)
@@ -203,7 +205,13 @@ def twoshot_peer_local(bits: int, xs, ys=None, stream=None):
     need = ops.workspace_bytes(bits, R, n)
     if need == 0:
         raise ValueError(f"unsupported two-shot shape: bits={bits} R={R} n={n}")
-    ws = [torch.empty(need, dtype=torch.uint8, device=dev) for _ in range(R)]
+    if workspaces is None:
+        ws = [torch.empty(need, dtype=torch.uint8, device=dev) for _ in range(R)]
+    else:
+        ws = list(workspaces)
+        if len(ws) != R or any(w.dtype != torch.uint8 or w.numel() < need or not w.is_contiguous()
+                               or w.device != dev for w in ws):
+            raise ValueError(f"workspaces must be {R} contiguous uint8 tensors of at least {need} bytes on {dev}")
     ys = [torch.empty_like(xs[0]) for _ in range(R)] if ys is None else list(ys)
     for y in ys:
         if y.dtype != xs[0].dtype or y.numel() != n or not y.is_contiguous() or y.device != dev:

@@ -425,8 +425,10 @@ qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R,
  * qr_segment_reduce_staged (`ctas` = 0 for one CTA per SM, else min(ctas,
  * #SMs); ctas < 0 is QR_ERR_INVALID_ARG).  qr_fc_segment_reduce itself
  * takes it from 48 tiles per SM when bits_in = 8 and R >= 4, and otherwise
- * runs a grid-stride kernel that keeps two tiles' loads in flight per
- * thread. */
+ * runs a grid-stride kernel from registers: one that issues the loads of a
+ * thread's next tile before reducing the current one when bits_in = 4 and
+ * R >= 4, or bits_in = 8 and R = 3, else one that loads two tiles at a
+ * time. */
 qr_status_t qr_fc_segment_reduce_staged(int bits_in, int bits_out, int R,
                                         const void *const *wires, size_t n,
                                         void *out_wire, int ctas, qr_stream_t stream);

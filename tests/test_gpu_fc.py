@@ -96,6 +96,15 @@ def test_every_rank_count(R):
             fc_full_check(*pair, dtype, _rand_ranks(R, n, dtype, 77 + R), f"R={R} {pair} dt={dtype}")
 
 
+@pytest.mark.parametrize("pair,R", [((4, 4), 8), ((4, 8), 5), ((4, 4), 4), ((8, 8), 3)])
+def test_phase1b_many_tiles_per_cta(pair, R):
+    """Enough tiles that every CTA of the Phase-1B grid-stride kernels reduces
+    several (odd and even counts: both register sets of the one-tile-ahead
+    kernel take turns), whole wire against the oracle."""
+    n = 2048 * 7001 + 5
+    fc_full_check(*pair, 1, _rand_ranks(R, n, 1, 500 + R), f"many tiles R={R} {pair}")
+
+
 def test_special_groups():
     n = 2048 * 2
     for dtype in (0, 1):
