@@ -140,11 +140,21 @@ def cpu_baseline(xs, budget_s=12.0) -> dict:
                                         f"{dt1:.1f} s"}}
 
 
-def _time_oracle(orc, xs, dtype, bits_list, tiles, threads, min_s=2.0):
+def _time_oracle(orc, xs, dtype, bits_list, tiles, threads, min_s=2.0, codec="qr"):
     """Input GB/s and values/s of the oracle's all-reduce over the first
-    `tiles` tiles of every rank (every width in `bits_list`), on `threads`
-    threads each taking a contiguous share of the tiles, repeated until
-    `min_s` seconds have passed."""
+    `tiles` tiles of every rank (every width in `bits_list`: a width for the
+    symmetric codec, a (reduce-scatter, all-gather) pair for the asymmetric
+    one, ignored for FP4), on `threads` threads each taking a contiguous
+    share of the tiles, repeated until `min_s` seconds have passed."""
+    if codec == "qr":
+        def allreduce(b, part):
+            orc.allreduce(b, dtype, part)
+    elif codec == "fc":
+        def allreduce(b, part):
+            orc.fc_allreduce(b[0], b[1], dtype, part)
+    else:
+        def allreduce(b, part):
+            orc.fp4_allreduce(dtype, part)
     R_ = len(xs)
     n = min(tiles * 2048, xs[0].size)
     per = -(-tiles // threads)
@@ -153,7 +163,7 @@ def _time_oracle(orc, xs, dtype, bits_list, tiles, threads, min_s=2.0):
 
     def work(sp):
         for b in bits_list:
-            orc.allreduce(b, dtype, [x[sp[0]:sp[1]] for x in xs])
+            allreduce(b, [x[sp[0]:sp[1]] for x in xs])
 
     reps, t = 0, time.perf_counter()
     with cf.ThreadPoolExecutor(len(spans)) as ex:
@@ -186,8 +196,13 @@ def run_cpu_sweep(args) -> None:
          4096, 5),
         ("sweep: R=8, 2^29 bf16 values per rank (1 GiB)", dict(R=8, N=1 << 29, dtype=W.BF16, bits=(4, 3)),
          4096, 5),
+        ("fc sweep: R=8, 2^27 bf16 values per rank, asymmetric group-128 codec",
+         dict(R=8, N=1 << 27, dtype=W.BF16, bits=((4, 4), (4, 8), (8, 8))), 4096, 5, "fc"),
+        ("fp4 sweep: R=8, 2^27 bf16 values per rank, E2M1 codec", dict(R=8, N=1 << 27, dtype=W.BF16, bits=(4,)),
+         4096, 5, "fp4"),
     ]
-    for name, cfg, sample_tiles, seed in cases:
+    for name, cfg, sample_tiles, seed, *rest in cases:
+        codec = rest[0] if rest else "qr"
         T = cfg["N"] // 2048 if cfg["N"] % 2048 == 0 else cfg["N"] // 2048 + 1
         tiles = T if sample_tiles is None else min(T, sample_tiles)
         if seed is None and sample_tiles is None:
@@ -197,8 +212,8 @@ def run_cpu_sweep(args) -> None:
         else:
             xs = [W.sweep_rank(r, tiles * 2048, cfg["dtype"], seed) for r in range(cfg["R"])]
         for threads in (1, cores):
-            gbs, vps, reps, dt, used = _time_oracle(orc, xs, cfg["dtype"], cfg["bits"], tiles, threads)
-            print(json.dumps({"cpu_sweep": name, "R": cfg["R"], "values_per_rank": cfg["N"],
+            gbs, vps, reps, dt, used = _time_oracle(orc, xs, cfg["dtype"], cfg["bits"], tiles, threads, codec=codec)
+            print(json.dumps({"cpu_sweep": name, "codec": codec, "R": cfg["R"], "values_per_rank": cfg["N"],
                               "bits": list(cfg["bits"]), "threads": used, "cores": cores,
                               "input_gbs": round(gbs, 4), "values_per_s": round(vps, 1),
                               "sample": f"{'all' if tiles == T else 'first'} {tiles} of {T} tiles per rank, "
