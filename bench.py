@@ -342,7 +342,7 @@ def measured_hbm() -> tuple[float, str]:
 
 # The sources that determine the benchmarked kernel's code and launch shape.
 FUSED16_SOURCES = ("qr_device.cuh", "qr_kernels.cuh", "qr_pipeline.cuh", "qr_staged.cuh", "qr_allreduce16.cuh",
-                   "qr_allreduce16_b3.cu", "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_grid.cu")
+                   "qr_allreduce16_b3.cu", "qr_allreduce16_b4.cu", "qr_allreduce.cu", "qr_grid.cu", "qr_launch.h")
 
 
 def _code_only(src: str) -> str:
@@ -829,8 +829,9 @@ def run_configs(args) -> None:
 def run_medium(args) -> None:
     """Medium messages, R = 8, INT4, bf16.  (1) Back to back with every call
     reading HBM: K sets of the inputs (and K outputs) spanning at least
-    640 MiB, one CUDA graph of K calls, set k by call k; beside it K device
-    copies of 9N bytes (the 18N bytes a fused call moves), the size-matched
+    640 MiB, one CUDA graph of K calls, set k by call k, and the same K
+    calls launched one by one on the stream; beside it K device copies of
+    9N bytes (the 18N bytes a fused call moves), the size-matched
     bandwidth.  (2) One call after an L2 eviction, for the default launch,
     the register-fed kernel at several CTA counts and the staged kernel at
     several CTA counts."""
@@ -870,6 +871,24 @@ def run_medium(args) -> None:
             ts.append(e0.elapsed_time(e1))
         return statistics.median(ts) / len(fns)
 
+    def stream_per_call(fns, reps):
+        # the calls launched one by one on the stream, queued behind a sleep
+        # kernel that outlasts their enqueueing, so the events time the device
+        for f in fns:
+            f()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            torch.cuda._sleep(1 << 22)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for f in fns:
+                f()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts) / len(fns)
+
     flush = L2Flush(dev)
     for n in sizes:
         K = max(2, -(-(640 << 20) // (2 * Rm * n)))
@@ -877,12 +896,15 @@ def run_medium(args) -> None:
         sets = [[b.clone() for b in base] for _ in range(K)]
         ys = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(K)]
         t_f = graph_per_call([(lambda k=k: qr.qr_allreduce(4, sets[k], y=ys[k])) for k in range(K)], args.reps)
+        t_s = stream_per_call([(lambda k=k: qr.qr_allreduce(4, sets[k], y=ys[k])) for k in range(K)], args.reps)
         alg = 2 * Rm * n + 2 * n
         src = [torch.empty(alg // 2, dtype=torch.uint8, device=dev) for _ in range(K)]
         dst = [torch.empty(alg // 2, dtype=torch.uint8, device=dev) for _ in range(K)]
         t_c = graph_per_call([(lambda k=k: dst[k].copy_(src[k])) for k in range(K)], args.reps)
         print(json.dumps({"medium": "back_to_back", "R": Rm, "bits": 4, "values_per_rank": n, "rotated_sets": K,
                           "fused_us": round(t_f * 1e3, 2), "fused_frac": round(alg / (t_f / 1e3) / 1e9 / peak, 3),
+                          "fused_stream_us": round(t_s * 1e3, 2),
+                          "fused_stream_frac": round(alg / (t_s / 1e3) / 1e9 / peak, 3),
                           "copy_of_same_bytes_us": round(t_c * 1e3, 2),
                           "copy_frac": round(alg / (t_c / 1e3) / 1e9 / peak, 3),
                           "fused_over_copy": round(t_c / t_f, 3), "peak_gbs": peak}), flush=True)

@@ -25,8 +25,8 @@ static cudaError_t run_allreduce(int R, const void *const *x, long long n, void 
     cudaError_t err = cudaSuccess;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads, T, ctas, 1, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads, 0, s>>>(xp, R, n, static_cast<uint16_t *>(y), wp, static_cast<uint8_t *>(red_out), T);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreads, 0, s, xp, R, n, static_cast<uint16_t *>(y), wp,
+                          static_cast<uint8_t *>(red_out), T);
 }
 
 cudaError_t launch_allreduce_staged(int bits, int dtype, int R, const void *const *x, long long n, void *y, int ctas,

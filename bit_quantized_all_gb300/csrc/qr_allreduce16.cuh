@@ -23,8 +23,7 @@ static cudaError_t run_allreduce16_r(const ConstPtrs &xp, long long n, void *y, 
     cudaError_t err = cudaSuccess;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads16, T, ctas, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads16, 0, s>>>(xp, n, static_cast<uint16_t *>(y), T);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreads16, 0, s, xp, n, static_cast<uint16_t *>(y), T);
 }
 
 template <int B, int DT>

@@ -17,8 +17,8 @@ static cudaError_t run_decode(const void *wire, long long n, void *y, cudaStream
     const long long units = (NH + kThreads32 * kDecodeUnroll - 1) / (kThreads32 * kDecodeUnroll);
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint8_t *>(wire), n, static_cast<uint16_t *>(y), NH);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint8_t *>(wire), n,
+                          static_cast<uint16_t *>(y), NH);
 }
 
 cudaError_t launch_decode(int bits, int dtype, const void *wire, long long n, void *y, cudaStream_t s) {

@@ -24,6 +24,23 @@
 
 namespace qrk {
 
+// Entry of every kernel launched by launch_chained (qr_launch.h), before its
+// first access to global memory: allow the next kernel on the stream to
+// start launching (its CTAs take SMs as this grid's CTAs leave, and run up
+// to their own entry), then wait until the previous kernel on the stream has
+// completed and its writes are visible.  So a chained kernel sees everything
+// its predecessor wrote, as with an ordinary launch, and the gap between
+// back-to-back launches shrinks to the predecessor's last CTAs.  Launched
+// without programmatic serialization both instructions return at once.
+__device__ __forceinline__ void chain_entry() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace qrk
+
+namespace qrk {
+
 constexpr int kTileValues = 2048;
 constexpr int kThreads = 256;  // one 8-value slot per thread
 constexpr int kMaxRanks = 8;

@@ -14,9 +14,8 @@ static cudaError_t run_encode(const void *x, long long n, void *wire, cudaStream
     const long long units = (NB + kThreads32 * kEncodeUnroll - 1) / (kThreads32 * kEncodeUnroll);
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint16_t *>(x), n,
+    return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint16_t *>(x), n,
                                      ContigTiles{static_cast<uint8_t *>(wire), Codec<B>::kTileBytes}, NB);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_encode(int bits, int dtype, const void *x, long long n, void *wire, cudaStream_t s) {

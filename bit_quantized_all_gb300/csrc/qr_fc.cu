@@ -15,8 +15,8 @@ static cudaError_t run_fc_encode_t(const void *x, long long n, void *wire, cudaS
     cudaError_t err = cudaSuccess;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreadsFc, 0, s>>>(static_cast<const uint16_t *>(x), n, static_cast<uint8_t *>(wire), T);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreadsFc, 0, s, static_cast<const uint16_t *>(x), n,
+                          static_cast<uint8_t *>(wire), T);
 }
 
 template <int B, int DT, bool A32>
@@ -26,8 +26,8 @@ static cudaError_t run_fc_decode_t(const void *wire, long long n, void *y, cudaS
     cudaError_t err = cudaSuccess;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreadsFc, 0, s>>>(static_cast<const uint8_t *>(wire), n, static_cast<uint16_t *>(y), T);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreadsFc, 0, s, static_cast<const uint8_t *>(wire), n,
+                          static_cast<uint16_t *>(y), T);
 }
 
 // Phase-1B on the staged kernel (the R wire tiles brought into shared memory
@@ -48,9 +48,8 @@ static cudaError_t run_fc_reduce_staged_t(const ConstPtrs &w, long long n, void 
     long long grid = ctas > 0 ? ctas : sms;
     if (grid > sms) grid = sms;
     if (grid > T) grid = T;
-    kern<<<static_cast<int>(grid), P::kThreads * Shape::kGroups, Shape::kSmemBytes, s>>>(
-        w, static_cast<uint8_t *>(out), T, n, timeouts);
-    return cudaGetLastError();
+    return launch_chained(kern, static_cast<int>(grid), P::kThreads * Shape::kGroups, Shape::kSmemBytes,
+                          s, w, static_cast<uint8_t *>(out), T, n, timeouts);
 }
 
 // Where the default takes the staged Phase-1B kernel (tiles per SM from which
@@ -99,15 +98,13 @@ static cudaError_t run_fc_reduce_t(const ConstPtrs &w, long long n, void *out, c
         auto kern = fc_reduce_ahead_kernel<BIN, BOUT, R, kAhead>;
         const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, 0, BIN == 4 ? 4 : 2, &err);
         if (grid <= 0) return err;
-        kern<<<grid, kThreadsFc, 0, s>>>(w, n, static_cast<uint8_t *>(out), T);
-        return cudaGetLastError();
+        return launch_chained(kern, grid, kThreadsFc, 0, s, w, n, static_cast<uint8_t *>(out), T);
     }
     auto kern = fc_reduce_kernel<BIN, BOUT, R, kFcReduceUnroll>;
     const long long units = (T + kFcReduceUnroll - 1) / kFcReduceUnroll;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, units, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreadsFc, 0, s>>>(w, n, static_cast<uint8_t *>(out), T);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreadsFc, 0, s, w, n, static_cast<uint8_t *>(out), T);
 }
 
 template <int B, int DT>

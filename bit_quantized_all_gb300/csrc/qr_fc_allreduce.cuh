@@ -26,8 +26,7 @@ static cudaError_t run_fc_allreduce_r(const ConstPtrs &xp, long long n, void *y,
     cudaError_t err = cudaSuccess;
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreadsFc, T, ctas, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreadsFc, 0, s>>>(xp, n, static_cast<uint16_t *>(y), T);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreadsFc, 0, s, xp, n, static_cast<uint16_t *>(y), T);
 }
 
 template <int BRS, int BAG, int DT, bool A32>

@@ -18,8 +18,8 @@ static cudaError_t run_fp4_encode(const void *x, long long n, void *wire, cudaSt
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, (NB + kThreads32 - 1) / kThreads32,
                               0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint16_t *>(x), n, static_cast<uint8_t *>(wire), NB);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint16_t *>(x), n,
+                          static_cast<uint8_t *>(wire), NB);
 }
 
 cudaError_t launch_fp4_encode(int dtype, const void *x, long long n, void *wire, cudaStream_t s) {
@@ -35,8 +35,8 @@ static cudaError_t run_fp4_decode(const void *wire, long long n, void *y, cudaSt
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, (NH + kThreads32 - 1) / kThreads32,
                               0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint8_t *>(wire), n, static_cast<uint16_t *>(y), NH);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint8_t *>(wire), n,
+                          static_cast<uint16_t *>(y), NH);
 }
 
 cudaError_t launch_fp4_decode(int dtype, const void *wire, long long n, void *y, cudaStream_t s) {
@@ -59,9 +59,8 @@ static cudaError_t run_fp4_reduce_r(const ConstPtrs &w, long long n, void *out, 
     long long grid = ctas > 0 ? ctas : sms;
     if (grid > sms) grid = sms;
     if (grid > T) grid = T;
-    kern<<<static_cast<int>(grid), Fp4Reduce::kThreads * Shape::kGroups, Shape::kSmemBytes, s>>>(
-        w, static_cast<uint8_t *>(out), T, n, timeouts);
-    return cudaGetLastError();
+    return launch_chained(kern, static_cast<int>(grid), Fp4Reduce::kThreads * Shape::kGroups, Shape::kSmemBytes,
+                          s, w, static_cast<uint8_t *>(out), T, n, timeouts);
 }
 
 cudaError_t launch_fp4_reduce(int R, const void *const *wires, long long n, void *out, int ctas, cudaStream_t s) {

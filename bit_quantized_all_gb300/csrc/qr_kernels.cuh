@@ -21,6 +21,7 @@ template <int B, int DT, bool EMIT>
 __global__ void __launch_bounds__(kThreads) allreduce_kernel(ConstPtrs x, int R, long long n, uint16_t *y,
                                                              MutPtrs wire_out, uint8_t *red_out,
                                                              long long T) {
+    chain_entry();
     const int k = threadIdx.x;
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const long long base = t * kTileValues + 8 * k;
@@ -127,6 +128,7 @@ __device__ __forceinline__ void allreduce16_tile(const uint32_t (&raw)[R][8], ui
 template <int B, int DT, int R>
 __global__ void __launch_bounds__(kThreads16, 4) allreduce16_kernel(ConstPtrs x, long long n, uint16_t *y,
                                                                     long long T) {
+    chain_entry();
     const int k = threadIdx.x;
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const long long base = t * kTileValues + 16 * k;

@@ -546,6 +546,7 @@ __device__ __forceinline__ void encode32_run(const uint16_t *__restrict__ x, lon
 template <int B, int DT, int U, class Addr = ContigTiles>
 __global__ void __launch_bounds__(kThreads32) encode32_kernel(const uint16_t *__restrict__ x, long long n,
                                                               Addr wire, long long NB) {
+    chain_entry();
     encode32_run<B, DT, U, Addr>(x, n, wire, NB);
 }
 
@@ -662,6 +663,7 @@ __device__ __forceinline__ void decode16_run(const uint8_t *__restrict__ wire, l
 template <int B, int DT, int U, bool Y32>
 __global__ void __launch_bounds__(kThreads32) decode16_kernel(const uint8_t *__restrict__ wire, long long n,
                                                               uint16_t *__restrict__ y, long long NH) {
+    chain_entry();
     decode16_run<B, DT, U, Y32>(wire, n, y, NH);
 }
 
@@ -789,6 +791,7 @@ __device__ __forceinline__ void reduce16_run(ConstPtrs wires, uint8_t *out, long
 
 template <int B, int R, int U>
 __global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, uint8_t *out, long long NH) {
+    chain_entry();
     reduce16_run<B, R, U>(wires, out, NH);
 }
 
@@ -974,6 +977,7 @@ __device__ __forceinline__ void reduce32_run(ConstPtrs wires, uint8_t *out, long
 
 template <int B, int R, int U>
 __global__ void __launch_bounds__(kThreads32) reduce32_kernel(ConstPtrs wires, uint8_t *out, long long NB) {
+    chain_entry();
     reduce32_run<B, R, U>(wires, out, NB);
 }
 
@@ -1029,6 +1033,7 @@ template <class P, int R, int G, int SG>
 __global__ void __launch_bounds__(P::kThreads * G, 1) staged_reduce_kernel(ConstPtrs wires, uint8_t *out,
                                                                           long long T, long long n,
                                                                           unsigned *timeouts) {
+    chain_entry();
     static_assert(G >= 1 && G <= 15 && SG >= 1, "named barriers 1..G, at least one stage per group");
     constexpr uint32_t kStageBytes = R * P::kTileIn;
     extern __shared__ __align__(128) uint8_t ring[];  // G * SG * R * P::kTileIn bytes

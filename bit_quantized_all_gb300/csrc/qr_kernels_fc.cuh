@@ -183,6 +183,7 @@ constexpr int kThreadsFc = 128;
 template <int BRS, int BAG, int DT, int R, bool A32>
 __global__ void __launch_bounds__(kThreadsFc, 4) fc_allreduce_kernel(ConstPtrs x, long long n, uint16_t *y,
                                                                      long long T) {
+    chain_entry();
     const int i = threadIdx.x;
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const long long base = t * kTileValues + 16 * i;
@@ -272,6 +273,7 @@ struct FcTile {
 template <int B, int DT, bool A32>
 __global__ void __launch_bounds__(kThreadsFc) fc_encode_kernel(const uint16_t *__restrict__ x, long long n,
                                                                uint8_t *__restrict__ wire, long long T) {
+    chain_entry();
     const int i = threadIdx.x;
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const long long base = t * kTileValues + 16 * i;
@@ -291,6 +293,7 @@ __global__ void __launch_bounds__(kThreadsFc) fc_encode_kernel(const uint16_t *_
 template <int B, int DT, bool A32>
 __global__ void __launch_bounds__(kThreadsFc) fc_decode_kernel(const uint8_t *__restrict__ wire, long long n,
                                                                uint16_t *__restrict__ y, long long T) {
+    chain_entry();
     const int i = threadIdx.x;
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         HalfWords<B> c;
@@ -343,6 +346,7 @@ __device__ __forceinline__ void fc_reduce_tile(const HalfWords<BIN> (&c)[R], con
 template <int BIN, int BOUT, int R, int U>
 __global__ void __launch_bounds__(kThreadsFc, 4) fc_reduce_kernel(ConstPtrs wires, long long n, uint8_t *out,
                                                                   long long T) {
+    chain_entry();
     const int i = threadIdx.x;
     const long long S = gridDim.x;
     for (long long t0 = blockIdx.x; t0 < T; t0 += U * S) {
@@ -390,6 +394,7 @@ __device__ __forceinline__ void fc_load_set(const ConstPtrs &wires, long long t,
 template <int BIN, int BOUT, int R, int MINB>
 __global__ void __launch_bounds__(kThreadsFc, MINB) fc_reduce_ahead_kernel(ConstPtrs wires, long long n,
                                                                            uint8_t *out, long long T) {
+    chain_entry();
     const int i = threadIdx.x;
     const long long S = gridDim.x;
     long long t = blockIdx.x;

@@ -82,6 +82,7 @@ __device__ __forceinline__ void fp4_quantize(const float2 *v, const Fp4Scale &sc
 template <int DT>
 __global__ void __launch_bounds__(kThreads32) fp4_encode_kernel(const uint16_t *__restrict__ x, long long n,
                                                                 uint8_t *__restrict__ wire, long long NB) {
+    chain_entry();
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long gb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb < NB; gb += S) {
         uint32_t raw[16];
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kThreads32) fp4_encode_kernel(const uint16_t *
 template <int DT, bool Y32>  // Y32: y is 32-byte aligned (one 256-bit store per thread)
 __global__ void __launch_bounds__(kThreads32) fp4_decode_kernel(const uint8_t *__restrict__ wire, long long n,
                                                                 uint16_t *__restrict__ y, long long NH) {
+    chain_entry();
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long hb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb < NH; hb += S) {
         const long long gb = hb >> 1;

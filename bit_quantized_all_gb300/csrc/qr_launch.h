@@ -6,6 +6,28 @@
 
 namespace qrk {
 
+// Launches `kernel` on `s` with programmatic stream serialization: the grid
+// may begin while the previous kernel on the stream is finishing; the kernel
+// must call chain_entry() (qr_device.cuh) before it touches global memory,
+// which makes it wait for that kernel's completion.  Returns the launch's
+// error, else any error already pending.
+template <class... Params, class... Args>
+cudaError_t launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                           Args &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // CTAs for a grid-stride launch over `tiles` work units: `ctas` if positive,
 // else `waves` full waves of resident CTAs of `kernel` (launched with
 // `threads` threads per CTA) on the current device; capped at `tiles`.

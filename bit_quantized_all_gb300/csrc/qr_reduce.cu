@@ -22,9 +22,8 @@ static cudaError_t run_reduce_staged_r(const ConstPtrs &w, long long n, void *ou
     long long grid = ctas > 0 ? ctas : sms;
     if (grid > sms) grid = sms;
     if (grid > T) grid = T;
-    kern<<<static_cast<int>(grid), QrReduce<B>::kThreads * Shape::kGroups, Shape::kSmemBytes, s>>>(
-        w, static_cast<uint8_t *>(out), T, n, timeouts);
-    return cudaGetLastError();
+    return launch_chained(kern, static_cast<int>(grid), QrReduce<B>::kThreads * Shape::kGroups, Shape::kSmemBytes, s,
+                          w, static_cast<uint8_t *>(out), T, n, timeouts);
 }
 
 // Where the default takes the staged kernel: INT4, INT6 and INT8 from 48
@@ -47,16 +46,15 @@ static cudaError_t run_reduce_r(const ConstPtrs &w, long long n, void *out, cuda
         const long long units = (NH + kThreads32 * U - 1) / (kThreads32 * U);
         const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
         if (grid <= 0) return err;
-        kern<<<grid, kThreads32, 0, s>>>(w, static_cast<uint8_t *>(out), NH);
+        return launch_chained(kern, grid, kThreads32, 0, s, w, static_cast<uint8_t *>(out), NH);
     } else {
         const long long NB = 64 * T;
         auto kern = reduce32_kernel<B, R, U>;
         const long long units = (NB + kThreads32 * U - 1) / (kThreads32 * U);
         const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
         if (grid <= 0) return err;
-        kern<<<grid, kThreads32, 0, s>>>(w, static_cast<uint8_t *>(out), NB);
+        return launch_chained(kern, grid, kThreads32, 0, s, w, static_cast<uint8_t *>(out), NB);
     }
-    return cudaGetLastError();
 }
 
 template <int B>

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(128 * G, 1) staged_allreduce_kernel(ConstPtrs 
         mbar_init_fence();
     }
     __syncthreads();
+    chain_entry();  // the rest reads and writes global memory
 
     const int g = threadIdx.x / 128, k = threadIdx.x & 127;
     const bool leader = k == 0;
@@ -165,9 +166,8 @@ cudaError_t launch_staged(const ConstPtrs &xp, long long n, void *y, int ctas, c
     if (grid > sms) grid = sms;
     if (grid > full_tiles) grid = full_tiles;
     if (grid < 1) grid = 1;  // a message shorter than one tile: CTA 0 does the ragged tile
-    kern<<<static_cast<int>(grid), 128 * Shape::kGroups, Shape::kSmemBytes, s>>>(
-        xp, n, static_cast<uint16_t *>(y), full_tiles, timeouts);
-    return cudaGetLastError();
+    return launch_chained(kern, static_cast<int>(grid), 128 * Shape::kGroups, Shape::kSmemBytes, s, xp, n,
+                          static_cast<uint16_t *>(y), full_tiles, timeouts);
 }
 
 template <class Tile>

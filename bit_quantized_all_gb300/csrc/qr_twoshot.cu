@@ -29,6 +29,7 @@ long long twoshot_segment_tiles(long long tiles, int R) { return (tiles + R - 1)
 template <int B, int DT, int U>
 __global__ void __launch_bounds__(kThreads32) twoshot_send_kernel(ConstPtrs x, long long n, uint8_t *ws,
                                                                   long long seg, long long NB) {
+    chain_entry();
     const int j = static_cast<int>(blockIdx.y);
     encode32_run<B, DT, U>(static_cast<const uint16_t *>(row_pointer(x.p, j)), n,
                            OwnerTiles{ws, seg, static_cast<int>(gridDim.y), j, Codec<B>::kTileBytes}, NB);
@@ -38,6 +39,7 @@ __global__ void __launch_bounds__(kThreads32) twoshot_send_kernel(ConstPtrs x, l
 // segment, in sender order, into its segment of the gathered wire.
 template <int B, int R, int U>
 __global__ void __launch_bounds__(kThreads32) twoshot_reduce_kernel(uint8_t *ws, long long T, long long seg) {
+    chain_entry();
     const long long k = blockIdx.y;
     const long long t0 = k * seg;
     const long long tiles = (T < t0 + seg ? T : t0 + seg) - t0;
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(kThreads32) twoshot_reduce_kernel(uint8_t *ws,
 template <int B, int DT, int U, bool Y32>
 __global__ void __launch_bounds__(kThreads32) twoshot_decode_kernel(const uint8_t *__restrict__ red, long long n,
                                                                     MutPtrs y, long long NH) {
+    chain_entry();
     decode16_run<B, DT, U, Y32>(red, n, static_cast<uint16_t *>(row_pointer(y.p, static_cast<int>(blockIdx.y))), NH);
 }
 
@@ -80,8 +83,7 @@ static cudaError_t send_all(int R, const void *const *x, long long n, uint8_t *w
     cudaError_t err = cudaSuccess;
     const int gx = row_ctas(reinterpret_cast<const void *>(kern), (NB + kThreads32 * U - 1) / (kThreads32 * U), R, &err);
     if (gx <= 0) return err;
-    kern<<<dim3(gx, R), kThreads32, 0, s>>>(xp, n, ws, seg, NB);
-    return cudaGetLastError();
+    return launch_chained(kern, dim3(gx, R), kThreads32, 0, s, xp, n, ws, seg, NB);
 }
 
 template <int B, int R>
@@ -93,8 +95,7 @@ static cudaError_t reduce_all_r(uint8_t *ws, long long T, long long seg, cudaStr
     const int gx = row_ctas(reinterpret_cast<const void *>(kern), (per_row + kThreads32 * U - 1) / (kThreads32 * U), R,
                             &err);
     if (gx <= 0) return err;
-    kern<<<dim3(gx, R), kThreads32, 0, s>>>(ws, T, seg);
-    return cudaGetLastError();
+    return launch_chained(kern, dim3(gx, R), kThreads32, 0, s, ws, T, seg);
 }
 
 template <int B>
@@ -126,8 +127,7 @@ static cudaError_t decode_all(int R, const uint8_t *red, long long n, void *cons
     cudaError_t err = cudaSuccess;
     const int gx = row_ctas(reinterpret_cast<const void *>(kern), (NH + kThreads32 * U - 1) / (kThreads32 * U), R, &err);
     if (gx <= 0) return err;
-    kern<<<dim3(gx, R), kThreads32, 0, s>>>(red, n, yp, NH);
-    return cudaGetLastError();
+    return launch_chained(kern, dim3(gx, R), kThreads32, 0, s, red, n, yp, NH);
 }
 
 template <int B, int DT>

@@ -64,6 +64,18 @@
  *     by the context's id, so after cudaDeviceReset (or any other teardown
  *     and re-creation of the context) the first call in the new context
  *     repeats the setup instead of reusing addresses of the old one.
+ *   - Stream order is kept, with the launches chained: every kernel is
+ *     launched with programmatic stream serialization and, before it reads
+ *     or writes global memory, waits until the previous kernel on the stream
+ *     has completed (griddepcontrol.wait), so it sees everything that kernel
+ *     wrote, as with an ordinary launch.  Its CTAs may take SMs, and run up
+ *     to that wait, while the previous kernel's last CTAs finish, which
+ *     removes the gap between back-to-back calls.  Each kernel also lets
+ *     the next kernel on the stream start launching early
+ *     (griddepcontrol.launch_dependents); a caller's own kernel launched
+ *     after it with programmatic serialization must wait likewise before
+ *     it reads this call's outputs.  (The per-rank two-shot calls, the
+ *     flag-joined two-shot and the self-tests are launched plainly.)
  *   - Failure of a device-side wait: the staged kernels and the flag-joined
  *     two-shot bound every wait (one second).  A wait that runs out (which
  *     a correct launch never does) makes the kernel stop early and count
