@@ -56,6 +56,7 @@ struct PeerOwnerTiles {
 template <int B, int DT, int U>
 __global__ void __launch_bounds__(kThreads32) peer_send_kernel(const uint16_t *__restrict__ x, long long n,
                                                                PeerOwnerTiles dst, long long NB) {
+    chain_entry();
     encode32_run<B, DT, U>(x, n, dst, NB);
 }
 
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kThreads32) peer_send_kernel(const uint16_t *_
 template <int B, int R, int U>
 __global__ void __launch_bounds__(kThreads32) peer_reduce_kernel(const uint8_t *__restrict__ own, MutPtrs ws,
                                                                  long long seg, long long tile0, long long NB) {
+    chain_entry();
     constexpr long long tb = Codec<B>::kTileBytes;
     const long long gathered = static_cast<long long>(R) * seg * tb;
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
@@ -116,8 +118,7 @@ cudaError_t run_peer_send(int R, int rank, const void *x, long long n, const Mut
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
     if (grid <= 0) return err;
     PeerOwnerTiles dst{ws, twoshot_segment_tiles(T, R), rank, Codec<B>::kTileBytes};
-    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint16_t *>(x), n, dst, NB);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint16_t *>(x), n, dst, NB);
 }
 
 template <int B, int R>
@@ -134,8 +135,7 @@ cudaError_t run_peer_reduce_r(int rank, long long n, const MutPtrs &ws, cudaStre
     const long long units = (NB + kThreads32 * U - 1) / (kThreads32 * U);
     const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
     if (grid <= 0) return err;
-    kern<<<grid, kThreads32, 0, s>>>(static_cast<const uint8_t *>(ws.p[rank]), ws, seg, t0, NB);
-    return cudaGetLastError();
+    return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint8_t *>(ws.p[rank]), ws, seg, t0, NB);
 }
 
 template <int B>

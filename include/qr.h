@@ -74,8 +74,8 @@
  *     the next kernel on the stream start launching early
  *     (griddepcontrol.launch_dependents); a caller's own kernel launched
  *     after it with programmatic serialization must wait likewise before
- *     it reads this call's outputs.  (The per-rank two-shot calls, the
- *     flag-joined two-shot and the self-tests are launched plainly.)
+ *     it reads this call's outputs.  (The flag-joined two-shot and the
+ *     self-tests are launched plainly.)
  *   - Failure of a device-side wait: the staged kernels and the flag-joined
  *     two-shot bound every wait (one second).  A wait that runs out (which
  *     a correct launch never does) makes the kernel stop early and count
