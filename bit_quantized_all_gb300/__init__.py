@@ -650,7 +650,8 @@ def qr_fp4_decode(wire: torch.Tensor, n: int, dtype: torch.dtype = torch.bfloat1
 
 def qr_fp4_segment_reduce(wires, n: int, out: torch.Tensor | None = None, stream=None,
                           ctas: int = 0) -> torch.Tensor:
-    """Phase-1B of the FP4 codec (the staged kernel)."""
+    """Phase-1B of the FP4 codec (the staged kernel with `ctas` persistent CTAs;
+    with ctas = 0 the library may take a register-fed kernel on long messages)."""
     wires = list(wires)
     if not 1 <= len(wires) <= QR_MAX_RANKS:
         raise ValueError(f"1 to {QR_MAX_RANKS} wires are supported, got {len(wires)}")

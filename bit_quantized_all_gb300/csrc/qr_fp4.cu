@@ -43,7 +43,10 @@ cudaError_t launch_fp4_decode(int dtype, const void *wire, long long n, void *y,
     return dtype ? run_fp4_decode<1>(wire, n, y, s) : run_fp4_decode<0>(wire, n, y, s);
 }
 
-// Phase-1B on the staged kernel with min(ctas or #SMs, #SMs, tiles) CTAs.
+// Phase-1B on the staged kernel with min(ctas or #SMs, #SMs, tiles) CTAs;
+// with ctas = 0, from 48 tiles per SM at the rank counts that
+// fp4_reduce_ahead_min_blocks names, the one-block-ahead kernel instead (two
+// waves of resident CTAs).
 template <int R>
 static cudaError_t run_fp4_reduce_r(const ConstPtrs &w, long long n, void *out, int ctas, cudaStream_t s) {
     using Shape = StagedReduceShape<Fp4Reduce, R>;
@@ -52,6 +55,16 @@ static cudaError_t run_fp4_reduce_r(const ConstPtrs &w, long long n, void *out, 
     cudaError_t err = cudaSuccess;
     const int sms = sm_count(&err);
     if (sms <= 0) return err;
+    constexpr int kAhead = fp4_reduce_ahead_min_blocks<R>();
+    if constexpr (kAhead > 0) {
+        if (ctas == 0 && T >= 48LL * sms) {
+            const long long NB = 64 * T;
+            auto ahead = reduce_ahead_kernel<Fp4BlockReducer, R, kAhead>;
+            const int grid = grid_for(reinterpret_cast<const void *>(ahead), kThreads32, NB, 0, 2, &err);
+            if (grid <= 0) return err;
+            return launch_chained(ahead, grid, kThreads32, 0, s, w, static_cast<uint8_t *>(out), NB);
+        }
+    }
     if ((err = allow_dynamic_smem(reinterpret_cast<const void *>(kern), Shape::kSmemBytes)) != cudaSuccess)
         return err;
     unsigned *timeouts = wait_timeout_counter(&err);

@@ -981,6 +981,81 @@ __global__ void __launch_bounds__(kThreads32) reduce32_kernel(ConstPtrs wires, u
     reduce32_run<B, R, U>(wires, out, NB);
 }
 
+// The per-block Phase-1B of the symmetric codec, as a policy of
+// reduce_ahead_kernel (the FP4 codec has its own, Fp4BlockReducer).
+template <int B>
+struct QrBlockReducer {
+    static constexpr int kBits = B;
+    template <int R>
+    static __device__ __forceinline__ void reduce(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
+                                                  uint8_t *tile, int g) {
+        reduce_block<B, R>(c, sb, tile, g);
+    }
+};
+
+// Block gb's codes and scale from each of the R wires.
+template <int B, int R>
+__device__ __forceinline__ void load_block_ranks(const ConstPtrs &wires, long long gb, BlockWords<B> (&c)[R],
+                                                 uint32_t (&sb)[R]) {
+    const long long off = (gb >> 6) * Codec<B>::kTileBytes;
+    const int g = static_cast<int>(gb & 63);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint8_t *tile = static_cast<const uint8_t *>(wires.p[r]) + off;
+        load_block_codes<B>(tile, g, c[r]);
+        sb[r] = load_block_scale_bits<B>(tile, g);
+    }
+}
+
+// Phase-1B from registers, one block per thread and one block ahead: the
+// loads of the thread's next block (a grid stride on) are issued before this
+// block is reduced, so every thread has loads in flight while it computes;
+// two register sets take turns.  MINB caps the registers (CTAs per SM).
+// Same results as reduce32_kernel and staged_reduce_kernel.
+template <class P, int R, int MINB>
+__global__ void __launch_bounds__(kThreads32, MINB) reduce_ahead_kernel(ConstPtrs wires, uint8_t *out,
+                                                                        long long NB) {
+    chain_entry();
+    constexpr int B = P::kBits;
+    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
+    long long gb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x;
+    if (gb >= NB) return;
+    BlockWords<B> ca[R], cb[R];
+    uint32_t sa[R], sbb[R];
+    load_block_ranks<B, R>(wires, gb, ca, sa);
+    while (true) {
+        if (gb + S < NB) load_block_ranks<B, R>(wires, gb + S, cb, sbb);
+        P::template reduce<R>(ca, sa, out + (gb >> 6) * Codec<B>::kTileBytes, static_cast<int>(gb & 63));
+        gb += S;
+        if (gb >= NB) break;
+        if (gb + S < NB) load_block_ranks<B, R>(wires, gb + S, ca, sa);
+        P::template reduce<R>(cb, sbb, out + (gb >> 6) * Codec<B>::kTileBytes, static_cast<int>(gb & 63));
+        gb += S;
+        if (gb >= NB) break;
+    }
+}
+
+// Where the symmetric codec's Phase-1B of a long message (from 48 tiles per
+// SM) runs reduce_ahead_kernel, with how many CTAs per SM (0 = not: the
+// staged kernel for INT4/6/8, reduce32_kernel for INT3).  Measured on GB300
+// at 2^27 (2^28) bf16 values per rank, fraction of the copy bandwidth,
+// default kernel -> one block ahead: INT8 R=4 0.965 (0.992) -> 0.988
+// (1.013); INT6 R=2 0.616 (0.639) -> 0.635 (0.660), R=3 0.648 -> 0.662, R=4
+// 0.684 (0.706) -> 0.706 (0.732); INT4 R=3 0.599 -> 0.633, R=8 0.749 (0.770)
+// -> 0.787 (0.815); INT3 R=2 0.418 (0.446) -> 0.434 (0.460).  Elsewhere it
+// was slower or within 1% (at R >= 5 more ranks' loads in flight than its
+// registers hold, except INT4 at R = 8).
+template <int B, int R>
+__host__ __device__ constexpr int reduce_ahead_min_blocks() {
+    return (B == 8 && R == 4)                       ? 2
+           : (B == 6 && R == 2)                     ? 3
+           : (B == 6 && (R == 3 || R == 4))         ? 2
+           : (B == 4 && R == 3)                     ? 3
+           : (B == 4 && R == 8)                     ? 2
+           : (B == 3 && R == 2)                     ? 2
+                                                    : 0;
+}
+
 // Which Phase-1B kernel: measured on GB300 at 2^24..2^30 values per rank, the
 // two-threads-per-block kernel is faster for INT4/INT6 with six or more
 // ranks (latency-bound there); one thread per block needs fewer

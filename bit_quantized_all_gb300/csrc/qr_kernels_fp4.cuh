@@ -198,6 +198,27 @@ struct Fp4Reduce {
     }
 };
 
+// The FP4 per-block Phase-1B as a policy of reduce_ahead_kernel.
+struct Fp4BlockReducer {
+    static constexpr int kBits = 4;
+    template <int R>
+    static __device__ __forceinline__ void reduce(const BlockWords<4> (&c)[R], const uint32_t (&sb)[R],
+                                                  uint8_t *tile, int g) {
+        fp4_reduce_block<R>(c, sb, tile, g);
+    }
+};
+
+// Where the FP4 Phase-1B of a long message (from 48 tiles per SM) runs
+// reduce_ahead_kernel instead of the staged kernel, with how many CTAs per
+// SM (0 = not).  Measured on GB300 at 2^27 (2^28) bf16 values per rank,
+// fraction of the copy bandwidth, staged -> one block ahead: R=2 0.677
+// (0.723) -> 0.732 (0.787), R=3 0.794 -> 0.826, R=8 0.898 (0.939) -> 0.974
+// (0.994); at R = 4..7 the staged kernel was faster.
+template <int R>
+__host__ __device__ constexpr int fp4_reduce_ahead_min_blocks() {
+    return R == 2 ? 4 : R == 3 ? 3 : R == 8 ? 2 : 0;
+}
+
 // ---------------------------------------------------------------------------
 // the fused all-reduce: the per-tile policy of staged_allreduce_kernel
 // (16 values per thread, two threads per block sharing the absmax)

@@ -27,18 +27,36 @@ static cudaError_t run_reduce_staged_r(const ConstPtrs &w, long long n, void *ou
 }
 
 // Where the default takes the staged kernel: INT4, INT6 and INT8 from 48
-// tiles per SM (INT3 is bound by the integer pipe and stays register-fed).
+// tiles per SM (INT3 is bound by the integer pipe and stays register-fed),
+// except where reduce_ahead_min_blocks names the one-block-ahead kernel.
 constexpr long long kStagedReduceMinTilesPerSm = 48;
+
+// The one-block-ahead kernel with two waves of resident CTAs.
+template <int B, int R, int MINB>
+static cudaError_t run_reduce_ahead_r(const ConstPtrs &w, long long T, void *out, cudaStream_t s) {
+    const long long NB = 64 * T;
+    auto kern = reduce_ahead_kernel<QrBlockReducer<B>, R, MINB>;
+    cudaError_t err = cudaSuccess;
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, NB, 0, 2, &err);
+    if (grid <= 0) return err;
+    return launch_chained(kern, grid, kThreads32, 0, s, w, static_cast<uint8_t *>(out), NB);
+}
 
 template <int B, int R>
 static cudaError_t run_reduce_r(const ConstPtrs &w, long long n, void *out, cudaStream_t s) {
     constexpr int U = reduce_units_per_thread<R>();  // work units per thread in flight
+    constexpr int kAhead = reduce_ahead_min_blocks<B, R>();
     const long long T = (n + kTileValues - 1) / kTileValues;
     cudaError_t err = cudaSuccess;
-    if constexpr (B != 3) {
+    if constexpr (B != 3 || kAhead > 0) {
         const int sms = sm_count(&err);
         if (sms <= 0) return err;
-        if (T >= kStagedReduceMinTilesPerSm * sms) return run_reduce_staged_r<B, R>(w, n, out, 0, s);
+        if (T >= kStagedReduceMinTilesPerSm * sms) {
+            if constexpr (kAhead > 0)
+                return run_reduce_ahead_r<B, R, kAhead>(w, T, out, s);
+            else
+                return run_reduce_staged_r<B, R>(w, n, out, 0, s);
+        }
     }
     if constexpr (reduce_two_threads_per_block<B, R>()) {
         const long long NH = 128 * T;

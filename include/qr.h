@@ -147,7 +147,11 @@ qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires,
  * `ctas` = 0 for one CTA per SM,
  * else min(ctas, #SMs) (at most one per tile); the result does not depend on
  * it; ctas < 0 is QR_ERR_INVALID_ARG.  qr_segment_reduce itself takes this
- * kernel for INT4, INT6 and INT8 from 48 tiles per SM.  Its waits on its
+ * kernel for INT4, INT6 and INT8 from 48 tiles per SM, except INT8 at R = 4,
+ * INT6 at R = 2..4 and INT4 at R = 3 and 8, where (as for INT3 at R = 2) it
+ * runs a kernel from registers that loads each thread's next block before
+ * reducing the current one; below 48 tiles per SM, and for INT3 otherwise,
+ * a kernel from registers with one block per thread.  Its waits on its
  * shared-memory barriers are bounded (see qr_wait_timeouts).  Same other
  * arguments and errors as qr_segment_reduce. */
 qr_status_t qr_segment_reduce_staged(int bits, int R, const void *const *wires,
@@ -506,7 +510,10 @@ qr_status_t qr_fp4_decode(qr_dtype_t dtype, const void *wire, size_t n, void *y,
 /* Phase-1B of the FP4 codec on the staged kernel (the R wire tiles brought
  * into shared memory by bulk copies), `ctas` = 0 for one CTA per SM, else
  * min(ctas, #SMs); the result does not depend on it; ctas < 0 is
- * QR_ERR_INVALID_ARG.  out_wire may equal one of the wires exactly. */
+ * QR_ERR_INVALID_ARG.  With ctas = 0 and R = 2, 3 or 8, from 48 tiles per
+ * SM, a kernel from registers that loads each thread's next block before
+ * reducing the current one runs instead (the same bytes).  out_wire may
+ * equal one of the wires exactly. */
 qr_status_t qr_fp4_segment_reduce(int R, const void *const *wires, size_t n,
                                   void *out_wire, int ctas, qr_stream_t stream);
 
