@@ -73,13 +73,15 @@ constexpr int kFcReduceUnroll = 2;  // tiles per thread in flight in the registe
 
 // Where the register-fed Phase-1B loads one tile ahead (fc_reduce_ahead_kernel)
 // instead of two tiles at once, and with how many CTAs per SM (0 = not).  At
-// 2^27 values per rank, two at once / one ahead: 4-bit inputs R=4 0.56 / 0.58,
-// R=6 0.57 / 0.59, R=8 0.58 / 0.62 (4 -> 4) and 0.62 / 0.67 (4 -> 8), with
-// five CTAs per SM and four waves (at R = 2 one ahead was slower); 8 -> 8 at
-// R=3 0.86 / 0.93 (0.89 / 0.96 at 2^28) with eight CTAs per SM and two waves.
+// 2^27 values per rank, two at once / one ahead: 4-bit inputs R=2 0.49 / 0.51
+// (4 -> 4) and 0.63 / 0.63 (4 -> 8), R=3 0.52 / 0.54 and 0.62 / 0.63, R=4
+// 0.56 / 0.58, R=6 0.57 / 0.59, R=8 0.58 / 0.62 (4 -> 4) and 0.62 / 0.67
+// (4 -> 8), with five CTAs per SM and four waves; 8 -> 8 at R=3 0.86 / 0.93
+// (0.89 / 0.96 at 2^28) with eight CTAs per SM and two waves (at R = 2
+// within 1% at 2^28).
 template <int BIN, int BOUT, int R>
 __host__ __device__ constexpr int fc_reduce_ahead_min_blocks() {
-    return (BIN == 4 && R >= 4) ? 5 : (BIN == 8 && R == 3) ? 8 : 0;
+    return (BIN == 4 && R >= 2) ? 5 : (BIN == 8 && R == 3) ? 8 : 0;
 }
 
 template <int BIN, int BOUT, int R>

@@ -443,7 +443,7 @@ qr_status_t qr_fc_segment_reduce(int bits_in, int bits_out, int R,
  * takes it from 48 tiles per SM when bits_in = 8 and R >= 4, and otherwise
  * runs a grid-stride kernel from registers: one that issues the loads of a
  * thread's next tile before reducing the current one when bits_in = 4 and
- * R >= 4, or bits_in = 8 and R = 3, else one that loads two tiles at a
+ * R >= 2, or bits_in = 8 and R = 3, else one that loads two tiles at a
  * time. */
 qr_status_t qr_fc_segment_reduce_staged(int bits_in, int bits_out, int R,
                                         const void *const *wires, size_t n,

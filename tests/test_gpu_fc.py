@@ -96,7 +96,7 @@ def test_every_rank_count(R):
             fc_full_check(*pair, dtype, _rand_ranks(R, n, dtype, 77 + R), f"R={R} {pair} dt={dtype}")
 
 
-@pytest.mark.parametrize("pair,R", [((4, 4), 8), ((4, 8), 5), ((4, 4), 4), ((8, 8), 3)])
+@pytest.mark.parametrize("pair,R", [((4, 4), 8), ((4, 8), 5), ((4, 4), 4), ((8, 8), 3), ((4, 4), 2), ((4, 8), 3)])
 def test_phase1b_many_tiles_per_cta(pair, R):
     """Enough tiles that every CTA of the Phase-1B grid-stride kernels reduces
     several (odd and even counts: both register sets of the one-tile-ahead
