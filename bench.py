@@ -607,8 +607,17 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                     fused_b = 2 * Rs * n + 2 * n
                     kernel_b = {"fused": fused_b, "fused_regs": fused_b, "unfused": fused_b + 2 * Rs * Wi + 2 * Wo,
                                 "encode": Rs * (2 * n + Wi), "reduce": Rs * Wi + Wo,
-                                "reduce_staged": Rs * Wi + Wo, "decode": Wo + 2 * n}
+                                "reduce_staged": Rs * Wi + Wo, "decode": Wo + 2 * n,
+                                # R sends (2N in, Wi out), the owners' R*Wi in and Wo
+                                # out, R decodes (Wo in, 2N out)
+                                "twoshot": 4 * Rs * n + 2 * Rs * Wi + (Rs + 1) * Wo}
                     do_flush = fused_b < (512 << 20)
+                    wst = torch.empty(qr.qr_fc_twoshot_workspace_bytes(brs, bag, Rs, n), dtype=torch.uint8,
+                                      device=dev)
+                    yst = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
+
+                    def twoshot():
+                        qr.qr_fc_allreduce_twoshot(brs, bag, xs, ys=yst, workspace=wst)
 
                     def fused():
                         qr.qr_fc_allreduce(brs, bag, xs, y=y)
@@ -636,11 +645,12 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
 
                     arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
                             ("encode", encode_all), ("reduce", reduce_only), ("reduce_staged", reduce_staged),
-                            ("decode", decode_only))
+                            ("decode", decode_only), ("twoshot", twoshot))
                     times = time_arms(arms, args, flush if do_flush else None,
-                                      warm=(fused, fused_regs, unfused, reduce_staged))
+                                      warm=(fused, fused_regs, unfused, reduce_staged, twoshot))
                     same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
-                        torch.equal(y.view(torch.int16), y2.view(torch.int16))) and bool(torch.equal(red, red2))
+                        torch.equal(y.view(torch.int16), y2.view(torch.int16))) and bool(torch.equal(red, red2)) and all(
+                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in yst)
                     for name, alg in kernel_b.items():
                         med = statistics.median(times[name])
                         print(json.dumps({
@@ -651,7 +661,7 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
                             "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None, "fused_equals_unfused": same, "reps": args.reps,
                             "burst": 1 if do_flush else args.burst}), flush=True)
-                    del wires, red, red2
+                    del wires, red, red2, wst, yst
                 del xs, y, yu, y2
                 torch.cuda.empty_cache()
 

@@ -184,6 +184,55 @@ size_t fc_wire_bytes(int bits, size_t n) {
 
 }  // namespace
 
+namespace {
+
+// R*R*seg reduce-scatter tiles, then T all-gather tiles (0 on overflow or an
+// unsupported pair or rank count).
+size_t fc_twoshot_ws_bytes(int bits_rs, int bits_ag, int R, size_t n) {
+    if (!fc_pair_ok(bits_rs, bits_ag) || R < 1 || R > QR_MAX_RANKS) return 0;
+    const size_t tbi = size_t(256) * size_t(bits_rs) + 128, tbo = size_t(256) * size_t(bits_ag) + 128;
+    const size_t tiles = n / kTile + (n % kTile != 0);
+    const size_t seg = tiles / size_t(R) + (tiles % size_t(R) != 0);
+    const size_t bufs = size_t(R) * size_t(R);
+    if (seg > SIZE_MAX / bufs || seg * bufs > SIZE_MAX / tbi || tiles > SIZE_MAX / tbo) return 0;
+    const size_t a = seg * bufs * tbi, b = tiles * tbo;
+    if (a > SIZE_MAX - b) return 0;
+    return a + b;
+}
+
+}  // namespace
+
+QR_EXPORT size_t qr_fc_twoshot_workspace_bytes(int bits_rs, int bits_ag, int R, size_t n) {
+    return fc_twoshot_ws_bytes(bits_rs, bits_ag, R, n);
+}
+
+QR_EXPORT qr_status_t qr_fc_allreduce_twoshot(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
+                                              const void *const *x, size_t n, void *const *y, void *workspace,
+                                              size_t workspace_bytes, qr_stream_t stream) {
+    if (!x || !y || !workspace || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!x[r] || !y[r]) return QR_ERR_INVALID_ARG;
+    if (!fc_pair_ok(bits_rs, bits_ag) || !dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    const size_t need = fc_twoshot_ws_bytes(bits_rs, bits_ag, R, n);
+    if (!value_bytes_ok(n) || need == 0) return QR_ERR_SIZE;
+    if (workspace_bytes < need) return QR_ERR_SIZE;
+    const size_t V = 2 * n;
+    if (!aligned16(workspace)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(x[r]) || !aligned16(y[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r) {
+        if (overlaps(workspace, need, x[r], V) || overlaps(workspace, need, y[r], V)) return QR_ERR_INVALID_ARG;
+        for (int i = 0; i < R; ++i) {
+            // every input is read in Phase-1, before any output is written: an
+            // output may be an input exactly (in place), never partly
+            if (bad_alias(y[r], V, x[i], V)) return QR_ERR_INVALID_ARG;
+            if (i < r && overlaps(y[r], V, y[i], V)) return QR_ERR_INVALID_ARG;
+        }
+    }
+    return from_cuda(qrk::launch_fc_twoshot(bits_rs, bits_ag, dtype, R, x, static_cast<long long>(n), y, workspace,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QR_EXPORT size_t qr_fc_tile_bytes(int bits) { return fc_bits_ok(bits) ? size_t(256) * size_t(bits) + 128 : 0; }
 
 QR_EXPORT size_t qr_fc_wire_bytes(int bits, size_t n) { return fc_wire_bytes(bits, n); }

@@ -478,6 +478,24 @@ qr_status_t qr_fc_allreduce_staged(int bits_rs, int bits_ag, qr_dtype_t dtype, i
                                    const void *const *x, size_t n, void *y,
                                    int ctas, qr_stream_t stream);
 
+/* The asymmetric codec's two-shot exchange laid out per rank and per owner
+ * ([FC] key machinery: quantize at the reduce-scatter width, all-to-all,
+ * local sum and re-quantization at the all-gather width, all-gather,
+ * dequantize), as qr_allreduce_twoshot for the symmetric codec: with
+ * seg = ceil(T/R) tiles per owner, owner k's copy of sender j's segment at
+ * reduce-scatter tile (k*R + j)*seg of `workspace`, then the gathered wire
+ * (T all-gather tiles, byte-identical to qr_fc_segment_reduce's output) at
+ * byte R*R*seg*qr_fc_tile_bytes(bits_rs).  Three launches on `stream`, one
+ * per phase, each with one grid row per rank or owner; every y[j] receives
+ * qr_fc_allreduce's output.  workspace_bytes >= qr_fc_twoshot_workspace_bytes
+ * (QR_ERR_SIZE otherwise); the workspace must not overlap any x or y; a y[j]
+ * may equal an x[i] exactly (in place), never partly; outputs must not
+ * overlap one another.  Widths and other errors as qr_fc_allreduce. */
+size_t qr_fc_twoshot_workspace_bytes(int bits_rs, int bits_ag, int R, size_t n); /* 0 if unsupported */
+qr_status_t qr_fc_allreduce_twoshot(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
+                                    const void *const *x, size_t n, void *const *y,
+                                    void *workspace, size_t workspace_bytes, qr_stream_t stream);
+
 /* ---- the FP4 codec -------------------------------------------------------
  * "QuickReduce INT3 quantization and benchmarking on MI355", introduction: a
  * hardware-accelerated FP4 quantization path on MI355, "essentially

@@ -248,6 +248,44 @@ def test_twoshot_workspace_bytes():
     assert qr.qr_twoshot_workspace_bytes(8, 8, 2**64 - 1) == 0
 
 
+def test_fc_twoshot_workspace_bytes():
+    for brs, bag in ((4, 4), (4, 8), (8, 8)):
+        ti, to = 256 * brs + 128, 256 * bag + 128
+        for R in (1, 2, 3, 8):
+            for n in (1, 2048, 2049, 2048 * 17 + 5, 2**27):
+                T = -(-n // 2048)
+                seg = -(-T // R)
+                assert qr.qr_fc_twoshot_workspace_bytes(brs, bag, R, n) == R * R * seg * ti + T * to
+    assert qr.qr_fc_twoshot_workspace_bytes(8, 4, 2, 100) == 0
+    assert qr.qr_fc_twoshot_workspace_bytes(4, 6, 2, 100) == 0
+    assert qr.qr_fc_twoshot_workspace_bytes(4, 4, 0, 100) == 0
+    assert qr.qr_fc_twoshot_workspace_bytes(4, 4, 9, 100) == 0
+    assert qr.qr_fc_twoshot_workspace_bytes(8, 8, 8, 2**64 - 1) == 0
+
+
+@no_gpu_only
+def test_fc_twoshot_validation():
+    n = 2048 * 5 + 3
+    need = qr.qr_fc_twoshot_workspace_bytes(4, 8, 2, n)
+    WS = 0x7F3000000000
+    xs, ys = [A, B], [Y, Y + 2**24]
+    call = capi.qr_fc_allreduce_twoshot
+    assert call(4, 8, 0, 2, xs, n, ys, None, need) == qr.QR_ERR_INVALID_ARG
+    assert call(4, 8, 0, 2, xs, n, [Y, None], WS, need) == qr.QR_ERR_INVALID_ARG
+    assert call(4, 8, 0, 2, xs, 0, ys, WS, need) == qr.QR_ERR_INVALID_ARG
+    assert call(8, 4, 0, 2, xs, n, ys, WS, need) == qr.QR_ERR_UNSUPPORTED       # no 8 -> 4 pair
+    assert call(4, 8, 2, 2, xs, n, ys, WS, need) == qr.QR_ERR_UNSUPPORTED       # dtype
+    assert call(4, 8, 0, 9, [A + 4096 * i for i in range(9)], n, [Y + 2**22 * i for i in range(9)], WS,
+                need) == qr.QR_ERR_UNSUPPORTED
+    assert call(4, 8, 0, 2, xs, n, ys, WS, need - 1) == qr.QR_ERR_SIZE
+    assert call(4, 8, 0, 2, xs, n, ys, WS + 8, need) == qr.QR_ERR_MISALIGNED
+    assert call(4, 8, 0, 2, [A + 8, B], n, ys, WS, need) == qr.QR_ERR_MISALIGNED
+    assert call(4, 8, 0, 2, xs, n, [Y, Y + 4096], WS, need) == qr.QR_ERR_INVALID_ARG   # outputs overlap
+    assert call(4, 8, 0, 2, xs, n, [A + 16, Y], WS, need) == qr.QR_ERR_INVALID_ARG      # partial in-place
+    assert call(4, 8, 0, 2, xs, n, ys, A, need) == qr.QR_ERR_INVALID_ARG              # workspace over an input
+    assert call(4, 8, 0, 2, xs, 2**63, ys, WS, need) == qr.QR_ERR_SIZE
+
+
 @no_gpu_only
 def test_twoshot_validation():
     n = 2048 * 5 + 3

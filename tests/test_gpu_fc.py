@@ -105,6 +105,50 @@ def test_phase1b_many_tiles_per_cta(pair, R):
     fc_full_check(*pair, 1, _rand_ranks(R, n, 1, 500 + R), f"many tiles R={R} {pair}")
 
 
+@pytest.mark.parametrize("n", [2048 * 40 + 37, 2048 * 3 + 1, 700])
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+def test_twoshot(n, R):
+    """The two-shot exchange laid out per rank and per owner: every rank's
+    output equals the fused all-reduce and the oracle's, the owners' receive
+    buffers hold the oracle's wire segments, the gathered wire is the
+    oracle's Phase-1B output; fewer tiles than ranks at the small sizes."""
+    T = -(-n // 2048)
+    seg = -(-T // R)
+    for brs, bag in PAIRS:
+        dt = 1 if brs == 4 else 0
+        xs = _rand_ranks(R, n, dt, 300 + 7 * R + brs + bag)
+        xs_dev = [to_dev(x, dt) for x in xs]
+        ys, ws = qr.qr_fc_allreduce_twoshot(brs, bag, xs_dev)
+        yf = qr.qr_fc_allreduce(brs, bag, xs_dev)
+        torch.cuda.synchronize()
+        y_ref = oracle.fc_allreduce(brs, bag, dt, xs)
+        for j in range(R):
+            assert np.array_equal(to_host_u16(ys[j]), y_ref), (brs, bag, R, n, j)
+            assert torch.equal(ys[j].view(torch.int16), yf.view(torch.int16))
+        ti, to = qr.qr_fc_tile_bytes(brs), qr.qr_fc_tile_bytes(bag)
+        host = to_host_u8(ws)
+        w_ref = [oracle.fc_encode(brs, dt, x) for x in xs]
+        for k in range(R):
+            t0, t1 = k * seg, min(T, (k + 1) * seg)
+            for j in range(R):
+                got = host[((k * R + j) * seg) * ti:((k * R + j) * seg + max(0, t1 - t0)) * ti]
+                assert np.array_equal(got, w_ref[j][t0 * ti:max(t0, t1) * ti]), (brs, bag, R, n, k, j)
+        g = R * R * seg * ti
+        assert np.array_equal(host[g:g + T * to], oracle.fc_segment_reduce(brs, bag, w_ref, n)), (brs, bag, R, n)
+    assert qr.qr_wait_timeouts() == 0
+
+
+def test_twoshot_in_place():
+    n = 2048 * 33 + 5
+    xs = _rand_ranks(4, n, 1, 77)
+    y_ref = oracle.fc_allreduce(4, 8, 1, xs)
+    xs_dev = [to_dev(x, 1) for x in xs]
+    ys, _ = qr.qr_fc_allreduce_twoshot(4, 8, xs_dev, ys=xs_dev)   # every output over its own input
+    torch.cuda.synchronize()
+    for j in range(4):
+        assert np.array_equal(to_host_u16(xs_dev[j]), y_ref)
+
+
 def test_special_groups():
     n = 2048 * 2
     for dtype in (0, 1):
