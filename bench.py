@@ -683,7 +683,10 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                 red = torch.empty(W, dtype=torch.uint8, device=dev)
                 fused_b = 2 * Rs * n + 2 * n
                 kernel_b = {"fused": fused_b, "unfused": fused_b + 2 * Rs * W + 2 * W,
-                            "encode": Rs * (2 * n + W), "reduce": (Rs + 1) * W, "decode": W + 2 * n}
+                            "encode": Rs * (2 * n + W), "reduce": (Rs + 1) * W, "decode": W + 2 * n,
+                            "twoshot": 4 * Rs * n + (3 * Rs + 1) * W}
+                wst = torch.empty(qr.qr_fp4_twoshot_workspace_bytes(Rs, n), dtype=torch.uint8, device=dev)
+                yst = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
                 do_flush = fused_b < (512 << 20)
 
                 def fused():
@@ -704,10 +707,14 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                     reduce_only()
                     decode_only()
 
+                def twoshot():
+                    qr.qr_fp4_allreduce_twoshot(xs, ys=yst, workspace=wst)
+
                 arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all), ("reduce", reduce_only),
-                        ("decode", decode_only))
-                times = time_arms(arms, args, flush if do_flush else None, warm=(fused, unfused))
-                same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16)))
+                        ("decode", decode_only), ("twoshot", twoshot))
+                times = time_arms(arms, args, flush if do_flush else None, warm=(fused, unfused, twoshot))
+                same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and all(
+                    torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in yst)
                 for name, alg in kernel_b.items():
                     med = statistics.median(times[name])
                     print(json.dumps({
@@ -719,7 +726,7 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                         "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None,
                         "fused_equals_unfused": same, "reps": args.reps,
                         "burst": 1 if do_flush else args.burst}), flush=True)
-                del wires, red
+                del wires, red, wst, yst
                 del xs, y, yu
                 torch.cuda.empty_cache()
 

@@ -45,7 +45,8 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_fp4_decode", "qr_fp4_segment_reduce", "qr_fp4_allreduce", "qr_selftest_twoshot_flags_drop",
            "qr_twoshot_peer_workspace_bytes", "qr_twoshot_peer_send", "qr_twoshot_peer_reduce",
            "qr_twoshot_peer_decode", "qr_ipc_handle_bytes", "qr_ipc_get_handle", "qr_ipc_open_handle",
-           "qr_ipc_close_handle", "qr_fc_twoshot_workspace_bytes", "qr_fc_allreduce_twoshot")
+           "qr_ipc_close_handle", "qr_fc_twoshot_workspace_bytes", "qr_fc_allreduce_twoshot",
+           "qr_fp4_twoshot_workspace_bytes", "qr_fp4_allreduce_twoshot")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
                 "qr_fc_allreduce_staged": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_fc_twoshot_workspace_bytes": (sz, [i32, i32, i32, sz]),
                 "qr_fc_allreduce_twoshot": (i32, [i32, i32, i32, i32, vpp, sz, vpp, vp, sz, vp]),
+                "qr_fp4_twoshot_workspace_bytes": (sz, [i32, sz]),
+                "qr_fp4_allreduce_twoshot": (i32, [i32, i32, vpp, sz, vpp, vp, sz, vp]),
                 "qr_fc_allreduce_ctas": (i32, [i32, i32, i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_segment_reduce_staged": (i32, [i32, i32, vpp, sz, vp, i32, vp]),
                 "qr_fc_segment_reduce_staged": (i32, [i32, i32, i32, vpp, sz, vp, i32, vp]),
@@ -177,6 +180,11 @@ class capi:
     @staticmethod
     def qr_allreduce_staged(bits, dtype, R, xs, n, y, ctas, stream=None):
         return lib().qr_allreduce_staged(bits, dtype, R, _ptr_array(xs), n, y, ctas, stream)
+
+    @staticmethod
+    def qr_fp4_allreduce_twoshot(dtype, R, xs, n, ys, workspace, workspace_bytes, stream=None):
+        return lib().qr_fp4_allreduce_twoshot(dtype, R, _ptr_array(xs), n, _ptr_array(ys), workspace,
+                                              workspace_bytes, stream)
 
     @staticmethod
     def qr_fc_allreduce_twoshot(bits_rs, bits_ag, dtype, R, xs, n, ys, workspace, workspace_bytes, stream=None):
@@ -643,6 +651,38 @@ def qr_fc_allreduce_twoshot(bits_rs: int, bits_ag: int, xs, ys=None, workspace: 
 # ---------------------------------------------------------------------------
 # the FP4 codec (the INT4 block framework with E2M1 elements)
 # ---------------------------------------------------------------------------
+def qr_fp4_twoshot_workspace_bytes(R: int, n: int) -> int:
+    return int(lib().qr_fp4_twoshot_workspace_bytes(R, n))
+
+
+def qr_fp4_allreduce_twoshot(xs, ys=None, workspace: torch.Tensor | None = None, stream=None):
+    """The FP4 codec's two-shot all-reduce with its exchange laid out per rank
+    and per owner in `workspace`: returns (the R outputs, the workspace)."""
+    xs, dt, n = _check_inputs(xs)
+    R = len(xs)
+    dev = _same_device(xs, "qr_fp4_allreduce_twoshot")
+    if ys is None:
+        ys = [torch.empty_like(xs[0]) for _ in range(R)]
+    ys = list(ys)
+    if len(ys) != R:
+        raise ValueError("one output per rank is needed")
+    for i, y in enumerate(ys):
+        _cuda_contig(y, f"ys[{i}]")
+        if y.dtype != xs[0].dtype or y.numel() != n:
+            raise ValueError(f"ys[{i}] must match the inputs' dtype and size")
+    need = qr_fp4_twoshot_workspace_bytes(R, n)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _cuda_contig(workspace, "workspace")
+    if workspace.dtype != torch.uint8:
+        raise TypeError(f"workspace must be torch.uint8, got {workspace.dtype}")
+    _same_device(xs + ys + [workspace], "qr_fp4_allreduce_twoshot")
+    _check(capi.qr_fp4_allreduce_twoshot(dt, R, [x.data_ptr() for x in xs], n, [y.data_ptr() for y in ys],
+                                         workspace.data_ptr(), workspace.numel(), _stream(dev, stream)),
+           "qr_fp4_allreduce_twoshot")
+    return ys, workspace
+
+
 def qr_fp4_tile_bytes() -> int:
     return int(lib().qr_fp4_tile_bytes())
 

@@ -202,6 +202,35 @@ size_t fc_twoshot_ws_bytes(int bits_rs, int bits_ag, int R, size_t n) {
 
 }  // namespace
 
+QR_EXPORT size_t qr_fp4_twoshot_workspace_bytes(int R, size_t n) { return twoshot_ws_bytes(4, R, n); }
+
+QR_EXPORT qr_status_t qr_fp4_allreduce_twoshot(qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                               void *const *y, void *workspace, size_t workspace_bytes,
+                                               qr_stream_t stream) {
+    if (!x || !y || !workspace || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
+    for (int r = 0; r < R && r < QR_MAX_RANKS; ++r)
+        if (!x[r] || !y[r]) return QR_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
+    const size_t need = twoshot_ws_bytes(4, R, n);
+    if (!value_bytes_ok(n) || need == 0 || wire_bytes(4, n) == 0) return QR_ERR_SIZE;
+    if (workspace_bytes < need) return QR_ERR_SIZE;
+    const size_t V = 2 * n;
+    if (!aligned16(workspace)) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r)
+        if (!aligned16(x[r]) || !aligned16(y[r])) return QR_ERR_MISALIGNED;
+    for (int r = 0; r < R; ++r) {
+        if (overlaps(workspace, need, x[r], V) || overlaps(workspace, need, y[r], V)) return QR_ERR_INVALID_ARG;
+        for (int i = 0; i < R; ++i) {
+            // every input is read in Phase-1, before any output is written: an
+            // output may be an input exactly (in place), never partly
+            if (bad_alias(y[r], V, x[i], V)) return QR_ERR_INVALID_ARG;
+            if (i < r && overlaps(y[r], V, y[i], V)) return QR_ERR_INVALID_ARG;
+        }
+    }
+    return from_cuda(qrk::launch_fp4_twoshot(dtype, R, x, static_cast<long long>(n), y, workspace,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QR_EXPORT size_t qr_fc_twoshot_workspace_bytes(int bits_rs, int bits_ag, int R, size_t n) {
     return fc_twoshot_ws_bytes(bits_rs, bits_ag, R, n);
 }

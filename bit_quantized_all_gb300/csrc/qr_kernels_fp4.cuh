@@ -79,32 +79,36 @@ __device__ __forceinline__ void fp4_quantize(const float2 *v, const Fp4Scale &sc
 // ---------------------------------------------------------------------------
 // send path: one 32-value block per thread
 // ---------------------------------------------------------------------------
+// Block gb of x quantized into block gb & 63 of `tile`.
+template <int DT>
+__device__ __forceinline__ void fp4_encode_block(const uint16_t *__restrict__ x, long long n, long long gb,
+                                                 uint8_t *tile) {
+    uint32_t raw[16];
+    load_block_values(x, gb * 32, n, raw);
+    float2 v[16];
+    widen_block<DT>(raw, v);
+    const Fp4Scale sc = fp4_scale(block_absmax(v));
+    BlockWords<4> c;
+    fp4_quantize<4>(v, sc, c.w);
+    store_block_codes<4>(tile, static_cast<int>(gb & 63), c);
+    store_block_scale<4>(tile, static_cast<int>(gb & 63), sc.bits);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads32) fp4_encode_kernel(const uint16_t *__restrict__ x, long long n,
                                                                 uint8_t *__restrict__ wire, long long NB) {
     chain_entry();
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
-    for (long long gb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb < NB; gb += S) {
-        uint32_t raw[16];
-        load_block_values(x, gb * 32, n, raw);
-        float2 v[16];
-        widen_block<DT>(raw, v);
-        const Fp4Scale sc = fp4_scale(block_absmax(v));
-        BlockWords<4> c;
-        fp4_quantize<4>(v, sc, c.w);
-        uint8_t *tile = wire + (gb >> 6) * Codec<4>::kTileBytes;
-        store_block_codes<4>(tile, static_cast<int>(gb & 63), c);
-        store_block_scale<4>(tile, static_cast<int>(gb & 63), sc.bits);
-    }
+    for (long long gb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; gb < NB; gb += S)
+        fp4_encode_block<DT>(x, n, gb, wire + (gb >> 6) * Codec<4>::kTileBytes);
 }
 
 // ---------------------------------------------------------------------------
 // receive path: two threads per block, 16 values and 32 output bytes each
 // ---------------------------------------------------------------------------
 template <int DT, bool Y32>  // Y32: y is 32-byte aligned (one 256-bit store per thread)
-__global__ void __launch_bounds__(kThreads32) fp4_decode_kernel(const uint8_t *__restrict__ wire, long long n,
-                                                                uint16_t *__restrict__ y, long long NH) {
-    chain_entry();
+__device__ __forceinline__ void fp4_decode_run(const uint8_t *__restrict__ wire, long long n, uint16_t *__restrict__ y,
+                                               long long NH) {
     const long long S = static_cast<long long>(gridDim.x) * kThreads32;
     for (long long hb = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb < NH; hb += S) {
         const long long gb = hb >> 1;
@@ -141,6 +145,13 @@ __global__ void __launch_bounds__(kThreads32) fp4_decode_kernel(const uint8_t *_
             }
         }
     }
+}
+
+template <int DT, bool Y32>
+__global__ void __launch_bounds__(kThreads32) fp4_decode_kernel(const uint8_t *__restrict__ wire, long long n,
+                                                                uint16_t *__restrict__ y, long long NH) {
+    chain_entry();
+    fp4_decode_run<DT, Y32>(wire, n, y, NH);
 }
 
 // ---------------------------------------------------------------------------

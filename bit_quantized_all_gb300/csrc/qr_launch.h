@@ -120,6 +120,10 @@ cudaError_t launch_fc_reduce(int bits_in, int bits_out, int R, const void *const
                              cudaStream_t s);
 cudaError_t launch_fc_reduce_staged(int bits_in, int bits_out, int R, const void *const *wires, long long n, void *out,
                                     int ctas, cudaStream_t s);
+// The FP4 codec's two-shot exchange (qr_fp4_twoshot.cu): the workspace of
+// qr_twoshot_workspace_bytes(4, R, n).
+cudaError_t launch_fp4_twoshot(int dtype, int R, const void *const *x, long long n, void *const *y, void *ws,
+                               cudaStream_t s);
 // The asymmetric codec's two-shot exchange (qr_fc_twoshot.cu): the workspace
 // holds R*R*seg reduce-scatter tiles, then T all-gather tiles.
 cudaError_t launch_fc_twoshot(int bits_rs, int bits_ag, int dtype, int R, const void *const *x, long long n,

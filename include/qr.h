@@ -535,6 +535,19 @@ qr_status_t qr_fp4_decode(qr_dtype_t dtype, const void *wire, size_t n, void *y,
 qr_status_t qr_fp4_segment_reduce(int R, const void *const *wires, size_t n,
                                   void *out_wire, int ctas, qr_stream_t stream);
 
+/* The FP4 codec's two-shot exchange laid out per rank and per owner, as
+ * qr_allreduce_twoshot for the integer codes: the workspace of
+ * qr_fp4_twoshot_workspace_bytes(R, n) (= qr_twoshot_workspace_bytes(4, R, n):
+ * owner k's copy of sender j's segment at tile (k*R + j)*seg, then the
+ * gathered wire, byte-identical to qr_fp4_segment_reduce's output, at tile
+ * R*R*seg); three launches, one per phase, with one grid row per rank or
+ * owner; every y[j] receives qr_fp4_allreduce's output.  Aliasing rules and
+ * errors as qr_allreduce_twoshot. */
+size_t qr_fp4_twoshot_workspace_bytes(int R, size_t n);      /* 0 if unsupported */
+qr_status_t qr_fp4_allreduce_twoshot(qr_dtype_t dtype, int R, const void *const *x, size_t n,
+                                     void *const *y, void *workspace, size_t workspace_bytes,
+                                     qr_stream_t stream);
+
 /* The fused FP4 all-reduce D(E(sum_r D(E(x_r)))) on the staged kernel;
  * every x[r] and y 32-byte aligned (QR_ERR_MISALIGNED otherwise); `ctas` as
  * above; y may equal one of the x[r] exactly (in place). */

@@ -263,6 +263,34 @@ def test_fc_twoshot_workspace_bytes():
     assert qr.qr_fc_twoshot_workspace_bytes(8, 8, 8, 2**64 - 1) == 0
 
 
+def test_fp4_twoshot_workspace_bytes():
+    for R in (1, 2, 3, 8):
+        for n in (1, 2048, 2049, 2048 * 17 + 5, 2**27):
+            assert qr.qr_fp4_twoshot_workspace_bytes(R, n) == qr.qr_twoshot_workspace_bytes(4, R, n)
+    assert qr.qr_fp4_twoshot_workspace_bytes(0, 100) == 0
+    assert qr.qr_fp4_twoshot_workspace_bytes(9, 100) == 0
+
+
+@no_gpu_only
+def test_fp4_twoshot_validation():
+    n = 2048 * 5 + 3
+    need = qr.qr_fp4_twoshot_workspace_bytes(2, n)
+    WS = 0x7F3000000000
+    xs, ys = [A, B], [Y, Y + 2**24]
+    call = capi.qr_fp4_allreduce_twoshot
+    assert call(0, 2, xs, n, ys, None, need) == qr.QR_ERR_INVALID_ARG
+    assert call(0, 2, xs, n, [Y, None], WS, need) == qr.QR_ERR_INVALID_ARG
+    assert call(0, 2, xs, 0, ys, WS, need) == qr.QR_ERR_INVALID_ARG
+    assert call(2, 2, xs, n, ys, WS, need) == qr.QR_ERR_UNSUPPORTED              # dtype
+    assert call(0, 9, [A + 4096 * i for i in range(9)], n, [Y + 2**22 * i for i in range(9)], WS,
+                need) == qr.QR_ERR_UNSUPPORTED
+    assert call(0, 2, xs, n, ys, WS, need - 1) == qr.QR_ERR_SIZE
+    assert call(0, 2, xs, n, ys, WS + 8, need) == qr.QR_ERR_MISALIGNED
+    assert call(0, 2, xs, n, [Y, Y + 4096], WS, need) == qr.QR_ERR_INVALID_ARG      # outputs overlap
+    assert call(0, 2, xs, n, [A + 16, Y], WS, need) == qr.QR_ERR_INVALID_ARG         # partial in-place
+    assert call(0, 2, xs, n, ys, A, need) == qr.QR_ERR_INVALID_ARG                 # workspace over an input
+
+
 @no_gpu_only
 def test_fc_twoshot_validation():
     n = 2048 * 5 + 3

@@ -41,6 +41,59 @@ def _check_all(xs, dt, what):
     assert qr.qr_wait_timeouts() == 0
 
 
+def _rand(R, n, dt, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for r in range(R):
+        v = (rng.standard_normal(n) * (1 + r)).astype(np.float32)
+        v[rng.integers(0, n, size=max(1, n // 300))] *= 40.0
+        out.append(oracle.narrow(dt, v))
+    return out
+
+
+@pytest.mark.parametrize("n", [2048 * 40 + 37, 2048 * 3 + 1, 700])
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+def test_twoshot(n, R):
+    """The two-shot exchange laid out per rank and per owner: every rank's
+    output equals the fused all-reduce and the oracle's, the owners' receive
+    buffers hold the oracle's wire segments, the gathered wire is the
+    oracle's Phase-1B output; fewer tiles than ranks at the small sizes."""
+    T = -(-n // 2048)
+    seg = -(-T // R)
+    tb = qr.qr_fp4_tile_bytes()
+    for dt in (0, 1):
+        xs = _rand(R, n, dt, 600 + 11 * R + dt)
+        xs_dev = [to_dev(x, dt) for x in xs]
+        ys, ws = qr.qr_fp4_allreduce_twoshot(xs_dev)
+        yf = qr.qr_fp4_allreduce(xs_dev)
+        torch.cuda.synchronize()
+        y_ref = oracle.fp4_allreduce(dt, xs)
+        for j in range(R):
+            assert np.array_equal(to_host_u16(ys[j]), y_ref), (R, n, dt, j)
+            assert torch.equal(ys[j].view(torch.int16), yf.view(torch.int16))
+        host = to_host_u8(ws)
+        w_ref = [oracle.fp4_encode(dt, x) for x in xs]
+        for k in range(R):
+            t0, t1 = k * seg, min(T, (k + 1) * seg)
+            for j in range(R):
+                got = host[((k * R + j) * seg) * tb:((k * R + j) * seg + max(0, t1 - t0)) * tb]
+                assert np.array_equal(got, w_ref[j][t0 * tb:max(t0, t1) * tb]), (R, n, dt, k, j)
+        g = R * R * seg * tb
+        assert np.array_equal(host[g:g + T * tb], oracle.fp4_segment_reduce(w_ref, n)), (R, n, dt)
+    assert qr.qr_wait_timeouts() == 0
+
+
+def test_twoshot_in_place():
+    n = 2048 * 33 + 5
+    xs = _rand(4, n, 1, 5)
+    y_ref = oracle.fp4_allreduce(1, xs)
+    xs_dev = [to_dev(x, 1) for x in xs]
+    qr.qr_fp4_allreduce_twoshot(xs_dev, ys=xs_dev)
+    torch.cuda.synchronize()
+    for j in range(4):
+        assert np.array_equal(to_host_u16(xs_dev[j]), y_ref)
+
+
 def test_c1_crafted_blocks():
     _check_all(workloads.ranks(workloads.C1), 0, "c1")
 
