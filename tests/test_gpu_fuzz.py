@@ -91,6 +91,9 @@ def test_asymmetric_codec_every_path(seed):
     assert np.array_equal(to_host_u8(red_st), red_ref), what + " reduced wire (staged)"
     y_u = qr.qr_fc_decode(bag, red, n, dtype=xs_dev[0].dtype)
     assert_outputs_match(to_host_u16(y_u), y_ref, dt, xmax, what + " unfused")
+    ys, _ = qr.qr_fc_allreduce_twoshot(brs, bag, xs_dev)
+    for j, y in enumerate(ys):
+        assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} two-shot rank {j}")
     assert qr.qr_wait_timeouts() == 0
 
 
@@ -157,4 +160,7 @@ def test_fp4_codec_every_path(seed):
     assert np.array_equal(to_host_u8(red), oracle.fp4_segment_reduce(w_ref, n)), what + " reduced wire"
     y_u = qr.qr_fp4_decode(red, n, dtype=xs_dev[0].dtype)
     assert_outputs_match(to_host_u16(y_u), y_ref, dt, xmax, what + " unfused")
+    ys, _ = qr.qr_fp4_allreduce_twoshot(xs_dev)
+    for j, y in enumerate(ys):
+        assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} two-shot rank {j}")
     assert qr.qr_wait_timeouts() == 0
