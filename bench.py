@@ -590,6 +590,8 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
     (the mixed "INT6") and (8,8), fused and unfused arms interleaved."""
     import torch
 
+    from bit_quantized_all_gb300.peer import CudaPeerOps, twoshot_peer_local
+
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for dtype in dtypes:
         tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
@@ -610,14 +612,24 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                                 "reduce_staged": Rs * Wi + Wo, "decode": Wo + 2 * n,
                                 # R sends (2N in, Wi out), the owners' R*Wi in and Wo
                                 # out, R decodes (Wo in, 2N out)
-                                "twoshot": 4 * Rs * n + 2 * Rs * Wi + (Rs + 1) * Wo}
+                                "twoshot": 4 * Rs * n + 2 * Rs * Wi + (Rs + 1) * Wo,
+                                # the per-rank calls: R sends, R owners reading R*Wi
+                                # and storing their segment into R workspaces, R decodes
+                                "twoshot_peer": 4 * Rs * n + 2 * Rs * Wi + 2 * Rs * Wo}
                     do_flush = fused_b < (512 << 20)
                     wst = torch.empty(qr.qr_fc_twoshot_workspace_bytes(brs, bag, Rs, n), dtype=torch.uint8,
                                       device=dev)
                     yst = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
+                    codec = ("fc", brs, bag)
+                    wsp = [torch.empty(CudaPeerOps(dev).workspace_bytes(codec, Rs, n), dtype=torch.uint8, device=dev)
+                           for _ in range(Rs)]
+                    ysp = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
 
                     def twoshot():
                         qr.qr_fc_allreduce_twoshot(brs, bag, xs, ys=yst, workspace=wst)
+
+                    def twoshot_peer():
+                        twoshot_peer_local(codec, xs, ys=ysp, workspaces=wsp)
 
                     def fused():
                         qr.qr_fc_allreduce(brs, bag, xs, y=y)
@@ -645,12 +657,12 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
 
                     arms = (("fused", fused), ("fused_regs", fused_regs), ("unfused", unfused),
                             ("encode", encode_all), ("reduce", reduce_only), ("reduce_staged", reduce_staged),
-                            ("decode", decode_only), ("twoshot", twoshot))
+                            ("decode", decode_only), ("twoshot", twoshot), ("twoshot_peer", twoshot_peer))
                     times = time_arms(arms, args, flush if do_flush else None,
-                                      warm=(fused, fused_regs, unfused, reduce_staged, twoshot))
+                                      warm=(fused, fused_regs, unfused, reduce_staged, twoshot, twoshot_peer))
                     same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and bool(
                         torch.equal(y.view(torch.int16), y2.view(torch.int16))) and bool(torch.equal(red, red2)) and all(
-                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in yst)
+                        torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in yst + ysp)
                     for name, alg in kernel_b.items():
                         med = statistics.median(times[name])
                         print(json.dumps({
@@ -661,7 +673,7 @@ def run_sweep_fc(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                             "frac": round(alg / (med / 1e3) / 1e9 / peak, 4),
                             "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None, "fused_equals_unfused": same, "reps": args.reps,
                             "burst": 1 if do_flush else args.burst}), flush=True)
-                    del wires, red, red2, wst, yst
+                    del wires, red, red2, wst, yst, wsp, ysp
                 del xs, y, yu, y2
                 torch.cuda.empty_cache()
 
@@ -670,6 +682,8 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
     """The sweep for the FP4 codec (the INT4 tile with E2M1 elements): the
     fused kernel and the three unfused steps, interleaved."""
     import torch
+
+    from bit_quantized_all_gb300.peer import CudaPeerOps, twoshot_peer_local
 
     for dtype in dtypes:
         tdt = torch.float16 if dtype == workloads.FP16 else torch.bfloat16
@@ -684,9 +698,12 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                 fused_b = 2 * Rs * n + 2 * n
                 kernel_b = {"fused": fused_b, "unfused": fused_b + 2 * Rs * W + 2 * W,
                             "encode": Rs * (2 * n + W), "reduce": (Rs + 1) * W, "decode": W + 2 * n,
-                            "twoshot": 4 * Rs * n + (3 * Rs + 1) * W}
+                            "twoshot": 4 * Rs * n + (3 * Rs + 1) * W, "twoshot_peer": 4 * Rs * n + 4 * Rs * W}
                 wst = torch.empty(qr.qr_fp4_twoshot_workspace_bytes(Rs, n), dtype=torch.uint8, device=dev)
                 yst = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
+                wsp = [torch.empty(CudaPeerOps(dev).workspace_bytes("fp4", Rs, n), dtype=torch.uint8, device=dev)
+                       for _ in range(Rs)]
+                ysp = [torch.empty(n, dtype=tdt, device=dev) for _ in range(Rs)]
                 do_flush = fused_b < (512 << 20)
 
                 def fused():
@@ -710,11 +727,14 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                 def twoshot():
                     qr.qr_fp4_allreduce_twoshot(xs, ys=yst, workspace=wst)
 
+                def twoshot_peer():
+                    twoshot_peer_local("fp4", xs, ys=ysp, workspaces=wsp)
+
                 arms = (("fused", fused), ("unfused", unfused), ("encode", encode_all), ("reduce", reduce_only),
-                        ("decode", decode_only), ("twoshot", twoshot))
-                times = time_arms(arms, args, flush if do_flush else None, warm=(fused, unfused, twoshot))
+                        ("decode", decode_only), ("twoshot", twoshot), ("twoshot_peer", twoshot_peer))
+                times = time_arms(arms, args, flush if do_flush else None, warm=(fused, unfused, twoshot, twoshot_peer))
                 same = bool(torch.equal(y.view(torch.int16), yu.view(torch.int16))) and all(
-                    torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in yst)
+                    torch.equal(y.view(torch.int16), v.view(torch.int16)) for v in yst + ysp)
                 for name, alg in kernel_b.items():
                     med = statistics.median(times[name])
                     print(json.dumps({
@@ -726,7 +746,7 @@ def run_sweep_fp4(args, qr, dev, peak, flush, sizes, dtypes, ranks) -> None:
                         "l2_flushed": do_flush, "l2_flush": "write then read 256 MiB" if do_flush else None,
                         "fused_equals_unfused": same, "reps": args.reps,
                         "burst": 1 if do_flush else args.burst}), flush=True)
-                del wires, red, wst, yst
+                del wires, red, wst, yst, wsp, ysp
                 del xs, y, yu
                 torch.cuda.empty_cache()
 

@@ -46,7 +46,10 @@ EXPORTS = ("qr_tile_values", "qr_tile_bytes", "qr_wire_bytes", "qr_encode", "qr_
            "qr_twoshot_peer_workspace_bytes", "qr_twoshot_peer_send", "qr_twoshot_peer_reduce",
            "qr_twoshot_peer_decode", "qr_ipc_handle_bytes", "qr_ipc_get_handle", "qr_ipc_open_handle",
            "qr_ipc_close_handle", "qr_fc_twoshot_workspace_bytes", "qr_fc_allreduce_twoshot",
-           "qr_fp4_twoshot_workspace_bytes", "qr_fp4_allreduce_twoshot")
+           "qr_fp4_twoshot_workspace_bytes", "qr_fp4_allreduce_twoshot", "qr_fc_twoshot_peer_workspace_bytes",
+           "qr_fc_twoshot_peer_send", "qr_fc_twoshot_peer_reduce", "qr_fc_twoshot_peer_decode",
+           "qr_fp4_twoshot_peer_workspace_bytes", "qr_fp4_twoshot_peer_send", "qr_fp4_twoshot_peer_reduce",
+           "qr_fp4_twoshot_peer_decode")
 TWOSHOT_STATIC_WORKSPACE_BYTES = 32 << 20  # QR_TWOSHOT_STATIC_WORKSPACE_BYTES
 FC_BITS = (4, 8)
 FC_PAIRS = ((4, 4), (4, 8), (8, 8))  # (reduce-scatter, all-gather) widths; (4, 8) is the mixed "INT6"

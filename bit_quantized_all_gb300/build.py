@@ -22,7 +22,7 @@ SOURCES = ["qr_capi.cu", "qr_grid.cu", "qr_encode.cu", "qr_decode.cu", "qr_reduc
            "qr_allreduce16_b3.cu", "qr_allreduce16_b4.cu", "qr_allreduce16_b6.cu", "qr_allreduce16_b8.cu",
            "qr_fc.cu", "qr_fc_allreduce_44.cu", "qr_fc_allreduce_48.cu", "qr_fc_allreduce_88.cu",
            "qr_twoshot.cu", "qr_twoshot_static.cu", "qr_twoshot_flags.cu", "qr_twoshot_peer.cu", "qr_timeouts.cu", "qr_fp4.cu",
-           "qr_fc_twoshot.cu", "qr_fp4_twoshot.cu"]
+           "qr_fc_twoshot.cu", "qr_fp4_twoshot.cu", "qr_codec_peer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17",

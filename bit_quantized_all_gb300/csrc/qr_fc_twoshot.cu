@@ -33,19 +33,10 @@ __global__ void __launch_bounds__(kThreadsFc) fc_twoshot_send_kernel(ConstPtrs x
     const int j = static_cast<int>(blockIdx.y);
     const long long R = gridDim.y;
     const uint16_t *xj = static_cast<const uint16_t *>(row_pointer(x.p, j));
-    const int i = threadIdx.x;
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const long long k = t / seg;
-        uint8_t *dst = ws + ((k * R + j) * seg + (t - k * seg)) * FcCodec<BRS>::kTileBytes;
-        uint32_t raw[8];
-        load16v<A32>(xj, t * kTileValues + 16 * i, n, raw);
-        float2 v[8], f[8];
-        widen16<DT>(raw, v);
-        float lo, hi;
-        group_minmax(v, lo, hi);
-        const FcParams p = fc_params<BRS>(lo, hi);
-        fc_quantize16<BRS>(v, p, f);
-        fc_store16<BRS>(dst, i, f, p);
+        fc_encode_tile16<BRS, DT, A32>(xj, n, t, threadIdx.x,
+                                       ws + ((k * R + j) * seg + (t - k * seg)) * FcCodec<BRS>::kTileBytes);
     }
 }
 

@@ -100,16 +100,22 @@ __device__ __forceinline__ void fc_unpack16(const HalfWords<B> &c, float2 (&u)[8
     }
 }
 
+// Thread i's packed codes and its group's (scale, zero point) into `tile`.
 template <int B>
-__device__ __forceinline__ void fc_store16(uint8_t *tile, int i, const float2 (&f)[8], const FcParams &p) {
-    HalfWords<B> c;
-    pack_half<B>(f, c);
+__device__ __forceinline__ void fc_store_packed16(uint8_t *tile, int i, const HalfWords<B> &c, const FcParams &p) {
     store_half_codes<B>(tile, i >> 1, i & 1, c);
     if ((i & 7) == 0) {
         const int g = i >> 3;
         *reinterpret_cast<float *>(tile + FcCodec<B>::kMeta + 4 * g) = p.s;
         *reinterpret_cast<float *>(tile + FcCodec<B>::kMeta + 64 + 4 * g) = p.z;
     }
+}
+
+template <int B>
+__device__ __forceinline__ void fc_store16(uint8_t *tile, int i, const float2 (&f)[8], const FcParams &p) {
+    HalfWords<B> c;
+    pack_half<B>(f, c);
+    fc_store_packed16<B>(tile, i, c, p);
 }
 
 template <int B>
@@ -269,24 +275,30 @@ struct FcTile {
     }
 };
 
+// Thread i's 16 values of tile t (values past n read as +0) quantized at B
+// bits into `tile`: group min / max over 8 lanes, parameters, codes.
+// Called by whole warps.
+template <int B, int DT, bool A32>
+__device__ __forceinline__ void fc_encode_tile16(const uint16_t *__restrict__ x, long long n, long long t, int i,
+                                                 uint8_t *tile) {
+    uint32_t raw[8];
+    load16v<A32>(x, t * kTileValues + 16 * i, n, raw);
+    float2 v[8], f[8];
+    widen16<DT>(raw, v);
+    float lo, hi;
+    group_minmax(v, lo, hi);
+    const FcParams p = fc_params<B>(lo, hi);
+    fc_quantize16<B>(v, p, f);
+    fc_store16<B>(tile, i, f, p);
+}
+
 // Send path: quantize into a BITS-wide Flash Communication wire.
 template <int B, int DT, bool A32>
 __global__ void __launch_bounds__(kThreadsFc) fc_encode_kernel(const uint16_t *__restrict__ x, long long n,
                                                                uint8_t *__restrict__ wire, long long T) {
     chain_entry();
-    const int i = threadIdx.x;
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        const long long base = t * kTileValues + 16 * i;
-        uint32_t raw[8];
-        load16v<A32>(x, base, n, raw);
-        float2 v[8], f[8];
-        widen16<DT>(raw, v);
-        float lo, hi;
-        group_minmax(v, lo, hi);
-        const FcParams p = fc_params<B>(lo, hi);
-        fc_quantize16<B>(v, p, f);
-        fc_store16<B>(wire + t * FcCodec<B>::kTileBytes, i, f, p);
-    }
+    for (long long t = blockIdx.x; t < T; t += gridDim.x)
+        fc_encode_tile16<B, DT, A32>(x, n, t, threadIdx.x, wire + t * FcCodec<B>::kTileBytes);
 }
 
 // Receive path / Phase-2: decode the first n values.
@@ -312,11 +324,13 @@ __global__ void __launch_bounds__(kThreadsFc) fc_decode_kernel(const uint8_t *__
 // re-quantize into a BOUT-wide wire.
 // Phase-1B of one tile for thread i (values base..base+15): decode the R
 // ranks' codes c[r] with their group scale s[r] and zero point z[r], add in
-// rank order, reset values past n, re-quantize at BOUT bits into tile_out.
-// Called by whole warps (the group min / max spans 8 lanes).
+// rank order, reset values past n, re-quantize at BOUT bits: the magic
+// floats of the codes in f, the group's parameters in p.  Called by whole
+// warps (the group min / max spans 8 lanes).
 template <int BIN, int BOUT, int R>
-__device__ __forceinline__ void fc_reduce_tile(const HalfWords<BIN> (&c)[R], const float (&s)[R], const float (&z)[R],
-                                               uint8_t *tile_out, int i, long long base, long long n) {
+__device__ __forceinline__ void fc_reduce_values(const HalfWords<BIN> (&c)[R], const float (&s)[R],
+                                                 const float (&z)[R], long long base, long long n, float2 (&f)[8],
+                                                 FcParams &p) {
     float2 acc[8];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -332,9 +346,17 @@ __device__ __forceinline__ void fc_reduce_tile(const HalfWords<BIN> (&c)[R], con
     if (base + 16 > n) zero_past_n(acc, base, n);
     float lo, hi;
     group_minmax(acc, lo, hi);
-    const FcParams p = fc_params<BOUT>(lo, hi);
-    float2 f[8];
+    p = fc_params<BOUT>(lo, hi);
     fc_quantize16<BOUT>(acc, p, f);
+}
+
+// fc_reduce_values, stored into tile_out.
+template <int BIN, int BOUT, int R>
+__device__ __forceinline__ void fc_reduce_tile(const HalfWords<BIN> (&c)[R], const float (&s)[R], const float (&z)[R],
+                                               uint8_t *tile_out, int i, long long base, long long n) {
+    float2 f[8];
+    FcParams p;
+    fc_reduce_values<BIN, BOUT, R>(c, s, z, base, n, f, p);
     fc_store16<BOUT>(tile_out, i, f, p);
 }
 

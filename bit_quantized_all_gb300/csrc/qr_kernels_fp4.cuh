@@ -162,9 +162,10 @@ __global__ void __launch_bounds__(kThreads32) fp4_decode_kernel(const uint8_t *_
 // same as fp32 fmas of the widened operands; acc starts at -0, so the first
 // fma returns the first rank's product exactly, signed zeros included (they
 // decide E2M1 codes 0 and 8 on re-quantization).
+// The re-quantized codes go to cw, the fp16 scale bits to scale_bits.
 template <int R>
-__device__ __forceinline__ void fp4_reduce_block(const BlockWords<4> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
-                                                 int g) {
+__device__ __forceinline__ void fp4_reduce_block_words(const BlockWords<4> (&c)[R], const uint32_t (&sb)[R],
+                                                       BlockWords<4> &cw, uint32_t &scale_bits) {
     float2 acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = make_float2(-0.0f, -0.0f);
@@ -180,10 +181,19 @@ __device__ __forceinline__ void fp4_reduce_block(const BlockWords<4> (&c)[R], co
         }
     }
     const Fp4Scale sc = fp4_scale(block_absmax(acc));
-    BlockWords<4> cw;
     fp4_quantize<4>(acc, sc, cw.w);
+    scale_bits = sc.bits;
+}
+
+// fp4_reduce_block_words, written into `tile` as its block g.
+template <int R>
+__device__ __forceinline__ void fp4_reduce_block(const BlockWords<4> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
+                                                 int g) {
+    BlockWords<4> cw;
+    uint32_t bits;
+    fp4_reduce_block_words<R>(c, sb, cw, bits);
     store_block_codes<4>(tile, g, cw);
-    store_block_scale<4>(tile, g, sc.bits);
+    store_block_scale<4>(tile, g, bits);
 }
 
 struct Fp4Reduce {

@@ -6,11 +6,8 @@
 // machinery (all-to-all, local sum and re-quantization, all-gather over
 // peer-to-peer GPU memory access).
 //
-// Rank j's workspace (seg = ceil(T/R) tiles of the T-tile wire):
-//   recv[s]   at tile s*seg (s = 0..R-1): sender s's quantized copy of the
-//             segment this rank owns (segment j: tiles [j*seg, (j+1)*seg));
-//   gathered  at tile R*seg: the reduced wire in tile order (tile t at
-//             R*seg + t), written by the owners.
+// Rank j's workspace is laid out as qr_peer.cuh states (recv[s] at tile
+// s*seg, the gathered wire at tile R*seg).
 // A step is three calls per rank, in order, each one launch on the rank's
 // stream: send (rank j quantizes its message and stores segment k of it into
 // recv[j] of rank k's workspace), reduce (owner j sums the R copies of its
@@ -33,25 +30,13 @@
 #include "../../include/qr.h"
 #include "qr_kernels32.cuh"
 #include "qr_launch.h"
+#include "qr_peer.cuh"
 
 #define QR_EXPORT extern "C" __attribute__((visibility("default")))
 
 namespace qrk {
 
 namespace {
-
-// Where the send path stores tile t of sender `sender`: recv[sender] of the
-// owner k = t / seg, at the tile's place in the owner's segment.
-struct PeerOwnerTiles {
-    MutPtrs ws;  // rank k's workspace at ws.p[k]
-    long long seg;
-    int sender, tile_bytes;
-    __device__ __forceinline__ uint8_t *operator()(long long t) const {
-        const int k = static_cast<int>(static_cast<unsigned long long>(t) / static_cast<unsigned long long>(seg));
-        uint8_t *base = static_cast<uint8_t *>(row_pointer(ws.p, k));
-        return base + (static_cast<long long>(sender) * seg + (t - k * seg)) * tile_bytes;
-    }
-};
 
 template <int B, int DT, int U>
 __global__ void __launch_bounds__(kThreads32) peer_send_kernel(const uint16_t *__restrict__ x, long long n,
@@ -115,7 +100,7 @@ cudaError_t run_peer_send(int R, int rank, const void *x, long long n, const Mut
     auto kern = peer_send_kernel<B, DT, kPeerSendUnroll>;
     cudaError_t err = cudaSuccess;
     const long long units = (NB + kThreads32 * kPeerSendUnroll - 1) / (kThreads32 * kPeerSendUnroll);
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
+    const int grid = peer_grid(reinterpret_cast<const void *>(kern), kThreads32, units, &err);
     if (grid <= 0) return err;
     PeerOwnerTiles dst{ws, twoshot_segment_tiles(T, R), rank, Codec<B>::kTileBytes};
     return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint16_t *>(x), n, dst, NB);
@@ -133,7 +118,7 @@ cudaError_t run_peer_reduce_r(int rank, long long n, const MutPtrs &ws, cudaStre
     auto kern = peer_reduce_kernel<B, R, U>;
     cudaError_t err = cudaSuccess;
     const long long units = (NB + kThreads32 * U - 1) / (kThreads32 * U);
-    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
+    const int grid = peer_grid(reinterpret_cast<const void *>(kern), kThreads32, units, &err);
     if (grid <= 0) return err;
     return launch_chained(kern, grid, kThreads32, 0, s, static_cast<const uint8_t *>(ws.p[rank]), ws, seg, t0, NB);
 }
@@ -173,33 +158,18 @@ MemGetAddressRangeFn address_range_fn() {
 std::mutex g_ipc_mu;
 std::multimap<uintptr_t, void *> g_ipc_open;
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + nb && y < x + na;
-}
-
-qr_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_CUDA; }
-
 // The checks shared by the send and reduce calls.
 qr_status_t check_peers(int bits, int R, int rank, size_t n, void *const *ws) {
     if (!ws || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
     if (qr_tile_bytes(bits) == 0 || R > QR_MAX_RANKS) return QR_ERR_UNSUPPORTED;
-    if (rank < 0 || rank >= R) return QR_ERR_INVALID_ARG;
-    for (int r = 0; r < R; ++r)
-        if (!ws[r]) return QR_ERR_INVALID_ARG;
-    if (n > SIZE_MAX / 4 || qr_twoshot_peer_workspace_bytes(bits, R, n) == 0) return QR_ERR_SIZE;
-    for (int r = 0; r < R; ++r)
-        if (!aligned16(ws[r])) return QR_ERR_MISALIGNED;
-    const size_t need = qr_twoshot_peer_workspace_bytes(bits, R, n);
-    for (int r = 0; r < R; ++r)
-        for (int i = 0; i < r; ++i)
-            if (overlaps(ws[r], need, ws[i], need)) return QR_ERR_INVALID_ARG;
-    return QR_OK;
+    return check_peer_set(R, rank, n, ws, n > SIZE_MAX / 4 ? 0 : qr_twoshot_peer_workspace_bytes(bits, R, n));
 }
 
 }  // namespace
+
+int peer_grid(const void *kern, int threads, long long units, cudaError_t *err) {
+    return grid_for(kern, threads, units, 0, 4, err);
+}
 
 }  // namespace qrk
 
@@ -219,10 +189,10 @@ QR_EXPORT qr_status_t qr_twoshot_peer_send(int bits, qr_dtype_t dtype, int R, in
     qr_status_t st = qrk::check_peers(bits, R, rank, n, workspaces);
     if (st != QR_OK) return st;
     if (dtype != QR_FP16 && dtype != QR_BF16) return QR_ERR_UNSUPPORTED;
-    if (!qrk::aligned16(x)) return QR_ERR_MISALIGNED;
+    if (!qrk::peer_aligned16(x)) return QR_ERR_MISALIGNED;
     const size_t need = qr_twoshot_peer_workspace_bytes(bits, R, n);
     for (int r = 0; r < R; ++r)
-        if (qrk::overlaps(x, 2 * n, workspaces[r], need)) return QR_ERR_INVALID_ARG;
+        if (qrk::peer_overlaps(x, 2 * n, workspaces[r], need)) return QR_ERR_INVALID_ARG;
     qrk::MutPtrs ws{};
     for (int r = 0; r < R; ++r) ws.p[r] = workspaces[r];
     const long long nn = static_cast<long long>(n);
@@ -240,7 +210,7 @@ QR_EXPORT qr_status_t qr_twoshot_peer_send(int bits, qr_dtype_t dtype, int R, in
         QR_CASE(8)
     }
 #undef QR_CASE
-    return qrk::from_cuda(e);
+    return qrk::peer_from_cuda(e);
 }
 
 QR_EXPORT qr_status_t qr_twoshot_peer_reduce(int bits, int R, int rank, size_t n, void *const *workspaces,
@@ -258,7 +228,7 @@ QR_EXPORT qr_status_t qr_twoshot_peer_reduce(int bits, int R, int rank, size_t n
         case 6: e = qrk::run_peer_reduce<6>(R, rank, nn, ws, s); break;
         case 8: e = qrk::run_peer_reduce<8>(R, rank, nn, ws, s); break;
     }
-    return qrk::from_cuda(e);
+    return qrk::peer_from_cuda(e);
 }
 
 QR_EXPORT qr_status_t qr_twoshot_peer_decode(int bits, qr_dtype_t dtype, int R, size_t n, const void *workspace,
@@ -266,16 +236,14 @@ QR_EXPORT qr_status_t qr_twoshot_peer_decode(int bits, qr_dtype_t dtype, int R, 
     if (!workspace || !y || n == 0 || R < 1) return QR_ERR_INVALID_ARG;
     if (qr_tile_bytes(bits) == 0 || R > QR_MAX_RANKS || (dtype != QR_FP16 && dtype != QR_BF16))
         return QR_ERR_UNSUPPORTED;
-    if (n > SIZE_MAX / 4) return QR_ERR_SIZE;
-    const size_t need = qr_twoshot_peer_workspace_bytes(bits, R, n);
-    if (need == 0) return QR_ERR_SIZE;
-    if (!qrk::aligned16(workspace) || !qrk::aligned16(y)) return QR_ERR_MISALIGNED;
-    if (qrk::overlaps(y, 2 * n, workspace, need)) return QR_ERR_INVALID_ARG;
+    const size_t need = n > SIZE_MAX / 4 ? 0 : qr_twoshot_peer_workspace_bytes(bits, R, n);
+    const qr_status_t st = qrk::check_peer_decode(n, workspace, y, need);
+    if (st != QR_OK) return st;
     const size_t T = n / QR_TILE_VALUES + (n % QR_TILE_VALUES != 0);
     const size_t seg = (T + R - 1) / R;
     const uint8_t *gathered = static_cast<const uint8_t *>(workspace) + static_cast<size_t>(R) * seg * qr_tile_bytes(bits);
-    return qrk::from_cuda(qrk::launch_decode(bits, static_cast<int>(dtype), gathered, static_cast<long long>(n), y,
-                                             reinterpret_cast<cudaStream_t>(stream)));
+    return qrk::peer_from_cuda(qrk::launch_decode(bits, static_cast<int>(dtype), gathered, static_cast<long long>(n),
+                                                  y, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 QR_EXPORT size_t qr_ipc_handle_bytes(void) { return QR_IPC_HANDLE_BYTES; }

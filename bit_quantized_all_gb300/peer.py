@@ -1,7 +1,12 @@
 """The two-shot all-reduce run by R separate processes, one per rank: the
-per-rank calls of ``libqr.so`` (``qr_twoshot_peer_send / _reduce / _decode``)
+per-rank calls of ``libqr.so`` (``qr_twoshot_peer_send / _reduce / _decode``,
+and their ``qr_fc_`` / ``qr_fp4_`` counterparts for the other two codecs)
 with the peers' workspaces mapped through CUDA IPC and the three phases
 joined by host barriers.
+
+The codec is named by ``bits``: 3, 4, 6 or 8 for the symmetric block codec,
+``("fc", bits_rs, bits_ag)`` for the asymmetric group-128 codec (width pairs
+(4, 4), (4, 8), (8, 8)), ``"fp4"`` for the FP4 codec.
 
 Each rank allocates one workspace in its own device memory, shares a handle
 to it with the other ranks (``torch.distributed.all_gather_object``) and maps
@@ -51,6 +56,14 @@ def _lib():
             "qr_twoshot_peer_send": (i32, [i32, i32, i32, i32, vp, sz, vpp, vp]),
             "qr_twoshot_peer_reduce": (i32, [i32, i32, i32, sz, vpp, vp]),
             "qr_twoshot_peer_decode": (i32, [i32, i32, i32, sz, vp, vp, vp]),
+            "qr_fc_twoshot_peer_workspace_bytes": (sz, [i32, i32, i32, sz]),
+            "qr_fc_twoshot_peer_send": (i32, [i32, i32, i32, i32, i32, vp, sz, vpp, vp]),
+            "qr_fc_twoshot_peer_reduce": (i32, [i32, i32, i32, i32, sz, vpp, vp]),
+            "qr_fc_twoshot_peer_decode": (i32, [i32, i32, i32, i32, sz, vp, vp, vp]),
+            "qr_fp4_twoshot_peer_workspace_bytes": (sz, [i32, sz]),
+            "qr_fp4_twoshot_peer_send": (i32, [i32, i32, i32, vp, sz, vpp, vp]),
+            "qr_fp4_twoshot_peer_reduce": (i32, [i32, i32, sz, vpp, vp]),
+            "qr_fp4_twoshot_peer_decode": (i32, [i32, i32, sz, vp, vp, vp]),
             "qr_ipc_handle_bytes": (sz, []),
             "qr_ipc_get_handle": (i32, [vp, vp]),
             "qr_ipc_open_handle": (i32, [vp, ctypes.POINTER(ctypes.c_void_p)]),
@@ -68,14 +81,31 @@ def _ptrs(ptrs):
     return (ctypes.c_void_p * len(ptrs))(*ptrs)
 
 
+def codec_of(bits):
+    """("qr", bits), ("fc", bits_rs, bits_ag) or ("fp4",) for a codec named
+    as this module's ``bits`` arguments name it."""
+    if isinstance(bits, str) and bits == "fp4":
+        return ("fp4",)
+    if isinstance(bits, tuple) and len(bits) == 3 and bits[0] == "fc":
+        return ("fc", int(bits[1]), int(bits[2]))
+    if isinstance(bits, int) and not isinstance(bits, bool):
+        return ("qr", bits)
+    raise ValueError(f"unknown two-shot codec {bits!r}: 3/4/6/8, ('fc', bits_rs, bits_ag) or 'fp4'")
+
+
 class CudaPeerOps:
     """The library's per-rank calls and CUDA IPC, on one device."""
 
     def __init__(self, device=None):
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
 
-    def workspace_bytes(self, bits: int, R: int, n: int) -> int:
-        return int(_lib().qr_twoshot_peer_workspace_bytes(bits, R, n))
+    def workspace_bytes(self, bits, R: int, n: int) -> int:
+        c, L = codec_of(bits), _lib()
+        if c[0] == "fc":
+            return int(L.qr_fc_twoshot_peer_workspace_bytes(c[1], c[2], R, n))
+        if c[0] == "fp4":
+            return int(L.qr_fp4_twoshot_peer_workspace_bytes(R, n))
+        return int(L.qr_twoshot_peer_workspace_bytes(c[1], R, n))
 
     def alloc(self, nbytes: int):
         buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
@@ -96,14 +126,33 @@ class CudaPeerOps:
         _check(_lib().qr_ipc_close_handle(ptr), "qr_ipc_close_handle")
 
     def send(self, bits, dtype, R, rank, x_ptr, n, peers, stream):
-        _check(_lib().qr_twoshot_peer_send(bits, dtype, R, rank, x_ptr, n, _ptrs(peers), stream),
-               "qr_twoshot_peer_send")
+        c, L, P = codec_of(bits), _lib(), _ptrs(peers)
+        if c[0] == "fc":
+            _check(L.qr_fc_twoshot_peer_send(c[1], c[2], dtype, R, rank, x_ptr, n, P, stream),
+                   "qr_fc_twoshot_peer_send")
+        elif c[0] == "fp4":
+            _check(L.qr_fp4_twoshot_peer_send(dtype, R, rank, x_ptr, n, P, stream), "qr_fp4_twoshot_peer_send")
+        else:
+            _check(L.qr_twoshot_peer_send(c[1], dtype, R, rank, x_ptr, n, P, stream), "qr_twoshot_peer_send")
 
     def reduce(self, bits, R, rank, n, peers, stream):
-        _check(_lib().qr_twoshot_peer_reduce(bits, R, rank, n, _ptrs(peers), stream), "qr_twoshot_peer_reduce")
+        c, L, P = codec_of(bits), _lib(), _ptrs(peers)
+        if c[0] == "fc":
+            _check(L.qr_fc_twoshot_peer_reduce(c[1], c[2], R, rank, n, P, stream), "qr_fc_twoshot_peer_reduce")
+        elif c[0] == "fp4":
+            _check(L.qr_fp4_twoshot_peer_reduce(R, rank, n, P, stream), "qr_fp4_twoshot_peer_reduce")
+        else:
+            _check(L.qr_twoshot_peer_reduce(c[1], R, rank, n, P, stream), "qr_twoshot_peer_reduce")
 
     def decode(self, bits, dtype, R, n, ws_ptr, y_ptr, stream):
-        _check(_lib().qr_twoshot_peer_decode(bits, dtype, R, n, ws_ptr, y_ptr, stream), "qr_twoshot_peer_decode")
+        c, L = codec_of(bits), _lib()
+        if c[0] == "fc":
+            _check(L.qr_fc_twoshot_peer_decode(c[1], c[2], dtype, R, n, ws_ptr, y_ptr, stream),
+                   "qr_fc_twoshot_peer_decode")
+        elif c[0] == "fp4":
+            _check(L.qr_fp4_twoshot_peer_decode(dtype, R, n, ws_ptr, y_ptr, stream), "qr_fp4_twoshot_peer_decode")
+        else:
+            _check(L.qr_twoshot_peer_decode(c[1], dtype, R, n, ws_ptr, y_ptr, stream), "qr_twoshot_peer_decode")
 
     def stream(self, stream=None):
         return _stream(self.device, stream)
@@ -115,13 +164,13 @@ class CudaPeerOps:
 class PeerTwoShot:
     """One rank of the per-rank two-shot all-reduce over a process group.
 
-    ``bits``: 3, 4, 6 or 8; ``n``: values per rank; ``dtype``: 0 (fp16) or 1
-    (bf16).  Construct it on every rank of ``group`` (collective: handles are
+    ``bits``: the codec (3, 4, 6 or 8; ``("fc", bits_rs, bits_ag)``;
+    ``"fp4"``); ``n``: values per rank; ``dtype``: 0 (fp16) or 1 (bf16).  Construct it on every rank of ``group`` (collective: handles are
     exchanged); ``allreduce(x_ptr, y_ptr)`` is collective too.  ``x_ptr`` /
     ``y_ptr`` are device pointers of n 16-bit values in this rank's memory
     (the tensor helpers take tensors)."""
 
-    def __init__(self, bits: int, n: int, dtype: int, group=None, ops=None):
+    def __init__(self, bits, n: int, dtype: int, group=None, ops=None):
         import torch.distributed as dist
         self.dist = dist
         self.group = group
@@ -189,14 +238,15 @@ class PeerTwoShot:
         self._opened = []
 
 
-def twoshot_peer_local(bits: int, xs, ys=None, workspaces=None, stream=None):
+def twoshot_peer_local(bits, xs, ys=None, workspaces=None, stream=None):
     """All R ranks' per-rank calls from one process, on one device and one
     stream: R workspaces in this process, every rank's send, then every
     owner's reduce, then every rank's decode (the stream order is the join).
-    Returns (the R outputs, the R workspaces).  Each output equals
-    qr_allreduce's.  `workspaces` (R uint8 tensors of
-    qr_twoshot_peer_workspace_bytes each) and `ys` may be passed in to reuse
-    them."""
+    Returns (the R outputs, the R workspaces).  Each output equals the
+    codec's fused all-reduce (qr_allreduce, qr_fc_allreduce or
+    qr_fp4_allreduce).  `bits` names the codec as for PeerTwoShot;
+    `workspaces` (R uint8 tensors of the codec's peer workspace bytes each)
+    and `ys` may be passed in to reuse them."""
     from . import _check_inputs, _same_device
     xs, dt, n = _check_inputs(xs)
     R = len(xs)
@@ -235,4 +285,5 @@ def init_group(rank: int, world: int, port: int, timeout_s: float = 60.0):
     return dist.group.WORLD
 
 
-__all__ = ["PeerTwoShot", "PeerError", "CudaPeerOps", "twoshot_peer_local", "init_group", "QR_IPC_HANDLE_BYTES"]
+__all__ = ["PeerTwoShot", "PeerError", "CudaPeerOps", "codec_of", "twoshot_peer_local", "init_group",
+           "QR_IPC_HANDLE_BYTES"]

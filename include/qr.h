@@ -496,6 +496,36 @@ qr_status_t qr_fc_allreduce_twoshot(int bits_rs, int bits_ag, qr_dtype_t dtype, 
                                     const void *const *x, size_t n, void *const *y,
                                     void *workspace, size_t workspace_bytes, qr_stream_t stream);
 
+/* The asymmetric codec's two-shot run by R separate ranks, as
+ * qr_twoshot_peer_send / _reduce / _decode for the symmetric codec (the same
+ * three calls per step, the same joins between them, the same `workspaces`
+ * array and aliasing rules; loads and stores only into peer memory).  With
+ * seg = ceil(T/R) tiles, rank j's workspace of
+ * qr_fc_twoshot_peer_workspace_bytes(bits_rs, bits_ag, R, n) bytes holds
+ *   recv[s]  at byte (s*seg) * qr_fc_tile_bytes(bits_rs): sender s's copy of
+ *            segment j at the reduce-scatter width;
+ *   gathered at byte (R*seg) * qr_fc_tile_bytes(bits_rs): the reduced wire
+ *            at the all-gather width, byte-identical to
+ *            qr_fc_segment_reduce's output.
+ * send quantizes rank `rank`'s message at bits_rs and stores segment k into
+ * recv[rank] of workspaces[k]; reduce sums owner `rank`'s R copies in
+ * sender order, re-quantizes at bits_ag and stores the tiles into the
+ * gathered wire of every workspace; decode dequantizes the caller's own
+ * gathered wire into y.  Every rank's output equals qr_fc_allreduce's.
+ * Width pairs as qr_fc_allreduce (QR_ERR_UNSUPPORTED otherwise); `rank`
+ * outside [0, R) is QR_ERR_INVALID_ARG; other errors as the symmetric
+ * per-rank calls.  0 from the size call means an unsupported pair or R,
+ * n == 0, or overflow. */
+size_t qr_fc_twoshot_peer_workspace_bytes(int bits_rs, int bits_ag, int R, size_t n);
+qr_status_t qr_fc_twoshot_peer_send(int bits_rs, int bits_ag, qr_dtype_t dtype, int R, int rank,
+                                    const void *x, size_t n, void *const *workspaces,
+                                    qr_stream_t stream);
+qr_status_t qr_fc_twoshot_peer_reduce(int bits_rs, int bits_ag, int R, int rank, size_t n,
+                                      void *const *workspaces, qr_stream_t stream);
+qr_status_t qr_fc_twoshot_peer_decode(int bits_rs, int bits_ag, qr_dtype_t dtype, int R,
+                                      size_t n, const void *workspace, void *y,
+                                      qr_stream_t stream);
+
 /* ---- the FP4 codec -------------------------------------------------------
  * "QuickReduce INT3 quantization and benchmarking on MI355", introduction: a
  * hardware-accelerated FP4 quantization path on MI355, "essentially
@@ -547,6 +577,21 @@ size_t qr_fp4_twoshot_workspace_bytes(int R, size_t n);      /* 0 if unsupported
 qr_status_t qr_fp4_allreduce_twoshot(qr_dtype_t dtype, int R, const void *const *x, size_t n,
                                      void *const *y, void *workspace, size_t workspace_bytes,
                                      qr_stream_t stream);
+
+/* The FP4 codec's two-shot run by R separate ranks: qr_twoshot_peer_send /
+ * _reduce / _decode with FP4 in place of the integer codes -- the same
+ * calls, joins, workspace layout at the 1152-byte tile
+ * (qr_fp4_twoshot_peer_workspace_bytes(R, n) =
+ * qr_twoshot_peer_workspace_bytes(4, R, n)), aliasing rules and errors.
+ * The gathered wire is byte-identical to qr_fp4_segment_reduce's output;
+ * every rank's output equals qr_fp4_allreduce's. */
+size_t qr_fp4_twoshot_peer_workspace_bytes(int R, size_t n);
+qr_status_t qr_fp4_twoshot_peer_send(qr_dtype_t dtype, int R, int rank, const void *x, size_t n,
+                                     void *const *workspaces, qr_stream_t stream);
+qr_status_t qr_fp4_twoshot_peer_reduce(int R, int rank, size_t n, void *const *workspaces,
+                                       qr_stream_t stream);
+qr_status_t qr_fp4_twoshot_peer_decode(qr_dtype_t dtype, int R, size_t n, const void *workspace,
+                                       void *y, qr_stream_t stream);
 
 /* The fused FP4 all-reduce D(E(sum_r D(E(x_r)))) on the staged kernel;
  * every x[r] and y 32-byte aligned (QR_ERR_MISALIGNED otherwise); `ctas` as

@@ -409,6 +409,100 @@ def test_peer_validation():
     assert L.qr_ipc_close_handle(W0) == qr.QR_ERR_INVALID_ARG                       # never opened
 
 
+def test_codec_peer_workspace_bytes():
+    """recv at the reduce-scatter width, then the gathered wire at the
+    all-gather width: R*seg tiles of each."""
+    from bit_quantized_all_gb300 import peer
+    L = peer._lib()
+    for rs, ag in qr.FC_PAIRS:
+        ti, to = qr.qr_fc_tile_bytes(rs), qr.qr_fc_tile_bytes(ag)
+        for R in (1, 2, 3, 8):
+            for n in (1, 2048, 2049, 2048 * 17 + 5, 2**27):
+                seg = -(-(-(-n // 2048)) // R)
+                assert L.qr_fc_twoshot_peer_workspace_bytes(rs, ag, R, n) == R * seg * (ti + to)
+    for R in (1, 2, 5, 8):
+        for n in (1, 2049, 2**26 + 3):
+            assert L.qr_fp4_twoshot_peer_workspace_bytes(R, n) == L.qr_twoshot_peer_workspace_bytes(4, R, n)
+    assert L.qr_fc_twoshot_peer_workspace_bytes(8, 4, 2, 100) == 0      # not a width pair
+    assert L.qr_fc_twoshot_peer_workspace_bytes(4, 6, 2, 100) == 0
+    assert L.qr_fc_twoshot_peer_workspace_bytes(4, 8, 9, 100) == 0
+    assert L.qr_fc_twoshot_peer_workspace_bytes(4, 8, 2, 0) == 0
+    assert L.qr_fc_twoshot_peer_workspace_bytes(8, 8, 8, 2**64 - 1) == 0
+    assert L.qr_fp4_twoshot_peer_workspace_bytes(0, 100) == 0
+    assert L.qr_fp4_twoshot_peer_workspace_bytes(9, 100) == 0
+    assert L.qr_fp4_twoshot_peer_workspace_bytes(8, 2**64 - 1) == 0
+
+
+@no_gpu_only
+@pytest.mark.parametrize("codec", ["fc", "fp4"])
+def test_codec_peer_validation(codec):
+    """The asymmetric and FP4 per-rank calls check their arguments as the
+    symmetric ones do, in the same order, before any CUDA call."""
+    from bit_quantized_all_gb300 import peer
+    L = peer._lib()
+    n = 2048 * 5 + 3
+    W0, W1 = 0x7F3000000000, 0x7F4000000000
+    ws = peer._ptrs([W0, W1])
+    if codec == "fc":
+        need = L.qr_fc_twoshot_peer_workspace_bytes(4, 8, 2, n)
+
+        def send(dt, R, rank, x, n_, w, rs=4, ag=8):
+            return L.qr_fc_twoshot_peer_send(rs, ag, dt, R, rank, x, n_, w, None)
+
+        def red(R, rank, n_, w, rs=4, ag=8):
+            return L.qr_fc_twoshot_peer_reduce(rs, ag, R, rank, n_, w, None)
+
+        def dec(dt, R, n_, w, y, rs=4, ag=8):
+            return L.qr_fc_twoshot_peer_decode(rs, ag, dt, R, n_, w, y, None)
+
+        assert send(0, 2, 0, A, n, ws, rs=8, ag=4) == qr.QR_ERR_UNSUPPORTED
+        assert red(2, 0, n, ws, rs=6) == qr.QR_ERR_UNSUPPORTED
+        assert dec(0, 2, n, W0, Y, ag=3) == qr.QR_ERR_UNSUPPORTED
+    else:
+        need = L.qr_fp4_twoshot_peer_workspace_bytes(2, n)
+
+        def send(dt, R, rank, x, n_, w):
+            return L.qr_fp4_twoshot_peer_send(dt, R, rank, x, n_, w, None)
+
+        def red(R, rank, n_, w):
+            return L.qr_fp4_twoshot_peer_reduce(R, rank, n_, w, None)
+
+        def dec(dt, R, n_, w, y):
+            return L.qr_fp4_twoshot_peer_decode(dt, R, n_, w, y, None)
+    assert need > 0
+    assert send(0, 2, 0, None, n, ws) == qr.QR_ERR_INVALID_ARG           # no input
+    assert send(0, 2, 0, A, n, None) == qr.QR_ERR_INVALID_ARG            # no workspaces
+    assert send(0, 2, 0, A, n, peer._ptrs([W0, None])) == qr.QR_ERR_INVALID_ARG
+    assert send(0, 2, 2, A, n, ws) == qr.QR_ERR_INVALID_ARG              # rank out of range
+    assert send(0, 2, -1, A, n, ws) == qr.QR_ERR_INVALID_ARG
+    assert send(0, 2, 0, A, 0, ws) == qr.QR_ERR_INVALID_ARG
+    assert send(0, 0, 0, A, n, ws) == qr.QR_ERR_INVALID_ARG              # R < 1
+    assert send(2, 2, 0, A, n, ws) == qr.QR_ERR_UNSUPPORTED              # dtype
+    assert send(0, 9, 0, A, n, peer._ptrs([W0 + 2**30 * i for i in range(9)])) == qr.QR_ERR_UNSUPPORTED
+    assert send(0, 2, 0, A, 2**62, ws) == qr.QR_ERR_SIZE
+    assert send(0, 2, 0, A + 8, n, ws) == qr.QR_ERR_MISALIGNED
+    assert send(0, 2, 0, A, n, peer._ptrs([W0, W1 + 8])) == qr.QR_ERR_MISALIGNED
+    assert send(0, 2, 0, A, n, peer._ptrs([W0, W0 + 64])) == qr.QR_ERR_INVALID_ARG   # overlapping
+    assert send(0, 2, 0, A, n, peer._ptrs([W0, W0 + need - 16])) == qr.QR_ERR_INVALID_ARG
+    assert send(0, 2, 0, W0 + 16, n, ws) == qr.QR_ERR_INVALID_ARG        # input in a workspace
+    assert red(2, 2, n, ws) == qr.QR_ERR_INVALID_ARG
+    assert red(2, 0, n, None) == qr.QR_ERR_INVALID_ARG
+    assert red(2, 0, 0, ws) == qr.QR_ERR_INVALID_ARG
+    assert red(9, 0, n, peer._ptrs([W0 + 2**30 * i for i in range(9)])) == qr.QR_ERR_UNSUPPORTED
+    assert red(2, 0, n, peer._ptrs([W0, W0 + need - 16])) == qr.QR_ERR_INVALID_ARG
+    assert red(2, 0, n, peer._ptrs([W0, W1 + 4])) == qr.QR_ERR_MISALIGNED
+    assert red(2, 0, 2**62, ws) == qr.QR_ERR_SIZE
+    assert dec(0, 2, n, None, Y) == qr.QR_ERR_INVALID_ARG
+    assert dec(0, 2, n, W0, None) == qr.QR_ERR_INVALID_ARG
+    assert dec(0, 2, 0, W0, Y) == qr.QR_ERR_INVALID_ARG
+    assert dec(0, 2, n, W0 + 8, Y) == qr.QR_ERR_MISALIGNED
+    assert dec(0, 2, n, W0, Y + 2) == qr.QR_ERR_MISALIGNED
+    assert dec(0, 2, n, W0, W0 + 32) == qr.QR_ERR_INVALID_ARG            # output in the workspace
+    assert dec(3, 2, n, W0, Y) == qr.QR_ERR_UNSUPPORTED
+    assert dec(0, 9, n, W0, Y) == qr.QR_ERR_UNSUPPORTED
+    assert dec(0, 2, 2**62, W0, Y) == qr.QR_ERR_SIZE
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qr, "LIB_PATH", str(tmp_path / "missing" / "libqr.so"))
     monkeypatch.setattr(qr, "_lib", None)

@@ -4,7 +4,8 @@ bf16, and messages that mix Gaussian and heavy-tailed values at scales from
 1e-3 to 1e3 with all-zero blocks, constant blocks and lone outliers
 (workloads.fuzz_case).  Every path: the fused kernel as the library picks
 it and forced onto the staged kernel, encode / Phase-1B / decode with their
-wires, the three-launch and the flag-joined two-shot, random grid sizes,
+wires, the three-launch and the flag-joined two-shot, the per-rank two-shot
+calls issued for every rank from one process, random grid sizes,
 16-byte-aligned buffers, the wire-emitting variant, the asymmetric codec's
 paths and the FP4 codec's."""
 import os
@@ -16,6 +17,7 @@ import torch
 import bit_quantized_all_gb300 as qr
 import oracle
 import workloads
+from bit_quantized_all_gb300.peer import twoshot_peer_local
 from qr_testlib import assert_outputs_match, assert_wire_equal, to_dev, to_host_u16, to_host_u8, xmax_of
 
 pytestmark = pytest.mark.gpu
@@ -58,6 +60,9 @@ def test_symmetric_codec_every_path(seed):
         ys, _ = qr.qr_allreduce_twoshot(bits, xs_dev, flags=flags)
         for j, y in enumerate(ys):
             assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} two-shot flags={flags} rank {j}")
+    ys, _ = twoshot_peer_local(bits, xs_dev)
+    for j, y in enumerate(ys):
+        assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} per-rank two-shot rank {j}")
     assert qr.qr_wait_timeouts() == 0
 
 
@@ -94,6 +99,9 @@ def test_asymmetric_codec_every_path(seed):
     ys, _ = qr.qr_fc_allreduce_twoshot(brs, bag, xs_dev)
     for j, y in enumerate(ys):
         assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} two-shot rank {j}")
+    ys, _ = twoshot_peer_local(("fc", brs, bag), xs_dev)
+    for j, y in enumerate(ys):
+        assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} per-rank two-shot rank {j}")
     assert qr.qr_wait_timeouts() == 0
 
 
@@ -163,4 +171,7 @@ def test_fp4_codec_every_path(seed):
     ys, _ = qr.qr_fp4_allreduce_twoshot(xs_dev)
     for j, y in enumerate(ys):
         assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} two-shot rank {j}")
+    ys, _ = twoshot_peer_local("fp4", xs_dev)
+    for j, y in enumerate(ys):
+        assert_outputs_match(to_host_u16(y), y_ref, dt, xmax, f"{what} per-rank two-shot rank {j}")
     assert qr.qr_wait_timeouts() == 0

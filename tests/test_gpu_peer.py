@@ -1,7 +1,9 @@
-"""The per-rank two-shot all-reduce with the library's kernels: R processes
-on the one GPU, each with its own CUDA context, its own workspace and its own
-message, the peers' workspaces mapped through CUDA IPC (qr_ipc_*), the
-phases joined by host barriers (no kernel waits on another process).
+"""The per-rank two-shot all-reduce with the library's kernels, for the
+symmetric, the asymmetric (Flash Communication) and the FP4 codec: R
+processes on the one GPU, each with its own CUDA context, its own workspace
+and its own message, the peers' workspaces mapped through CUDA IPC
+(qr_ipc_*), the phases joined by host barriers (no kernel waits on another
+process).
 
 Every rank's output equals the oracle's all-reduce of the R messages bit for
 bit, and the fused kernel's output in that process; the gathered wire in
@@ -49,6 +51,41 @@ def _inputs(R, n, dtype, seed):
     return out
 
 
+def _codec_refs(bits, dtype, xs, n, R):
+    """The oracle's all-reduce output and gathered (Phase-1B) wire for the
+    codec `bits` names (3/4/6/8, ("fc", bits_rs, bits_ag) or "fp4"), with the
+    gathered wire's byte offset in a rank's peer workspace and its length."""
+    import oracle
+    T = -(-n // 2048)
+    seg = -(-T // R)
+    if bits == "fp4":
+        ref = oracle.fp4_allreduce(dtype, xs)
+        red = oracle.fp4_segment_reduce([oracle.fp4_encode(dtype, x) for x in xs], n)
+        tbi = tbo = oracle.fp4_tile_bytes()
+    elif isinstance(bits, tuple):
+        _, rs, ag = bits
+        ref = oracle.fc_allreduce(rs, ag, dtype, xs)
+        red = oracle.fc_segment_reduce(rs, ag, [oracle.fc_encode(rs, dtype, x) for x in xs], n)
+        tbi, tbo = oracle.fc_tile_bytes(rs), oracle.fc_tile_bytes(ag)
+    else:
+        ref = oracle.allreduce(bits, dtype, xs)
+        red = oracle.segment_reduce(bits, [oracle.encode(bits, dtype, x) for x in xs], n)
+        tbi = tbo = oracle.tile_bytes(bits)
+    return ref, red, R * seg * tbi, T * tbo
+
+
+def _fused(bits, dev):
+    """The codec's fused all-reduce of the R device tensors, as host uint16."""
+    import bit_quantized_all_gb300 as qr
+    if bits == "fp4":
+        y = qr.qr_fp4_allreduce(dev)
+    elif isinstance(bits, tuple):
+        y = qr.qr_fc_allreduce(bits[1], bits[2], dev)
+    else:
+        y = qr.qr_allreduce(bits, dev)
+    return y.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
 def _worker(rank, world, port, cases, q):
     sys.path.insert(0, ROOT)
     os.environ["PYTORCH_CUDA_ALLOC_CONF"] = "expandable_segments:False"  # IPC needs plain allocations
@@ -56,27 +93,21 @@ def _worker(rank, world, port, cases, q):
     import torch.distributed as dist
     torch.cuda.set_device(0)
     import bit_quantized_all_gb300 as qr
-    import oracle
     from bit_quantized_all_gb300.peer import PeerTwoShot, init_group
     tdt = {0: torch.float16, 1: torch.bfloat16}
     group = init_group(rank, world, port, timeout_s=120.0)
     try:
         for ci, (bits, n, dtype) in enumerate(cases):
             peer = PeerTwoShot(bits, n, dtype, group=group)
-            T = -(-n // 2048)
-            seg = -(-T // world)
-            tb = qr.qr_tile_bytes(bits)
             for step in range(2):
                 xs = _inputs(world, n, dtype, 1000 * ci + 10 * step + 3)
                 dev = [torch.from_numpy(x.view(np.int16)).cuda().view(tdt[dtype]) for x in xs]
                 y = peer.allreduce_tensor(dev[rank])
                 torch.cuda.synchronize()
                 got = y.view(torch.int16).cpu().numpy().view(np.uint16)
-                ref = oracle.allreduce(bits, dtype, xs)
-                fused = qr.qr_allreduce(bits, dev).view(torch.int16).cpu().numpy().view(np.uint16)
-                red_ref = oracle.segment_reduce(bits, [oracle.encode(bits, dtype, x) for x in xs], n)
-                g = world * seg * tb
-                red = peer.workspace[g: g + T * tb].cpu().numpy()
+                ref, red_ref, g, glen = _codec_refs(bits, dtype, xs, n, world)
+                fused = _fused(bits, dev)
+                red = peer.workspace[g: g + glen].cpu().numpy()
                 status = []
                 if not np.array_equal(got, ref):
                     status.append(f"output differs from the oracle at {np.flatnonzero(got != ref)[:5]}")
@@ -146,11 +177,47 @@ def test_one_process_driving_every_rank(bits, R):
     assert qr.qr_wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("codec", [("fc", 4, 4), ("fc", 4, 8), ("fc", 8, 8), "fp4"], ids=["fc44", "fc48", "fc88", "fp4"])
+def test_one_process_driving_every_rank_codecs(codec, R):
+    """As above for the asymmetric and the FP4 codec: every output equals the
+    oracle's all-reduce and the codec's fused kernel, every gathered wire
+    the oracle's Phase-1B output, ragged tail and fewer tiles than ranks
+    included."""
+    import bit_quantized_all_gb300 as qr
+    from bit_quantized_all_gb300.peer import twoshot_peer_local
+    for n in (2048 * 13 + 77, 1500):
+        dtype = (R + n) % 2
+        xs = _inputs(R, n, dtype, 7 * R + n + (0 if codec == "fp4" else codec[1] + 3 * codec[2]))
+        tdt = {0: torch.float16, 1: torch.bfloat16}[dtype]
+        dev = [torch.from_numpy(x.view(np.int16)).cuda().view(tdt) for x in xs]
+        ys, ws = twoshot_peer_local(codec, dev)
+        torch.cuda.synchronize()
+        ref, red_ref, g, glen = _codec_refs(codec, dtype, xs, n, R)
+        fused = _fused(codec, dev)
+        for j in range(R):
+            got = ys[j].view(torch.int16).cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, ref), (codec, R, n, j)
+            assert np.array_equal(got, fused), (codec, R, n, j)
+            assert np.array_equal(ws[j][g: g + glen].cpu().numpy(), red_ref), (codec, R, n, j)
+        # the workspaces reused with other data: nothing left over matters
+        xs2 = _inputs(R, n, dtype, 99 + R + n)
+        dev2 = [torch.from_numpy(x.view(np.int16)).cuda().view(tdt) for x in xs2]
+        ys2, _ = twoshot_peer_local(codec, dev2, workspaces=ws)
+        ref2 = _codec_refs(codec, dtype, xs2, n, R)[0]
+        for j in range(R):
+            assert np.array_equal(ys2[j].view(torch.int16).cpu().numpy().view(np.uint16), ref2), (codec, R, n, j)
+    assert qr.qr_wait_timeouts() == 0
+
+
 @pytest.mark.parametrize("world,cases", [
     (2, [(4, 2048 * 40 + 37, 1), (3, 2048 * 9, 0), (8, 2048 * 3 + 1, 1), (6, 100, 0)]),
     (4, [(4, 2048 * 40 + 37, 1), (3, 2048 * 9 + 5, 1), (6, 2048 * 2, 0), (8, 700, 1)]),
     (8, [(4, 2048 * 64 + 11, 1), (3, 2048 * 5, 1)]),
-], ids=["R2", "R4", "R8"])
+    (2, [(("fc", 4, 8), 2048 * 40 + 37, 1), (("fc", 4, 4), 2048 * 9, 0), ("fp4", 2048 * 3 + 16, 1)]),
+    (3, [(("fc", 8, 8), 2048 * 17 + 5, 0), ("fp4", 2048 * 11, 0), (("fc", 4, 8), 1000, 1)]),
+    (8, [(("fc", 4, 8), 2048 * 64 + 11, 1), ("fp4", 2048 * 64 + 32, 1)]),
+], ids=["R2", "R4", "R8", "codecs-R2", "codecs-R3", "codecs-R8"])
 def test_every_rank_matches_the_oracle(world, cases):
     res = _run(world, cases)
     steps = [r for r in res if r[1] >= 0]

@@ -5,8 +5,8 @@ The GPU calls are replaced by a stand-in with the same methods (ShmOps):
 each rank's workspace lives in POSIX shared memory, the handle a rank shares
 is the memory's name, and the send / reduce / decode steps move bytes between
 the workspaces exactly as include/qr.h lays them out (recv[s] at s*seg
-tiles, the gathered wire at R*seg tiles), with the oracle doing the
-quantization arithmetic.  So this checks the protocol itself -- handle
+tiles, the gathered wire at R*seg tiles; for the symmetric, the asymmetric
+and the FP4 codec), with the oracle doing the quantization arithmetic.  So this checks the protocol itself -- handle
 exchange, which rank writes where, the joins between the phases -- end to
 end against the oracle's all-reduce, at world sizes 2, 3 and 4, and that a
 rank which leaves between steps makes the others fail at their next join
@@ -40,6 +40,35 @@ def _inputs(R, n, dtype, seed):
     return out
 
 
+def _codec(bits):
+    """The oracle's (recv tile bytes, gathered tile bytes, encode, segment
+    reduce, decode) for a codec as bit_quantized_all_gb300.peer names it:
+    3/4/6/8, ("fc", bits_rs, bits_ag) or "fp4"."""
+    import oracle
+    from bit_quantized_all_gb300.peer import codec_of
+    c = codec_of(bits)
+    if c[0] == "fc":
+        rs, ag = c[1], c[2]
+        return (oracle.fc_tile_bytes(rs), oracle.fc_tile_bytes(ag), lambda dt, x: oracle.fc_encode(rs, dt, x),
+                lambda ws, n: oracle.fc_segment_reduce(rs, ag, ws, n), lambda dt, w, n: oracle.fc_decode(ag, dt, w, n))
+    if c[0] == "fp4":
+        tb = oracle.fp4_tile_bytes()
+        return tb, tb, oracle.fp4_encode, oracle.fp4_segment_reduce, oracle.fp4_decode
+    b = c[1]
+    tb = oracle.tile_bytes(b)
+    return (tb, tb, lambda dt, x: oracle.encode(b, dt, x), lambda ws, n: oracle.segment_reduce(b, ws, n),
+            lambda dt, w, n: oracle.decode(b, dt, w, n))
+
+
+def _allreduce_ref(bits, dtype, xs):
+    import oracle
+    if bits == "fp4":
+        return oracle.fp4_allreduce(dtype, xs)
+    if isinstance(bits, tuple):
+        return oracle.fc_allreduce(bits[1], bits[2], dtype, xs)
+    return oracle.allreduce(bits, dtype, xs)
+
+
 class ShmOps:
     """Host stand-ins for the per-rank library calls (see the module docstring)."""
 
@@ -55,9 +84,9 @@ class ShmOps:
         return T, -(-T // R)
 
     def workspace_bytes(self, bits, R, n):
-        import oracle
+        tbi, tbo = _codec(bits)[:2]
         T, seg = self._seg(R, n)
-        return 2 * R * seg * oracle.tile_bytes(bits)
+        return R * seg * (tbi + tbo)
 
     def _register(self, shm):
         p = self.next
@@ -83,36 +112,33 @@ class ShmOps:
         shm.close()
 
     def send(self, bits, dtype, R, rank, x_ptr, n, peers, stream):
-        import oracle
+        tb, _, encode, _, _ = _codec(bits)
         T, seg = self._seg(R, n)
-        tb = oracle.tile_bytes(bits)
-        wire = oracle.encode(bits, dtype, self.inputs[x_ptr])
+        wire = encode(dtype, self.inputs[x_ptr])
         for k in range(R):
             t0, t1 = k * seg, min(T, (k + 1) * seg)
             if t0 < t1:
                 self.mem[peers[k]][1][rank * seg * tb: (rank * seg + t1 - t0) * tb] = wire[t0 * tb: t1 * tb]
 
     def reduce(self, bits, R, rank, n, peers, stream):
-        import oracle
+        tb, tbo, _, segment_reduce, _ = _codec(bits)
         T, seg = self._seg(R, n)
-        tb = oracle.tile_bytes(bits)
         t0, t1 = rank * seg, min(T, (rank + 1) * seg)
         if t0 >= t1:
             return
         own = self.mem[peers[rank]][1]
         copies = [own[s * seg * tb: (s * seg + t1 - t0) * tb].copy() for s in range(R)]
         n_seg = min(n, t1 * 2048) - t0 * 2048
-        red = oracle.segment_reduce(bits, copies, n_seg)
+        red = segment_reduce(copies, n_seg)
         for j in range(R):
             g = R * seg * tb
-            self.mem[peers[j]][1][g + t0 * tb: g + t1 * tb] = red
+            self.mem[peers[j]][1][g + t0 * tbo: g + t1 * tbo] = red
 
     def decode(self, bits, dtype, R, n, ws_ptr, y_ptr, stream):
-        import oracle
+        tb, tbo, _, _, decode = _codec(bits)
         T, seg = self._seg(R, n)
-        tb = oracle.tile_bytes(bits)
         g = R * seg * tb
-        self.outputs[y_ptr] = oracle.decode(bits, dtype, self.mem[ws_ptr][1][g: g + T * tb].copy(), n)
+        self.outputs[y_ptr] = decode(dtype, self.mem[ws_ptr][1][g: g + T * tbo].copy(), n)
 
     def stream(self, stream=None):
         return None
@@ -154,7 +180,7 @@ def _worker(rank, world, port, cases, leave_after, q):
                     q.put((rank, ci, step, f"peer error: {e}"))
                     ops.release()
                     return
-                ref = oracle.allreduce(bits, dtype, xs)
+                ref = _allreduce_ref(bits, dtype, xs)
                 q.put((rank, ci, step, "ok" if np.array_equal(outputs[2], ref) else "MISMATCH"))
             peer.close()
             ops.release()
@@ -223,7 +249,8 @@ def _run(world, cases, leave_after=None):
 
 @pytest.mark.parametrize("world", [2, 3, 4])
 def test_every_rank_gets_the_oracle_allreduce(world):
-    cases = [(4, 2048 * 5 + 37, 1), (3, 2048 * 2, 0), (8, 100, 1)]  # the last: fewer tiles than ranks
+    cases = [(4, 2048 * 5 + 37, 1), (3, 2048 * 2, 0), (8, 100, 1),  # the last: fewer tiles than ranks
+             (("fc", 4, 8), 2048 * 4 + 9, 1), ("fp4", 2048 * 3 + 16, 0)]
     res = _run(world, cases)
     assert len(res) == world * len(cases) * 2, res
     assert all(r[3] == "ok" for r in res), res
