@@ -7,6 +7,10 @@
  *     the two-shot exchange give the same bytes;
  *   - every wire, the reduced wire and the output equal the C oracle's
  *     (oracle/qr_oracle.h, test infrastructure), byte for byte;
+ *   - the per-rank two-shot calls of every codec (symmetric INT4, the
+ *     asymmetric 4->8 pair, FP4), each rank's send, then each owner's
+ *     reduce, then each rank's decode into R workspaces of this process:
+ *     every rank's output equals the oracle's all-reduce;
  *   - bad arguments return their status codes without launching anything;
  *   - no device-side wait ran out.
  * Exit status 0 and the line "qr_c_client ok" on success.
@@ -44,6 +48,44 @@ static void expect(int cond, const char *what) {
 static uint32_t lcg(uint32_t *s) {
     *s = *s * 1664525u + 1013904223u;
     return *s;
+}
+
+/* The per-rank calls of one codec (0: symmetric INT4, 1: asymmetric 4->8,
+ * 2: FP4) for all R ranks from this process; every rank's output is compared
+ * with `ref`. */
+static void per_rank(int codec, void *const *dx, size_t n, void *const *dys, const uint16_t *ref, uint16_t *host) {
+    const size_t need = codec == 0   ? qr_twoshot_peer_workspace_bytes(4, R, n)
+                        : codec == 1 ? qr_fc_twoshot_peer_workspace_bytes(4, 8, R, n)
+                                     : qr_fp4_twoshot_peer_workspace_bytes(R, n);
+    expect(need > 0, "peer workspace bytes");
+    void *ws[R];
+    for (int r = 0; r < R; ++r) CUDA_OK(cudaMalloc(&ws[r], need));
+    for (int j = 0; j < R; ++j) {
+        const qr_status_t st = codec == 0   ? qr_twoshot_peer_send(4, QR_BF16, R, j, dx[j], n, ws, NULL)
+                               : codec == 1 ? qr_fc_twoshot_peer_send(4, 8, QR_BF16, R, j, dx[j], n, ws, NULL)
+                                            : qr_fp4_twoshot_peer_send(QR_BF16, R, j, dx[j], n, ws, NULL);
+        expect(st == QR_OK, "per-rank send");
+    }
+    for (int j = 0; j < R; ++j) {
+        const qr_status_t st = codec == 0   ? qr_twoshot_peer_reduce(4, R, j, n, ws, NULL)
+                               : codec == 1 ? qr_fc_twoshot_peer_reduce(4, 8, R, j, n, ws, NULL)
+                                            : qr_fp4_twoshot_peer_reduce(R, j, n, ws, NULL);
+        expect(st == QR_OK, "per-rank reduce");
+    }
+    for (int j = 0; j < R; ++j) {
+        const qr_status_t st = codec == 0   ? qr_twoshot_peer_decode(4, QR_BF16, R, n, ws[j], dys[j], NULL)
+                               : codec == 1 ? qr_fc_twoshot_peer_decode(4, 8, QR_BF16, R, n, ws[j], dys[j], NULL)
+                                            : qr_fp4_twoshot_peer_decode(QR_BF16, R, n, ws[j], dys[j], NULL);
+        expect(st == QR_OK, "per-rank decode");
+    }
+    expect(qr_twoshot_peer_send(4, QR_BF16, R, R, dx[0], n, ws, NULL) == QR_ERR_INVALID_ARG, "rank out of range");
+    expect(qr_fc_twoshot_peer_reduce(8, 4, R, 0, n, ws, NULL) == QR_ERR_UNSUPPORTED, "width pair 8->4");
+    CUDA_OK(cudaDeviceSynchronize());
+    for (int j = 0; j < R; ++j) {
+        CUDA_OK(cudaMemcpy(host, dys[j], n * 2, cudaMemcpyDeviceToHost));
+        expect(memcmp(host, ref, n * 2) == 0, "per-rank output equals the oracle's");
+    }
+    for (int r = 0; r < R; ++r) CUDA_OK(cudaFree(ws[r]));
 }
 
 int main(void) {
@@ -116,6 +158,17 @@ int main(void) {
         CUDA_OK(cudaFree(dred));
         CUDA_OK(cudaFree(dws));
         printf("INT%d: fused, unfused and two-shot equal the oracle\n", bits);
+    }
+
+    /* the per-rank two-shot of each codec */
+    static const char *const codec_names[3] = {"symmetric INT4", "asymmetric 4->8", "FP4"};
+    for (int codec = 0; codec < 3; ++codec) {
+        const int rc = codec == 0   ? orc_allreduce(4, 1, R, (const uint16_t *const *)hx, n, href)
+                       : codec == 1 ? orc_fc_allreduce(4, 8, 1, R, (const uint16_t *const *)hx, n, href)
+                                    : orc_fp4_allreduce(1, R, (const uint16_t *const *)hx, n, href);
+        expect(rc == 0, "oracle all-reduce");
+        per_rank(codec, dx, n, dys, href, hy);
+        printf("%s: the per-rank two-shot equals the oracle on every rank\n", codec_names[codec]);
     }
 
     /* bad arguments: status codes, nothing launched */

@@ -1,8 +1,9 @@
 """The C ABI from a plain C program: tests/c_client/qr_c_client.c, compiled
 with gcc as C11 against include/qr.h and linked to libqr.so (and, for its
 checks, the C oracle and the CUDA runtime), runs every code width through the
-fused, unfused and two-shot entry points and compares each wire and output
-with the oracle's; see the program's header."""
+fused, unfused and two-shot entry points, and every codec through the
+per-rank two-shot calls, and compares each wire and output with the oracle's;
+see the program's header."""
 import os
 import subprocess
 
