@@ -7,6 +7,7 @@ every symbol hidden except the ``qr_*`` entry points of include/qr.h.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -55,11 +56,26 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile csrc/*.cu into libqr.so (skipped when up to date)."""
+    """Compile csrc/*.cu into libqr.so (skipped when up to date).  Processes
+    that build at the same time (the ranks of one job, parallel test
+    workers) take turns on a lock file, and each re-checks whether the
+    library is still stale once it holds the lock, so the objects are never
+    written by two compilers at once."""
     if not force and not ptxas_info and not _stale():
         return LIB_PATH
-    nvcc = _nvcc()
     os.makedirs(OBJ_DIR, exist_ok=True)
+    with open(os.path.join(OBJ_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not ptxas_info and not _stale():
+                return LIB_PATH
+            return _build_locked(verbose, ptxas_info)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool, ptxas_info: bool) -> str:
+    nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src: str) -> tuple[str, str]:

@@ -517,3 +517,33 @@ def test_product_package_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"\boracle\b|qr_oracle|liboracle|orc_", text), f
+
+
+def test_concurrent_builds_take_turns(monkeypatch):
+    """Two builds at once (as the ranks of one job may start them) never
+    compile at the same time: the second waits for the lock, then finds the
+    library up to date and compiles nothing."""
+    import threading
+    import time
+
+    from bit_quantized_all_gb300 import build as b
+    state = {"active": 0, "overlap": False, "compiles": 0, "stale": True}
+
+    def fake_build(verbose, ptxas_info):
+        state["active"] += 1
+        state["overlap"] |= state["active"] > 1
+        state["compiles"] += 1
+        time.sleep(0.3)
+        state["stale"] = False
+        state["active"] -= 1
+        return b.LIB_PATH
+
+    monkeypatch.setattr(b, "_build_locked", fake_build)
+    monkeypatch.setattr(b, "_stale", lambda: state["stale"])
+    threads = [threading.Thread(target=b.build) for _ in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=30)
+    assert not state["overlap"]
+    assert state["compiles"] == 1
