@@ -1,8 +1,9 @@
 // qr_kernels32.cuh -- the standalone encode, Phase-1B reduce and decode
-// kernels: one 32-value block per thread (encode32, reduce32) or two threads
-// per block (decode16, reduce16); and the staged Phase-1B kernel
+// kernels: one 32-value block per thread (encode32, reduce32, reduce_ahead)
+// or two threads per block (decode16); the staged Phase-1B kernel
 // (staged_reduce_kernel, wire tiles brought into shared memory by bulk
-// copies) with the symmetric codec's policy QrReduce.
+// copies) with the symmetric codec's policy QrReduce; and Phase-1B's exact
+// integer sum.
 //
 // A block's codes are contiguous in each section of the wire tile (slots
 // 4g..4g+3), so a thread reads or writes them with one vector access per
@@ -713,86 +714,147 @@ __device__ __forceinline__ void store_half_codes(uint8_t *tile, int g, int half,
     }
 }
 
-// Phase-1B in-segment reduction [QR Quantization and Dequantization Paths;
-// FC key machinery], with two threads per block (lanes 2k and 2k+1 own the
-// two halves of one block, so the pair shares the absmax by one shuffle):
-// decode the R rank copies, add them in fp32 in rank order (fma(q, s, acc) =
-// RN(acc + q*s): q*s is exact), re-quantize.  Half-blocks hb and hb^1 are
-// always both in or both out of range, and every lane reaches the shuffle.
-template <int B, int R, int U>
-__device__ __forceinline__ void reduce16_run(ConstPtrs wires, uint8_t *out, long long NH) {
-    const long long S = static_cast<long long>(gridDim.x) * kThreads32;
-    for (long long hb0 = static_cast<long long>(blockIdx.x) * kThreads32 + threadIdx.x; hb0 - (threadIdx.x & 31) < NH;
-         hb0 += U * S) {
-        HalfWords<B> c[U][R];
-        uint32_t sb[U][R];
+// ---------------------------------------------------------------------------
+// Phase-1B by exact integer arithmetic
+// ---------------------------------------------------------------------------
+// Every decoded value q*s is exact in fp32 (a code of at most 6 bits times an
+// fp16 scale), and every fp16 scale s_r >= smin is an integer multiple M_r of
+// unit = 2^(floor(log2 smin) - 10), smin the block's smallest nonzero scale
+// over the R ranks.  When M_r < 2^16 for every rank (the scales lie within
+// about 5 binades of each other), every partial sum of the rank order is an
+// integer multiple of unit below bias * R * 2^16 <= 2^24 units in magnitude,
+// so the fp32 rank-order sum that defines Phase-1B rounds nothing: it equals
+// the exact sum unit * S, S = sum_r M_r * q_r, in any order.  S is then summed in
+// integers: the codes of two ranks for one value sit in adjacent bytes (one
+// byte permute per four values), and one two-way dot product (dp2a: two
+// 16x8-bit products and an add) takes both ranks' M_r * u_r.  u = q + bias is
+// the stored code.  At INT3 and INT4 (|S| < 2^22) the accumulator starts at
+// 1.5*2^23 - bias * sum_r M_r as an fp32 bit pattern, so it ends as the
+// pattern of the float 1.5*2^23 + S, and one fma per value pair turns it
+// into unit * S; at INT6 (|S| < 2^24) it starts at -bias * sum_r M_r and
+// ends as S, converted exactly to fp32 and scaled by unit.  The result is the
+// rank-order sum up to the sign of a zero, which the re-quantization does not
+// see (a zero gives the same code with either sign).  Blocks outside the
+// condition (scales further apart, a negative, infinite or NaN scale bit
+// pattern, every scale zero) return false and take the float path.
+constexpr uint32_t kExactLimit = 1u << 16;  // M_r < kExactLimit
+
+// The codes of one rank's block as 8 words of 4 byte-sized codes: word x,
+// byte t is the code of value 2 * exact_pair<B>(x, t) + (x >= 4 at INT3,
+// else x & 1).
+template <int B>
+__device__ __forceinline__ void block_code_bytes(const BlockWords<B> &c, uint32_t (&X)[8]) {
+    if constexpr (B == 3) {
+        uint32_t e01, o01, e23, o23;  // nibble 4i+m: lane 2m (e) / 2m+1 (o) of slot i (+2)
+        q3_nibbles(c.w[0], c.w[2], e01, o01);
+        q3_nibbles(c.w[1], c.w[2] >> 16, e23, o23);
+        X[0] = e01 & 0x0F0F0F0Fu;
+        X[1] = (e01 >> 4) & 0x0F0F0F0Fu;
+        X[2] = e23 & 0x0F0F0F0Fu;
+        X[3] = (e23 >> 4) & 0x0F0F0F0Fu;
+        X[4] = o01 & 0x0F0F0F0Fu;
+        X[5] = (o01 >> 4) & 0x0F0F0F0Fu;
+        X[6] = o23 & 0x0F0F0F0Fu;
+        X[7] = (o23 >> 4) & 0x0F0F0F0Fu;
+    } else {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const long long hb = hb0 + u * S;
-            if (hb < NH) {
-                const long long gb = hb >> 1;
-                const long long off = (gb >> 6) * Codec<B>::kTileBytes;
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint8_t *tile = static_cast<const uint8_t *>(wires.p[r]) + off;
-                    load_half_codes<B>(tile, static_cast<int>(gb & 63), static_cast<int>(hb & 1), c[u][r]);
-                    sb[u][r] = load_block_scale_bits<B>(tile, static_cast<int>(gb & 63));
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const long long hb = hb0 + u * S;
-            const bool valid = hb < NH;
-            float2 acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
-            if (valid) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float s = f16_bits_to_float(sb[u][r]);
-                    const float2 s2 = make_float2(s, s);
-#pragma unroll
-                    for (int sl = 0; sl < 2; ++sl) {
-                        float2 q[4];
-                        unpack_slot_q2<B>(half_slot_codes<B>(c[u][r], sl), q);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            acc[4 * sl + i] = (r == 0) ? __fmul2_rn(q[i], s2) : __ffma2_rn(q[i], s2, acc[4 * sl + i]);
-                    }
-                }
-            }
-            const BlockScale2 sc = block_scale2<B>(pair_absmax(acc));
-            if (valid) {
-                float2 f[8];
-                const float2 r2 = make_float2(sc.r, sc.r);
-                const float2 m2 = make_float2(Codec<B>::kMagic, Codec<B>::kMagic);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float2 t = __fmul2_rn(acc[i], r2);
-                    if (sc.low_clip) {
-                        t.x = fmaxf(t.x, Codec<B>::kQmin);
-                        t.y = fmaxf(t.y, Codec<B>::kQmin);
-                    }
-                    t.x = fminf(t.x, Codec<B>::kQmax);
-                    t.y = fminf(t.y, Codec<B>::kQmax);
-                    f[i] = __fadd2_rn(t, m2);
-                }
-                HalfWords<B> cw;
-                pack_half<B>(f, cw);
-                const long long gb = hb >> 1;
-                uint8_t *tile = out + (gb >> 6) * Codec<B>::kTileBytes;
-                store_half_codes<B>(tile, static_cast<int>(gb & 63), static_cast<int>(hb & 1), cw);
-                if ((hb & 1) == 0) store_block_scale<B>(tile, static_cast<int>(gb & 63), sc.bits);
-            }
-        }
+        for (int sl = 0; sl < 4; ++sl) slot_even_odd_codes<B>(slot_codes<B>(c, sl), X[2 * sl], X[2 * sl + 1]);
     }
 }
 
-template <int B, int R, int U>
-__global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, uint8_t *out, long long NH) {
-    chain_entry();
-    reduce16_run<B, R, U>(wires, out, NH);
+// The value pair (index j: values 2j, 2j+1 of the block) of byte t of code
+// word x, and whether the byte holds the pair's odd value.
+template <int B>
+__device__ __forceinline__ constexpr int exact_pair(int x, int t) {
+    return B == 3 ? ((x & 1) + 8 * ((x >> 1) & 1) + 2 * t) : (4 * (x >> 1) + t);
+}
+template <int B>
+__device__ __forceinline__ constexpr bool exact_odd(int x) {
+    return B == 3 ? x >= 4 : (x & 1) != 0;
+}
+
+template <int B, int R>
+__device__ __forceinline__ bool exact_int_sum(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
+                                              float2 (&acc)[16]) {
+    // the largest scale pattern (unsigned: a sign bit, infinity and NaN all
+    // compare above 0x7BFF) and the smallest nonzero one
+    uint32_t hi = 0, lo_m1 = 0xFFFFFFFFu;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        hi = max(hi, sb[r]);
+        lo_m1 = min(lo_m1, sb[r] - 1u);
+    }
+    if (hi > 0x7BFFu || lo_m1 == 0xFFFFFFFFu) return false;
+    const uint32_t unit_bits = (__float_as_uint(f16_bits_to_float(lo_m1 + 1u)) & 0x7F800000u) - (10u << 23);
+    const float unit = __uint_as_float(unit_bits), inv = __uint_as_float(0x7F000000u - unit_bits);  // 2^k, 2^-k
+    if (!(__fmul_rn(f16_bits_to_float(hi), inv) < float(kExactLimit))) return false;
+    // M_r in the low half of the pattern of 2^23 + M_r; the sum of the
+    // scales (exact: multiples of unit below 2^19 units)
+    uint32_t m[R];
+    float ssum = 0.0f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float s = f16_bits_to_float(sb[r]);
+        m[r] = __float_as_uint(__fmaf_rn(s, inv, 8388608.0f));
+        ssum = __fadd_rn(ssum, s);
+    }
+    uint32_t base;
+    if constexpr (B == 6)  // -bias * sum M (sum M < 2^19, from the pattern of 2^23 + sum M)
+        base = (0x4B000000u - __float_as_uint(__fmaf_rn(ssum, inv, 8388608.0f))) * uint32_t(Codec<B>::kBias);
+    else  // the pattern of 1.5*2^23 - bias * sum M
+        base = __float_as_uint(__fmaf_rn(ssum, -float(Codec<B>::kBias) * inv, kRoundMagic));
+    uint32_t ax[16], ay[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ax[j] = ay[j] = base;
+#pragma unroll
+    for (int r = 0; r + 1 < R; r += 2) {
+        const uint32_t a = __byte_perm(m[r], m[r + 1], 0x5410);  // (M_r, M_r+1) as 16-bit halves
+        uint32_t X0[8], X1[8];
+        block_code_bytes<B>(c[r], X0);
+        block_code_bytes<B>(c[r + 1], X1);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            const uint32_t p01 = __byte_perm(X0[x], X1[x], 0x5140), p23 = __byte_perm(X0[x], X1[x], 0x7362);
+            uint32_t *d = exact_odd<B>(x) ? ay : ax;
+            d[exact_pair<B>(x, 0)] = __dp2a_lo(a, p01, d[exact_pair<B>(x, 0)]);
+            d[exact_pair<B>(x, 1)] = __dp2a_hi(a, p01, d[exact_pair<B>(x, 1)]);
+            d[exact_pair<B>(x, 2)] = __dp2a_lo(a, p23, d[exact_pair<B>(x, 2)]);
+            d[exact_pair<B>(x, 3)] = __dp2a_hi(a, p23, d[exact_pair<B>(x, 3)]);
+        }
+    }
+    if constexpr (R % 2 == 1) {  // the last rank alone: (M, 0) against bytes 0, 2 and 1, 3
+        const uint32_t a = m[R - 1] & 0xFFFFu;
+        uint32_t X0[8];
+        block_code_bytes<B>(c[R - 1], X0);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            uint32_t *d = exact_odd<B>(x) ? ay : ax;
+            d[exact_pair<B>(x, 0)] = __dp2a_lo(a, X0[x], d[exact_pair<B>(x, 0)]);
+            d[exact_pair<B>(x, 2)] = __dp2a_hi(a, X0[x], d[exact_pair<B>(x, 2)]);
+            d[exact_pair<B>(x, 1)] = __dp2a_lo(a, X0[x] >> 8, d[exact_pair<B>(x, 1)]);
+            d[exact_pair<B>(x, 3)] = __dp2a_hi(a, X0[x] >> 8, d[exact_pair<B>(x, 3)]);
+        }
+    }
+    const float2 u2 = make_float2(unit, unit);
+    if constexpr (B == 6) {  // S exactly (|S| < 2^24), times unit (a power of two: exact)
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            acc[j] = __fmul2_rn(make_float2(__int2float_rn(static_cast<int>(ax[j])),
+                                            __int2float_rn(static_cast<int>(ay[j]))), u2);
+    } else {
+        const float2 c2 = make_float2(-kRoundMagic * unit, -kRoundMagic * unit);  // exact: a power of two
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            acc[j] = __ffma2_rn(make_float2(__uint_as_float(ax[j]), __uint_as_float(ay[j])), u2, c2);
+    }
+    return true;
+}
+
+// Where Phase-1B takes the exact integer sum first (the float path below
+// remains the fallback for blocks outside its condition).
+template <int B, int R>
+__host__ __device__ constexpr bool exact_sum_enabled() {
+    return (B == 3 || B == 4 || B == 6) && R >= 2;
 }
 
 // Phase-1B in-segment reduction with one thread per block (fewer
@@ -803,10 +865,10 @@ __global__ void __launch_bounds__(kThreads32) reduce16_kernel(ConstPtrs wires, u
 // Phase-1B of one 32-value block from its R ranks' codes c[r] and fp16 scale
 // bits sb[r]: decode, add in fp32 in rank order (fma(q, s, acc) =
 // RN(acc + q*s): q*s is exact), re-quantize; the block's codes go to cw and
-// its fp16 scale bits to scale_bits.
+// its fp16 scale bits to scale_bits.  The float path.
 template <int B, int R>
-__device__ __forceinline__ void reduce_block_words(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
-                                                   BlockWords<B> &cw, uint32_t &scale_bits) {
+__device__ __forceinline__ void reduce_block_words_float(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
+                                                         BlockWords<B> &cw, uint32_t &scale_bits) {
     float2 acc[16];
     if constexpr (B == 3 && R <= 4) {
         // codes decoded to fp16 through the fp16 1024 (logic operations and
@@ -936,6 +998,25 @@ __device__ __forceinline__ void reduce_block_words(const BlockWords<B> (&c)[R], 
     scale_bits = sc.bits;
 }
 
+// Phase-1B of one block (as reduce_block_words_float): the exact integer sum
+// where it applies, the float path otherwise; the same bytes either way.
+template <int B, int R>
+__device__ __forceinline__ void reduce_block_words(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
+                                                   BlockWords<B> &cw, uint32_t &scale_bits) {
+    if constexpr (exact_sum_enabled<B, R>()) {
+        float2 acc[16];
+        if (exact_int_sum<B, R>(c, sb, acc)) {
+            const BlockScale2 sc = block_scale2<B>(block_absmax(acc));
+            float2 f[16];
+            quantize_block_magic<B>(acc, sc.r, sc.low_clip, f);
+            pack_block<B>(f, cw);
+            scale_bits = sc.bits;
+            return;
+        }
+    }
+    reduce_block_words_float<B, R>(c, sb, cw, scale_bits);
+}
+
 // reduce_block_words, written into `tile` as its block g.
 template <int B, int R>
 __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
@@ -1038,30 +1119,34 @@ __global__ void __launch_bounds__(kThreads32, MINB) reduce_ahead_kernel(ConstPtr
 // Where the symmetric codec's Phase-1B of a long message (from 48 tiles per
 // SM) runs reduce_ahead_kernel, with how many CTAs per SM (0 = not: the
 // staged kernel for INT4/6/8, reduce32_kernel for INT3).  Measured on GB300
-// at 2^27 (2^28) bf16 values per rank, fraction of the copy bandwidth,
-// default kernel -> one block ahead: INT8 R=4 0.965 (0.992) -> 0.988
-// (1.013); INT6 R=2 0.616 (0.639) -> 0.635 (0.660), R=3 0.648 -> 0.662, R=4
-// 0.684 (0.706) -> 0.706 (0.732); INT4 R=3 0.599 -> 0.633, R=8 0.749 (0.770)
-// -> 0.787 (0.815); INT3 R=2 0.418 (0.446) -> 0.434 (0.460).  Elsewhere it
-// was slower or within 1% (at R >= 5 more ranks' loads in flight than its
-// registers hold, except INT4 at R = 8).
+// at 2^27 (2^28) bf16 values per rank, fraction of the copy bandwidth, with
+// the exact integer sum: default kernel -> one block ahead, INT4 R=2 0.634
+// (0.660) -> 0.685 (0.711) at three CTAs per SM, R=4 0.788 (0.822) -> 0.834
+// (0.863), R=5 0.814 (0.842) -> 0.880 (0.911), R=6 0.898 (0.928) -> 0.940
+// (0.976), R=7 0.928 (0.959) -> 0.950 (0.981), R=8 0.970 (1.000) -> 0.980
+// (1.003); INT6 R=5 0.822 (0.844) -> 0.839 (0.859); INT3 R=7 0.610 (0.631)
+// -> 0.626 (0.640), R=8 0.634 (0.652) -> 0.649 (0.663); and the other
+// choices below still the fastest of 0, 2, 3 (and 4 at R = 2) CTAs per SM
+// (INT6 R=2 three, R=3 and 4 two; INT4 R=3 three; INT3 R=2 two).  With the
+// float sum, INT8 R=4 0.965 (0.992) -> 0.988 (1.013).  Elsewhere the one
+// block ahead was slower or within 1%.
 template <int B, int R>
 __host__ __device__ constexpr int reduce_ahead_min_blocks() {
     return (B == 8 && R == 4)                       ? 2
            : (B == 6 && R == 2)                     ? 3
-           : (B == 6 && (R == 3 || R == 4))         ? 2
-           : (B == 4 && R == 3)                     ? 3
-           : (B == 4 && R == 8)                     ? 2
-           : (B == 3 && R == 2)                     ? 2
+           : (B == 6 && R >= 3 && R <= 5)           ? 2
+           : (B == 4 && (R == 2 || R == 3))         ? 3
+           : (B == 4 && R >= 4)                     ? 2
+           : (B == 3 && (R == 2 || R >= 7))         ? 2
                                                     : 0;
 }
 
-// Which Phase-1B kernel: measured on GB300 at 2^24..2^30 values per rank, the
-// two-threads-per-block kernel is faster for INT4/INT6 with six or more
-// ranks (latency-bound there); one thread per block needs fewer
-// instructions and wins everywhere else (INT3 and small R are ALU-bound).
-template <int B, int R>
-__host__ __device__ constexpr bool reduce_two_threads_per_block() { return (B == 4 || B == 6) && R >= 6; }
+// Phase-1B's register-fed kernels take one block per thread.  (A kernel with
+// two threads per block, the pair sharing the absmax by a shuffle, was
+// faster for INT4 / INT6 at six or more ranks while the sum was in fp32;
+// with the exact integer sum one thread per block was faster there too: at
+// 2^23 values per rank 0.34-0.44 -> 0.39-0.46 of the copy bandwidth, and
+// the two-shot's owner reductions at 2^27 0.89-0.94 -> 0.93-0.98.)
 template <int R>
 __host__ __device__ constexpr int reduce_units_per_thread() { return (R <= 2) ? 2 : 1; }
 

@@ -1,6 +1,6 @@
 // qr_reduce.cu -- launchers of the Phase-1B reduction kernels (reduce32_kernel,
-// reduce16_kernel and staged_reduce_kernel), R dispatched to a compile-time
-// constant.
+// reduce_ahead_kernel and staged_reduce_kernel), R dispatched to a
+// compile-time constant.
 #include "qr_kernels32.cuh"
 #include "qr_launch.h"
 
@@ -58,21 +58,12 @@ static cudaError_t run_reduce_r(const ConstPtrs &w, long long n, void *out, cuda
                 return run_reduce_staged_r<B, R>(w, n, out, 0, s);
         }
     }
-    if constexpr (reduce_two_threads_per_block<B, R>()) {
-        const long long NH = 128 * T;
-        auto kern = reduce16_kernel<B, R, U>;
-        const long long units = (NH + kThreads32 * U - 1) / (kThreads32 * U);
-        const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
-        if (grid <= 0) return err;
-        return launch_chained(kern, grid, kThreads32, 0, s, w, static_cast<uint8_t *>(out), NH);
-    } else {
-        const long long NB = 64 * T;
-        auto kern = reduce32_kernel<B, R, U>;
-        const long long units = (NB + kThreads32 * U - 1) / (kThreads32 * U);
-        const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
-        if (grid <= 0) return err;
-        return launch_chained(kern, grid, kThreads32, 0, s, w, static_cast<uint8_t *>(out), NB);
-    }
+    const long long NB = 64 * T;
+    auto kern = reduce32_kernel<B, R, U>;
+    const long long units = (NB + kThreads32 * U - 1) / (kThreads32 * U);
+    const int grid = grid_for(reinterpret_cast<const void *>(kern), kThreads32, units, 0, 4, &err);
+    if (grid <= 0) return err;
+    return launch_chained(kern, grid, kThreads32, 0, s, w, static_cast<uint8_t *>(out), NB);
 }
 
 template <int B>

@@ -49,10 +49,7 @@ __global__ void __launch_bounds__(kThreads32) twoshot_reduce_kernel(uint8_t *ws,
 #pragma unroll
     for (int j = 0; j < R; ++j) w.p[j] = ws + (k * R + j) * seg * tb;
     uint8_t *red = ws + static_cast<long long>(R) * R * seg * tb + t0 * tb;
-    if constexpr (reduce_two_threads_per_block<B, R>())
-        reduce16_run<B, R, U>(w, red, 128 * tiles);
-    else
-        reduce32_run<B, R, U>(w, red, 64 * tiles);
+    reduce32_run<B, R, U>(w, red, 64 * tiles);
 }
 
 // Phase-2: rank j = blockIdx.y decodes the gathered wire into its output.
@@ -89,7 +86,7 @@ static cudaError_t send_all(int R, const void *const *x, long long n, uint8_t *w
 template <int B, int R>
 static cudaError_t reduce_all_r(uint8_t *ws, long long T, long long seg, cudaStream_t s) {
     constexpr int U = reduce_units_per_thread<R>();
-    const long long per_row = (reduce_two_threads_per_block<B, R>() ? 128 : 64) * seg;
+    const long long per_row = 64 * seg;
     auto kern = twoshot_reduce_kernel<B, R, U>;
     cudaError_t err = cudaSuccess;
     const int gx = row_ctas(reinterpret_cast<const void *>(kern), (per_row + kThreads32 * U - 1) / (kThreads32 * U), R,

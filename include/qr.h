@@ -136,7 +136,13 @@ qr_status_t qr_encode(int bits, qr_dtype_t dtype, const void *x, size_t n,
  * [FC] key machinery "sums locally, re-quantizes the partial sums"): decode
  * the R wires (host array of R device pointers, each qr_wire_bytes(bits, n)
  * bytes), add them in fp32 in rank order, re-quantize into `out_wire`.
- * 1 <= R <= 8.  `out_wire` may equal one of `wires` exactly. */
+ * 1 <= R <= 8.  `out_wire` may equal one of `wires` exactly.  At INT3, INT4
+ * and INT6 with R >= 2, a block whose nonzero scales are all integer
+ * multiples below 2^16 of the smallest one's unit (2^(floor(log2 smin) -
+ * 10); about five binades) is summed exactly in integers (two-way 16x8-bit
+ * dot products): then no partial sum of the rank order rounds, so the
+ * result is the fp32 rank-order sum's, bit for bit; other blocks are summed
+ * in fp32. */
 qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires,
                               size_t n, void *out_wire, qr_stream_t stream);
 
@@ -148,10 +154,10 @@ qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires,
  * else min(ctas, #SMs) (at most one per tile); the result does not depend on
  * it; ctas < 0 is QR_ERR_INVALID_ARG.  qr_segment_reduce itself takes this
  * kernel for INT4, INT6 and INT8 from 48 tiles per SM, except INT8 at R = 4,
- * INT6 at R = 2..4 and INT4 at R = 3 and 8, where (as for INT3 at R = 2) it
- * runs a kernel from registers that loads each thread's next block before
- * reducing the current one; below 48 tiles per SM, and for INT3 otherwise,
- * a kernel from registers with one block per thread.  Its waits on its
+ * INT6 at R = 2..5 and INT4 at every R >= 2, where (as for INT3 at R = 2, 7
+ * and 8) it runs a kernel from registers that loads each thread's next
+ * block before reducing the current one; below 48 tiles per SM, and for
+ * INT3 otherwise, a kernel from registers with one block per thread.  Its waits on its
  * shared-memory barriers are bounded (see qr_wait_timeouts).  Same other
  * arguments and errors as qr_segment_reduce. */
 qr_status_t qr_segment_reduce_staged(int bits, int R, const void *const *wires,
