@@ -1017,13 +1017,18 @@ __device__ __forceinline__ void reduce_block_words(const BlockWords<B> (&c)[R], 
     reduce_block_words_float<B, R>(c, sb, cw, scale_bits);
 }
 
-// reduce_block_words, written into `tile` as its block g.
-template <int B, int R>
+// reduce_block_words, written into `tile` as its block g; kFloatOnly skips
+// the exact integer sum (the same bytes, for a kernel that has no registers
+// to spare for it).
+template <int B, int R, bool kFloatOnly = false>
 __device__ __forceinline__ void reduce_block(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R], uint8_t *tile,
                                              int g) {
     BlockWords<B> cw;
     uint32_t bits;
-    reduce_block_words<B, R>(c, sb, cw, bits);
+    if constexpr (kFloatOnly)
+        reduce_block_words_float<B, R>(c, sb, cw, bits);
+    else
+        reduce_block_words<B, R>(c, sb, cw, bits);
     store_block_codes<B>(tile, g, cw);
     store_block_scale<B>(tile, g, bits);
 }

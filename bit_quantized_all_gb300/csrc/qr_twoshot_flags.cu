@@ -157,7 +157,12 @@ __global__ void __launch_bounds__(64) twoshot_flags_kernel(ConstPtrs x, long lon
                 uint32_t sb[R];
 #pragma unroll
                 for (int j = 0; j < R; ++j) load_block_cg<B>(recv_tile(t, j), k, cw[j], sb[j]);
-                reduce_block<B, R>(cw, sb, red + t * kTile, k);
+                // INT4 from six ranks keeps the fp32 sum: with the exact
+                // integer sum the kernel took 95 registers a thread, fewer of
+                // its cooperative CTAs were resident, and R = 8 ran at 0.92
+                // of the copy bandwidth instead of 0.96 (2^27 bf16 values per
+                // rank); at INT6 and at INT4 up to R = 4 the exact sum was faster.
+                reduce_block<B, R, (B == 4 && R >= 6)>(cw, sb, red + t * kTile, k);
             }
         }
         __syncthreads();
