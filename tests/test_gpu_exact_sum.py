@@ -12,7 +12,8 @@ ranks; every rank zero; subnormal scales; scales near the fp16 maximum; a
 negative zero and a negative scale; a spread of 10^6; and log-uniform random
 scales.  The codes are random bytes.  Every reduced wire equals the oracle's
 Phase-1B output byte for byte, through the default kernel choice and the
-staged kernel, at rank counts that pair every rank and that leave one alone.
+staged kernel, at rank counts that pair every rank and that leave one alone,
+and at the sizes where the one-block-ahead and staged kernels run.
 """
 import numpy as np
 import pytest
@@ -90,6 +91,57 @@ def _wires(bits, R, T, seed):
                 off = t * tb + code_bytes + 2 * g
                 wires[r][off: off + 2] = np.array([s[r]], dtype=np.uint16).view(np.uint8)
     return wires
+
+
+def _wires_fast(bits, R, T, seed):
+    """_wires' mix of block kinds for many tiles at once (vectorized): each
+    block takes one of the kinds above, its scales drawn per rank."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    tb = qr.qr_tile_bytes(bits)
+    code_bytes = 256 * bits
+    nb = 64 * T
+    kind = rng.integers(0, 11, nb)
+    u = rng.uniform(size=(R, nb))
+    s = np.exp2(rng.uniform(-20.0, 15.0, (R, nb)))                        # log-uniform
+    s = np.where(kind == 0, 1.0 + u, s)                                   # one binade
+    s = np.where(kind == 1, 1.0 + 62.96875 * u, s)                        # to the limit
+    s = np.where(kind == 3, np.where(u < 0.4, 0.0, 0.5 + 3.5 * u), s)     # zeros in some ranks
+    s = np.where(kind == 4, 0.0, s)                                       # every rank zero
+    s = np.where(kind == 5, 2.0**-24 + (2.0**-14 - 2.0**-24) * u, s)      # subnormal
+    s = np.where(kind == 6, 16384.0 + (65504.0 - 16384.0) * u, s)         # near the maximum
+    s = np.where(kind == 9, (1.0 + u) * 1e-3, s)                          # spread of 10^6
+    bits16 = s.astype(np.float16).view(np.uint16).copy()
+    j = rng.integers(0, R, nb)
+    col = np.arange(nb)
+    bits16[j, col] = np.where(kind == 1, _f16(63.96875), bits16[j, col])  # M = 65504
+    bits16[j, col] = np.where(kind == 2, _f16(64.0), bits16[j, col])      # M = 65536 ...
+    bits16[(j + 1) % R, col] = np.where(kind == 2, _f16(1.0), bits16[(j + 1) % R, col])  # ... with smin = 1
+    bits16[j, col] = np.where(kind == 7, 0x8000, bits16[j, col])          # a negative zero
+    bits16[j, col] = np.where(kind == 8, _f16(-1.5), bits16[j, col])      # a negative scale
+    bits16[j, col] = np.where(kind == 9, _f16(1000.0), bits16[j, col])
+    wires = []
+    for r in range(R):
+        w = np.empty((T, tb), dtype=np.uint8)
+        w[:, :code_bytes] = rng.integers(0, 256, (T, code_bytes), dtype=np.uint8)
+        w[:, code_bytes:] = bits16[r].reshape(T, 64).view(np.uint8)
+        wires.append(w.reshape(-1))
+    return wires
+
+
+@pytest.mark.parametrize("R", [2, 8])
+@pytest.mark.parametrize("bits", [3, 4, 6])
+def test_long_message_kernels_on_both_sides_of_the_condition(bits, R):
+    """At 48 tiles per SM and more, where Phase-1B runs the one-block-ahead
+    or the staged kernel (a ragged tail included)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 48 * sms + 3
+    n = T * 2048 - 777
+    wires = _wires_fast(bits, R, T, 77 * bits + R)
+    ref = oracle.segment_reduce(bits, wires, n)
+    dev = [torch.from_numpy(w).cuda() for w in wires]
+    got = to_host_u8(qr.qr_segment_reduce(bits, dev, n))
+    assert_wire_equal(got, ref, bits, f"INT{bits} R={R} n={n} long message")
+    assert qr.qr_wait_timeouts() == 0
 
 
 @pytest.mark.parametrize("R", [2, 3, 5, 8])
