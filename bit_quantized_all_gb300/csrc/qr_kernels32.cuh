@@ -857,15 +857,10 @@ __host__ __device__ constexpr bool exact_sum_enabled() {
     return (B == 3 || B == 4 || B == 6) && R >= 2;
 }
 
-// Phase-1B in-segment reduction with one thread per block (fewer
-// instructions than reduce16_kernel, which wins where the 8-rank loads need
-// more warps to hide their latency): decode the R rank copies of the block,
-// add them in fp32 in rank order (fma(q, s, acc) = RN(acc + q*s): q*s is
-// exact), re-quantize.
 // Phase-1B of one 32-value block from its R ranks' codes c[r] and fp16 scale
-// bits sb[r]: decode, add in fp32 in rank order (fma(q, s, acc) =
-// RN(acc + q*s): q*s is exact), re-quantize; the block's codes go to cw and
-// its fp16 scale bits to scale_bits.  The float path.
+// bits sb[r] (one thread per block): decode, add in fp32 in rank order
+// (fma(q, s, acc) = RN(acc + q*s): q*s is exact), re-quantize; the block's
+// codes go to cw and its fp16 scale bits to scale_bits.  The float path.
 template <int B, int R>
 __device__ __forceinline__ void reduce_block_words_float(const BlockWords<B> (&c)[R], const uint32_t (&sb)[R],
                                                          BlockWords<B> &cw, uint32_t &scale_bits) {
