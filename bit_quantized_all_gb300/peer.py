@@ -34,6 +34,7 @@ from __future__ import annotations
 
 import ctypes
 import datetime
+import numbers
 
 import torch
 
@@ -88,8 +89,8 @@ def codec_of(bits):
         return ("fp4",)
     if isinstance(bits, tuple) and len(bits) == 3 and bits[0] == "fc":
         return ("fc", int(bits[1]), int(bits[2]))
-    if isinstance(bits, int) and not isinstance(bits, bool):
-        return ("qr", bits)
+    if isinstance(bits, numbers.Integral) and not isinstance(bits, bool):
+        return ("qr", int(bits))
     raise ValueError(f"unknown two-shot codec {bits!r}: 3/4/6/8, ('fc', bits_rs, bits_ag) or 'fp4'")
 
 

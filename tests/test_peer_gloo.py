@@ -267,3 +267,14 @@ def test_a_rank_that_leaves_between_steps_fails_the_next_join():
         steps = dict(by_rank[rank])
         assert steps[0] == "ok", by_rank
         assert steps[1].startswith("peer error"), by_rank
+
+
+def test_codec_names():
+    """How the per-rank calls name a codec: a width, ("fc", rs, ag) or "fp4"."""
+    from bit_quantized_all_gb300.peer import codec_of
+    assert codec_of(4) == ("qr", 4) and codec_of(np.int64(3)) == ("qr", 3)
+    assert codec_of(("fc", 4, 8)) == ("fc", 4, 8)
+    assert codec_of("fp4") == ("fp4",)
+    for bad in (True, "int4", ("fc", 4), ("qr", 4, 4), 4.0, None):
+        with pytest.raises(ValueError):
+            codec_of(bad)
