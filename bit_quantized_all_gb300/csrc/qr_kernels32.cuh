@@ -742,9 +742,27 @@ constexpr uint32_t kExactLimit = 1u << 16;  // M_r < kExactLimit
 // The codes of one rank's block as 8 words of 4 byte-sized codes: word x,
 // byte t is the code of value 2 * exact_pair<B>(x, t) + (x >= 4 at INT3,
 // else x & 1).
+// The 8 INT6 codes of a slot as bytes, lanes 0,2,4,6 in `even` and 1,3,5,7
+// in `odd`, from the slot's low nibbles `a` (lane j at bits 4j) and its
+// high-bit pairs in the low 16 bits of `b` (lane j at bits 2j): one byte
+// permute looks each lane's two high bits up in a table of the four values
+// already shifted to bits 4..5, with the lane's bits in the low bits of a
+// selector nibble (the nibble's top bit is cleared: set, it would make the
+// permute replicate a sign).  8 integer operations per slot where spreading
+// the high bits by shifts and masks took 11.
+__device__ __forceinline__ void q6_even_odd_bytes(uint32_t a, uint32_t b, uint32_t &even, uint32_t &odd) {
+    constexpr uint32_t kHi = 0x30201000u;  // byte i = i << 4
+    even = (a & 0x0F0F0F0Fu) | __byte_perm(kHi, kHi, b & 0x7777u);
+    odd = ((a >> 4) & 0x0F0F0F0Fu) | __byte_perm(kHi, kHi, (b >> 2) & 0x7777u);
+}
+
 template <int B>
 __device__ __forceinline__ void block_code_bytes(const BlockWords<B> &c, uint32_t (&X)[8]) {
-    if constexpr (B == 3) {
+    if constexpr (B == 6) {
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl)
+            q6_even_odd_bytes(c.w[sl], c.w[4 + sl / 2] >> (16 * (sl % 2)), X[2 * sl], X[2 * sl + 1]);
+    } else if constexpr (B == 3) {
         uint32_t e01, o01, e23, o23;  // nibble 4i+m: lane 2m (e) / 2m+1 (o) of slot i (+2)
         q3_nibbles(c.w[0], c.w[2], e01, o01);
         q3_nibbles(c.w[1], c.w[2] >> 16, e23, o23);
