@@ -38,7 +38,7 @@ def _f16(v):
     return np.array(v, dtype=np.float16).view(np.uint16)
 
 
-def _block_scales(rng, kind, R, bits):
+def _block_scales(rng, kind, R):
     """fp16 scale bit patterns of one block for R ranks."""
     top = 63.96875  # the largest scale with M below the limit 2^16 when smin = 1
     past = 64.0     # the smallest with M at the limit
@@ -86,7 +86,7 @@ def _wires(bits, R, T, seed):
             wires[r][t * tb: t * tb + code_bytes] = rng.integers(0, 256, code_bytes, dtype=np.uint8)
         for g in range(64):
             kind = int(rng.integers(0, 11)) if rng.random() < 0.5 else (g % 11)
-            s = _block_scales(rng, kind, R, bits)
+            s = _block_scales(rng, kind, R)
             for r in range(R):
                 off = t * tb + code_bytes + 2 * g
                 wires[r][off: off + 2] = np.array([s[r]], dtype=np.uint16).view(np.uint8)
