@@ -225,3 +225,29 @@ def test_every_rank_matches_the_oracle(world, cases):
     assert all(r[3] == "ok" for r in steps), [r for r in steps if r[3] != "ok"]
     assert sorted(r[3] for r in res if r[1] == -1) == ["timeouts=0"] * world, res
     assert not [r for r in res if r[1] == -2], res
+
+
+def _offset_by_16_bytes(x: torch.Tensor) -> torch.Tensor:
+    """x's values in a buffer that starts 16 bytes past a 32-byte boundary."""
+    buf = torch.empty(x.numel() + 16, dtype=x.dtype, device=x.device)
+    v = buf[8: 8 + x.numel()]
+    assert v.data_ptr() % 32 == 16
+    v.copy_(x)
+    return v
+
+
+@pytest.mark.parametrize("codec", [4, 3, ("fc", 4, 8), ("fc", 8, 8), "fp4"], ids=["int4", "int3", "fc48", "fc88", "fp4"])
+def test_sixteen_byte_aligned_inputs_and_outputs(codec):
+    """The per-rank calls with every input and output 16 but not 32 bytes
+    aligned (the narrower loads and stores): the same outputs as the
+    oracle's."""
+    from bit_quantized_all_gb300.peer import twoshot_peer_local
+    R, n = 5, 2048 * 9 + 333
+    xs = _inputs(R, n, 1, 4242)
+    dev = [_offset_by_16_bytes(torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)) for x in xs]
+    ys = [_offset_by_16_bytes(torch.zeros(n, dtype=torch.bfloat16, device="cuda")) for _ in range(R)]
+    twoshot_peer_local(codec, dev, ys=ys)
+    torch.cuda.synchronize()
+    ref = _codec_refs(codec, 1, xs, n, R)[0]
+    for j in range(R):
+        assert np.array_equal(ys[j].view(torch.int16).cpu().numpy().view(np.uint16), ref), (codec, j)
