@@ -40,7 +40,8 @@ def _long_n():
     return 2048 * (48 * sms + 301) + 7  # past the 48-tiles-per-SM threshold, a ragged tail
 
 
-@pytest.mark.parametrize("bits,R", [(8, 4), (6, 2), (6, 3), (6, 4), (4, 3), (4, 8), (3, 2)])
+@pytest.mark.parametrize("bits,R", [(8, 4), (6, 2), (6, 3), (6, 4), (6, 5), (4, 2), (4, 3), (4, 4), (4, 5), (4, 6),
+                                    (4, 7), (4, 8), (3, 2), (3, 7), (3, 8)])
 def test_symmetric_phase1b_one_block_ahead(bits, R):
     n = _long_n()
     xs = [to_dev(x, 1) for x in _ranks(R, n, 40 + 7 * bits + R)]
