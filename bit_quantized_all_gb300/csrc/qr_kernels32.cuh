@@ -186,6 +186,19 @@ __device__ __forceinline__ void pack_pair_q3_lanes(const float2 (&F)[8], uint32_
                            W, X);
 }
 
+// The INT6 sections of one slot from its codes as bytes (`even`: lanes
+// 0,2,4,6, `odd`: lanes 1,3,5,7, each byte a code below 64): the q4w word
+// (lane j's low nibble at bits 4j), and `y`, whose bytes 0 and 2 are the
+// slot's q2w field (lane j's high two bits at bits 2j): byte k of c holds
+// lanes 2k and 2k+1, and one shift-or pairs neighbouring bytes, so that a
+// byte permute finishes the field (7 operations where three shift-and-mask
+// compress steps took 12).
+__device__ __forceinline__ void q6_slot_fields(uint32_t even, uint32_t odd, uint32_t &q4w, uint32_t &y) {
+    q4w = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
+    const uint32_t c = ((even >> 4) & 0x03030303u) | ((odd >> 2) & 0x0C0C0C0Cu);
+    y = c | (c >> 4);
+}
+
 template <int B>
 __device__ __forceinline__ void pack_block(const float2 (&f)[16], BlockWords<B> &c) {
     if constexpr (B == 3) {
@@ -204,15 +217,10 @@ __device__ __forceinline__ void pack_block(const float2 (&f)[16], BlockWords<B> 
             if constexpr (B == 8) {
                 c.w[2 * s] = __byte_perm(even, odd, 0x5140);
                 c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
-            } else {
-                c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
-                const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
-                const uint32_t q2 = compress_2_of_4(hi);
-                if (s % 2 == 0) {
-                    c.w[4 + s / 2] = q2;
-                } else {
-                    c.w[4 + s / 2] |= q2 << 16;
-                }
+            } else {  // slot s's q2w field into the low (even s) or high half of its word
+                uint32_t y;
+                q6_slot_fields(even, odd, c.w[s], y);
+                c.w[4 + s / 2] = s % 2 == 0 ? __byte_perm(y, 0u, 0x4420) : __byte_perm(c.w[4 + s / 2], y, 0x6410);
             }
         }
     }
@@ -668,16 +676,14 @@ __global__ void __launch_bounds__(kThreads32) decode16_kernel(const uint8_t *__r
     decode16_run<B, DT, U, Y32>(wire, n, y, NH);
 }
 
-// Codes of two slots (one half-block) from 16 magic floats f[0..7] (pairs).
+// Codes of two slots (one half-block) from 16 magic floats f[0..7] (pairs):
+// the asymmetric codec's INT4 and INT8 halves.
 template <int B>
 __device__ __forceinline__ void pack_half(const float2 (&f)[8], HalfWords<B> &c) {
+    static_assert(B == 4 || B == 8, "half-block packing is used at INT4 and INT8");
     if constexpr (B == 4) {
         c.w[0] = slot_nibbles(&f[0]);
         c.w[1] = slot_nibbles(&f[4]);
-    } else if constexpr (B == 3) {
-        const uint32_t n0 = slot_nibbles(&f[0]), n1 = slot_nibbles(&f[4]);
-        c.w[0] = compress_2_of_4(n0) | (compress_2_of_4(n1) << 16);
-        c.w[1] = compress_1_of_4(n0 >> 2) | (compress_1_of_4(n1 >> 2) << 8);
     } else {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -685,16 +691,8 @@ __device__ __forceinline__ void pack_half(const float2 (&f)[8], HalfWords<B> &c)
                                                    __float_as_uint(f[4 * s + 2].x), __float_as_uint(f[4 * s + 3].x));
             const uint32_t odd = gather_low_bytes(__float_as_uint(f[4 * s].y), __float_as_uint(f[4 * s + 1].y),
                                                   __float_as_uint(f[4 * s + 2].y), __float_as_uint(f[4 * s + 3].y));
-            if constexpr (B == 8) {
-                c.w[2 * s] = __byte_perm(even, odd, 0x5140);
-                c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
-            } else {
-                c.w[s] = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
-                const uint32_t hi = ((even >> 4) & 0x03030303u) | (((odd >> 4) & 0x03030303u) << 4);
-                const uint32_t q2 = compress_2_of_4(hi);
-                if (s == 0) c.w[2] = q2;
-                else c.w[2] |= q2 << 16;
-            }
+            c.w[2 * s] = __byte_perm(even, odd, 0x5140);
+            c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
         }
     }
 }
