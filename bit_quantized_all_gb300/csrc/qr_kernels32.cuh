@@ -65,6 +65,26 @@ __device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
     return absmax_n<32>(reinterpret_cast<const float *>(v));
 }
 
+// RN(RN(v * r) + m) in both lanes: a packed multiply, then the add as a
+// packed fma by `one`, which must equal 1 without being a constant the
+// compiler can see.  A packed multiply followed by a packed add was merged
+// into one fma (one rounding), which changes the codes; a multiply feeding
+// the multiplicand of an fma has no such merge.
+__device__ __forceinline__ float2 mul_then_add2(float2 v, float r, float one, float m) {
+    float2 d;
+    asm("{\n\t.reg .b64 pv, pr, pt, po, pm, pd;\n\t"
+        "mov.b64 pv, {%2, %3};\n\t"
+        "mov.b64 pr, {%4, %4};\n\t"
+        "mov.b64 po, {%5, %5};\n\t"
+        "mov.b64 pm, {%6, %6};\n\t"
+        "mul.rn.f32x2 pt, pv, pr;\n\t"
+        "fma.rn.f32x2 pd, pt, po, pm;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(v.x), "f"(v.y), "f"(r), "f"(one), "f"(m));
+    return d;
+}
+
 // f = clip(RN(v*r), qmin, qmax) + 1.5*2^23 + bias (the code in the low byte),
 // with the clip at qmin only where block_scale2 says it can matter.
 //
@@ -74,9 +94,9 @@ __device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
 // builds and where one subtraction per eight codes turns 8 into 7 -- the same
 // code as clipping t at qmax first (t <= 3 is unchanged by the clip; for
 // t > 3, RNE(t) + 4 is 7 or 8 and becomes 7, as RNE(3) + 4 is).  That
-// removes one float minimum (integer-pipe work) per value.  The products are then scalar multiplies: a packed multiply whose
-// only use is a packed add is contracted into one rounding by the compiler,
-// which would change the codes.
+// removes one float minimum (integer-pipe work) per value.  The product and
+// the add are then two packed operations (mul_then_add2): contracted into one
+// rounding they would change the codes.
 template <int B>
 __device__ __forceinline__ void quantize_block_magic(const float2 (&v)[16], float r, bool low_clip,
                                                      float2 (&f)[16]) {
@@ -84,8 +104,9 @@ __device__ __forceinline__ void quantize_block_magic(const float2 (&v)[16], floa
     const float2 m2 = make_float2(Codec<B>::kMagic, Codec<B>::kMagic);
     if constexpr (B == 3) {
         if (!low_clip) {
+            const float one = __fmaf_rn(r, 0.0f, 1.0f);  // 1: r is finite
 #pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = __fadd2_rn(make_float2(__fmul_rn(v[i].x, r), __fmul_rn(v[i].y, r)), m2);
+            for (int i = 0; i < 16; ++i) f[i] = mul_then_add2(v[i], r, one, Codec<B>::kMagic);
             return;
         }
     }
@@ -726,16 +747,21 @@ __device__ __forceinline__ void store_half_codes(uint8_t *tile, int g, int half,
 // integers: the codes of two ranks for one value sit in adjacent bytes (one
 // byte permute per four values), and one two-way dot product (dp2a: two
 // 16x8-bit products and an add) takes both ranks' M_r * u_r.  u = q + bias is
-// the stored code.  At INT3 and INT4 (|S| < 2^22) the accumulator starts at
-// 1.5*2^23 - bias * sum_r M_r as an fp32 bit pattern, so it ends as the
-// pattern of the float 1.5*2^23 + S, and one fma per value pair turns it
-// into unit * S; at INT6 (|S| < 2^24) it starts at -bias * sum_r M_r and
-// ends as S, converted exactly to fp32 and scaled by unit.  The result is the
+// the stored code.  The accumulator starts at 1.5*2^23 - bias * sum_r M_r as
+// an fp32 bit pattern, so it ends as the pattern of the float 1.5*2^23 + S,
+// and one fma per value pair turns it into unit * S.  That needs |S| below
+// 2^22, which holds at INT3 and INT4 (|S| <= 8 * 8 * 2^16).  INT6 with at
+// most four ranks adds it to the condition: bias * sum_r M_r < 2^22, i.e.
+// sum_r M_r < 2^17 (always true at R = 2; an INT6 block further spread takes
+// the float path).  INT6 from five ranks, where outlier channels put many
+// blocks past that sum, starts at -bias * sum_r M_r instead and ends as S
+// (|S| < 2^24), converted exactly to fp32 and scaled by unit.  The result is the
 // rank-order sum up to the sign of a zero, which the re-quantization does not
 // see (a zero gives the same code with either sign).  Blocks outside the
 // condition (scales further apart, a negative, infinite or NaN scale bit
 // pattern, every scale zero) return false and take the float path.
-constexpr uint32_t kExactLimit = 1u << 16;  // M_r < kExactLimit
+constexpr uint32_t kExactLimit = 1u << 16;     // M_r < kExactLimit
+constexpr uint32_t kExactSumLimit6 = 1u << 17;  // INT6, R <= 4: sum_r M_r < kExactSumLimit6
 
 // The codes of one rank's block as 8 words of 4 byte-sized codes: word x,
 // byte t is the code of value 2 * exact_pair<B>(x, t) + (x >= 4 at INT3,
@@ -814,11 +840,14 @@ __device__ __forceinline__ bool exact_int_sum(const BlockWords<B> (&c)[R], const
         m[r] = __float_as_uint(__fmaf_rn(s, inv, 8388608.0f));
         ssum = __fadd_rn(ssum, s);
     }
+    constexpr bool kMagic = B != 6 || R <= 4;  // the accumulator as the pattern of 1.5*2^23 + S
+    if constexpr (B == 6 && R > 2 && kMagic)
+        if (!(__fmul_rn(ssum, inv) < float(kExactSumLimit6))) return false;
     uint32_t base;
-    if constexpr (B == 6)  // -bias * sum M (sum M < 2^19, from the pattern of 2^23 + sum M)
-        base = (0x4B000000u - __float_as_uint(__fmaf_rn(ssum, inv, 8388608.0f))) * uint32_t(Codec<B>::kBias);
-    else  // the pattern of 1.5*2^23 - bias * sum M
+    if constexpr (kMagic)  // the pattern of 1.5*2^23 - bias * sum M (exact: bias * sum M < 2^22)
         base = __float_as_uint(__fmaf_rn(ssum, -float(Codec<B>::kBias) * inv, kRoundMagic));
+    else  // -bias * sum M (sum M < 2^19, from the pattern of 2^23 + sum M)
+        base = (0x4B000000u - __float_as_uint(__fmaf_rn(ssum, inv, 8388608.0f))) * uint32_t(Codec<B>::kBias);
     uint32_t ax[16], ay[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) ax[j] = ay[j] = base;
@@ -852,16 +881,16 @@ __device__ __forceinline__ bool exact_int_sum(const BlockWords<B> (&c)[R], const
         }
     }
     const float2 u2 = make_float2(unit, unit);
-    if constexpr (B == 6) {  // S exactly (|S| < 2^24), times unit (a power of two: exact)
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            acc[j] = __fmul2_rn(make_float2(__int2float_rn(static_cast<int>(ax[j])),
-                                            __int2float_rn(static_cast<int>(ay[j]))), u2);
-    } else {
+    if constexpr (kMagic) {
         const float2 c2 = make_float2(-kRoundMagic * unit, -kRoundMagic * unit);  // exact: a power of two
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             acc[j] = __ffma2_rn(make_float2(__uint_as_float(ax[j]), __uint_as_float(ay[j])), u2, c2);
+    } else {  // S exactly (|S| < 2^24), times unit (a power of two: exact)
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            acc[j] = __fmul2_rn(make_float2(__int2float_rn(static_cast<int>(ax[j])),
+                                            __int2float_rn(static_cast<int>(ay[j]))), u2);
     }
     return true;
 }

@@ -3,14 +3,15 @@ both sides of the condition that selects it.
 
 The symmetric codec's Phase-1B sums a block's R decoded copies with integer
 dot products when the ranks' nonzero scales are all integer multiples M_r of
-the smallest one's unit (2^(floor(log2 smin) - 10)) below 2^16;
-then no partial sum of the rank order rounds, and the integer sum equals the
-oracle's fp32 sum.  Every other block takes the float path.  These wires mix,
-within every warp, blocks of each kind: scales in one binade; spread to just
-inside the limit (M = 65504) and just past it (M = 65536); zero scales in some
-ranks; every rank zero; subnormal scales; scales near the fp16 maximum; a
-negative zero and a negative scale; a spread of 10^6; and log-uniform random
-scales.  The codes are random bytes.  Every reduced wire equals the oracle's
+the smallest one's unit (2^(floor(log2 smin) - 10)) below 2^16, and at INT6
+also sum_r M_r < 2^17; then no partial sum of the rank order rounds, and the
+integer sum equals the oracle's fp32 sum.  Every other block takes the float
+path.  These wires mix, within every warp, blocks of each kind: scales in one
+binade; spread to just inside the limit (M = 65504) and just past it
+(M = 65536); zero scales in some ranks; every rank zero; subnormal scales;
+scales near the fp16 maximum; a negative zero and a negative scale; a spread
+of 10^6; log-uniform random scales; and, from three ranks, sum_r M_r just
+below 2^17 (131071) and at it (131072).  The codes are random bytes.  Every reduced wire equals the oracle's
 Phase-1B output byte for byte, through the default kernel choice and the
 staged kernel, at rank counts that pair every rank and that leave one alone,
 and at the sizes where the one-block-ahead and staged kernels run.
@@ -71,6 +72,12 @@ def _block_scales(rng, kind, R):
     elif kind == 9:  # a spread of 10^6
         s = _f16(rng.uniform(1.0, 2.0, R) * 1e-3)
         s[rng.integers(R)] = _f16(1000.0)
+    elif kind in (11, 12) and R >= 3:  # sum M = 2047 + 63520 + 65504 = 2^17 - 1, or 2016 + 63552 + 65504 = 2^17
+        s = np.zeros(R, dtype=np.uint16)
+        j = rng.permutation(R)
+        s[j[0]] = _f16(2047 / 1024 if kind == 11 else 2016 / 1024)
+        s[j[1]] = _f16(63520 / 1024 if kind == 11 else 63552 / 1024)
+        s[j[2]] = _f16(63.96875)
     else:            # log-uniform over most of the fp16 range
         s = _f16(np.exp2(rng.uniform(-20.0, 15.0, R)))
     return s.astype(np.uint16)
@@ -85,7 +92,7 @@ def _wires(bits, R, T, seed):
         for r in range(R):
             wires[r][t * tb: t * tb + code_bytes] = rng.integers(0, 256, code_bytes, dtype=np.uint8)
         for g in range(64):
-            kind = int(rng.integers(0, 11)) if rng.random() < 0.5 else (g % 11)
+            kind = int(rng.integers(0, 13)) if rng.random() < 0.5 else (g % 13)
             s = _block_scales(rng, kind, R)
             for r in range(R):
                 off = t * tb + code_bytes + 2 * g
@@ -100,7 +107,7 @@ def _wires_fast(bits, R, T, seed):
     tb = qr.qr_tile_bytes(bits)
     code_bytes = 256 * bits
     nb = 64 * T
-    kind = rng.integers(0, 11, nb)
+    kind = rng.integers(0, 13, nb)
     u = rng.uniform(size=(R, nb))
     s = np.exp2(rng.uniform(-20.0, 15.0, (R, nb)))                        # log-uniform
     s = np.where(kind == 0, 1.0 + u, s)                                   # one binade
@@ -119,6 +126,12 @@ def _wires_fast(bits, R, T, seed):
     bits16[j, col] = np.where(kind == 7, 0x8000, bits16[j, col])          # a negative zero
     bits16[j, col] = np.where(kind == 8, _f16(-1.5), bits16[j, col])      # a negative scale
     bits16[j, col] = np.where(kind == 9, _f16(1000.0), bits16[j, col])
+    if R >= 3:  # sum M just below 2^17 (kind 11) and at it (kind 12)
+        for k, m in ((11, (2047, 63520, 65504)), (12, (2016, 63552, 65504))):
+            sel = kind == k
+            bits16[:, sel] = 0
+            for d in range(3):
+                bits16[(j[sel] + d) % R, col[sel]] = _f16(m[d] / 1024)
     wires = []
     for r in range(R):
         w = np.empty((T, tb), dtype=np.uint8)
