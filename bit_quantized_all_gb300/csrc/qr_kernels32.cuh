@@ -85,28 +85,36 @@ __device__ __forceinline__ float2 mul_then_add2(float2 v, float r, float one, fl
     return d;
 }
 
-// f = clip(RN(v*r), qmin, qmax) + 1.5*2^23 + bias (the code in the low byte),
-// with the clip at qmin only where block_scale2 says it can matter.
+// INT6 codes leave the quantizer 64 above the code (kMagic6): a code of 64
+// (qmax + 1, which the packing turns into 63) then has bit 7 of its byte set.
+constexpr float kMagic6 = Codec<6>::kMagic + 64.0f;
+
+// f = clip(RN(v*r), qmin, qmax) + 1.5*2^23 + bias (the code in the low byte;
+// INT6: plus 64), with the clip at qmin only where block_scale2 says it can
+// matter.
 //
-// INT3 without the lower clip leaves the upper one to the packing: for a
-// normal scale every t = RN(v*r) is at most |qmin|*(1 + 2^-10.9), so its code
-// is at most |qmin| + bias = 8, which still fits the nibble that pack_pair_q3
-// builds and where one subtraction per eight codes turns 8 into 7 -- the same
-// code as clipping t at qmax first (t <= 3 is unchanged by the clip; for
-// t > 3, RNE(t) + 4 is 7 or 8 and becomes 7, as RNE(3) + 4 is).  That
+// INT3 and INT6 without the lower clip leave the upper one to the packing:
+// for a normal scale every t = RN(v*r) is at most |qmin|*(1 + 2^-10.9), so its
+// code is at most |qmin| + bias (INT3: 8, INT6: 64), and the packing maps that
+// one out-of-range code to qmax + bias (INT3: one subtraction per eight codes
+// in pack_pair_q3's nibbles; INT6: a sign-replicating byte permute of the
+// code bytes in pack_block) -- the same code as clipping t at qmax first (t
+// <= qmax is unchanged by the clip; for t > qmax, RNE(t) + bias is qmax + bias
+// or one more, and becomes qmax + bias, as RNE(qmax) + bias is).  That
 // removes one float minimum (integer-pipe work) per value.  The product and
 // the add are then two packed operations (mul_then_add2): contracted into one
 // rounding they would change the codes.
 template <int B>
 __device__ __forceinline__ void quantize_block_magic(const float2 (&v)[16], float r, bool low_clip,
                                                      float2 (&f)[16]) {
+    constexpr float kM = (B == 6) ? kMagic6 : Codec<B>::kMagic;
     const float2 r2 = make_float2(r, r);
-    const float2 m2 = make_float2(Codec<B>::kMagic, Codec<B>::kMagic);
-    if constexpr (B == 3) {
+    const float2 m2 = make_float2(kM, kM);
+    if constexpr (B == 3 || B == 6) {
         if (!low_clip) {
             const float one = __fmaf_rn(r, 0.0f, 1.0f);  // 1: r is finite
 #pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = mul_then_add2(v[i], r, one, Codec<B>::kMagic);
+            for (int i = 0; i < 16; ++i) f[i] = mul_then_add2(v[i], r, one, kM);
             return;
         }
     }
@@ -208,7 +216,8 @@ __device__ __forceinline__ void pack_pair_q3_lanes(const float2 (&F)[8], uint32_
 }
 
 // The INT6 sections of one slot from its codes as bytes (`even`: lanes
-// 0,2,4,6, `odd`: lanes 1,3,5,7, each byte a code below 64): the q4w word
+// 0,2,4,6, `odd`: lanes 1,3,5,7, each byte's low six bits a code; the bits
+// above are not read): the q4w word
 // (lane j's low nibble at bits 4j), and `y`, whose bytes 0 and 2 are the
 // slot's q2w field (lane j's high two bits at bits 2j): byte k of c holds
 // lanes 2k and 2k+1, and one shift-or pairs neighbouring bytes, so that a
@@ -218,6 +227,15 @@ __device__ __forceinline__ void q6_slot_fields(uint32_t even, uint32_t odd, uint
     q4w = (even & 0x0F0F0F0Fu) | ((odd & 0x0F0F0F0Fu) << 4);
     const uint32_t c = ((even >> 4) & 0x03030303u) | ((odd >> 2) & 0x0C0C0C0Cu);
     y = c | (c >> 4);
+}
+
+// Each byte of x replaced by 0xFF where its bit 7 is set, else 0 (one byte
+// permute in its sign-replicating mode, which the __byte_perm intrinsic does
+// not promise).
+__device__ __forceinline__ uint32_t sign_bytes(uint32_t x) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %1, 0xBA98;" : "=r"(d) : "r"(x));
+    return d;
 }
 
 template <int B>
@@ -239,6 +257,10 @@ __device__ __forceinline__ void pack_block(const float2 (&f)[16], BlockWords<B> 
                 c.w[2 * s] = __byte_perm(even, odd, 0x5140);
                 c.w[2 * s + 1] = __byte_perm(even, odd, 0x7362);
             } else {  // slot s's q2w field into the low (even s) or high half of its word
+                // code bytes are 64 + code, 0..64 (quantize_block_magic): bit 7
+                // is set only by 64 + 64, whose six code bits become all ones
+                even |= sign_bytes(even);
+                odd |= sign_bytes(odd);
                 uint32_t y;
                 q6_slot_fields(even, odd, c.w[s], y);
                 c.w[4 + s / 2] = s % 2 == 0 ? __byte_perm(y, 0u, 0x4420) : __byte_perm(c.w[4 + s / 2], y, 0x6410);

@@ -38,9 +38,11 @@ namespace qrk {
 
 namespace {
 
+// Three CTAs per SM, as the contiguous encode has (INT6 took 86 registers a
+// thread without the bound, and two CTAs per SM).
 template <int B, int DT, int U>
-__global__ void __launch_bounds__(kThreads32) peer_send_kernel(const uint16_t *__restrict__ x, long long n,
-                                                               PeerOwnerTiles dst, long long NB) {
+__global__ void __launch_bounds__(kThreads32, 3) peer_send_kernel(const uint16_t *__restrict__ x, long long n,
+                                                                  PeerOwnerTiles dst, long long NB) {
     chain_entry();
     encode32_run<B, DT, U>(x, n, dst, NB);
 }
