@@ -139,10 +139,11 @@ qr_status_t qr_encode(int bits, qr_dtype_t dtype, const void *x, size_t n,
  * 1 <= R <= 8.  `out_wire` may equal one of `wires` exactly.  At INT3, INT4
  * and INT6 with R >= 2, a block whose nonzero scales are all integer
  * multiples below 2^16 of the smallest one's unit (2^(floor(log2 smin) -
- * 10); about five binades) is summed exactly in integers (two-way 16x8-bit
- * dot products): then no partial sum of the rank order rounds, so the
- * result is the fp32 rank-order sum's, bit for bit; other blocks are summed
- * in fp32. */
+ * 10); about five binades; INT6 with at most four ranks also needs the
+ * multiples to sum below 2^17) is summed exactly in integers (two-way
+ * 16x8-bit dot products): then no partial sum of the rank order rounds, so
+ * the result is the fp32 rank-order sum's, bit for bit; other blocks are
+ * summed in fp32.  Which way a block went never shows in the bytes. */
 qr_status_t qr_segment_reduce(int bits, int R, const void *const *wires,
                               size_t n, void *out_wire, qr_stream_t stream);
 
