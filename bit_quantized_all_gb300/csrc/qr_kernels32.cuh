@@ -86,7 +86,8 @@ __device__ __forceinline__ float2 mul_then_add2(float2 v, float r, float one, fl
 }
 
 // INT6 codes leave the quantizer 64 above the code (kMagic6): a code of 64
-// (qmax + 1, which the packing turns into 63) then has bit 7 of its byte set.
+// (one past the top code 63; the packing turns it into 63) then has bit 7 of
+// its byte set, and no other code has.
 constexpr float kMagic6 = Codec<6>::kMagic + 64.0f;
 
 // f = clip(RN(v*r), qmin, qmax) + 1.5*2^23 + bias (the code in the low byte;
